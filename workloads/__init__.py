@@ -1,0 +1,145 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module only draws random numbers and lays out shapes. It holds none of the
+attention arithmetic, so both the float64 oracle (``oracle/``) and the CUDA path
+(``exact_io_aware_13_gb300``) can take their inputs from it without sharing any
+part of the computation.
+
+Workloads follow the LLM shapes on the pages: head dimension 128 from a 4096-wide
+model with 32 heads and sequences of 8192 tokens ("FlashAttention-3 y
+torch.compile", section 4 "Tutorial Práctico" and section 5 "Benchmarks"), plus the
+FlexAttention variants named in "El FlexAttention de PyTorch con FlashAttention-4 es
+un cambio radical" (ALiBi, sliding window, document masking, soft-capping).
+
+Recipe (the same on every machine):
+  * generator ``torch.Generator('cpu').manual_seed(seed)``;
+  * ``randn`` in float32 for Q, K, V and then dO, in that order, each rounded to
+    bfloat16 (round to nearest even) after drawing;
+  * document lengths from ``numpy.random.default_rng(seed).integers(512, 4096,
+    endpoint=True)``, drawn until their sum reaches N, the last one truncated.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+# Mask kinds and score-mod flags, numbered as in include/attn.h.
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_SLIDING_WINDOW = 2
+MASK_DOCUMENT_CAUSAL = 3
+
+SCORE_NONE = 0
+SCORE_ALIBI = 1
+SCORE_SOFTCAP = 2
+
+MASK_NAMES = {MASK_NONE: "none", MASK_CAUSAL: "causal",
+              MASK_SLIDING_WINDOW: "window", MASK_DOCUMENT_CAUSAL: "document"}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    seed: int
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nkv: int
+    d: int
+    mask_kind: int = MASK_NONE
+    window: int = 0
+    score_kind: int = SCORE_NONE
+    softcap: float = 0.0
+    backward: bool = False
+    doc_min: int = 512
+    doc_max: int = 4096
+
+    @property
+    def scale(self) -> float:
+        """1/sqrt(d), rounded to float32 (the value the kernels receive)."""
+        return float(np.float32(1.0 / math.sqrt(self.d)))
+
+    def describe(self) -> str:
+        s = (f"{self.name}: B={self.B} Hq={self.Hq} Hkv={self.Hkv} Nq={self.Nq} "
+             f"Nkv={self.Nkv} d={self.d} mask={MASK_NAMES[self.mask_kind]}")
+        if self.mask_kind == MASK_SLIDING_WINDOW:
+            s += f" W={self.window}"
+        if self.score_kind & SCORE_ALIBI:
+            s += " +alibi"
+        if self.score_kind & SCORE_SOFTCAP:
+            s += f" +softcap{self.softcap:g}"
+        return s
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads, in this order; seed = position in the list.
+TINY = Workload("tiny non-causal fwd", 0, B=1, Hq=2, Hkv=2, Nq=256, Nkv=256, d=64)
+CAUSAL = Workload("causal fwd", 1, B=4, Hq=16, Hkv=16, Nq=8192, Nkv=8192, d=128,
+                  mask_kind=MASK_CAUSAL)
+GQA_WINDOW = Workload("GQA sliding-window fwd", 2, B=2, Hq=32, Hkv=8, Nq=16384,
+                      Nkv=16384, d=128, mask_kind=MASK_SLIDING_WINDOW, window=1024)
+DOCS = Workload("packed-document fwd with ALiBi and soft-cap", 3, B=1, Hq=16, Hkv=16,
+                Nq=32768, Nkv=32768, d=128, mask_kind=MASK_DOCUMENT_CAUSAL,
+                score_kind=SCORE_ALIBI | SCORE_SOFTCAP, softcap=50.0)
+CAUSAL_FWD_BWD = Workload("causal fwd+bwd", 4, B=2, Hq=16, Hkv=16, Nq=8192, Nkv=8192,
+                          d=128, mask_kind=MASK_CAUSAL, backward=True)
+
+WORKLOADS = [TINY, CAUSAL, GQA_WINDOW, DOCS, CAUSAL_FWD_BWD]
+
+
+def document_lengths(total: int, seed: int, lo: int = 512, hi: int = 4096) -> list[int]:
+    """Draw document lengths uniformly from [lo, hi] until they cover ``total``.
+
+    The last document is cut so that the lengths sum to exactly ``total``.
+    """
+    rng = np.random.default_rng(seed)
+    lengths: list[int] = []
+    covered = 0
+    while covered < total:
+        n = int(rng.integers(lo, hi, endpoint=True))
+        n = min(n, total - covered)
+        lengths.append(n)
+        covered += n
+    return lengths
+
+
+def document_offsets(total: int, seed: int, lo: int = 512, hi: int = 4096) -> np.ndarray:
+    """Start offsets of the packed documents plus the end: int32[n_docs + 1]."""
+    lengths = document_lengths(total, seed, lo, hi)
+    return np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+
+
+def offsets_from_lengths(lengths) -> np.ndarray:
+    return np.concatenate([[0], np.cumsum(np.asarray(lengths, dtype=np.int64))]).astype(np.int32)
+
+
+def make_inputs(w: Workload, *, with_dout: Optional[bool] = None):
+    """Return bf16 CPU tensors q [B,Hq,Nq,d], k/v [B,Hkv,Nkv,d] and, for backward
+    workloads, dO [B,Hq,Nq,d]; plus int32 document offsets (or None).
+
+    Layout is [B, H, N, d] with d fastest.
+    """
+    g = torch.Generator("cpu").manual_seed(w.seed)
+    q = torch.randn((w.B, w.Hq, w.Nq, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((w.B, w.Hkv, w.Nkv, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((w.B, w.Hkv, w.Nkv, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    want_do = w.backward if with_dout is None else with_dout
+    do = None
+    if want_do:
+        do = torch.randn((w.B, w.Hq, w.Nq, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    offs = None
+    if w.mask_kind == MASK_DOCUMENT_CAUSAL:
+        offs = document_offsets(w.Nq, w.seed, w.doc_min, w.doc_max)
+    return q, k, v, do, offs
+
+
+def random_doc_offsets(total: int, seed: int, lo: int, hi: int) -> np.ndarray:
+    """Offsets for a small packed sequence (test sizes), same drawing rule."""
+    return document_offsets(total, seed, lo, hi)
