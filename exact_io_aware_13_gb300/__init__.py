@@ -1,0 +1,8 @@
+"""Exact, IO-aware tiled attention on GB300 (sm_103a): forward, backward and the
+FlexAttention-style score/mask modifications, as a C-ABI CUDA library with a thin
+Python binding."""
+from .attention import (MASK_CAUSAL, MASK_DOCUMENT_CAUSAL, MASK_NONE,  # noqa: F401
+                        MASK_SLIDING_WINDOW, SCORE_ALIBI, SCORE_NONE, SCORE_SOFTCAP,
+                        TILE_EMPTY, TILE_FULL, TILE_PARTIAL, backward, bwd_into,
+                        bwd_workspace_size, classify_tiles, device_status, forward, fwd_into)
+from ._lib import AttnError  # noqa: F401

@@ -1,0 +1,146 @@
+"""Python face of libattn.so: torch tensors in, the C ABI called, torch tensors out.
+
+PyTorch only provides device memory and the current CUDA stream here; every step
+of the computation runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+MASK_NONE, MASK_CAUSAL, MASK_SLIDING_WINDOW, MASK_DOCUMENT_CAUSAL = 0, 1, 2, 3
+SCORE_NONE, SCORE_ALIBI, SCORE_SOFTCAP = 0, 1, 2
+TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
+TILE = 128
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _params(mask_kind: int, window: int, doc_offsets: Optional[torch.Tensor],
+            softcap: float):
+    mp = _lib.MaskParams(int(window), None, 0)
+    if doc_offsets is not None:
+        if doc_offsets.dtype != torch.int32 or not doc_offsets.is_cuda:
+            raise ValueError("doc_offsets must be an int32 CUDA tensor")
+        mp.doc_offsets = doc_offsets.data_ptr()
+        mp.n_docs = doc_offsets.numel() - 1
+    sp = _lib.ScoreParams(float(softcap))
+    return ctypes.byref(mp), ctypes.byref(sp), (mp, sp)
+
+
+def _dims(q: torch.Tensor, k: torch.Tensor):
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nkv, dk = k.shape
+    if Bk != B or dk != d:
+        raise ValueError("q and k disagree on batch or head dimension")
+    return B, Hq, Hkv, Nq, Nkv, d
+
+
+def _check_tensors(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def fwd_into(q, k, v, o, lse, *, scale: float, mask_kind: int = MASK_NONE, window: int = 0,
+             doc_offsets=None, score_kind: int = SCORE_NONE, softcap: float = 0.0,
+             stream=None, impl: str = "tc") -> None:
+    """Run attn_fwd (impl="tc") or attn_fwd_simt (impl="simt") into o and lse."""
+    _check_tensors(q, k, v, o, lse, doc_offsets)
+    lib = _lib.load()
+    B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
+    mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap)
+    fn = lib.attn_fwd if impl == "tc" else lib.attn_fwd_simt
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nkv, d,
+            ctypes.c_float(scale), mask_kind, mp, score_kind, sp, _stream(stream))
+    del keep
+    _lib.check(st, fn.__name__)
+
+
+def forward(q, k, v, *, scale: Optional[float] = None, mask_kind: int = MASK_NONE,
+            window: int = 0, doc_offsets=None, score_kind: int = SCORE_NONE,
+            softcap: float = 0.0, stream=None, impl: str = "tc"):
+    """Exact attention forward. q: bf16 [B,Hq,Nq,d], k/v: bf16 [B,Hkv,Nkv,d] on CUDA.
+    Returns (o bf16 [B,Hq,Nq,d], lse fp32 [B,Hq,Nq])."""
+    d = q.shape[-1]
+    if scale is None:
+        scale = float(torch.tensor(d, dtype=torch.float32).rsqrt())
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    fwd_into(q, k, v, o, lse, scale=scale, mask_kind=mask_kind, window=window,
+             doc_offsets=doc_offsets, score_kind=score_kind, softcap=softcap, stream=stream,
+             impl=impl)
+    return o, lse
+
+
+def bwd_workspace_size(q, k) -> int:
+    B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
+    return int(_lib.load().attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d))
+
+
+def bwd_into(q, k, v, o, lse, dout, dq, dk, dv, workspace, *, scale: float,
+             mask_kind: int = MASK_NONE, window: int = 0, doc_offsets=None,
+             score_kind: int = SCORE_NONE, softcap: float = 0.0, stream=None,
+             impl: str = "tc") -> None:
+    """Run attn_bwd (impl="tc") or attn_bwd_simt into dq, dk, dv."""
+    _check_tensors(q, k, v, o, lse, dout, dq, dk, dv, workspace, doc_offsets)
+    lib = _lib.load()
+    B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
+    mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap)
+    fn = lib.attn_bwd if impl == "tc" else lib.attn_bwd_simt
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+            _ptr(dv), B, Hq, Hkv, Nq, Nkv, d, ctypes.c_float(scale), mask_kind, mp,
+            score_kind, sp, _ptr(workspace), ctypes.c_size_t(ws_bytes), _stream(stream))
+    del keep
+    _lib.check(st, fn.__name__)
+
+
+def backward(q, k, v, o, lse, dout, *, scale: Optional[float] = None,
+             mask_kind: int = MASK_NONE, window: int = 0, doc_offsets=None,
+             score_kind: int = SCORE_NONE, softcap: float = 0.0, stream=None,
+             impl: str = "tc"):
+    """Gradients (dq, dk, dv) of sum(dout * o), rebuilding P from lse."""
+    d = q.shape[-1]
+    if scale is None:
+        scale = float(torch.tensor(d, dtype=torch.float32).rsqrt())
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws = torch.empty(max(bwd_workspace_size(q, k), 256), dtype=torch.uint8, device=q.device)
+    bwd_into(q, k, v, o, lse, dout, dq, dk, dv, ws, scale=scale, mask_kind=mask_kind,
+             window=window, doc_offsets=doc_offsets, score_kind=score_kind, softcap=softcap,
+             stream=stream, impl=impl)
+    return dq, dk, dv
+
+
+def classify_tiles(mask_kind: int, Nq: int, Nkv: int, *, window: int = 0, doc_offsets=None,
+                   device="cuda", stream=None) -> torch.Tensor:
+    """Tile classes [ceil(Nq/128), ceil(Nkv/128)] int32: 0 empty, 1 partial, 2 full."""
+    lib = _lib.load()
+    nqt, nkt = -(-Nq // TILE), -(-Nkv // TILE)
+    out = torch.empty((nqt, nkt), dtype=torch.int32, device=device)
+    mp, _, keep = _params(mask_kind, window, doc_offsets, 0.0)
+    st = lib.attn_classify_tiles(mask_kind, mp, Nq, Nkv, _ptr(out), _stream(stream))
+    del keep
+    _lib.check(st, "attn_classify_tiles")
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise and return the library's device status (0 = no kernel gave up)."""
+    return int(_lib.load().attn_device_status(_stream(stream)))

@@ -1,0 +1,307 @@
+// The C ABI of libattn.so: argument checks, TMA tensor maps, the device status
+// word, and the launch sequence of each entry point. Nothing here allocates device
+// memory; every buffer comes from the caller.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "kernels.h"
+
+namespace attn {
+namespace {
+
+// Sticky device status word of this library (one per device that loads it).
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool is_sm103 = false;
+  int* status = nullptr;  // device address of g_device_status on this device
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Device checks and per-device state, done once per device with it current.
+attn_status current_device(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+    d.is_sm103 = (major == 10 && minor == 3);
+    if (d.is_sm103) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return ATTN_ERR_LAUNCH;
+      d.status = static_cast<int*>(ptr);
+      if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+          return ATTN_ERR_LAUNCH;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+    }
+    d.probed = true;
+  }
+  if (!d.is_sm103) return ATTN_ERR_ARCH;
+  *out = &d;
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Shared argument checks of the forward and backward entry points; fills `p`.
+attn_status check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale,
+                          int mask_kind, const attn_mask_params* mp, int score_kind,
+                          const attn_score_params* sp, Problem* p) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || Nq < 0 || Nkv < 0) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_SHAPE;
+  if (Hkv == 0 ? Hq != 0 : (Hq % Hkv) != 0) return ATTN_ERR_SHAPE;
+  const long long rows_q = (long long)B * Hq * Nq, rows_k = (long long)B * Hkv * Nkv;
+  if (rows_q * d > 0x7fffffffLL * 16 || rows_k * d > 0x7fffffffLL * 16) return ATTN_ERR_SHAPE;
+  if ((long long)B * Hq > 0x7fffffff / 2) return ATTN_ERR_SHAPE;
+  if (!std::isfinite(scale)) return ATTN_ERR_ARG;
+  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_DOCUMENT_CAUSAL) return ATTN_ERR_ARG;
+  if (score_kind & ~(ATTN_SCORE_ALIBI | ATTN_SCORE_SOFTCAP)) return ATTN_ERR_ARG;
+  std::memset(p, 0, sizeof(*p));
+  p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->Nq = Nq; p->Nkv = Nkv; p->d = d;
+  p->scale = scale;
+  p->score_kind = score_kind;
+  p->mask.kind = mask_kind;
+  p->mask.nq = Nq;
+  p->mask.nkv = Nkv;
+  if (score_kind & ATTN_SCORE_SOFTCAP) {
+    if (!sp || !(sp->softcap > 0.f) || !std::isfinite(sp->softcap)) return ATTN_ERR_ARG;
+    p->softcap = sp->softcap;
+  }
+  if (mask_kind == ATTN_MASK_SLIDING_WINDOW) {
+    if (!mp || mp->window < 0) return ATTN_ERR_ARG;
+    p->mask.window = mp->window;
+  }
+  if (mask_kind == ATTN_MASK_DOCUMENT_CAUSAL) {
+    if (!mp || !mp->doc_offsets || mp->n_docs < 1) return ATTN_ERR_ARG;
+    if (Nq != Nkv) return ATTN_ERR_SHAPE;
+    p->mask.doc = mp->doc_offsets;
+    p->mask.n_docs = mp->n_docs;
+  }
+  return ATTN_OK;
+}
+
+// 3-D tensor map over a [BH, N, d] bf16 tensor: boxes of 64 elements (128 bytes,
+// the 128-byte swizzle span) x 128 rows x 1 head. Rows past N read as zeros.
+attn_status make_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+attn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH; }
+
+attn_status fwd_common(bool simt, const void* q, const void* k, const void* v, void* o,
+                       float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale,
+                       int mask_kind, const attn_mask_params* mp, int score_kind,
+                       const attn_score_params* sp, void* stream) {
+  Problem p;
+  attn_status s = check_problem(B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind, mp, score_kind, sp, &p);
+  if (s != ATTN_OK) return s;
+  const long long rows_q = (long long)B * Hq * Nq;
+  if (rows_q == 0) return ATTN_OK;
+  if (!q || !o || !lse) return ATTN_ERR_ARG;
+  if (Nkv > 0 && (!k || !v)) return ATTN_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != ATTN_OK) return s;
+  p.status = dev->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto* ob = static_cast<__nv_bfloat16*>(o);
+  if (Nkv == 0) return from_cuda(launch_fill_masked(rows_q, d, ob, lse, st));
+  const auto* qb = static_cast<const __nv_bfloat16*>(q);
+  const auto* kb = static_cast<const __nv_bfloat16*>(k);
+  const auto* vb = static_cast<const __nv_bfloat16*>(v);
+  if (simt) return from_cuda(launch_fwd_simt(p, qb, kb, vb, ob, lse, st));
+  CUtensorMap tq, tk, tv;
+  if ((s = make_map(&tq, q, B * Hq, Nq, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tk, k, B * Hkv, Nkv, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tv, v, B * Hkv, Nkv, d)) != ATTN_OK) return s;
+  return from_cuda(launch_fwd_tc(p, tq, tk, tv, ob, lse, st));
+}
+
+attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int mask_kind,
+                       const attn_mask_params* mp, int score_kind, const attn_score_params* sp,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  Problem p;
+  attn_status s = check_problem(B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind, mp, score_kind, sp, &p);
+  if (s != ATTN_OK) return s;
+  const long long rows_q = (long long)B * Hq * Nq, rows_k = (long long)B * Hkv * Nkv;
+  if (rows_q == 0 && rows_k == 0) return ATTN_OK;
+  if (rows_q > 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_ERR_ARG;
+  if (rows_k > 0 && (!k || !v || !dk || !dv)) return ATTN_ERR_ARG;
+  const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return ATTN_ERR_ALIGN;
+  const size_t need = attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nkv, d);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != ATTN_OK) return s;
+  p.status = dev->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // With no queries nothing reaches the keys, and with no keys nothing reaches the
+  // queries: those gradients are zero.
+  if (rows_q == 0 || rows_k == 0) {
+    if (rows_q > 0 && cudaMemsetAsync(dq, 0, (size_t)rows_q * d * 2, st) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+    if (rows_k > 0 && cudaMemsetAsync(dk, 0, (size_t)rows_k * d * 2, st) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+    if (rows_k > 0 && cudaMemsetAsync(dv, 0, (size_t)rows_k * d * 2, st) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+    return ATTN_OK;
+  }
+  float* delta = static_cast<float*>(workspace);
+  const auto* qb = static_cast<const __nv_bfloat16*>(q);
+  const auto* kb = static_cast<const __nv_bfloat16*>(k);
+  const auto* vb = static_cast<const __nv_bfloat16*>(v);
+  const auto* dob = static_cast<const __nv_bfloat16*>(dout);
+  auto* dqb = static_cast<__nv_bfloat16*>(dq);
+  auto* dkb = static_cast<__nv_bfloat16*>(dk);
+  auto* dvb = static_cast<__nv_bfloat16*>(dv);
+  if ((s = from_cuda(launch_bwd_rowdot(p, static_cast<const __nv_bfloat16*>(o), dob, delta,
+                                       st))) != ATTN_OK)
+    return s;
+  if (simt) return from_cuda(launch_bwd_simt(p, qb, kb, vb, lse, dob, delta, dqb, dkb, dvb, st));
+  CUtensorMap tq, tk, tv, tdo;
+  if ((s = make_map(&tq, q, B * Hq, Nq, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tk, k, B * Hkv, Nkv, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tv, v, B * Hkv, Nkv, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tdo, dout, B * Hq, Nq, d)) != ATTN_OK) return s;
+  return from_cuda(launch_bwd_tc(p, tq, tk, tv, tdo, lse, delta, dqb, dkb, dvb, st));
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int mask_kind,
+                     const attn_mask_params* mask_params, int score_kind,
+                     const attn_score_params* score_params, void* stream) {
+  return fwd_common(false, q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind,
+                    mask_params, score_kind, score_params, stream);
+}
+
+attn_status attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale,
+                          int mask_kind, const attn_mask_params* mask_params, int score_kind,
+                          const attn_score_params* score_params, void* stream) {
+  return fwd_common(true, q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind,
+                    mask_params, score_kind, score_params, stream);
+}
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d) {
+  (void)Hkv; (void)Nkv; (void)d;
+  if (B <= 0 || Hq <= 0 || Nq <= 0) return 0;
+  return round256((size_t)B * Hq * Nq * sizeof(float));  // D, one float per query row
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                     int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int mask_kind,
+                     const attn_mask_params* mask_params, int score_kind,
+                     const attn_score_params* score_params, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return bwd_common(false, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale,
+                    mask_kind, mask_params, score_kind, score_params, workspace,
+                    workspace_bytes, stream);
+}
+
+attn_status attn_bwd_simt(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                          int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale,
+                          int mask_kind, const attn_mask_params* mask_params, int score_kind,
+                          const attn_score_params* score_params, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  return bwd_common(true, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale,
+                    mask_kind, mask_params, score_kind, score_params, workspace,
+                    workspace_bytes, stream);
+}
+
+attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_params, int Nq,
+                                int Nkv, int32_t* classes, void* stream) {
+  Problem p;
+  attn_status s = check_problem(1, 1, 1, Nq, Nkv, 64, 1.0f, mask_kind, mask_params, 0, nullptr,
+                                &p);
+  if (s != ATTN_OK) return s;
+  if (Nq == 0 || Nkv == 0) return ATTN_OK;
+  if (!classes) return ATTN_ERR_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != ATTN_OK) return s;
+  return from_cuda(launch_classify(p.mask, classes, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_device_status(void* stream) {
+  DeviceInfo* dev = nullptr;
+  attn_status s = current_device(&dev);
+  if (s != ATTN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  int value = 0;
+  if (cudaMemcpy(&value, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  if (value != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+    return ATTN_ERR_DEVICE_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+const char* attn_strerror(attn_status status) {
+  switch (status) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_ARG: return "invalid argument (null pointer, unknown kind or bad parameter)";
+    case ATTN_ERR_SHAPE: return "unsupported shape (d must be 64 or 128, Hq a multiple of Hkv)";
+    case ATTN_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+    case ATTN_ERR_ARCH: return "current device is not an sm_103 (GB300) GPU";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or smaller than attn_bwd_workspace_size";
+    case ATTN_ERR_LAUNCH: return "CUDA launch or driver call failed";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

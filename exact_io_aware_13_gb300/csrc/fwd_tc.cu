@@ -1,0 +1,424 @@
+// Forward attention on the fifth-generation tensor cores (tcgen05, sm_103a).
+//
+// The algorithm is the tiled forward of "FlashAttention/es" ("El algoritmo
+// FlashAttention"): for a block of query rows keep a running max m, a running
+// normaliser l and an output accumulator O; for each key/value tile compute the
+// score tile S = Q K^T, update m, rescale O and l by exp(m_old - m_new), add
+// P V and the row sums of P; at the end divide O by l and store L = m + log l.
+// Like FlashAttention-2 ("Variantes y sucesores") the outer loop is over query
+// blocks (one CTA each) and the division by l is deferred to the end.
+//
+// GB300 mapping (the FlashAttention-4 ideas named in "El FlexAttention de PyTorch
+// con FlashAttention-4 es un cambio radical": tensor memory, asynchronous MMAs,
+// warp specialisation, 256 x 128 tiles on Blackwell):
+//   * one CTA = 2 query tiles of 128 rows (256 rows) against key tiles of 128;
+//   * warp 8 streams Q once and K_j, V_j through a shared-memory ring with TMA
+//     (128-byte swizzle), skipping the key tiles the mask empties;
+//   * warp 9 allocates tensor memory and issues every tcgen05.mma from one thread:
+//     S_t = Q_t K_j^T into TMEM, then O_t += P_t V_j with P_t read from TMEM;
+//     the two query tiles ping-pong so that the softmax of one tile overlaps the
+//     MMAs of the other;
+//   * warps 0-3 and 4-7 are the softmax warpgroups of tiles 0 and 1: one thread
+//     per query row reads its 128 scores from TMEM, applies the score and mask
+//     modifications, updates m and l with exp2, writes P as bf16 back into the
+//     score columns, and rescales its O row in TMEM when the max has grown by more
+//     than 2^8 (a stale max is exact: O and l share it until the final division).
+// Tensor memory: S0 cols [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d).
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;        // query rows per query tile (= MMA M, TMEM lanes)
+constexpr int BN = 128;        // keys per key tile (= MMA N of S)
+constexpr int kQTiles = 2;     // query tiles per CTA
+constexpr int kStages = 4;     // K/V shared-memory ring depth (each stage one tile)
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kHeadGroup = 4;  // heads whose CTAs are scheduled together (L2 reuse)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+
+template <int D>
+struct Layout {
+  static constexpr int kChunk = BM * 128;               // one 64-column slab: 16 KB
+  static constexpr int kTile = BM * D * 2;              // one Q/K/V tile
+  static constexpr int kQ = 0;
+  static constexpr int kRing = kQ + kQTiles * kTile;
+  static constexpr int kBars = kRing + kStages * kTile;
+  static constexpr int kBytes = kBars + 256;
+  static constexpr int kAlloc = kBytes + 1024;          // room to align the base
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[kQTiles];
+  uint64_t p_full[kQTiles];
+  uint64_t o_full[kQTiles];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct FwdArgs {
+  Problem p;
+  __nv_bfloat16* o;
+  float* lse;
+  int num_qblocks;  // ceil(Nq / 256)
+};
+
+// CTA -> (batch*head, 256-row query block). Heads are taken kHeadGroup at a time
+// so the CTAs running together share K/V in L2; inside a group the longest query
+// blocks (most key tiles under causal masks) come first.
+__device__ __forceinline__ void cta_work(const FwdArgs& a, int& bh, int& qb) {
+  const int BH = a.p.B * a.p.Hq, nqb = a.num_qblocks;
+  const int per_group = kHeadGroup * nqb;
+  const int grp = blockIdx.x / per_group;
+  const int rem = blockIdx.x - grp * per_group;
+  const int gh = imin(kHeadGroup, BH - grp * kHeadGroup);
+  qb = nqb - 1 - rem / gh;
+  bh = grp * kHeadGroup + rem % gh;
+}
+
+template <int D, bool kAlibi, bool kSoftcap>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::kBars);
+  const Problem& p = a.p;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int bh, qb;
+  cta_work(a, bh, qb);
+  const int b = bh / p.Hq, h = bh - b * p.Hq;
+  const int g = h / (p.Hq / p.Hkv);
+  const int bg = b * p.Hkv + g;
+  const int q0 = qb * (kQTiles * BM);
+
+  TileRange rng[kQTiles];
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) rng[t] = kv_tiles_for_rows(p.mask, q0 + t * BM, BM);
+  int lo = 1 << 30, hi = 0;
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t)
+    if (rng[t].hi > rng[t].lo) { lo = imin(lo, rng[t].lo); hi = imax(hi, rng[t].hi); }
+
+  if (hi <= lo) {  // the mask leaves these rows no key: O = 0, L = -inf
+    for (int r = threadIdx.x; r < kQTiles * BM; r += kThreads) {
+      const int i = q0 + r;
+      if (i >= p.Nq) continue;
+      uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * p.Nq + i) * D);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+      a.lse[(size_t)bh * p.Nq + i] = -INFINITY;
+    }
+    return;
+  }
+  const int n_kv = hi - lo;
+
+  WaitCtx wc{&bars->abort_flag, p.status};
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->q_full), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars->kv_full[s]), 1);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(smem_u32(&bars->s_full[t]), 1);
+      mbar_init(smem_u32(&bars->p_full[t]), BM);
+      mbar_init(smem_u32(&bars->o_full[t]), 1);
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&bars->tmem_base), L::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before_sync();
+  }
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint32_t qbar = smem_u32(&bars->q_full);
+      mbar_arrive_expect_tx(qbar, kQTiles * L::kTile);
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t)
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem_u32(smem + L::kQ + t * L::kTile + c * L::kChunk), &tm_q, qbar, c * 64,
+                      q0 + t * BM, bh);
+      for (int u = 0; u < 2 * n_kv; ++u) {
+        const int s = u % kStages, use = u / kStages;
+        if (!mbar_wait(smem_u32(&bars->kv_empty[s]), (use & 1) ^ 1, wc)) break;
+        const uint32_t fb = smem_u32(&bars->kv_full[s]);
+        mbar_arrive_expect_tx(fb, L::kTile);
+        const CUtensorMap* map = (u & 1) ? &tm_v : &tm_k;
+        const int krow = (lo + (u >> 1)) * BN;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem_u32(smem + L::kRing + s * L::kTile + c * L::kChunk), map, fb, c * 64,
+                      krow, bg);
+      }
+      // Do not leave while copies into this CTA's shared memory are in flight.
+      mbar_wait(qbar, 0, wc);
+      for (int u = imax(0, 2 * n_kv - kStages); u < 2 * n_kv; ++u)
+        mbar_wait(smem_u32(&bars->kv_full[u % kStages]), (u / kStages) & 1, wc);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
+      const uint32_t colS[2] = {L::kColS0, L::kColS1};
+      const uint32_t colO[2] = {L::kColO0, L::kColO1};
+      const uint32_t q_base = smem_u32(smem + L::kQ);
+      const uint32_t ring = smem_u32(smem + L::kRing);
+      int np[kQTiles] = {0, 0};  // P tiles consumed per query tile
+      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, wc);
+
+      auto issue_s = [&](int t, int u) {  // S_t = Q_t K^T with K in ring use u
+        const uint32_t kb = ring + (u % kStages) * L::kTile;
+        const uint32_t qt = q_base + t * L::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kChunk + (kk & 3) * 32;
+          mma_ss(tmem + colS[t], smem_desc_sw128(qt + off, 16, 1024),
+                 smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->s_full[t]));
+      };
+      auto issue_pv = [&](int t, int u) {  // O_t += P_t V with V in ring use u
+        const uint32_t vb = ring + (u % kStages) * L::kTile;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8,
+                 smem_desc_sw128(vb + kk * 16 * 128, L::kChunk, 1024), idO,
+                 (np[t] > 0 || kk > 0) ? 1u : 0u);
+      };
+
+      if (ok) {
+        ok = mbar_wait(smem_u32(&bars->kv_full[0]), 0, wc);
+        tc_fence_after_sync();
+        if (ok) {
+#pragma unroll
+          for (int t = 0; t < kQTiles; ++t)
+            if (lo >= rng[t].lo && lo < rng[t].hi) issue_s(t, 0);
+          mma_commit(smem_u32(&bars->kv_empty[0]));
+        }
+      }
+      for (int jj = 0; ok && jj < n_kv; ++jj) {
+        const int j = lo + jj;
+        const int uv = 2 * jj + 1, uk = 2 * jj + 2;
+        const bool next = jj + 1 < n_kv;
+        if (!mbar_wait(smem_u32(&bars->kv_full[uv % kStages]), (uv / kStages) & 1, wc)) break;
+        bool k_ready = false;
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t) {
+          if (j >= rng[t].lo && j < rng[t].hi) {
+            if (!mbar_wait(smem_u32(&bars->p_full[t]), np[t] & 1, wc)) { ok = false; break; }
+            tc_fence_after_sync();
+            issue_pv(t, uv);
+            ++np[t];
+          }
+          if (next) {
+            if (!k_ready) {
+              if (!mbar_wait(smem_u32(&bars->kv_full[uk % kStages]), (uk / kStages) & 1, wc)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+              k_ready = true;
+            }
+            if (j + 1 >= rng[t].lo && j + 1 < rng[t].hi) issue_s(t, uk);
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&bars->kv_empty[uv % kStages]));
+        if (next) mma_commit(smem_u32(&bars->kv_empty[uk % kStages]));
+      }
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) mma_commit(smem_u32(&bars->o_full[t]));
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;                 // query tile of this warpgroup
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane = row in the tile
+    const int i = q0 + t * BM + row;         // query position
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (t == 0 ? L::kColS0 : L::kColS1);
+    const uint32_t tO = tmem + lane_base + (t == 0 ? L::kColO0 : L::kColO1);
+    const int fk = first_key(p.mask, i < p.Nq ? i : p.Nq - 1);
+    // Scores in log2 units: s2 = x * k1 + (j - i) * kb, then the soft-cap.
+    const float slope = kAlibi ? alibi_slope(h, p.Hq) : 0.f;
+    const float cap2 = kSoftcap ? 2.0f * kLog2e / p.softcap : 0.f;
+    const float k1 = kSoftcap ? p.scale * cap2 : p.scale * kLog2e;
+    const float kb = kSoftcap ? slope * cap2 : slope * kLog2e;
+    const float capA = kSoftcap ? p.softcap * kLog2e : 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    int n = 0;
+    for (int j = rng[t].lo; j < rng[t].hi; ++j, ++n) {
+      // Keep every decision warp-uniform: tcgen05.ld/st are warp-collective.
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[t]), n & 1, wc))) break;
+      tc_fence_after_sync();
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, r[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence32(r[c]);
+      const int k0 = j * BN;
+      const bool masked = tile_needs_mask(p.mask, q0 + t * BM, k0, BN);
+      const float base = kAlibi ? (float)(k0 - i) * kb : 0.f;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = c * 32 + e;
+          float x = __uint_as_float(r[c][e]);
+          float s2 = kAlibi ? fmaf(x, k1, fmaf((float)col, kb, base)) : x * k1;
+          if (kSoftcap) s2 = capA - 2.0f * capA * rcp_approx(1.0f + ex2_approx(s2));
+          if (masked && !allowed(p.mask, i, k0 + col, fk)) s2 = -INFINITY;
+          mt = fmaxf(mt, s2);
+          r[c][e] = __float_as_uint(s2);
+        }
+      const float m_new = fmaxf(m_run, mt);
+      const bool grow = m_new > m_run + kRescaleLog2;
+      const bool warp_grow = __any_sync(0xffffffffu, grow);
+      float corr = 1.f;
+      if (warp_grow) {
+        // exp2(m_old - m_new): 0 when only m_old is -inf, 1 when the row is still empty
+        corr = m_new == -INFINITY ? 1.f : ex2_approx(m_run - m_new);
+        m_run = m_new;
+        l_run *= corr;
+      }
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(__uint_as_float(r[c][2 * e]) - m_use);
+          const float p1 = ex2_approx(__uint_as_float(r[c][2 * e + 1]) - m_use);
+          lsum += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + c * 16, pk);
+      }
+      l_run += lsum;
+      if (warp_grow && n > 0) {  // O_t already holds P V of earlier tiles: rescale it
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
+          reg_fence32(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bars->p_full[t]));
+    }
+    // ---------------------------------------------------------- epilogue
+    bool have_o = n > 0;  // O_t holds at least one P V product
+    if (have_o) have_o = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full[t]), 0, wc));
+    tc_fence_after_sync();
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * p.Nq + (i < p.Nq ? i : 0)) * D);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      if (have_o) {  // warp-uniform
+        tmem_ld32(tO + c * 32, o);
+        tmem_wait_ld();
+        reg_fence32(o);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+      if (i < p.Nq) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+          orow[c * 4 + e] = w;
+        }
+      }
+    }
+    if (i < p.Nq)
+      a.lse[(size_t)bh * p.Nq + i] =
+          l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+  }
+  __syncwarp();
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int D, bool kAlibi, bool kSoftcap>
+cudaError_t launch_variant(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, int grid, cudaStream_t st) {
+  auto kern = fwd_tc_kernel<D, kAlibi, kSoftcap>;
+  const int smem = Layout<D>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv, int grid, cudaStream_t st) {
+  const bool al = a.p.score_kind & ATTN_SCORE_ALIBI, sc = a.p.score_kind & ATTN_SCORE_SOFTCAP;
+  if (al && sc) return launch_variant<D, true, true>(a, tq, tk, tv, grid, st);
+  if (al) return launch_variant<D, true, false>(a, tq, tk, tv, grid, st);
+  if (sc) return launch_variant<D, false, true>(a, tq, tk, tv, grid, st);
+  return launch_variant<D, false, false>(a, tq, tk, tv, grid, st);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, __nv_bfloat16* o, float* lse,
+                          cudaStream_t st) {
+  FwdArgs a;
+  a.p = p;
+  a.o = o;
+  a.lse = lse;
+  a.num_qblocks = ceil_div(p.Nq, kQTiles * BM);
+  const long long grid = (long long)a.num_qblocks * p.B * p.Hq;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (p.d == 64) return launch_d<64>(a, tq, tk, tv, (int)grid, st);
+  return launch_d<128>(a, tq, tk, tv, (int)grid, st);
+}
+
+}  // namespace attn

@@ -1,0 +1,54 @@
+// Launch interfaces shared between the translation units of libattn.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mask.cuh"
+
+namespace attn {
+
+// Everything a kernel needs to know about one attention problem.
+struct Problem {
+  int B, Hq, Hkv, Nq, Nkv, d;
+  float scale;        // multiplies Q K^T
+  int score_kind;     // ATTN_SCORE_* flags
+  float softcap;      // c of the soft-cap
+  MaskSpec mask;      // mask kind and parameters (doc offsets in device memory)
+  int* status;        // device status word (bounded waits write DEV_TIMEOUT)
+};
+
+// ALiBi slope of query head h: 2^(-8 (h+1) / Hq).
+__host__ __device__ inline float alibi_slope(int h, int Hq) {
+  return exp2f(-8.0f * (float)(h + 1) / (float)Hq);
+}
+
+// ---- CUDA-core (SIMT) kernels: cross-check path and shared backward helpers.
+cudaError_t launch_fwd_simt(const Problem& p, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                            const __nv_bfloat16* v, __nv_bfloat16* o, float* lse,
+                            cudaStream_t st);
+cudaError_t launch_bwd_simt(const Problem& p, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                            const __nv_bfloat16* v, const float* lse, const __nv_bfloat16* dout,
+                            const float* delta, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                            __nv_bfloat16* dv, cudaStream_t st);
+// D_i = sum_c dO_ic * O_ic over every query row (fp32), the backward's row term.
+cudaError_t launch_bwd_rowdot(const Problem& p, const __nv_bfloat16* o,
+                              const __nv_bfloat16* dout, float* delta, cudaStream_t st);
+// O = 0 and lse = -inf for `rows` rows (the answer when there are no keys).
+cudaError_t launch_fill_masked(long long rows, int d, __nv_bfloat16* o, float* lse,
+                               cudaStream_t st);
+cudaError_t launch_classify(const MaskSpec& m, int32_t* classes, cudaStream_t st);
+
+// ---- tcgen05 tensor-core kernels.
+cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, __nv_bfloat16* o, float* lse,
+                          cudaStream_t st);
+cudaError_t launch_bwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const float* lse,
+                          const float* delta, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                          __nv_bfloat16* dv, cudaStream_t st);
+
+}  // namespace attn

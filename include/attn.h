@@ -1,0 +1,175 @@
+/*
+ * attn.h - C ABI of libattn.so: exact, IO-aware tiled attention on GB300 (sm_103a).
+ *
+ * The operation is scaled-dot-product attention, O = softmax(Q K^T / sqrt(d)) V
+ * ("FlashAttention/es", section "Por qué la atención estándar es lenta"), computed
+ * exactly with the tiled online-softmax recurrence ("El truco del softmax en línea"
+ * and "El algoritmo FlashAttention" on the same page) so that no N x N matrix ever
+ * reaches device memory. The forward pass also writes the per-row log-sum-exp
+ * L_i = m_i + log(l_i) (natural log) that the backward pass uses to rebuild P
+ * ("Paso hacia atrás y recomputación", same page).
+ *
+ * Attention variants follow the FlexAttention list in "El FlexAttention de PyTorch
+ * con FlashAttention-4 es un cambio radical" (first section): score modifications
+ * ALiBi and tanh soft-capping, mask modifications causal, sliding window and
+ * document masking; tiles in which the mask allows nothing are skipped.
+ *
+ * Conventions shared by every call:
+ *   - Tensors are DEVICE pointers owned by the caller, contiguous, row-major:
+ *       q, o, dout, dq : bf16 [B, Hq,  Nq,  d]   (d fastest)
+ *       k, v, dk, dv   : bf16 [B, Hkv, Nkv, d]
+ *       lse            : fp32 [B, Hq, Nq]
+ *     Every tensor pointer must be 16-byte aligned (ATTN_ERR_ALIGN otherwise).
+ *   - Query head h reads kv head h / (Hq / Hkv) (grouped-query attention).
+ *   - d must be 64 or 128. Hq must be a multiple of Hkv.
+ *   - scale multiplies Q K^T (usually 1/sqrt(d)); it must be finite.
+ *   - Scores are modified in the order: scale, ALiBi, soft-cap, mask.
+ *       ALiBi:    s_ij -= slope_h * (i - j), slope_h = 2^(-8 (h+1) / Hq),
+ *                 h the 0-based query head.
+ *       soft-cap: s_ij  = c * tanh(s_ij / c), c = attn_score_params.softcap > 0.
+ *   - Masks (i = query position, j = key position, both from 0):
+ *       ATTN_MASK_NONE               every pair
+ *       ATTN_MASK_CAUSAL             j <= i (top-left aligned, also when Nq != Nkv)
+ *       ATTN_MASK_SLIDING_WINDOW     j <= i and i - j < window (window >= 0;
+ *                                    window 0 masks every pair)
+ *       ATTN_MASK_DOCUMENT_CAUSAL    doc(i) == doc(j) and j <= i, with documents
+ *                                    given by int32 DEVICE offsets
+ *                                    doc_offsets[0..n_docs]: doc_offsets[0] = 0,
+ *                                    non-decreasing, doc_offsets[n_docs] = Nq = Nkv.
+ *                                    The offsets are trusted (not read on the host).
+ *     A query row with no allowed key gets O = 0 and lse = -inf, and zero gradients.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). They allocate no device memory; the backward pass takes a
+ *     caller-provided workspace. Results are deterministic: the same inputs give
+ *     bitwise-identical outputs.
+ *   - Errors are returned, never hidden: there is no fallback path. A call that
+ *     returns an error launched nothing.
+ *   - Sizes of 0 (B, heads, Nq or Nkv) are valid; Nkv = 0 gives masked rows.
+ */
+#ifndef EXACT_IO_AWARE_ATTN_H
+#define EXACT_IO_AWARE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_ARG = 1,            /* null pointer, unknown kind, bad scale/window/softcap */
+  ATTN_ERR_SHAPE = 2,          /* unsupported d, Hq % Hkv != 0, negative size,
+                                  document mask with Nq != Nkv, size over 2^31 */
+  ATTN_ERR_ALIGN = 3,          /* a tensor pointer is not 16-byte aligned */
+  ATTN_ERR_ARCH = 4,           /* the current device is not compute capability 10.3 */
+  ATTN_ERR_WORKSPACE = 5,      /* workspace NULL or smaller than attn_bwd_workspace_size */
+  ATTN_ERR_LAUNCH = 6,         /* a CUDA runtime/driver call or a launch failed */
+  ATTN_ERR_DEVICE_TIMEOUT = 7  /* a kernel's bounded wait expired (attn_device_status) */
+} attn_status;
+
+enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_MASK_CAUSAL = 1,
+  ATTN_MASK_SLIDING_WINDOW = 2,
+  ATTN_MASK_DOCUMENT_CAUSAL = 3
+};
+
+/* Score modification flags (OR-able; ALiBi is applied before soft-cap). */
+enum {
+  ATTN_SCORE_NONE = 0,
+  ATTN_SCORE_ALIBI = 1,
+  ATTN_SCORE_SOFTCAP = 2
+};
+
+/* Tile classes written by attn_classify_tiles. */
+enum { ATTN_TILE_EMPTY = 0, ATTN_TILE_PARTIAL = 1, ATTN_TILE_FULL = 2 };
+
+/* Side of the square tiles the kernels iterate over (query rows x key columns). */
+#define ATTN_TILE 128
+
+typedef struct {
+  int32_t window;              /* ATTN_MASK_SLIDING_WINDOW: keys i-window+1 .. i */
+  const int32_t* doc_offsets;  /* ATTN_MASK_DOCUMENT_CAUSAL: DEVICE int32[n_docs+1] */
+  int32_t n_docs;
+} attn_mask_params;
+
+typedef struct {
+  float softcap;               /* ATTN_SCORE_SOFTCAP: the cap c > 0 */
+} attn_score_params;
+
+/*
+ * Forward pass ("FlashAttention/es", "El algoritmo FlashAttention"): writes
+ * o = softmax(modified, masked scores) v and lse = m + log(l) per query row.
+ * mask_params / score_params are HOST pointers and may be NULL when the kind
+ * needs no parameter. Runs the tcgen05 tensor-core kernel.
+ */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale,
+                     int mask_kind, const attn_mask_params* mask_params,
+                     int score_kind, const attn_score_params* score_params,
+                     void* stream);
+
+/* Bytes of device workspace attn_bwd needs for these sizes (a multiple of 256). */
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d);
+
+/*
+ * Backward pass ("FlashAttention/es", "Paso hacia atrás y recomputación"): from
+ * q, k, v, the forward's o and lse, and the output gradient dout, rebuilds P
+ * tile by tile and writes dq, dk, dv (bf16, overwritten, not accumulated). The
+ * gradient algebra is the standard one: dV = P^T dO, dP = dO V^T,
+ * D_i = rowsum(dO o O), dS = P o (dP - D) (times the soft-cap derivative),
+ * dQ = scale dS K, dK = scale dS^T Q, with dK and dV summed over the query heads
+ * of a group. workspace: DEVICE memory of at least attn_bwd_workspace_size bytes,
+ * 256-byte aligned, not shared with a concurrent call.
+ */
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale,
+                     int mask_kind, const attn_mask_params* mask_params,
+                     int score_kind, const attn_score_params* score_params,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Block-sparsity classifier ("El FlexAttention de PyTorch con FlashAttention-4 es
+ * un cambio radical", "Limitaciones actuales", names block sparsity): writes
+ * classes[r * ceil(Nkv/128) + c] = EMPTY / PARTIAL / FULL for query tile r and key
+ * tile c, with the same tile rule the forward and backward kernels use to skip
+ * and to mask tiles. classes: DEVICE int32 [ceil(Nq/128) * ceil(Nkv/128)].
+ */
+attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_params,
+                                int Nq, int Nkv, int32_t* classes, void* stream);
+
+/*
+ * Plain CUDA-core versions of the forward and backward passes (one thread per
+ * row, fp32 arithmetic, no tensor cores). They exist to cross-check the tensor-core
+ * kernels and are never chosen automatically. Same arguments and contract as
+ * attn_fwd / attn_bwd (attn_bwd_simt needs the same workspace).
+ */
+attn_status attn_fwd_simt(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale,
+                          int mask_kind, const attn_mask_params* mask_params,
+                          int score_kind, const attn_score_params* score_params,
+                          void* stream);
+attn_status attn_bwd_simt(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                          int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale,
+                          int mask_kind, const attn_mask_params* mask_params,
+                          int score_kind, const attn_score_params* score_params,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream` and reports whether a kernel of this library on the
+ * current device gave up a bounded wait since the last call (ATTN_ERR_DEVICE_TIMEOUT),
+ * or whether the stream itself failed (ATTN_ERR_LAUNCH). Clears the flag.
+ */
+attn_status attn_device_status(void* stream);
+
+/* Static, human-readable text for a status code. */
+const char* attn_strerror(attn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_IO_AWARE_ATTN_H */

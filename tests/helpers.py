@@ -1,0 +1,110 @@
+"""Shared helpers of the GPU parity tests: run the library and the oracle on the same
+seeded inputs and compare with the stated tolerances.
+
+Tolerances (bf16 inputs, fp32 accumulation):
+  forward : max|O - O_ref| <= 1e-2 ; max|LSE - LSE_ref| <= 1e-3 on finite entries,
+            and -inf exactly where the oracle has -inf;
+  backward: max|dX - dX_ref| <= 2e-2 * max|dX_ref| for each of dq, dk, dv.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from workloads import MASK_DOCUMENT_CAUSAL, Workload, make_inputs
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+GRAD_REL_TOL = 2e-2
+
+
+def to_dev(*ts):
+    return [None if t is None else t.cuda() for t in ts]
+
+
+def doc_tensor(offs):
+    return None if offs is None else torch.from_numpy(np.asarray(offs, dtype=np.int32)).cuda()
+
+
+def mask_kwargs(w: Workload, offs):
+    return dict(mask_kind=w.mask_kind, window=w.window, score_kind=w.score_kind,
+                softcap=w.softcap)
+
+
+def oracle_kwargs(w: Workload, offs):
+    return dict(mask_kind=w.mask_kind, window=w.window, doc_offsets=offs,
+                score_kind=w.score_kind, softcap=w.softcap)
+
+
+def check_forward(o, lse, o_ref, lse_ref, what=""):
+    o = np.asarray(o, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    assert o.shape == o_ref.shape and lse.shape == lse_ref.shape
+    err_o = float(np.abs(o - o_ref).max()) if o.size else 0.0
+    ninf_ref = np.isneginf(lse_ref)
+    assert (np.isneginf(lse) == ninf_ref).all(), f"{what}: -inf pattern of LSE differs"
+    fin = ~ninf_ref
+    err_l = float(np.abs(lse[fin] - lse_ref[fin]).max()) if fin.any() else 0.0
+    assert err_o <= O_TOL, f"{what}: max|dO| = {err_o}"
+    assert err_l <= LSE_TOL, f"{what}: max|dLSE| = {err_l}"
+    return err_o, err_l
+
+
+def check_grads(got, ref, what=""):
+    errs = []
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        g = np.asarray(g, dtype=np.float64)
+        assert np.isfinite(g).all(), f"{what}: {name} not finite"
+        scale = float(np.abs(r).max()) if r.size else 0.0
+        err = float(np.abs(g - r).max()) if r.size else 0.0
+        assert err <= GRAD_REL_TOL * max(scale, 1e-30) or err == 0.0, \
+            f"{what}: max|d{name}| = {err} vs {GRAD_REL_TOL} * {scale}"
+        errs.append(err / max(scale, 1e-30))
+    return errs
+
+
+def run_forward(w: Workload, impl="tc", inputs=None):
+    import exact_io_aware_13_gb300 as ea
+    q, k, v, do, offs = inputs if inputs is not None else make_inputs(w)
+    qd, kd, vd = to_dev(q, k, v)
+    o, lse = ea.forward(qd, kd, vd, scale=w.scale, doc_offsets=doc_tensor(offs), impl=impl,
+                        **mask_kwargs(w, offs))
+    torch.cuda.synchronize()
+    assert ea.device_status() == 0
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def run_backward(w: Workload, impl="tc", inputs=None):
+    import exact_io_aware_13_gb300 as ea
+    q, k, v, do, offs = inputs if inputs is not None else make_inputs(w, with_dout=True)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    dt = doc_tensor(offs)
+    o, lse = ea.forward(qd, kd, vd, scale=w.scale, doc_offsets=dt, impl=impl,
+                        **mask_kwargs(w, offs))
+    dq, dk, dv = ea.backward(qd, kd, vd, o, lse, dod, scale=w.scale, doc_offsets=dt, impl=impl,
+                             **mask_kwargs(w, offs))
+    torch.cuda.synchronize()
+    assert ea.device_status() == 0
+    return [t.float().cpu().numpy() for t in (dq, dk, dv)]
+
+
+def small_workload(name, mask_kind, score_kind=0, *, B=1, Hq=4, Hkv=2, N=300, Nkv=None, d=64,
+                   window=0, softcap=0.0, seed=7, doc_lo=40, doc_hi=260):
+    return Workload(name, seed, B=B, Hq=Hq, Hkv=Hkv, Nq=N, Nkv=N if Nkv is None else Nkv, d=d,
+                    mask_kind=mask_kind, window=window, score_kind=score_kind,
+                    softcap=softcap, doc_min=doc_lo, doc_max=doc_hi)
+
+
+def is_document(w):
+    return w.mask_kind == MASK_DOCUMENT_CAUSAL
+
+
+def oracle_forward(w, inputs, rows=None, heads=None):
+    q, k, v, _, offs = inputs
+    return oracle.forward(q, k, v, w.scale, rows=rows, heads=heads, **oracle_kwargs(w, offs))
+
+
+def oracle_backward(w, inputs, kv_heads=None):
+    q, k, v, do, offs = inputs
+    return oracle.backward(q, k, v, do, w.scale, kv_heads=kv_heads, **oracle_kwargs(w, offs))
