@@ -1,0 +1,312 @@
+"""Benchmark: one step = the whole hot path (tile classification, forward with the
+online softmax, backward rebuilding P from the LSE) on the causal fwd+bwd workload
+(B=2, H=16, N=8192, d=128, bf16), timed with CUDA events.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. `value` is useful TFLOP/s (masked-out work excluded) summed
+over ranks; with N > 1 each rank runs its own replica of the workload (the heads
+are independent, so there is no data-path collective). --impl reference times the
+float64 CPU oracle on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import CAUSAL_FWD_BWD, make_inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return {"bf16_tflops": m["bf16_tflops"], "bf16_sustained": m["bf16_tflops_sustained"],
+                "hbm_gbs": m["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[3:7]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.describe(), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.Nq, "d": w.d,
+           "mask": "causal", "seed": w.seed,
+           "l2": "flushed between steps (256 MiB write); inputs 256 MiB > L2"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def run_ours(args):
+    from exact_io_aware_13_gb300 import build as libbuild
+    libbuild.build()  # compiles libattn.so from source if it is missing or stale
+    import exact_io_aware_13_gb300 as ea
+    from exact_io_aware_13_gb300 import flops
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = CAUSAL_FWD_BWD
+    pairs = flops.allowed_pairs(w.mask_kind, w.Nq, w.Nkv)
+    f_fwd = flops.attention_flops(w.B, w.Hq, w.d, pairs, backward=False)
+    f_bwd = flops.attention_flops(w.B, w.Hq, w.d, pairs, backward=True)
+    f_step = f_fwd + f_bwd
+
+    q, k, v, do, _ = make_inputs(w)
+    host = [t.pin_memory() for t in (q, k, v, do)]
+    qd, kd, vd, dod = (t.to(dev) for t in host)
+    o = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[:-1], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(ea.bwd_workspace_size(qd, kd), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    kw = dict(scale=w.scale, mask_kind=w.mask_kind)
+
+    def step():
+        ea.fwd_into(qd, kd, vd, o, lse, **kw)
+        ea.bwd_into(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ea.device_status() != 0:
+        raise RuntimeError("a kernel gave up a bounded wait during warm-up")
+
+    # ------------------------------------------------------------ device-timed steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(args.steps):
+            flush.zero_()  # evict the previous step's tensors from L2 (untimed)
+            ev[s][0].record(stream)
+            ea.fwd_into(qd, kd, vd, o, lse, **kw)
+            ev[s][1].record(stream)
+            ea.bwd_into(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, **kw)
+            ev[s][2].record(stream)
+        torch.cuda.synchronize()
+    if ea.device_status() != 0:
+        raise RuntimeError("a kernel gave up a bounded wait during the timed steps")
+    t_fwd = [e[0].elapsed_time(e[1]) for e in ev]
+    t_bwd = [e[1].elapsed_time(e[2]) for e in ev]
+    t_step = sum(a + b for a, b in zip(t_fwd, t_bwd))  # ms over K steps
+    if world > 1:
+        tt = torch.tensor([t_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_step = float(tt.item())
+        torch.distributed.barrier()
+    ms_step = t_step / args.steps
+    value = world * f_step / (ms_step * 1e-3) / 1e12
+
+    # ------------------------------------------------------------ end to end, host buffers
+    outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                 for t in (o, lse, dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in outs_host)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for dst, src in zip((qd, kd, vd, dod), host):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(outs_host, (o, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    e2e_value = world * f_step / (ms_e2e * 1e-3) / 1e12
+
+    pk = peaks()
+    ms_fwd = statistics.mean(t_fwd)
+    ms_bwd = statistics.mean(t_bwd)
+    fwd_tf = f_fwd / (ms_fwd * 1e-3) / 1e12
+    bwd_tf = f_bwd / (ms_bwd * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded randn rounded to bf16)",
+        "config": workload_config(w, {"parallelism": f"replicas x{world}"}),
+        "pct_of_peak": round(100 * value / world / pk["bf16_tflops"], 1),
+        "fwd": {"tflops": round(fwd_tf, 2), "ms": round(ms_fwd, 4),
+                "pct_of_peak": round(100 * fwd_tf / pk["bf16_tflops"], 1)},
+        "bwd": {"tflops": round(bwd_tf, 2), "ms": round(ms_bwd, 4),
+                "pct_of_peak": round(100 * bwd_tf / pk["bf16_tflops"], 1)},
+        "roofline": {"bound": "tensor", "kernel": "fwd_tc_kernel (attn_fwd)",
+                     "achieved": round(fwd_tf, 2), "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(fwd_tf / pk["bf16_tflops"], 4),
+                     "peak_source": pk["source"] + " bf16 burst", "traffic": None},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, seconds: float = 20.0, heads: int = 1):
+    """Time the float64 oracle (forward + backward) on `heads` (b, h) heads of the
+    workload, full sequence, on the host cores."""
+    import oracle
+    from exact_io_aware_13_gb300 import flops
+    q, k, v, do, _ = make_inputs(w)
+    done, t0 = 0, time.perf_counter()
+    pairs = flops.allowed_pairs(w.mask_kind, w.Nq, w.Nkv)
+    while done < heads or (time.perf_counter() - t0 < seconds and done < w.B * w.Hq):
+        b, h = divmod(done, w.Hq)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        oracle.forward(q[sl], k[sl], v[sl], w.scale, mask_kind=w.mask_kind)
+        oracle.backward(q[sl], k[sl], v[sl], do[sl], w.scale, mask_kind=w.mask_kind)
+        done += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    el = time.perf_counter() - t0
+    f = flops.attention_flops(1, done, w.d, pairs, True) + flops.attention_flops(1, done, w.d,
+                                                                                  pairs, False)
+    return {"value": round(f / el / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(el, 2),
+            "sample": f"{done} of {w.B * w.Hq} heads (full N={w.Nq}), forward + backward, "
+                      "float64 numpy oracle (BLAS threads = all cores)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = CAUSAL_FWD_BWD
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; warm-up steps are accepted and skipped
+    times, cb = [], None
+    for _ in range(args.steps):
+        cb = cpu_baseline(w, seconds=0.0, heads=1)
+        times.append(cb["seconds"])
+    value = statistics.mean([cb["value"]]) if cb else 0.0
+    from exact_io_aware_13_gb300 import flops
+    pairs = flops.allowed_pairs(w.mask_kind, w.Nq, w.Nkv)
+    f_head = (flops.attention_flops(1, 1, w.d, pairs, True)
+              + flops.attention_flops(1, 1, w.d, pairs, False))
+    ms = statistics.mean(times) * 1e3
+    value = f_head / (ms * 1e-3) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn rounded to bf16)",
+            "config": workload_config(w, {"sample": "1 of 32 heads per step"}),
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": "1 of 32 heads (full N=8192), forward + backward per step"},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

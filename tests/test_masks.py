@@ -106,3 +106,16 @@ def test_workload_tile_counts(host):
                        len(doc) - 1, n, n, cls.ctypes.data_as(ctypes.c_void_p))
     brute = ref.classify_tiles(MASK_DOCUMENT_CAUSAL, n, n, T, T, 0, offs)
     assert (cls == brute).all()
+
+
+def test_flop_pair_counts_match_brute_force():
+    from exact_io_aware_13_gb300 import flops
+    for kind, nq, nkv, w, offs in [(MASK_NONE, 300, 200, 0, None), (MASK_CAUSAL, 300, 300, 0, None),
+                                   (MASK_CAUSAL, 300, 120, 0, None), (MASK_CAUSAL, 120, 300, 0, None),
+                                   (MASK_SLIDING_WINDOW, 500, 500, 77, None),
+                                   (MASK_SLIDING_WINDOW, 500, 500, 0, None),
+                                   (MASK_DOCUMENT_CAUSAL, 900, 900, 0, offsets_from_lengths([100, 500, 300]))]:
+        assert flops.allowed_pairs(kind, nq, nkv, w, offs) == ref.allowed_pairs(kind, nq, nkv, w, offs)
+    n = 8192
+    assert flops.allowed_pairs(MASK_CAUSAL, n, n) == 33558528
+    assert flops.attention_flops(4, 16, 128, 33558528, False) == 1099645845504.0  # 4 * d * pairs * B * H
