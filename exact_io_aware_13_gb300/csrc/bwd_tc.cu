@@ -172,9 +172,11 @@ __device__ __forceinline__ void mma_tmem_x_tile(uint32_t d_tmem, uint32_t a_tmem
 }
 
 // Write one accumulator row (D fp32 columns at TMEM `t`) times `mul` as bf16.
+// tcgen05.ld is warp-collective: every lane of the warp must call this with the same
+// `live`; `store` (per lane) only decides whether the row is written.
 template <int D>
 __device__ __forceinline__ void store_acc_row(uint32_t t, float mul, __nv_bfloat16* dst,
-                                              bool live) {
+                                              bool live, bool store) {
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
     uint32_t r[32];
@@ -186,15 +188,17 @@ __device__ __forceinline__ void store_acc_row(uint32_t t, float mul, __nv_bfloat
 #pragma unroll
       for (int e = 0; e < 32; ++e) r[e] = 0u;
     }
-    uint4* o = reinterpret_cast<uint4*>(dst) + c * 4;
+    if (store) {
+      uint4* o = reinterpret_cast<uint4*>(dst) + c * 4;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      uint4 w;
-      w.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * mul, __uint_as_float(r[8 * e + 1]) * mul);
-      w.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * mul, __uint_as_float(r[8 * e + 3]) * mul);
-      w.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * mul, __uint_as_float(r[8 * e + 5]) * mul);
-      w.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * mul, __uint_as_float(r[8 * e + 7]) * mul);
-      o[e] = w;
+      for (int e = 0; e < 4; ++e) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * mul, __uint_as_float(r[8 * e + 1]) * mul);
+        w.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * mul, __uint_as_float(r[8 * e + 3]) * mul);
+        w.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * mul, __uint_as_float(r[8 * e + 5]) * mul);
+        w.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * mul, __uint_as_float(r[8 * e + 7]) * mul);
+        o[e] = w;
+      }
     }
   }
 }
@@ -396,16 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warpgroup 0 writes dV, warpgroup 1 writes dK (times the softmax scale)
     const uint32_t tacc = tmem + lane_base + (wg == 0 ? L::kColDV : L::kColDK);
     __nv_bfloat16* dst = (wg == 0 ? a.dv : a.dk) + krow * D;
-    if (j < p.Nkv) {
-      store_acc_row<D>(tacc, wg == 0 ? 1.f : p.scale, dst, have);
-    } else if (have) {
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {  // warp-collective loads, results unused
-        uint32_t r[32];
-        tmem_ld32(tacc + c * 32, r);
-        tmem_wait_ld();
-      }
-    }
+    store_acc_row<D>(tacc, wg == 0 ? 1.f : p.scale, dst, have, j < p.Nkv);
   }
   __syncwarp();
   tc_fence_before_sync();
@@ -570,16 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warpgroup 0 writes dQ columns [0, D/2), warpgroup 1 columns [D/2, D)
     const uint32_t tq = tmem + lane_base + L::kColDQ + wg * (D / 2);
     __nv_bfloat16* dst = a.dq + ((size_t)bh * p.Nq + (row_ok ? i : 0)) * D + wg * (D / 2);
-    if (row_ok) {
-      store_acc_row<D / 2>(tq, p.scale, dst, have);
-    } else if (have) {
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tq + c * 32, r);
-        tmem_wait_ld();
-      }
-    }
+    store_acc_row<D / 2>(tq, p.scale, dst, have, row_ok);
   }
   __syncwarp();
   tc_fence_before_sync();

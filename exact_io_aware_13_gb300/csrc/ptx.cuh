@@ -153,9 +153,14 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint
   return base + (lane << 16) + col;
 }
 
+// tcgen05.ld / tcgen05.st / tcgen05.wait are warp-collective (.sync.aligned): every
+// lane of the warp must execute them together. Each wrapper first reconverges the
+// warp with __syncwarp(); a caller must still reach it from warp-uniform control flow.
+
 // 32 lanes x 32 columns of 32-bit: thread t of the warp gets lane (base lane + t),
 // columns col .. col+31 in r[0..31]. The values are valid only after tmem_wait_ld().
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  __syncwarp();
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
       "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -169,9 +174,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {
+  __syncwarp();
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
+  __syncwarp();
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
@@ -191,6 +198,7 @@ __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
 
 // 32 lanes x 16 columns store (thread t writes lane base+t, columns col..col+15).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  __syncwarp();
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
       "%13,%14,%15,%16};" ::"r"(taddr),
@@ -201,6 +209,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  __syncwarp();
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
       "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
