@@ -4,7 +4,10 @@ seeded inputs and compare with the stated tolerances.
 Tolerances (bf16 inputs, fp32 accumulation):
   forward : max|O - O_ref| <= 1e-2 ; max|LSE - LSE_ref| <= 1e-3 on finite entries,
             and -inf exactly where the oracle has -inf;
-  backward: max|dX - dX_ref| <= 2e-2 * max|dX_ref| for each of dq, dk, dv.
+  backward: max|dX - dX_ref| <= 2e-2 * max|dX_ref| + 1e-5 for each of dq, dk, dv.
+            The 1e-5 floor only matters where the exact gradient vanishes (one allowed
+            key per row: P = 1 and dP - D = 0): there the kernels leave fp32
+            accumulation-order residue of |dO||V| * 2^-23 * d, about 1e-6.
 """
 from __future__ import annotations
 
@@ -17,6 +20,7 @@ from workloads import MASK_DOCUMENT_CAUSAL, Workload, make_inputs
 O_TOL = 1e-2
 LSE_TOL = 1e-3
 GRAD_REL_TOL = 2e-2
+GRAD_ABS_FLOOR = 1e-5
 
 
 def to_dev(*ts):
@@ -58,8 +62,8 @@ def check_grads(got, ref, what=""):
         assert np.isfinite(g).all(), f"{what}: {name} not finite"
         scale = float(np.abs(r).max()) if r.size else 0.0
         err = float(np.abs(g - r).max()) if r.size else 0.0
-        assert err <= GRAD_REL_TOL * max(scale, 1e-30) or err == 0.0, \
-            f"{what}: max|d{name}| = {err} vs {GRAD_REL_TOL} * {scale}"
+        assert err <= GRAD_REL_TOL * scale + GRAD_ABS_FLOOR, \
+            f"{what}: max|d{name}| = {err} vs {GRAD_REL_TOL} * {scale} + {GRAD_ABS_FLOOR}"
         errs.append(err / max(scale, 1e-30))
     return errs
 
