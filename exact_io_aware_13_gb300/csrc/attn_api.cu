@@ -208,6 +208,32 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
   return from_cuda(launch_bwd_tc(p, tq, tk, tv, tdo, lse, delta, dqb, dkb, dvb, st));
 }
 
+// ---------------------------------------------------------------- static workspace
+// Scratch of attn_bwd_static_workspace: the backward's row term D (one float per
+// query row) for callers that cannot allocate. One copy per device, shared by every
+// call on that device.
+static __device__ __align__(256) float g_static_workspace[ATTN_STATIC_WORKSPACE_ROWS];
+
+std::mutex g_static_mu;
+float* g_static_ptr[kMaxDevices];  // device address of g_static_workspace, per device
+
+// Device address of g_static_workspace on the current device. The host-side name
+// of the array is only a stand-in for it, so the address is looked up once per
+// device, with that device current, and cached.
+attn_status static_workspace_ptr(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || ptr == nullptr)
+      return ATTN_ERR_LAUNCH;
+    g_static_ptr[dev] = static_cast<float*>(ptr);
+  }
+  *out = g_static_ptr[dev];
+  return ATTN_OK;
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -257,6 +283,27 @@ attn_status attn_bwd_simt(const void* q, const void* k, const void* v, const voi
   return bwd_common(true, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale,
                     mask_kind, mask_params, score_kind, score_params, workspace,
                     workspace_bytes, stream);
+}
+
+attn_status attn_bwd_static_workspace(const void* q, const void* k, const void* v,
+                                      const void* o, const float* lse, const void* dout,
+                                      void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                                      int Nq, int Nkv, int d, float scale, int mask_kind,
+                                      const attn_mask_params* mask_params, int score_kind,
+                                      const attn_score_params* score_params, void* stream) {
+  if (B < 0 || Hq < 0 || Nq < 0) return ATTN_ERR_SHAPE;
+  const long long rows = (long long)B * Hq * Nq;
+  if (rows > ATTN_STATIC_WORKSPACE_ROWS) return ATTN_ERR_WORKSPACE;
+  float* ws = nullptr;
+  if (rows > 0) {
+    DeviceInfo* dev = nullptr;
+    attn_status s = current_device(&dev);  // rejects devices other than sm_103 first
+    if (s != ATTN_OK) return s;
+    if ((s = static_workspace_ptr(&ws)) != ATTN_OK) return s;
+  }
+  return bwd_common(false, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale,
+                    mask_kind, mask_params, score_kind, score_params, ws,
+                    ws ? (size_t)ATTN_STATIC_WORKSPACE_ROWS * sizeof(float) : 0, stream);
 }
 
 attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_params, int Nq,

@@ -131,6 +131,38 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward pass that allocates nothing and takes no workspace argument.
+ *
+ * The method on the pages has no counterpart of this call; it exists for callers
+ * that cannot call cudaMalloc (or any allocator) where they run the backward pass:
+ * for example a host program whose device memory is already handed out in full to
+ * another allocator, or a runtime that forbids new allocations once it has started.
+ * Such a caller still owns and passes every input and output, exactly as for
+ * attn_bwd; only the backward's scratch (one fp32 row term per query row) lives in
+ * a fixed array inside this library instead of a caller workspace.
+ *
+ * - The array holds ATTN_STATIC_WORKSPACE_ROWS floats (8 MiB) on every device that
+ *   loads the library, for the life of the process. B * Hq * Nq must not exceed
+ *   ATTN_STATIC_WORKSPACE_ROWS; larger problems return ATTN_ERR_WORKSPACE and
+ *   launch nothing (use attn_bwd with a workspace for them).
+ * - The first call on a device looks up the array's device address with that device
+ *   current (a one-time set-up per device); make that first call before any stream
+ *   capture on the device.
+ * - Every call on a device shares the one array, and the array keeps whatever the
+ *   last call left there (each call overwrites every row it uses before reading it).
+ *   Calls whose kernels can overlap on the GPU (other streams, other host threads)
+ *   race on the array: order them on one stream or synchronise between them.
+ * - Arguments, results, determinism and errors are otherwise those of attn_bwd.
+ */
+#define ATTN_STATIC_WORKSPACE_ROWS (1 << 21)
+attn_status attn_bwd_static_workspace(const void* q, const void* k, const void* v,
+                                      const void* o, const float* lse, const void* dout,
+                                      void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                                      int Nq, int Nkv, int d, float scale, int mask_kind,
+                                      const attn_mask_params* mask_params, int score_kind,
+                                      const attn_score_params* score_params, void* stream);
+
+/*
  * Block-sparsity classifier ("El FlexAttention de PyTorch con FlashAttention-4 es
  * un cambio radical", "Limitaciones actuales", names block sparsity): writes
  * classes[r * ceil(Nkv/128) + c] = EMPTY / PARTIAL / FULL for query tile r and key
