@@ -271,6 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float k1 = kSoftcap ? p.scale * cap2 : p.scale * kLog2e;
     const float kb = kSoftcap ? slope * cap2 : slope * kLog2e;
     const float capA = kSoftcap ? p.softcap * kLog2e : 0.f;
+    // The common case (no score mod, positive scale, tile fully allowed) works on the
+    // raw scores x: max over x, then p = exp2(x * k1 - m) in one FFMA + ex2.
+    const bool raw_ok = !kAlibi && !kSoftcap && k1 > 0.f;
+    const int last_key = (p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1));
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0;
     for (int j = rng[t].lo; j < rng[t].hi; ++j, ++n) {
@@ -285,20 +289,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c) reg_fence32(r[c]);
       const int k0 = j * BN;
       const bool masked = tile_needs_mask(p.mask, q0 + t * BM, k0, BN);
-      const float base = kAlibi ? (float)(k0 - i) * kb : 0.f;
-      float mt = -INFINITY;
+      const bool fast = raw_ok && !masked;  // warp-uniform
+      // Row max in eight independent chains (the scores stay in r).
+      float mx[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+      if (fast) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = c * 32 + e;
-          float x = __uint_as_float(r[c][e]);
-          float s2 = kAlibi ? fmaf(x, k1, fmaf((float)col, kb, base)) : x * k1;
-          if (kSoftcap) s2 = capA - 2.0f * capA * rcp_approx(1.0f + ex2_approx(s2));
-          if (masked && !allowed(p.mask, i, k0 + col, fk)) s2 = -INFINITY;
-          mt = fmaxf(mt, s2);
-          r[c][e] = __float_as_uint(s2);
-        }
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(r[c][e]));
+      } else {
+        // Allowed columns of this row in this tile: [c_lo, c_hi].
+        const int c_lo = fk - k0, c_hi = last_key - k0;
+        const float base = kAlibi ? (float)(k0 - i) * kb : 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = c * 32 + e;
+            const float x = __uint_as_float(r[c][e]);
+            float s2 = kAlibi ? fmaf(x, k1, fmaf((float)col, kb, base)) : x * k1;
+            if (kSoftcap) s2 = capA - 2.0f * capA * rcp_approx(1.0f + ex2_approx(s2));
+            if (masked) s2 = (col >= c_lo && col <= c_hi) ? s2 : -INFINITY;
+            mx[e & 7] = fmaxf(mx[e & 7], s2);
+            r[c][e] = __float_as_uint(s2);
+          }
+      }
+      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      if (fast) mt *= k1;  // into log2 units
       const float m_new = fmaxf(m_run, mt);
       const bool grow = m_new > m_run + kRescaleLog2;
       const bool warp_grow = __any_sync(0xffffffffu, grow);
@@ -309,21 +329,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_new;
         l_run *= corr;
       }
-      const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      float lsum = 0.f;
+      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+      const float mul = fast ? k1 : 1.f;  // p = exp2(v * mul - m)
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(__uint_as_float(r[c][2 * e]) - m_use);
-          const float p1 = ex2_approx(__uint_as_float(r[c][2 * e + 1]) - m_use);
-          lsum += p0 + p1;
+          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), mul, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
+          acc[(2 * e) & 7] += p0;
+          acc[(2 * e + 1) & 7] += p1;
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + c * 16, pk);
       }
-      l_run += lsum;
+      l_run += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       if (warp_grow && n > 0) {  // O_t already holds P V of earlier tiles: rescale it
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
