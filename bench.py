@@ -99,6 +99,35 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# DRAM bytes (read + write) per launch from one ncu capture of each kernel on this
+# workload, with the SHA-256 of the kernel's source file at capture time. A kernel
+# whose source has changed since reports null.
+NCU_TRAFFIC = {}
+
+
+def ncu_traffic(kernel: str):
+    import hashlib
+    entry = NCU_TRAFFIC.get(kernel)
+    if not entry:
+        return None
+    path = os.path.join(ROOT, "exact_io_aware_13_gb300", "csrc", entry["source"])
+    try:
+        with open(path, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return entry["bytes"] if sha == entry["sha256"] else None
+
+
+def max_over_ranks(x: float, device) -> float:
+    """Largest x over all ranks (the job's time is its slowest replica's)."""
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -154,7 +183,11 @@ def run_ours(args):
         raise RuntimeError("a kernel gave up a bounded wait during warm-up")
 
     # ------------------------------------------------------------ device-timed steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # Per step: attn_fwd, then the backward's three kernels through attn_bwd_phases
+    # (the same launches attn_bwd makes), with an event between kernels so that each
+    # kernel's own duration is measured on the stream it runs on.
+    names = ["fwd_tc_kernel", "rowdot_kernel", "dkdv_kernel", "dq_kernel"]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -164,19 +197,18 @@ def run_ours(args):
             ev[s][0].record(stream)
             ea.fwd_into(qd, kd, vd, o, lse, **kw)
             ev[s][1].record(stream)
-            ea.bwd_into(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, **kw)
-            ev[s][2].record(stream)
+            for k_, ph in enumerate((ea.BWD_ROWDOT, ea.BWD_DKDV, ea.BWD_DQ)):
+                ea.bwd_phases_into(ph, qd, kd, vd, o, lse, dod, dq, dk, dv, ws, **kw)
+                ev[s][2 + k_].record(stream)
         torch.cuda.synchronize()
     if ea.device_status() != 0:
         raise RuntimeError("a kernel gave up a bounded wait during the timed steps")
-    t_fwd = [e[0].elapsed_time(e[1]) for e in ev]
-    t_bwd = [e[1].elapsed_time(e[2]) for e in ev]
+    per_kernel = {n: [e[i].elapsed_time(e[i + 1]) for e in ev] for i, n in enumerate(names)}
+    t_fwd = per_kernel["fwd_tc_kernel"]
+    t_bwd = [sum(per_kernel[n][s] for n in names[1:]) for s in range(args.steps)]
     t_step = sum(a + b for a, b in zip(t_fwd, t_bwd))  # ms over K steps
     if world > 1:
-        tt = torch.tensor([t_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_step = float(tt.item())
-        torch.distributed.barrier()
+        t_step = max_over_ranks(t_step, dev)
     ms_step = t_step / args.steps
     value = world * f_step / (ms_step * 1e-3) / 1e12
 
@@ -207,6 +239,22 @@ def run_ours(args):
     ms_bwd = statistics.mean(t_bwd)
     fwd_tf = f_fwd / (ms_fwd * 1e-3) / 1e12
     bwd_tf = f_bwd / (ms_bwd * 1e-3) / 1e12
+    # Algorithmic work of one launch of each kernel: FLOPs of the
+    # contractions it performs per allowed pair, or bytes for the row-dot kernel.
+    units = w.B * w.Hq * pairs
+    algo = {"fwd_tc_kernel": (4 * w.d * units, "TFLOP/s"),
+            "dkdv_kernel": (8 * w.d * units, "TFLOP/s"),
+            "dq_kernel": (6 * w.d * units, "TFLOP/s"),
+            "rowdot_kernel": (w.B * w.Hq * w.Nq * (4 * w.d + 4), "GB/s")}
+    kernels = {}
+    for n in names:
+        ms = statistics.mean(per_kernel[n])
+        work, unit = algo[n]
+        ach = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+        peak = pk["bf16_tflops"] if unit == "TFLOP/s" else pk["hbm_gbs"]
+        kernels[n] = {"ms": round(ms, 4), "achieved": round(ach, 2), "unit": unit,
+                      "frac": round(ach / peak, 4)}
+    dom = max(names, key=lambda n: kernels[n]["ms"])
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -218,10 +266,14 @@ def run_ours(args):
                 "pct_of_peak": round(100 * fwd_tf / pk["bf16_tflops"], 1)},
         "bwd": {"tflops": round(bwd_tf, 2), "ms": round(ms_bwd, 4),
                 "pct_of_peak": round(100 * bwd_tf / pk["bf16_tflops"], 1)},
-        "roofline": {"bound": "tensor", "kernel": "fwd_tc_kernel (attn_fwd)",
-                     "achieved": round(fwd_tf, 2), "peak": pk["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": round(fwd_tf / pk["bf16_tflops"], 4),
-                     "peak_source": pk["source"] + " bf16 burst", "traffic": None},
+        "kernels": kernels,
+        "roofline": {"bound": "tensor" if algo[dom][1] == "TFLOP/s" else "hbm", "kernel": dom,
+                     "achieved": kernels[dom]["achieved"],
+                     "peak": pk["bf16_tflops"] if algo[dom][1] == "TFLOP/s" else pk["hbm_gbs"],
+                     "unit": algo[dom][1], "frac": kernels[dom]["frac"],
+                     "peak_source": pk["source"] + (" bf16 burst" if algo[dom][1] == "TFLOP/s"
+                                                    else " HBM copy"),
+                     "traffic": ncu_traffic(dom)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
         "gpu_launches": 4 * args.steps,

@@ -45,6 +45,7 @@ SIGNATURES = {
     "attn_bwd": (_I, _BWD_ARGS),
     "attn_bwd_simt": (_I, _BWD_ARGS),
     "attn_bwd_static_workspace": (_I, _BWD_ARGS[:20] + [_P]),
+    "attn_bwd_phases": (_I, [_I] + _BWD_ARGS),
     "attn_classify_tiles": (_I, [_I, _MP, _I, _I, _P, _P]),
     "attn_device_status": (_I, [_P]),
     "attn_strerror": (ctypes.c_char_p, [_I]),

@@ -15,6 +15,7 @@ from . import _lib
 MASK_NONE, MASK_CAUSAL, MASK_SLIDING_WINDOW, MASK_DOCUMENT_CAUSAL = 0, 1, 2, 3
 SCORE_NONE, SCORE_ALIBI, SCORE_SOFTCAP = 0, 1, 2
 TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
+BWD_ROWDOT, BWD_DKDV, BWD_DQ, BWD_ALL = 1, 2, 4, 7
 TILE = 128
 
 
@@ -108,6 +109,24 @@ def bwd_into(q, k, v, o, lse, dout, dq, dk, dv, workspace, *, scale: float,
             score_kind, sp, _ptr(workspace), ctypes.c_size_t(ws_bytes), _stream(stream))
     del keep
     _lib.check(st, fn.__name__)
+
+
+def bwd_phases_into(phases: int, q, k, v, o, lse, dout, dq, dk, dv, workspace, *, scale: float,
+                    mask_kind: int = MASK_NONE, window: int = 0, doc_offsets=None,
+                    score_kind: int = SCORE_NONE, softcap: float = 0.0, stream=None) -> None:
+    """Run some of the backward's kernels (BWD_ROWDOT | BWD_DKDV | BWD_DQ) via
+    attn_bwd_phases; BWD_ROWDOT must have run on the same workspace first."""
+    _check_tensors(q, k, v, o, lse, dout, dq, dk, dv, workspace, doc_offsets)
+    lib = _lib.load()
+    B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
+    mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.attn_bwd_phases(int(phases), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                             _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nkv, d,
+                             ctypes.c_float(scale), mask_kind, mp, score_kind, sp,
+                             _ptr(workspace), ctypes.c_size_t(ws_bytes), _stream(stream))
+    del keep
+    _lib.check(st, "attn_bwd_phases")
 
 
 def backward(q, k, v, o, lse, dout, *, scale: Optional[float] = None,

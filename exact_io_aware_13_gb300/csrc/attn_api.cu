@@ -159,7 +159,9 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                        int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int mask_kind,
                        const attn_mask_params* mp, int score_kind, const attn_score_params* sp,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+                       void* workspace, size_t workspace_bytes, void* stream,
+                       int phases = ATTN_BWD_ALL) {
+  if (phases & ~ATTN_BWD_ALL) return ATTN_ERR_ARG;
   Problem p;
   attn_status s = check_problem(B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind, mp, score_kind, sp, &p);
   if (s != ATTN_OK) return s;
@@ -180,11 +182,13 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
   // With no queries nothing reaches the keys, and with no keys nothing reaches the
   // queries: those gradients are zero.
   if (rows_q == 0 || rows_k == 0) {
-    if (rows_q > 0 && cudaMemsetAsync(dq, 0, (size_t)rows_q * d * 2, st) != cudaSuccess)
+    const bool zq = rows_q > 0 && (phases & ATTN_BWD_DQ);
+    const bool zk = rows_k > 0 && (phases & ATTN_BWD_DKDV);
+    if (zq && cudaMemsetAsync(dq, 0, (size_t)rows_q * d * 2, st) != cudaSuccess)
       return ATTN_ERR_LAUNCH;
-    if (rows_k > 0 && cudaMemsetAsync(dk, 0, (size_t)rows_k * d * 2, st) != cudaSuccess)
+    if (zk && cudaMemsetAsync(dk, 0, (size_t)rows_k * d * 2, st) != cudaSuccess)
       return ATTN_ERR_LAUNCH;
-    if (rows_k > 0 && cudaMemsetAsync(dv, 0, (size_t)rows_k * d * 2, st) != cudaSuccess)
+    if (zk && cudaMemsetAsync(dv, 0, (size_t)rows_k * d * 2, st) != cudaSuccess)
       return ATTN_ERR_LAUNCH;
     return ATTN_OK;
   }
@@ -196,16 +200,25 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
   auto* dqb = static_cast<__nv_bfloat16*>(dq);
   auto* dkb = static_cast<__nv_bfloat16*>(dk);
   auto* dvb = static_cast<__nv_bfloat16*>(dv);
-  if ((s = from_cuda(launch_bwd_rowdot(p, static_cast<const __nv_bfloat16*>(o), dob, delta,
+  CUtensorMap tq, tk, tv, tdo;  // built before the first launch: errors launch nothing
+  if (!simt && (phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ))) {
+    if ((s = make_map(&tq, q, B * Hq, Nq, d)) != ATTN_OK) return s;
+    if ((s = make_map(&tk, k, B * Hkv, Nkv, d)) != ATTN_OK) return s;
+    if ((s = make_map(&tv, v, B * Hkv, Nkv, d)) != ATTN_OK) return s;
+    if ((s = make_map(&tdo, dout, B * Hq, Nq, d)) != ATTN_OK) return s;
+  }
+  if ((phases & ATTN_BWD_ROWDOT) &&
+      (s = from_cuda(launch_bwd_rowdot(p, static_cast<const __nv_bfloat16*>(o), dob, delta,
                                        st))) != ATTN_OK)
     return s;
-  if (simt) return from_cuda(launch_bwd_simt(p, qb, kb, vb, lse, dob, delta, dqb, dkb, dvb, st));
-  CUtensorMap tq, tk, tv, tdo;
-  if ((s = make_map(&tq, q, B * Hq, Nq, d)) != ATTN_OK) return s;
-  if ((s = make_map(&tk, k, B * Hkv, Nkv, d)) != ATTN_OK) return s;
-  if ((s = make_map(&tv, v, B * Hkv, Nkv, d)) != ATTN_OK) return s;
-  if ((s = make_map(&tdo, dout, B * Hq, Nq, d)) != ATTN_OK) return s;
-  return from_cuda(launch_bwd_tc(p, tq, tk, tv, tdo, lse, delta, dqb, dkb, dvb, st));
+  if (simt) {
+    if ((phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ)) != (ATTN_BWD_DKDV | ATTN_BWD_DQ))
+      return phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ) ? ATTN_ERR_ARG : ATTN_OK;
+    return from_cuda(launch_bwd_simt(p, qb, kb, vb, lse, dob, delta, dqb, dkb, dvb, st));
+  }
+  if (!(phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ))) return ATTN_OK;
+  return from_cuda(launch_bwd_tc(p, tq, tk, tv, tdo, lse, delta, dqb, dkb, dvb,
+                                 (phases & ATTN_BWD_DKDV) != 0, (phases & ATTN_BWD_DQ) != 0, st));
 }
 
 // ---------------------------------------------------------------- static workspace
@@ -283,6 +296,17 @@ attn_status attn_bwd_simt(const void* q, const void* k, const void* v, const voi
   return bwd_common(true, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale,
                     mask_kind, mask_params, score_kind, score_params, workspace,
                     workspace_bytes, stream);
+}
+
+attn_status attn_bwd_phases(int phases, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dout, void* dq,
+                            void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                            float scale, int mask_kind, const attn_mask_params* mask_params,
+                            int score_kind, const attn_score_params* score_params,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_common(false, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale,
+                    mask_kind, mask_params, score_kind, score_params, workspace,
+                    workspace_bytes, stream, phases);
 }
 
 attn_status attn_bwd_static_workspace(const void* q, const void* k, const void* v,

@@ -8,15 +8,17 @@
 //     dK = scale dS^T Q,   dQ = scale dS K.
 // Two kernels, both deterministic (fixed summation order, no atomics):
 //   * dkdv: one CTA per (batch, kv head, 128-key tile); it walks the query heads of
-//     its group and the query tiles the mask leaves, computing S^T = K Q^T and
-//     dP^T = V dO^T into tensor memory, P^T and dS^T (bf16) back into tensor
-//     memory, and accumulating dV += P^T dO and dK += dS^T Q in tensor memory;
-//   * dq: one CTA per (batch, query head, 128-row tile); it walks the key tiles,
-//     computing S = Q K^T and dP = dO V^T, dS into tensor memory, and
-//     accumulating dQ += dS K.
-// Warps 0-7 do the element-wise work (warpgroup 0 the first 64 columns of a tile,
-// warpgroup 1 the last 64; one thread per TMEM lane = row), warp 8 streams tiles
-// with TMA, warp 9 owns tensor memory and issues the MMAs.
+//     its group and the query tiles the mask leaves, 64 query rows at a time
+//     ("sub-steps"): S^T = K Q^T and dP^T = V dO^T into tensor memory, P^T and dS^T
+//     (bf16) back into tensor memory, then dV += P^T dO and dK += dS^T Q;
+//   * dq: one CTA per (batch, query head, 128-row tile); it walks the key tiles 64
+//     keys at a time: S = Q K^T and dP = dO V^T, dS back into tensor memory, then
+//     dQ += dS K.
+// S and dP are double-buffered in tensor memory (two 64-column buffers each), so
+// the MMAs of the next sub-step run while the element-wise warps work on this one.
+// Warps 0-7 do the element-wise work (warpgroup w takes columns [32w, 32w+32) of a
+// sub-step; one thread per TMEM lane = row), warp 8 streams tiles with TMA, warp 9
+// owns tensor memory and issues the MMAs.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -24,12 +26,18 @@ namespace attn {
 namespace {
 
 constexpr int BT = 128;          // tile side (rows, keys)
+constexpr int SUB = 64;          // columns per sub-step
 constexpr int kThreads = 320;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kStages = 2;       // ring depth for the streamed operand pairs
 constexpr int kHeadGroup = 4;
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Tensor memory columns: S buffers, dP buffers (64 each), then the accumulators.
+__device__ __forceinline__ uint32_t col_s(int x) { return x * 64; }
+__device__ __forceinline__ uint32_t col_dp(int x) { return 128 + x * 64; }
+constexpr uint32_t kColAcc = 256;
 
 // Element-wise constants: s2 = x*k1 + kb*(j - i) (log2 units), then the soft-cap.
 struct ScoreK {
@@ -53,8 +61,8 @@ __device__ __forceinline__ ScoreK score_consts(const Problem& p, int h) {
   return s;
 }
 
-// P and dS of one element. pre = x*k1 + ALiBi term (log2 units, or 2 log2e/c units
-// under the soft-cap); lse2 = L * log2e (+inf for a row with no key).
+// P and dS of one element from the pre-cap score in log2 units (or in 2 log2e / c
+// units under the soft-cap); lse2 = L * log2e (+inf for a row with no key).
 template <bool kSoftcap>
 __device__ __forceinline__ void p_and_ds(float pre, float lse2, float dp, float delta,
                                          float capA, bool ok, float& pr, float& ds) {
@@ -80,7 +88,6 @@ struct KVLayout {  // dkdv kernel shared memory
   static constexpr int kRowStage = 3 * BT * 4;
   static constexpr int kBars = kRows + kStages * kRowStage;
   static constexpr int kAlloc = kBars + 256 + 1024;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 };
 
 template <int D>
@@ -93,15 +100,14 @@ struct QLayout {  // dq kernel shared memory
   static constexpr int kStage = 2 * kTile;
   static constexpr int kBars = kRing + kStages * kStage;
   static constexpr int kAlloc = kBars + 256 + 1024;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
 };
 
 struct BwdBars {
   uint64_t fixed_full;             // the tiles loaded once (K,V or Q,dO)
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t s_full;                 // S and dP in TMEM
-  uint64_t p_full;                 // P / dS written back to TMEM
+  uint64_t s_full[2];              // S_x and dP_x in TMEM
+  uint64_t p_full[2];              // P_x / dS_x written back to TMEM
   uint64_t acc_full;               // accumulators final
   uint32_t tmem_base;
   int abort_flag;
@@ -137,18 +143,20 @@ __device__ __forceinline__ void setup_common(BwdBars* bars, uint32_t stage_full_
     mbar_init(smem_u32(&bars->full[s]), stage_full_count);
     mbar_init(smem_u32(&bars->empty[s]), stage_empty_count);
   }
-  mbar_init(smem_u32(&bars->s_full), 1);
-  mbar_init(smem_u32(&bars->p_full), 8);  // one arrival per element-wise warp
+  for (int x = 0; x < 2; ++x) {
+    mbar_init(smem_u32(&bars->s_full[x]), 1);
+    mbar_init(smem_u32(&bars->p_full[x]), 8);  // one arrival per element-wise warp
+  }
   mbar_init(smem_u32(&bars->acc_full), 1);
   bars->abort_flag = 0;
   fence_barrier_init();
 }
 
-// Issue the SS MMA D = A B^T over the head dimension (both operands K-major tiles
-// of BT rows x D written by TMA with 128-byte swizzle).
+// D[128 x 64] = A B^T over the head dimension: A a K-major tile of 128 rows, B the
+// 64 rows starting at `b` of a K-major tile (both written by TMA, 128-byte swizzle).
 template <int D>
-__device__ __forceinline__ void mma_rows_x_rows(uint32_t d_tmem, uint32_t a, uint32_t b) {
-  constexpr uint32_t id = idesc_bf16_f32(BT, BT, false, false);
+__device__ __forceinline__ void mma_128x64(uint32_t d_tmem, uint32_t a, uint32_t b) {
+  constexpr uint32_t id = idesc_bf16_f32(BT, SUB, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk >> 2) * (BT * 128) + (kk & 3) * 32;
@@ -157,15 +165,16 @@ __device__ __forceinline__ void mma_rows_x_rows(uint32_t d_tmem, uint32_t a, uin
   }
 }
 
-// D (+)= A_tmem B where A (BT lanes x BT bf16, split as two 64-column halves stored at
-// TMEM columns [0,32) and [64,96) of a_tmem) and B a BT x D tile used MN-major.
+// D[128 x D] (+)= A_tmem[128 x 64] B[64 x D]: A = bf16 pairs in TMEM, written by the
+// two element-wise warpgroups at columns [0,16) and [32,48) of a_tmem; B = the 64
+// rows starting at `b` of a tile used MN-major.
 template <int D>
-__device__ __forceinline__ void mma_tmem_x_tile(uint32_t d_tmem, uint32_t a_tmem, uint32_t b,
-                                                bool accumulate) {
+__device__ __forceinline__ void mma_tmem64_x_tile(uint32_t d_tmem, uint32_t a_tmem, uint32_t b,
+                                                  bool accumulate) {
   constexpr uint32_t id = idesc_bf16_f32(BT, D, false, true);
 #pragma unroll
-  for (int kk = 0; kk < BT / 16; ++kk) {
-    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+  for (int kk = 0; kk < SUB / 16; ++kk) {
+    const uint32_t acol = (kk < 2) ? kk * 8 : 32 + (kk - 2) * 8;
     mma_ts(d_tmem, a_tmem + acol, smem_desc_sw128(b + kk * 16 * 128, BT * 128, 1024), id,
            (accumulate || kk > 0) ? 1u : 0u);
   }
@@ -225,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const TileRange qr = q_tiles_for_keys(p.mask, k0, BT);
   const int n_q = imax(qr.hi - qr.lo, 0);
   const int steps = n_q * G;  // (head, query tile) pairs, head-major
+  const int subs = 2 * steps; // 64-row sub-steps
   if (steps == 0) {  // no query sees these keys: zero gradients
     for (int r = threadIdx.x; r < BT; r += kThreads) {
       const int j = k0 + r;
@@ -246,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
+  const uint32_t colDV = kColAcc, colDK = kColAcc + D;
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ loader
@@ -287,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < BT / 32; ++e) {
         const int r = e * 32 + lane, i = q0 + r;
         float lv = INFINITY, dv = 0.f;
-        int f = 0;
+        int f = 0x7fffffff;  // rows past Nq see no key
         if (i < p.Nq) {
           const float l = a.lse[(size_t)bh * p.Nq + i];
           lv = l == -INFINITY ? INFINITY : l * kLog2e;
@@ -310,95 +321,121 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
       bool ok = mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
-      for (int st = 0; ok && st < steps; ++st) {
-        const int s = st % kStages;
-        if (!mbar_wait(smem_u32(&bars->full[s]), (st / kStages) & 1, wc)) break;
-        tc_fence_after_sync();
-        const uint32_t sQ = smem_u32(smem + L::kRing + s * L::kStage);
+      // S^T and dP^T of sub-step u into buffer u & 1 (query rows 64*(u&1) of step u/2).
+      auto issue_sdp = [&](int u) -> bool {
+        const int st = u >> 1, s = st % kStages, x = u & 1;
+        if (x == 0) {
+          if (!mbar_wait(smem_u32(&bars->full[s]), (st / kStages) & 1, wc)) return false;
+          tc_fence_after_sync();
+        }
+        const uint32_t sQ = smem_u32(smem + L::kRing + s * L::kStage) + x * SUB * 128;
         const uint32_t sDO = sQ + L::kTile;
-        mma_rows_x_rows<D>(tmem + L::kColS, sK, sQ);    // S^T = K Q^T
-        mma_rows_x_rows<D>(tmem + L::kColDP, sV, sDO);  // dP^T = V dO^T
-        mma_commit(smem_u32(&bars->s_full));
-        if (!mbar_wait(smem_u32(&bars->p_full), st & 1, wc)) break;
+        mma_128x64<D>(tmem + col_s(x), sK, sQ);    // S^T = K Q^T
+        mma_128x64<D>(tmem + col_dp(x), sV, sDO);  // dP^T = V dO^T
+        mma_commit(smem_u32(&bars->s_full[x]));
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      if (ok && subs > 1) ok = issue_sdp(1);
+      for (int u = 0; ok && u < subs; ++u) {
+        const int st = u >> 1, s = st % kStages, x = u & 1;
+        if (!mbar_wait(smem_u32(&bars->p_full[x]), (u >> 1) & 1, wc)) break;
         tc_fence_after_sync();
-        mma_tmem_x_tile<D>(tmem + L::kColDV, tmem + L::kColS, sDO, st > 0);   // dV += P^T dO
-        mma_tmem_x_tile<D>(tmem + L::kColDK, tmem + L::kColDP, sQ, st > 0);   // dK += dS^T Q
-        mma_commit(smem_u32(&bars->empty[s]));
+        const uint32_t sQ = smem_u32(smem + L::kRing + s * L::kStage) + x * SUB * 128;
+        const uint32_t sDO = sQ + L::kTile;
+        mma_tmem64_x_tile<D>(tmem + colDV, tmem + col_s(x), sDO, u > 0);   // dV += P^T dO
+        mma_tmem64_x_tile<D>(tmem + colDK, tmem + col_dp(x), sQ, u > 0);   // dK += dS^T Q
+        if (x == 1) mma_commit(smem_u32(&bars->empty[s]));  // step fully consumed
+        if (u + 2 < subs) ok = issue_sdp(u + 2);
       }
       mma_commit(smem_u32(&bars->acc_full));
     }
   } else {
     // ------------------------------------------------------------ element-wise
-    const int wg = warp >> 2;                  // column half
+    const int wg = warp >> 2;                  // which 32 columns of a sub-step
     const int row = (warp & 3) * 32 + lane;    // key row in the tile
     const int j = k0 + row;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int c0 = wg * 64;
-    const uint32_t tS = tmem + lane_base + L::kColS + c0;
-    const uint32_t tDP = tmem + lane_base + L::kColDP + c0;
+    const int c0 = wg * 32;
+    const bool causal_type = p.mask.kind != ATTN_MASK_NONE;
     int done = 0;
-    for (int st = 0; st < steps; ++st, ++done) {
-      const int s = st % kStages;
+    for (int u = 0; u < subs; ++u, ++done) {
+      const int st = u >> 1, s = st % kStages, x = u & 1;
       const int h = g * G + st / n_q;
       const int q0 = (qr.lo + st % n_q) * BT;
+      const int qs = q0 + x * SUB + c0;          // query of this thread's column 0
       const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), st & 1, wc))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc)))
+        break;
+      // the row data were written before full[s] completed; observe them
+      if (x == 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (st / kStages) & 1, wc)))
+        break;
       tc_fence_after_sync();
-      const float* lse2 = reinterpret_cast<const float*>(smem + L::kRows + s * L::kRowStage);
+      const int roff = x * SUB + c0;
+      const float* lse2 = reinterpret_cast<const float*>(smem + L::kRows + s * L::kRowStage) + roff;
       const float* dl = lse2 + BT;
       const int* fk = reinterpret_cast<const int*>(dl + BT);
-      // the row data were written by the loader before it arrived on full[s], and the
-      // MMA warp waited on full[s] before S could complete; wait on it here as well so
-      // that this thread observes those writes.
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (st / kStages) & 1, wc)))
-        break;
-      uint32_t sr[2][32], dr[2][32];
-      tmem_ld32(tS, sr[0]);
-      tmem_ld32(tS + 32, sr[1]);
-      tmem_ld32(tDP, dr[0]);
-      tmem_ld32(tDP + 32, dr[1]);
+      const uint32_t tS = tmem + lane_base + col_s(x) + c0;
+      const uint32_t tDP = tmem + lane_base + col_dp(x) + c0;
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tS, sr);
+      tmem_ld32(tDP, dr);
       tmem_wait_ld();
-      reg_fence32(sr[0]); reg_fence32(sr[1]); reg_fence32(dr[0]); reg_fence32(dr[1]);
+      reg_fence32(sr);
+      reg_fence32(dr);
       const bool masked = tile_needs_mask(p.mask, q0, k0, BT);
-      const float base = kAlibi ? sk.kb * (float)(j - q0 - c0) : 0.f;  // kb*(j - i) at col 0
+      const float base = kAlibi ? sk.kb * (float)(j - qs) : 0.f;  // kb*(j - i) at column 0
+      uint32_t pp[16], dd[16];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t pp[16], dd[16];
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 lv = reinterpret_cast<const float4*>(lse2)[e4];
+        const float4 dv = reinterpret_cast<const float4*>(dl)[e4];
+        const float lvs[4] = {lv.x, lv.y, lv.z, lv.w};
+        const float dvs[4] = {dv.x, dv.y, dv.z, dv.w};
+        float pv[4], dsv[4];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = hh * 32 + 2 * e + u;      // column within this half
-            const int ci = c0 + col;                  // query index within the tile
-            const int i = q0 + ci;
-            const float x = __uint_as_float(sr[hh][2 * e + u]);
-            const float pre = kAlibi ? fmaf(x, sk.k1, fmaf(-(float)col, sk.kb, base)) : x * sk.k1;
-            const bool ok = !masked || (i < p.Nq && allowed(p.mask, i, j, fk[ci]));
-            p_and_ds<kSoftcap>(pre, lse2[ci], __uint_as_float(dr[hh][2 * e + u]), dl[ci],
-                               sk.capA, ok, pv[u], dsv[u]);
+        for (int q = 0; q < 4; ++q) {
+          const int col = e4 * 4 + q;
+          const float xs = __uint_as_float(sr[col]);
+          bool ok = true;
+          if (masked) {
+            const int i = qs + col;
+            ok = j < p.Nkv && (!causal_type || (i >= j && fk[col] <= j));
           }
-          pp[e] = pack_bf16x2(pv[0], pv[1]);
-          dd[e] = pack_bf16x2(dsv[0], dsv[1]);
+          if (!kAlibi && !kSoftcap) {
+            const float pr = ok ? ex2_approx(fmaf(xs, sk.k1, -lvs[q])) : 0.f;
+            pv[q] = pr;
+            dsv[q] = pr * (__uint_as_float(dr[col]) - dvs[q]);
+          } else {
+            const float pre =
+                kAlibi ? fmaf(xs, sk.k1, fmaf(-(float)col, sk.kb, base)) : xs * sk.k1;
+            p_and_ds<kSoftcap>(pre, lvs[q], __uint_as_float(dr[col]), dvs[q], sk.capA, ok,
+                               pv[q], dsv[q]);
+          }
         }
-        tmem_st16(tS + hh * 16, pp);   // P^T, bf16, columns [c0/2 ... )
-        tmem_st16(tDP + hh * 16, dd);  // dS^T
+        pp[2 * e4] = pack_bf16x2(pv[0], pv[1]);
+        pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
+        dd[2 * e4] = pack_bf16x2(dsv[0], dsv[1]);
+        dd[2 * e4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
       }
+      tmem_st16(tS, pp);   // P^T, bf16 pairs, in this warpgroup's first 16 columns
+      tmem_st16(tDP, dd);  // dS^T
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&bars->p_full));
-        mbar_arrive(smem_u32(&bars->empty[s]));  // done with this stage's row data
+        mbar_arrive(smem_u32(&bars->p_full[x]));
+        if (x == 1) mbar_arrive(smem_u32(&bars->empty[s]));  // done with the row data
       }
     }
     // ---------------------------------------------------------- epilogue
-    bool have = done == steps;
+    bool have = done == subs;
     have = __all_sync(0xffffffffu, have && mbar_wait(smem_u32(&bars->acc_full), 0, wc));
     tc_fence_after_sync();
     const size_t krow = (size_t)bg * p.Nkv + (j < p.Nkv ? j : 0);
     // warpgroup 0 writes dV, warpgroup 1 writes dK (times the softmax scale)
-    const uint32_t tacc = tmem + lane_base + (wg == 0 ? L::kColDV : L::kColDK);
+    const uint32_t tacc = tmem + lane_base + (wg == 0 ? colDV : colDK);
     __nv_bfloat16* dst = (wg == 0 ? a.dv : a.dk) + krow * D;
     store_acc_row<D>(tacc, wg == 0 ? 1.f : p.scale, dst, have, j < p.Nkv);
   }
@@ -432,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = qt * BT;
   const TileRange kr = kv_tiles_for_rows(p.mask, q0, BT);
   const int n_k = imax(kr.hi - kr.lo, 0);
+  const int subs = 2 * n_k;
 
   if (n_k == 0) {
     for (int r = threadIdx.x; r < BT; r += kThreads) {
@@ -486,19 +524,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
       bool ok = mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
-      for (int st = 0; ok && st < n_k; ++st) {
-        const int s = st % kStages;
-        if (!mbar_wait(smem_u32(&bars->full[s]), (st / kStages) & 1, wc)) break;
-        tc_fence_after_sync();
-        const uint32_t sK = smem_u32(smem + L::kRing + s * L::kStage);
+      // S and dP of sub-step u into buffer u & 1 (keys 64*(u&1) of key tile u/2).
+      auto issue_sdp = [&](int u) -> bool {
+        const int st = u >> 1, s = st % kStages, x = u & 1;
+        if (x == 0) {
+          if (!mbar_wait(smem_u32(&bars->full[s]), (st / kStages) & 1, wc)) return false;
+          tc_fence_after_sync();
+        }
+        const uint32_t sK = smem_u32(smem + L::kRing + s * L::kStage) + x * SUB * 128;
         const uint32_t sV = sK + L::kTile;
-        mma_rows_x_rows<D>(tmem + L::kColS, sQ, sK);     // S = Q K^T
-        mma_rows_x_rows<D>(tmem + L::kColDP, sDO, sV);   // dP = dO V^T
-        mma_commit(smem_u32(&bars->s_full));
-        if (!mbar_wait(smem_u32(&bars->p_full), st & 1, wc)) break;
+        mma_128x64<D>(tmem + col_s(x), sQ, sK);     // S = Q K^T
+        mma_128x64<D>(tmem + col_dp(x), sDO, sV);   // dP = dO V^T
+        mma_commit(smem_u32(&bars->s_full[x]));
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      if (ok && subs > 1) ok = issue_sdp(1);
+      for (int u = 0; ok && u < subs; ++u) {
+        const int st = u >> 1, s = st % kStages, x = u & 1;
+        if (!mbar_wait(smem_u32(&bars->p_full[x]), (u >> 1) & 1, wc)) break;
         tc_fence_after_sync();
-        mma_tmem_x_tile<D>(tmem + L::kColDQ, tmem + L::kColS, sK, st > 0);  // dQ += dS K
-        mma_commit(smem_u32(&bars->empty[s]));
+        const uint32_t sK = smem_u32(smem + L::kRing + s * L::kStage) + x * SUB * 128;
+        mma_tmem64_x_tile<D>(tmem + kColAcc, tmem + col_s(x), sK, u > 0);  // dQ += dS K
+        if (x == 1) mma_commit(smem_u32(&bars->empty[s]));  // key tile fully consumed
+        if (u + 2 < subs) ok = issue_sdp(u + 2);
       }
       mma_commit(smem_u32(&bars->acc_full));
     }
@@ -508,9 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = q0 + row;
     const bool row_ok = i < p.Nq;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int c0 = wg * 64;
-    const uint32_t tS = tmem + lane_base + L::kColS + c0;
-    const uint32_t tDP = tmem + lane_base + L::kColDP + c0;
+    const int c0 = wg * 32;
     const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
     float lse2 = INFINITY, dlt = 0.f;
     int fk = 0;
@@ -520,50 +567,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       dlt = a.delta[(size_t)bh * p.Nq + i];
       fk = first_key(p.mask, i);
     }
+    const int last_key = (p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1));
+    const float nlse2 = -lse2;
     int done = 0;
-    for (int st = 0; st < n_k; ++st, ++done) {
-      const int k0 = (kr.lo + st) * BT;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), st & 1, wc))) break;
+    for (int u = 0; u < subs; ++u, ++done) {
+      const int st = u >> 1, x = u & 1;
+      const int kt0 = (kr.lo + st) * BT;
+      const int ks = kt0 + x * SUB + c0;  // key of this thread's column 0
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc)))
+        break;
       tc_fence_after_sync();
-      uint32_t sr[2][32], dr[2][32];
-      tmem_ld32(tS, sr[0]);
-      tmem_ld32(tS + 32, sr[1]);
-      tmem_ld32(tDP, dr[0]);
-      tmem_ld32(tDP + 32, dr[1]);
+      const uint32_t tS = tmem + lane_base + col_s(x) + c0;
+      const uint32_t tDP = tmem + lane_base + col_dp(x) + c0;
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tS, sr);
+      tmem_ld32(tDP, dr);
       tmem_wait_ld();
-      reg_fence32(sr[0]); reg_fence32(sr[1]); reg_fence32(dr[0]); reg_fence32(dr[1]);
-      const bool masked = tile_needs_mask(p.mask, q0, k0, BT);
-      const float base = kAlibi ? sk.kb * (float)(k0 + c0 - i) : 0.f;  // kb*(j - i) at col 0
+      reg_fence32(sr);
+      reg_fence32(dr);
+      const bool masked = tile_needs_mask(p.mask, q0, kt0, BT);
+      const int c_lo = fk - ks, c_hi = last_key - ks;  // allowed columns of this row
+      const float base = kAlibi ? sk.kb * (float)(ks - i) : 0.f;  // kb*(j - i) at column 0
+      uint32_t dd[16];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t dd[16];
+      for (int e = 0; e < 16; ++e) {
+        float dsv[2];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = hh * 32 + 2 * e + u;
-            const int jj = k0 + c0 + col;
-            const float x = __uint_as_float(sr[hh][2 * e + u]);
-            const float pre = kAlibi ? fmaf(x, sk.k1, fmaf((float)col, sk.kb, base)) : x * sk.k1;
-            const bool ok = !masked || allowed(p.mask, i, jj, fk);
-            p_and_ds<kSoftcap>(pre, lse2, __uint_as_float(dr[hh][2 * e + u]), dlt, sk.capA, ok,
-                               pv[u], dsv[u]);
+        for (int q = 0; q < 2; ++q) {
+          const int col = 2 * e + q;
+          const float xs = __uint_as_float(sr[col]);
+          const bool ok = !masked || (col >= c_lo && col <= c_hi);
+          if (!kAlibi && !kSoftcap) {
+            const float pr = ok ? ex2_approx(fmaf(xs, sk.k1, nlse2)) : 0.f;
+            dsv[q] = pr * (__uint_as_float(dr[col]) - dlt);
+          } else {
+            const float pre =
+                kAlibi ? fmaf(xs, sk.k1, fmaf((float)col, sk.kb, base)) : xs * sk.k1;
+            float pr;
+            p_and_ds<kSoftcap>(pre, lse2, __uint_as_float(dr[col]), dlt, sk.capA, ok, pr,
+                               dsv[q]);
           }
-          dd[e] = pack_bf16x2(dsv[0], dsv[1]);
         }
-        tmem_st16(tS + hh * 16, dd);  // dS, bf16
+        dd[e] = pack_bf16x2(dsv[0], dsv[1]);
       }
+      tmem_st16(tS, dd);  // dS, bf16 pairs
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[x]));
     }
-    bool have = done == n_k;
+    bool have = done == subs;
     have = __all_sync(0xffffffffu, have && mbar_wait(smem_u32(&bars->acc_full), 0, wc));
     tc_fence_after_sync();
     // warpgroup 0 writes dQ columns [0, D/2), warpgroup 1 columns [D/2, D)
-    const uint32_t tq = tmem + lane_base + L::kColDQ + wg * (D / 2);
+    const uint32_t tq = tmem + lane_base + kColAcc + wg * (D / 2);
     __nv_bfloat16* dst = a.dq + ((size_t)bh * p.Nq + (row_ok ? i : 0)) * D + wg * (D / 2);
     store_acc_row<D / 2>(tq, p.scale, dst, have, row_ok);
   }
@@ -609,11 +666,11 @@ cudaError_t launch_d(const BwdArgs& ka, const BwdArgs& qa, const CUtensorMap& tq
 cudaError_t launch_bwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const float* lse,
                           const float* delta, __nv_bfloat16* dq, __nv_bfloat16* dk,
-                          __nv_bfloat16* dv, cudaStream_t st) {
+                          __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st) {
   BwdArgs ka{p, lse, delta, dq, dk, dv, ceil_div(p.Nkv, BT)};
   BwdArgs qa{p, lse, delta, dq, dk, dv, ceil_div(p.Nq, BT)};
-  const long long gk = (long long)ka.n_tiles * p.B * p.Hkv;
-  const long long gq = (long long)qa.n_tiles * p.B * p.Hq;
+  const long long gk = run_dkdv ? (long long)ka.n_tiles * p.B * p.Hkv : 0;
+  const long long gq = run_dq ? (long long)qa.n_tiles * p.B * p.Hq : 0;
   if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (p.d == 64) return launch_d<64>(ka, qa, tq, tk, tv, tdo, (int)gk, (int)gq, st);
   return launch_d<128>(ka, qa, tq, tk, tv, tdo, (int)gk, (int)gq, st);

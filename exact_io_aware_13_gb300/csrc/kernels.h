@@ -49,6 +49,6 @@ cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtenso
 cudaError_t launch_bwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const float* lse,
                           const float* delta, __nv_bfloat16* dq, __nv_bfloat16* dk,
-                          __nv_bfloat16* dv, cudaStream_t st);
+                          __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st);
 
 }  // namespace attn

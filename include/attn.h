@@ -130,6 +130,29 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      int score_kind, const attn_score_params* score_params,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Kernels of the backward pass, for attn_bwd_phases. */
+enum {
+  ATTN_BWD_ROWDOT = 1,   /* D = rowsum(dO o O) into the workspace */
+  ATTN_BWD_DKDV = 2,     /* dK and dV (reads D) */
+  ATTN_BWD_DQ = 4,       /* dQ (reads D) */
+  ATTN_BWD_ALL = 7
+};
+
+/*
+ * attn_bwd split into its kernels: runs the ones named in `phases`, in the order
+ * ROWDOT, DKDV, DQ, with attn_bwd's arguments and checks. DKDV and DQ read D from
+ * the workspace, so ROWDOT must have run on the same workspace and inputs before
+ * them (in this call or an earlier one in stream order). DKDV and DQ do not depend
+ * on each other: a caller may time them separately or put them on two streams.
+ * attn_bwd(...) is attn_bwd_phases(ATTN_BWD_ALL, ...).
+ */
+attn_status attn_bwd_phases(int phases, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dout, void* dq,
+                            void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                            float scale, int mask_kind, const attn_mask_params* mask_params,
+                            int score_kind, const attn_score_params* score_params,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Backward pass that allocates nothing and takes no workspace argument.
  *

@@ -34,3 +34,21 @@ def test_forward_and_backward_are_bitwise_repeatable(mask, score):
         for a, b in zip(runs[0], r):
             assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
                                b.view(torch.uint8) if b.dtype == torch.bfloat16 else b)
+
+
+def test_backward_phases_equal_attn_bwd():
+    """attn_bwd_phases run kernel by kernel gives the same bits as attn_bwd."""
+    import exact_io_aware_13_gb300 as ea
+    w = H.small_workload("phases", MASK_CAUSAL, B=1, Hq=4, Hkv=2, N=640, d=128)
+    q, k, v, do, offs = make_inputs(w, with_dout=True)
+    qd, kd, vd, dod = H.to_dev(q, k, v, do)
+    kw = H.mask_kwargs(w, offs)
+    o, lse = ea.forward(qd, kd, vd, scale=w.scale, **kw)
+    ref = ea.backward(qd, kd, vd, o, lse, dod, scale=w.scale, **kw)
+    got = [torch.empty_like(t) for t in ref]
+    ws = torch.empty(ea.bwd_workspace_size(qd, kd), dtype=torch.uint8, device="cuda")
+    for ph in (ea.BWD_ROWDOT, ea.BWD_DQ, ea.BWD_DKDV):  # dq before dkdv: independent
+        ea.bwd_phases_into(ph, qd, kd, vd, o, lse, dod, *got, ws, scale=w.scale, **kw)
+    torch.cuda.synchronize()
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
