@@ -100,23 +100,35 @@ class ClockSampler:
 
 
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel on this
-# workload, with the SHA-256 of the kernel's source file at capture time. A kernel
-# whose source has changed since reports null.
-NCU_TRAFFIC = {}
+# workload, keyed by the SHA-256 of the kernel's sources (its .cu file plus the shared
+# headers) at capture time. A kernel whose sources have changed since reports null.
+KERNEL_SOURCES = {"fwd_tc_kernel": "fwd_tc.cu", "dkdv_kernel": "bwd_tc.cu",
+                  "dq_kernel": "bwd_tc.cu", "rowdot_kernel": "simt.cu"}
+SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
+NCU_TRAFFIC = {
+    "fwd_tc_kernel": {"bytes": 248563712,
+                      "sha256": "8dedac898de439b4b2a60de199fce6479434e8e2a47816336bf850578578c62c"},
+}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_io_aware_13_gb300", "csrc")
+    for name in (KERNEL_SOURCES[kernel],) + SHARED_HEADERS:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def ncu_traffic(kernel: str):
-    import hashlib
     entry = NCU_TRAFFIC.get(kernel)
     if not entry:
         return None
-    path = os.path.join(ROOT, "exact_io_aware_13_gb300", "csrc", entry["source"])
     try:
-        with open(path, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        return entry["bytes"] if kernel_source_sha(kernel) == entry["sha256"] else None
     except OSError:
         return None
-    return entry["bytes"] if sha == entry["sha256"] else None
 
 
 def max_over_ranks(x: float, device) -> float:

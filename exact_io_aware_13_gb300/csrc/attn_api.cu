@@ -110,11 +110,12 @@ attn_status check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float 
 }
 
 // 3-D tensor map over a [BH, N, d] bf16 tensor: boxes of 64 elements (128 bytes,
-// the 128-byte swizzle span) x 128 rows x 1 head. Rows past N read as zeros.
-attn_status make_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+// the 128-byte swizzle span) x box_rows rows x 1 head. Rows past N read as zeros.
+attn_status make_map(CUtensorMap* map, const void* base, int BH, int N, int d,
+                     unsigned box_rows = 128) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -200,12 +201,17 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
   auto* dqb = static_cast<__nv_bfloat16*>(dq);
   auto* dkb = static_cast<__nv_bfloat16*>(dk);
   auto* dvb = static_cast<__nv_bfloat16*>(dv);
-  CUtensorMap tq, tk, tv, tdo;  // built before the first launch: errors launch nothing
+  BwdMaps maps;  // built before the first launch: errors launch nothing
   if (!simt && (phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ))) {
-    if ((s = make_map(&tq, q, B * Hq, Nq, d)) != ATTN_OK) return s;
-    if ((s = make_map(&tk, k, B * Hkv, Nkv, d)) != ATTN_OK) return s;
-    if ((s = make_map(&tv, v, B * Hkv, Nkv, d)) != ATTN_OK) return s;
-    if ((s = make_map(&tdo, dout, B * Hq, Nq, d)) != ATTN_OK) return s;
+    // 128-row boxes for the tiles a CTA loads once, 64-row boxes for the streamed ones
+    if ((s = make_map(&maps.q128, q, B * Hq, Nq, d)) != ATTN_OK) return s;
+    if ((s = make_map(&maps.do128, dout, B * Hq, Nq, d)) != ATTN_OK) return s;
+    if ((s = make_map(&maps.k128, k, B * Hkv, Nkv, d)) != ATTN_OK) return s;
+    if ((s = make_map(&maps.v128, v, B * Hkv, Nkv, d)) != ATTN_OK) return s;
+    if ((s = make_map(&maps.q64, q, B * Hq, Nq, d, 64)) != ATTN_OK) return s;
+    if ((s = make_map(&maps.do64, dout, B * Hq, Nq, d, 64)) != ATTN_OK) return s;
+    if ((s = make_map(&maps.k64, k, B * Hkv, Nkv, d, 64)) != ATTN_OK) return s;
+    if ((s = make_map(&maps.v64, v, B * Hkv, Nkv, d, 64)) != ATTN_OK) return s;
   }
   if ((phases & ATTN_BWD_ROWDOT) &&
       (s = from_cuda(launch_bwd_rowdot(p, static_cast<const __nv_bfloat16*>(o), dob, delta,
@@ -217,7 +223,7 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
     return from_cuda(launch_bwd_simt(p, qb, kb, vb, lse, dob, delta, dqb, dkb, dvb, st));
   }
   if (!(phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ))) return ATTN_OK;
-  return from_cuda(launch_bwd_tc(p, tq, tk, tv, tdo, lse, delta, dqb, dkb, dvb,
+  return from_cuda(launch_bwd_tc(p, maps, lse, delta, dqb, dkb, dvb,
                                  (phases & ATTN_BWD_DKDV) != 0, (phases & ATTN_BWD_DQ) != 0, st));
 }
 

@@ -8,16 +8,19 @@
 //     dK = scale dS^T Q,   dQ = scale dS K.
 // Two kernels, both deterministic (fixed summation order, no atomics):
 //   * dkdv: one CTA per (batch, kv head, 128-key tile); it walks the query heads of
-//     its group and the query tiles the mask leaves, 64 query rows at a time
-//     ("sub-steps"): S^T = K Q^T and dP^T = V dO^T into tensor memory, P^T and dS^T
-//     (bf16) back into tensor memory, then dV += P^T dO and dK += dS^T Q;
+//     its group and the query rows the mask leaves, 64 rows at a time ("sub-steps"):
+//     S^T = K Q^T and dP^T = V dO^T into tensor memory, P^T and dS^T (bf16) back
+//     into tensor memory, then dV += P^T dO and dK += dS^T Q;
 //   * dq: one CTA per (batch, query head, 128-row tile); it walks the key tiles 64
 //     keys at a time: S = Q K^T and dP = dO V^T, dS back into tensor memory, then
 //     dQ += dS K.
-// S and dP are double-buffered in tensor memory (two 64-column buffers each), so
-// the MMAs of the next sub-step run while the element-wise warps work on this one.
-// Warps 0-7 do the element-wise work (warpgroup w takes columns [32w, 32w+32) of a
-// sub-step; one thread per TMEM lane = row), warp 8 streams tiles with TMA, warp 9
+// Each sub-step streams its own 64-row slice of the two operands it walks (Q and dO,
+// or K and V) through a 4-deep shared-memory ring, so loads run three sub-steps
+// ahead. S and dP are double-buffered in tensor memory (two 64-column buffers each),
+// so the MMAs of one sub-step run while the element-wise warps work on another.
+// Warps 0-15 do the element-wise work in two pairs of warpgroups: pair p takes the
+// sub-steps u with u % 2 == p (buffer p); inside a pair, warpgroup w takes columns
+// [32w, 32w+32) (one thread per TMEM lane = row). Warp 16 loads with TMA, warp 17
 // owns tensor memory and issues the MMAs.
 #include "kernels.h"
 #include "ptx.cuh"
@@ -25,12 +28,13 @@
 namespace attn {
 namespace {
 
-constexpr int BT = 128;          // tile side (rows, keys)
-constexpr int SUB = 64;          // columns per sub-step
-constexpr int kThreads = 320;
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kStages = 2;       // ring depth for the streamed operand pairs
+constexpr int BT = 128;          // rows of the tile a CTA owns
+constexpr int SUB = 64;          // rows (columns of S) per sub-step
+constexpr int kEwWarps = 16;     // element-wise warps: two pairs of warpgroups
+constexpr int kThreads = (kEwWarps + 2) * 32;
+constexpr int kLoadWarp = kEwWarps;
+constexpr int kMmaWarp = kEwWarps + 1;
+constexpr int kStages = 4;       // ring depth, in sub-steps
 constexpr int kHeadGroup = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -76,34 +80,27 @@ __device__ __forceinline__ void p_and_ds(float pre, float lse2, float dp, float 
   ds = pr * (dp - delta) * dcap;
 }
 
+// Shared-memory layout shared by both kernels: two fixed 128-row tiles, then a ring
+// of kStages stages, each holding a 64-row slice of two operands (and, for dkdv, the
+// per-row data of those 64 query rows).
 template <int D>
-struct KVLayout {  // dkdv kernel shared memory
-  static constexpr int kChunk = BT * 128;
-  static constexpr int kTile = BT * D * 2;
-  static constexpr int kK = 0;
-  static constexpr int kV = kTile;
-  static constexpr int kRing = 2 * kTile;             // stages of {Q, dO}
-  static constexpr int kStage = 2 * kTile;
+struct Layout {
+  static constexpr int kFixChunk = BT * 128;        // 64-column slab of a fixed tile
+  static constexpr int kFixTile = BT * D * 2;
+  static constexpr int kSubChunk = SUB * 128;       // 64-column slab of a stage slice
+  static constexpr int kSubTile = SUB * D * 2;
+  static constexpr int kFixA = 0;
+  static constexpr int kFixB = kFixTile;
+  static constexpr int kRing = 2 * kFixTile;
+  static constexpr int kStage = 2 * kSubTile;
   static constexpr int kRows = kRing + kStages * kStage;  // per stage: lse2, delta, first key
-  static constexpr int kRowStage = 3 * BT * 4;
+  static constexpr int kRowStage = 3 * SUB * 4;
   static constexpr int kBars = kRows + kStages * kRowStage;
   static constexpr int kAlloc = kBars + 256 + 1024;
 };
 
-template <int D>
-struct QLayout {  // dq kernel shared memory
-  static constexpr int kChunk = BT * 128;
-  static constexpr int kTile = BT * D * 2;
-  static constexpr int kQ = 0;
-  static constexpr int kDO = kTile;
-  static constexpr int kRing = 2 * kTile;             // stages of {K, V}
-  static constexpr int kStage = 2 * kTile;
-  static constexpr int kBars = kRing + kStages * kStage;
-  static constexpr int kAlloc = kBars + 256 + 1024;
-};
-
 struct BwdBars {
-  uint64_t fixed_full;             // the tiles loaded once (K,V or Q,dO)
+  uint64_t fixed_full;             // the two fixed tiles
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t s_full[2];              // S_x and dP_x in TMEM
@@ -145,37 +142,40 @@ __device__ __forceinline__ void setup_common(BwdBars* bars, uint32_t stage_full_
   }
   for (int x = 0; x < 2; ++x) {
     mbar_init(smem_u32(&bars->s_full[x]), 1);
-    mbar_init(smem_u32(&bars->p_full[x]), 8);  // one arrival per element-wise warp
+    mbar_init(smem_u32(&bars->p_full[x]), 8);  // one arrival per warp of pair x
   }
   mbar_init(smem_u32(&bars->acc_full), 1);
   bars->abort_flag = 0;
   fence_barrier_init();
 }
 
-// D[128 x 64] = A B^T over the head dimension: A a K-major tile of 128 rows, B the
-// 64 rows starting at `b` of a K-major tile (both written by TMA, 128-byte swizzle).
+// D[128 x 64] = A B^T over the head dimension: A = a fixed 128-row K-major tile, B =
+// a 64-row K-major stage slice (both written by TMA with 128-byte swizzle). The
+// descriptors are built once; each K step adds its byte offset (in 16-byte units).
 template <int D>
 __device__ __forceinline__ void mma_128x64(uint32_t d_tmem, uint32_t a, uint32_t b) {
   constexpr uint32_t id = idesc_bf16_f32(BT, SUB, false, false);
+  const uint64_t da = smem_desc_sw128(a, 16, 1024), db = smem_desc_sw128(b, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * (BT * 128) + (kk & 3) * 32;
-    mma_ss(d_tmem, smem_desc_sw128(a + off, 16, 1024), smem_desc_sw128(b + off, 16, 1024), id,
-           kk > 0 ? 1u : 0u);
+    const uint32_t oa = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+    const uint32_t ob = ((kk >> 2) * (SUB * 128) + (kk & 3) * 32) >> 4;
+    mma_ss(d_tmem, da + oa, db + ob, id, kk > 0 ? 1u : 0u);
   }
 }
 
 // D[128 x D] (+)= A_tmem[128 x 64] B[64 x D]: A = bf16 pairs in TMEM, written by the
-// two element-wise warpgroups at columns [0,16) and [32,48) of a_tmem; B = the 64
-// rows starting at `b` of a tile used MN-major.
+// two element-wise warpgroups of a pair at columns [0,16) and [32,48) of a_tmem;
+// B = a 64-row stage slice used MN-major (its 64-column slabs 8 KB apart).
 template <int D>
-__device__ __forceinline__ void mma_tmem64_x_tile(uint32_t d_tmem, uint32_t a_tmem, uint32_t b,
-                                                  bool accumulate) {
+__device__ __forceinline__ void mma_tmem64_x_slice(uint32_t d_tmem, uint32_t a_tmem, uint32_t b,
+                                                   bool accumulate) {
   constexpr uint32_t id = idesc_bf16_f32(BT, D, false, true);
+  const uint64_t db = smem_desc_sw128(b, SUB * 128, 1024);
 #pragma unroll
   for (int kk = 0; kk < SUB / 16; ++kk) {
     const uint32_t acol = (kk < 2) ? kk * 8 : 32 + (kk - 2) * 8;
-    mma_ts(d_tmem, a_tmem + acol, smem_desc_sw128(b + kk * 16 * 128, BT * 128, 1024), id,
+    mma_ts(d_tmem, a_tmem + acol, db + ((kk * 16 * 128) >> 4), id,
            (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -212,13 +212,61 @@ __device__ __forceinline__ void store_acc_row(uint32_t t, float mul, __nv_bfloat
   }
 }
 
+// Loads the two fixed tiles (rows r0.. of head z) and then, for every sub-step u,
+// the 64-row slices of the two streamed operands into stage u % kStages. `slice`
+// gives (row, head) of sub-step u. `rows` (dkdv only) fills the stage's row data.
+template <int D, typename SliceFn, typename RowsFn>
+__device__ __forceinline__ void load_loop(uint8_t* smem, BwdBars* bars, const WaitCtx& wc,
+                                          int lane, const CUtensorMap* fa, const CUtensorMap* fb,
+                                          int r0, int z, const CUtensorMap* sa,
+                                          const CUtensorMap* sb, int subs, SliceFn slice,
+                                          RowsFn rows, bool with_rows) {
+  using L = Layout<D>;
+  if (lane == 0) {
+    tma_prefetch_desc(sa);
+    tma_prefetch_desc(sb);
+    const uint32_t bar = smem_u32(&bars->fixed_full);
+    mbar_arrive_expect_tx(bar, 2 * L::kFixTile);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      tma_load_3d(smem_u32(smem + L::kFixA + c * L::kFixChunk), fa, bar, c * 64, r0, z);
+      tma_load_3d(smem_u32(smem + L::kFixB + c * L::kFixChunk), fb, bar, c * 64, r0, z);
+    }
+  }
+  for (int u = 0; u < subs; ++u) {
+    const int s = u % kStages, use = u / kStages;
+    int row, head;
+    slice(u, row, head);
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(smem_u32(&bars->empty[s]), (use & 1) ^ 1, wc);
+    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    const uint32_t full = smem_u32(&bars->full[s]);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(full, L::kStage);
+      uint8_t* stg = smem + L::kRing + s * L::kStage;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(smem_u32(stg + c * L::kSubChunk), sa, full, c * 64, row, head);
+        tma_load_3d(smem_u32(stg + L::kSubTile + c * L::kSubChunk), sb, full, c * 64, row, head);
+      }
+    }
+    if (with_rows) {
+      rows(u, reinterpret_cast<float*>(smem + L::kRows + s * L::kRowStage), row, head);
+      mbar_arrive(full);
+    }
+  }
+  if (lane == 0) {  // let in-flight copies land before the CTA can exit
+    mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
+    for (int u = imax(0, subs - kStages); u < subs; ++u)
+      mbar_wait(smem_u32(&bars->full[u % kStages]), (u / kStages) & 1, wc);
+  }
+}
+
 // ============================================================================ dK, dV
 template <int D, bool kAlibi, bool kSoftcap>
 __global__ void __launch_bounds__(kThreads, 1)
-    dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const BwdArgs a) {
-  using L = KVLayout<D>;
+    dkdv_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
+  using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -233,9 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int k0 = kt * BT;
   const TileRange qr = q_tiles_for_keys(p.mask, k0, BT);
   const int n_q = imax(qr.hi - qr.lo, 0);
-  const int steps = n_q * G;  // (head, query tile) pairs, head-major
-  const int subs = 2 * steps; // 64-row sub-steps
-  if (steps == 0) {  // no query sees these keys: zero gradients
+  const int subs = 2 * n_q * G;  // (head, query tile, half) triples, head-major
+  if (subs == 0) {  // no query sees these keys: zero gradients
     for (int r = threadIdx.x; r < BT; r += kThreads) {
       const int j = k0 + r;
       if (j >= p.Nkv) continue;
@@ -245,6 +292,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return;
   }
+  // sub-step u: query head g*G + (u/2)/n_q, query rows q0 + 64*(u&1)
+  auto slice = [&](int u, int& row, int& head) {
+    const int st = u >> 1;
+    head = b * p.Hq + g * G + st / n_q;
+    row = (qr.lo + st % n_q) * BT + (u & 1) * SUB;
+  };
 
   WaitCtx wc{&bars->abort_flag, p.status};
   if (threadIdx.x == 0) setup_common(bars, 1 + 32, 1 + 8);
@@ -259,43 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t colDV = kColAcc, colDK = kColAcc + D;
 
   if (warp == kLoadWarp) {
-    // ------------------------------------------------------------ loader
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
-      const uint32_t fb = smem_u32(&bars->fixed_full);
-      mbar_arrive_expect_tx(fb, 2 * L::kTile);
+    // Row data of the 64 query rows of a sub-step: L * log2e (+inf for a row with no
+    // key, so that exp2(s - lse2) = 0), D, and the row's first allowed key.
+    auto rows = [&](int, float* lse2, int q0, int bh) {
+      float* dl = lse2 + SUB;
+      int* fk = reinterpret_cast<int*>(dl + SUB);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem_u32(smem + L::kK + c * L::kChunk), &tm_k, fb, c * 64, k0, bg);
-        tma_load_3d(smem_u32(smem + L::kV + c * L::kChunk), &tm_v, fb, c * 64, k0, bg);
-      }
-    }
-    for (int st = 0; st < steps; ++st) {
-      const int s = st % kStages, use = st / kStages;
-      const int h = g * G + st / n_q;
-      const int q0 = (qr.lo + st % n_q) * BT;
-      const int bh = b * p.Hq + h;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(smem_u32(&bars->empty[s]), (use & 1) ^ 1, wc);
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      const uint32_t full = smem_u32(&bars->full[s]);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full, 2 * L::kTile);
-        uint8_t* stg = smem + L::kRing + s * L::kStage;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(smem_u32(stg + c * L::kChunk), &tm_q, full, c * 64, q0, bh);
-          tma_load_3d(smem_u32(stg + L::kTile + c * L::kChunk), &tm_do, full, c * 64, q0, bh);
-        }
-      }
-      // Row data of the 128 query rows: L * log2e (+inf for a row with no key, so
-      // that exp2(s - lse2) = 0), D, and the row's first allowed key.
-      float* lse2 = reinterpret_cast<float*>(smem + L::kRows + s * L::kRowStage);
-      float* dl = lse2 + BT;
-      int* fk = reinterpret_cast<int*>(dl + BT);
-#pragma unroll
-      for (int e = 0; e < BT / 32; ++e) {
+      for (int e = 0; e < SUB / 32; ++e) {
         const int r = e * 32 + lane, i = q0 + r;
         float lv = INFINITY, dv = 0.f;
         int f = 0x7fffffff;  // rows past Nq see no key
@@ -309,27 +332,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         dl[r] = dv;
         fk[r] = f;
       }
-      mbar_arrive(full);
-    }
-    if (lane == 0) {  // let in-flight copies land before the CTA can exit
-      mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
-      for (int st = imax(0, steps - kStages); st < steps; ++st)
-        mbar_wait(smem_u32(&bars->full[st % kStages]), (st / kStages) & 1, wc);
-    }
+    };
+    load_loop<D>(smem, bars, wc, lane, &maps.k128, &maps.v128, k0, bg, &maps.q64, &maps.do64,
+                 subs, slice, rows, true);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+      const uint32_t sK = smem_u32(smem + L::kFixA), sV = smem_u32(smem + L::kFixB);
+      const uint32_t ring = smem_u32(smem + L::kRing);
       bool ok = mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
-      // S^T and dP^T of sub-step u into buffer u & 1 (query rows 64*(u&1) of step u/2).
+      // S^T and dP^T of sub-step u into buffer u & 1
       auto issue_sdp = [&](int u) -> bool {
-        const int st = u >> 1, s = st % kStages, x = u & 1;
-        if (x == 0) {
-          if (!mbar_wait(smem_u32(&bars->full[s]), (st / kStages) & 1, wc)) return false;
-          tc_fence_after_sync();
-        }
-        const uint32_t sQ = smem_u32(smem + L::kRing + s * L::kStage) + x * SUB * 128;
-        const uint32_t sDO = sQ + L::kTile;
+        const int s = u % kStages, x = u & 1;
+        if (!mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc)) return false;
+        tc_fence_after_sync();
+        const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
         mma_128x64<D>(tmem + col_s(x), sK, sQ);    // S^T = K Q^T
         mma_128x64<D>(tmem + col_dp(x), sV, sDO);  // dP^T = V dO^T
         mma_commit(smem_u32(&bars->s_full[x]));
@@ -338,44 +355,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = issue_sdp(0);
       if (ok && subs > 1) ok = issue_sdp(1);
       for (int u = 0; ok && u < subs; ++u) {
-        const int st = u >> 1, s = st % kStages, x = u & 1;
+        const int s = u % kStages, x = u & 1;
         if (!mbar_wait(smem_u32(&bars->p_full[x]), (u >> 1) & 1, wc)) break;
         tc_fence_after_sync();
-        const uint32_t sQ = smem_u32(smem + L::kRing + s * L::kStage) + x * SUB * 128;
-        const uint32_t sDO = sQ + L::kTile;
-        mma_tmem64_x_tile<D>(tmem + colDV, tmem + col_s(x), sDO, u > 0);   // dV += P^T dO
-        mma_tmem64_x_tile<D>(tmem + colDK, tmem + col_dp(x), sQ, u > 0);   // dK += dS^T Q
-        if (x == 1) mma_commit(smem_u32(&bars->empty[s]));  // step fully consumed
+        const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
+        mma_tmem64_x_slice<D>(tmem + colDV, tmem + col_s(x), sDO, u > 0);   // dV += P^T dO
+        mma_tmem64_x_slice<D>(tmem + colDK, tmem + col_dp(x), sQ, u > 0);   // dK += dS^T Q
+        mma_commit(smem_u32(&bars->empty[s]));  // stage consumed once these complete
         if (u + 2 < subs) ok = issue_sdp(u + 2);
       }
       mma_commit(smem_u32(&bars->acc_full));
     }
   } else {
     // ------------------------------------------------------------ element-wise
-    const int wg = warp >> 2;                  // which 32 columns of a sub-step
+    const int pair = warp >> 3;                // sub-steps u with u % 2 == pair
+    const int wg = (warp >> 2) & 1;            // which 32 columns of a sub-step
     const int row = (warp & 3) * 32 + lane;    // key row in the tile
     const int j = k0 + row;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int c0 = wg * 32;
+    const int x = pair;                        // TMEM buffer of this pair
     const bool causal_type = p.mask.kind != ATTN_MASK_NONE;
-    int done = 0;
-    for (int u = 0; u < subs; ++u, ++done) {
-      const int st = u >> 1, s = st % kStages, x = u & 1;
-      const int h = g * G + st / n_q;
-      const int q0 = (qr.lo + st % n_q) * BT;
-      const int qs = q0 + x * SUB + c0;          // query of this thread's column 0
+    bool ok_all = true;
+    for (int u = pair; u < subs; u += 2) {
+      const int s = u % kStages;
+      int qrow, bh;
+      slice(u, qrow, bh);
+      const int h = bh - b * p.Hq;
+      const int qs = qrow + c0;                  // query of this thread's column 0
       const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc)))
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc))) {
+        ok_all = false;
         break;
+      }
       // the row data were written before full[s] completed; observe them
-      if (x == 0 &&
-          !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (st / kStages) & 1, wc)))
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc))) {
+        ok_all = false;
         break;
+      }
       tc_fence_after_sync();
-      const int roff = x * SUB + c0;
-      const float* lse2 = reinterpret_cast<const float*>(smem + L::kRows + s * L::kRowStage) + roff;
-      const float* dl = lse2 + BT;
-      const int* fk = reinterpret_cast<const int*>(dl + BT);
+      const float* lse2 = reinterpret_cast<const float*>(smem + L::kRows + s * L::kRowStage) + c0;
+      const float* dl = lse2 + SUB;
+      const int* fk = reinterpret_cast<const int*>(dl + SUB);
       const uint32_t tS = tmem + lane_base + col_s(x) + c0;
       const uint32_t tDP = tmem + lane_base + col_dp(x) + c0;
       uint32_t sr[32], dr[32];
@@ -384,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       reg_fence32(sr);
       reg_fence32(dr);
-      const bool masked = tile_needs_mask(p.mask, q0, k0, BT);
+      const bool masked = tile_needs_mask(p.mask, qrow & ~(BT - 1), k0, BT);
       const float base = kAlibi ? sk.kb * (float)(j - qs) : 0.f;  // kb*(j - i) at column 0
       uint32_t pp[16], dd[16];
 #pragma unroll
@@ -426,18 +447,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&bars->p_full[x]));
-        if (x == 1) mbar_arrive(smem_u32(&bars->empty[s]));  // done with the row data
+        mbar_arrive(smem_u32(&bars->empty[s]));  // done with the stage's row data
       }
     }
     // ---------------------------------------------------------- epilogue
-    bool have = done == subs;
-    have = __all_sync(0xffffffffu, have && mbar_wait(smem_u32(&bars->acc_full), 0, wc));
+    // pair 0 writes dV, pair 1 writes dK (times the softmax scale); warpgroup wg of
+    // the pair writes columns [wg * D/2, (wg + 1) * D/2)
+    const bool have =
+        __all_sync(0xffffffffu, ok_all && mbar_wait(smem_u32(&bars->acc_full), 0, wc));
     tc_fence_after_sync();
     const size_t krow = (size_t)bg * p.Nkv + (j < p.Nkv ? j : 0);
-    // warpgroup 0 writes dV, warpgroup 1 writes dK (times the softmax scale)
-    const uint32_t tacc = tmem + lane_base + (wg == 0 ? colDV : colDK);
-    __nv_bfloat16* dst = (wg == 0 ? a.dv : a.dk) + krow * D;
-    store_acc_row<D>(tacc, wg == 0 ? 1.f : p.scale, dst, have, j < p.Nkv);
+    const uint32_t tacc = tmem + lane_base + (pair == 0 ? colDV : colDK) + wg * (D / 2);
+    __nv_bfloat16* dst = (pair == 0 ? a.dv : a.dk) + krow * D + wg * (D / 2);
+    store_acc_row<D / 2>(tacc, pair == 0 ? 1.f : p.scale, dst, have, j < p.Nkv);
   }
   __syncwarp();
   tc_fence_before_sync();
@@ -451,10 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================================ dQ
 template <int D, bool kAlibi, bool kSoftcap>
 __global__ void __launch_bounds__(kThreads, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const BwdArgs a) {
-  using L = QLayout<D>;
+    dq_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
+  using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -480,6 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return;
   }
+  auto slice = [&](int u, int& row, int& head) {  // keys of sub-step u
+    head = bg;
+    row = kr.lo * BT + u * SUB;
+  };
 
   WaitCtx wc{&bars->abort_flag, p.status};
   if (threadIdx.x == 0) setup_common(bars, 1, 1);
@@ -493,46 +517,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == kLoadWarp) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      const uint32_t fb = smem_u32(&bars->fixed_full);
-      mbar_arrive_expect_tx(fb, 2 * L::kTile);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem_u32(smem + L::kQ + c * L::kChunk), &tm_q, fb, c * 64, q0, bh);
-        tma_load_3d(smem_u32(smem + L::kDO + c * L::kChunk), &tm_do, fb, c * 64, q0, bh);
-      }
-      for (int st = 0; st < n_k; ++st) {
-        const int s = st % kStages, use = st / kStages;
-        if (!mbar_wait(smem_u32(&bars->empty[s]), (use & 1) ^ 1, wc)) break;
-        const uint32_t full = smem_u32(&bars->full[s]);
-        mbar_arrive_expect_tx(full, 2 * L::kTile);
-        uint8_t* stg = smem + L::kRing + s * L::kStage;
-        const int krow = (kr.lo + st) * BT;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(smem_u32(stg + c * L::kChunk), &tm_k, full, c * 64, krow, bg);
-          tma_load_3d(smem_u32(stg + L::kTile + c * L::kChunk), &tm_v, full, c * 64, krow, bg);
-        }
-      }
-      mbar_wait(fb, 0, wc);
-      for (int st = imax(0, n_k - kStages); st < n_k; ++st)
-        mbar_wait(smem_u32(&bars->full[st % kStages]), (st / kStages) & 1, wc);
-    }
+    auto no_rows = [](int, float*, int, int) {};
+    load_loop<D>(smem, bars, wc, lane, &maps.q128, &maps.do128, q0, bh, &maps.k64, &maps.v64,
+                 subs, slice, no_rows, false);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
+      const uint32_t sQ = smem_u32(smem + L::kFixA), sDO = smem_u32(smem + L::kFixB);
+      const uint32_t ring = smem_u32(smem + L::kRing);
       bool ok = mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
-      // S and dP of sub-step u into buffer u & 1 (keys 64*(u&1) of key tile u/2).
+      // S and dP of sub-step u into buffer u & 1
       auto issue_sdp = [&](int u) -> bool {
-        const int st = u >> 1, s = st % kStages, x = u & 1;
-        if (x == 0) {
-          if (!mbar_wait(smem_u32(&bars->full[s]), (st / kStages) & 1, wc)) return false;
-          tc_fence_after_sync();
-        }
-        const uint32_t sK = smem_u32(smem + L::kRing + s * L::kStage) + x * SUB * 128;
-        const uint32_t sV = sK + L::kTile;
+        const int s = u % kStages, x = u & 1;
+        if (!mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc)) return false;
+        tc_fence_after_sync();
+        const uint32_t sK = ring + s * L::kStage, sV = sK + L::kSubTile;
         mma_128x64<D>(tmem + col_s(x), sQ, sK);     // S = Q K^T
         mma_128x64<D>(tmem + col_dp(x), sDO, sV);   // dP = dO V^T
         mma_commit(smem_u32(&bars->s_full[x]));
@@ -541,23 +539,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = issue_sdp(0);
       if (ok && subs > 1) ok = issue_sdp(1);
       for (int u = 0; ok && u < subs; ++u) {
-        const int st = u >> 1, s = st % kStages, x = u & 1;
+        const int s = u % kStages, x = u & 1;
         if (!mbar_wait(smem_u32(&bars->p_full[x]), (u >> 1) & 1, wc)) break;
         tc_fence_after_sync();
-        const uint32_t sK = smem_u32(smem + L::kRing + s * L::kStage) + x * SUB * 128;
-        mma_tmem64_x_tile<D>(tmem + kColAcc, tmem + col_s(x), sK, u > 0);  // dQ += dS K
-        if (x == 1) mma_commit(smem_u32(&bars->empty[s]));  // key tile fully consumed
+        const uint32_t sK = ring + s * L::kStage;
+        mma_tmem64_x_slice<D>(tmem + kColAcc, tmem + col_s(x), sK, u > 0);  // dQ += dS K
+        mma_commit(smem_u32(&bars->empty[s]));  // stage consumed once this completes
         if (u + 2 < subs) ok = issue_sdp(u + 2);
       }
       mma_commit(smem_u32(&bars->acc_full));
     }
   } else {
-    const int wg = warp >> 2;
+    const int pair = warp >> 3;                // sub-steps u with u % 2 == pair
+    const int wg = (warp >> 2) & 1;            // which 32 key columns of a sub-step
     const int row = (warp & 3) * 32 + lane;
     const int i = q0 + row;
     const bool row_ok = i < p.Nq;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int c0 = wg * 32;
+    const int x = pair;
     const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
     float lse2 = INFINITY, dlt = 0.f;
     int fk = 0;
@@ -569,13 +569,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int last_key = (p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1));
     const float nlse2 = -lse2;
-    int done = 0;
-    for (int u = 0; u < subs; ++u, ++done) {
-      const int st = u >> 1, x = u & 1;
-      const int kt0 = (kr.lo + st) * BT;
-      const int ks = kt0 + x * SUB + c0;  // key of this thread's column 0
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc)))
+    bool ok_all = true;
+    for (int u = pair; u < subs; u += 2) {
+      const int kt0 = (kr.lo + (u >> 1)) * BT;
+      const int ks = kr.lo * BT + u * SUB + c0;  // key of this thread's column 0
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc))) {
+        ok_all = false;
         break;
+      }
       tc_fence_after_sync();
       const uint32_t tS = tmem + lane_base + col_s(x) + c0;
       const uint32_t tDP = tmem + lane_base + col_dp(x) + c0;
@@ -616,13 +617,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[x]));
     }
-    bool have = done == subs;
-    have = __all_sync(0xffffffffu, have && mbar_wait(smem_u32(&bars->acc_full), 0, wc));
+    // pair 0 writes dQ: warpgroup wg writes columns [wg * D/2, (wg + 1) * D/2)
+    const bool have =
+        __all_sync(0xffffffffu, ok_all && mbar_wait(smem_u32(&bars->acc_full), 0, wc));
     tc_fence_after_sync();
-    // warpgroup 0 writes dQ columns [0, D/2), warpgroup 1 columns [D/2, D)
-    const uint32_t tq = tmem + lane_base + kColAcc + wg * (D / 2);
-    __nv_bfloat16* dst = a.dq + ((size_t)bh * p.Nq + (row_ok ? i : 0)) * D + wg * (D / 2);
-    store_acc_row<D / 2>(tq, p.scale, dst, have, row_ok);
+    if (pair == 0) {  // warp-uniform
+      const uint32_t tq = tmem + lane_base + kColAcc + wg * (D / 2);
+      __nv_bfloat16* dst = a.dq + ((size_t)bh * p.Nq + (row_ok ? i : 0)) * D + wg * (D / 2);
+      store_acc_row<D / 2>(tq, p.scale, dst, have, row_ok);
+    }
   }
   __syncwarp();
   tc_fence_before_sync();
@@ -634,37 +637,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool kA, bool kS>
-cudaError_t launch_variant(const BwdArgs& kv_args, const BwdArgs& q_args, const CUtensorMap& tq,
-                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+cudaError_t launch_variant(const BwdArgs& kv_args, const BwdArgs& q_args, const BwdMaps& maps,
                            int grid_kv, int grid_q, cudaStream_t st) {
   auto k1 = dkdv_kernel<D, kA, kS>;
   auto k2 = dq_kernel<D, kA, kS>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       KVLayout<D>::kAlloc);
+                                       Layout<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, QLayout<D>::kAlloc);
+  e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  if (grid_kv > 0) k1<<<grid_kv, kThreads, KVLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, kv_args);
+  if (grid_kv > 0) k1<<<grid_kv, kThreads, Layout<D>::kAlloc, st>>>(maps, kv_args);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (grid_q > 0) k2<<<grid_q, kThreads, QLayout<D>::kAlloc, st>>>(tq, tk, tv, tdo, q_args);
+  if (grid_q > 0) k2<<<grid_q, kThreads, Layout<D>::kAlloc, st>>>(maps, q_args);
   return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_d(const BwdArgs& ka, const BwdArgs& qa, const CUtensorMap& tq,
-                     const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                     int gk, int gq, cudaStream_t st) {
+cudaError_t launch_d(const BwdArgs& ka, const BwdArgs& qa, const BwdMaps& maps, int gk, int gq,
+                     cudaStream_t st) {
   const bool al = ka.p.score_kind & ATTN_SCORE_ALIBI, sc = ka.p.score_kind & ATTN_SCORE_SOFTCAP;
-  if (al && sc) return launch_variant<D, true, true>(ka, qa, tq, tk, tv, tdo, gk, gq, st);
-  if (al) return launch_variant<D, true, false>(ka, qa, tq, tk, tv, tdo, gk, gq, st);
-  if (sc) return launch_variant<D, false, true>(ka, qa, tq, tk, tv, tdo, gk, gq, st);
-  return launch_variant<D, false, false>(ka, qa, tq, tk, tv, tdo, gk, gq, st);
+  if (al && sc) return launch_variant<D, true, true>(ka, qa, maps, gk, gq, st);
+  if (al) return launch_variant<D, true, false>(ka, qa, maps, gk, gq, st);
+  if (sc) return launch_variant<D, false, true>(ka, qa, maps, gk, gq, st);
+  return launch_variant<D, false, false>(ka, qa, maps, gk, gq, st);
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const float* lse,
+cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const float* lse,
                           const float* delta, __nv_bfloat16* dq, __nv_bfloat16* dk,
                           __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st) {
   BwdArgs ka{p, lse, delta, dq, dk, dv, ceil_div(p.Nkv, BT)};
@@ -672,8 +672,8 @@ cudaError_t launch_bwd_tc(const Problem& p, const CUtensorMap& tq, const CUtenso
   const long long gk = run_dkdv ? (long long)ka.n_tiles * p.B * p.Hkv : 0;
   const long long gq = run_dq ? (long long)qa.n_tiles * p.B * p.Hq : 0;
   if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (p.d == 64) return launch_d<64>(ka, qa, tq, tk, tv, tdo, (int)gk, (int)gq, st);
-  return launch_d<128>(ka, qa, tq, tk, tv, tdo, (int)gk, (int)gq, st);
+  if (p.d == 64) return launch_d<64>(ka, qa, maps, (int)gk, (int)gq, st);
+  return launch_d<128>(ka, qa, maps, (int)gk, (int)gq, st);
 }
 
 }  // namespace attn
