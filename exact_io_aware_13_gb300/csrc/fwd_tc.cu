@@ -36,7 +36,13 @@ constexpr int kQTiles = 2;     // query tiles per CTA
 constexpr int kStages = 4;     // K/V shared-memory ring depth (each stage one tile)
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kRelayWarp = 10;  // turns TMA completions into named-barrier arrivals
+constexpr int kThreads = 352;
+// Named barriers (the MMA warp waits only on these; see nb_sync in ptx.cuh):
+//   kNbP + t      P_t written to TMEM: softmax warpgroup t (128) + MMA warp (32)
+//   kNbKv + s     ring stage s loaded: relay warp (32) + MMA warp (32)
+constexpr uint32_t kNbP = 1, kNbPCount = 160;
+constexpr uint32_t kNbKv = 3, kNbKvCount = 64;
 constexpr int kHeadGroup = 4;  // heads whose CTAs are scheduled together (L2 reuse)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
@@ -59,7 +65,6 @@ struct Bars {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[kQTiles];
-  uint64_t p_full[kQTiles];
   uint64_t o_full[kQTiles];
   uint32_t tmem_base;
   int abort_flag;
@@ -135,7 +140,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(smem_u32(&bars->s_full[t]), 1);
-      mbar_init(smem_u32(&bars->p_full[t]), BM);
       mbar_init(smem_u32(&bars->o_full[t]), 1);
     }
     bars->abort_flag = 0;
@@ -181,78 +185,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = imax(0, 2 * n_kv - kStages); u < 2 * n_kv; ++u)
         mbar_wait(smem_u32(&bars->kv_full[u % kStages]), (u / kStages) & 1, wc);
     }
+  } else if (warp == kRelayWarp) {
+    // ------------------------------------------------------------ relay
+    // Ring use u is stage u % kStages; after its TMA bytes land, arrive on that
+    // stage's named barrier for the MMA warp. After an abort, rendezvous instead.
+    bool live = true;
+    for (int u = 0; u < 2 * n_kv; ++u) {
+      const int s = u % kStages;
+      if (live)
+        live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->kv_full[s]), (u / kStages) & 1, wc));
+      if (live) nb_arrive(kNbKv + s, kNbKvCount);
+      else nb_sync(kNbKv + s, kNbKvCount);
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
-      const uint32_t colS[2] = {L::kColS0, L::kColS1};
-      const uint32_t colO[2] = {L::kColO0, L::kColO1};
-      const uint32_t q_base = smem_u32(smem + L::kQ);
-      const uint32_t ring = smem_u32(smem + L::kRing);
-      int np[kQTiles] = {0, 0};  // P tiles consumed per query tile
-      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, wc);
+    // The whole warp walks the schedule and waits on named barriers; lane 0 issues.
+    // After an abort the warp keeps every barrier operation and issues nothing.
+    constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
+    constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
+    const uint32_t q_base = smem_u32(smem + L::kQ);
+    const uint32_t ring = smem_u32(smem + L::kRing);
+    int np[kQTiles] = {0, 0};  // P tiles consumed per query tile
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->q_full), 0, wc));
+    const bool issuer = ok && lane == 0;
 
-      auto issue_s = [&](int t, int u) {  // S_t = Q_t K^T with K in ring use u
-        const uint32_t kb = ring + (u % kStages) * L::kTile;
-        const uint32_t qt = q_base + t * L::kTile;
+    auto sync_stage = [&](int u) {
+      nb_sync(kNbKv + u % kStages, kNbKvCount);
+      tc_fence_after_sync();
+    };
+    auto issue_s = [&](int t, int u) {  // S_t = Q_t K^T with K in ring use u
+      const uint32_t kb = ring + (u % kStages) * L::kTile;
+      const uint32_t qt = q_base + t * L::kTile;
+      const uint64_t dq = smem_desc_sw128(qt, 16, 1024), dk = smem_desc_sw128(kb, 16, 1024);
+      const uint32_t col = t == 0 ? L::kColS0 : L::kColS1;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunk + (kk & 3) * 32;
-          mma_ss(tmem + colS[t], smem_desc_sw128(qt + off, 16, 1024),
-                 smem_desc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+        mma_ss(tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&bars->s_full[t]));
+    };
+    auto issue_pv = [&](int t, int u) {  // O_t += P_t V with V in ring use u
+      const uint32_t vb = ring + (u % kStages) * L::kTile;
+      const uint64_t dv = smem_desc_sw128(vb, L::kChunk, 1024);
+      const uint32_t colS = t == 0 ? L::kColS0 : L::kColS1;
+      const uint32_t colO = t == 0 ? L::kColO0 : L::kColO1;
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)
+        mma_ts(tmem + colO, tmem + colS + kk * 8, dv + ((kk * 16 * 128) >> 4), idO,
+               (np[t] > 0 || kk > 0) ? 1u : 0u);
+    };
+
+    sync_stage(0);
+    if (issuer) {
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t)
+        if (lo >= rng[t].lo && lo < rng[t].hi) issue_s(t, 0);
+      mma_commit(smem_u32(&bars->kv_empty[0]));
+    }
+    __syncwarp();
+    for (int jj = 0; jj < n_kv; ++jj) {
+      const int j = lo + jj;
+      const int uv = 2 * jj + 1, uk = 2 * jj + 2;
+      const bool next = jj + 1 < n_kv;
+      sync_stage(uv);
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) {
+        if (j >= rng[t].lo && j < rng[t].hi) {
+          nb_sync(kNbP + t, kNbPCount);
+          tc_fence_after_sync();
+          if (issuer) issue_pv(t, uv);
+          __syncwarp();
+          ++np[t];
         }
-        mma_commit(smem_u32(&bars->s_full[t]));
-      };
-      auto issue_pv = [&](int t, int u) {  // O_t += P_t V with V in ring use u
-        const uint32_t vb = ring + (u % kStages) * L::kTile;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8,
-                 smem_desc_sw128(vb + kk * 16 * 128, L::kChunk, 1024), idO,
-                 (np[t] > 0 || kk > 0) ? 1u : 0u);
-      };
-
-      if (ok) {
-        ok = mbar_wait(smem_u32(&bars->kv_full[0]), 0, wc);
-        tc_fence_after_sync();
-        if (ok) {
-#pragma unroll
-          for (int t = 0; t < kQTiles; ++t)
-            if (lo >= rng[t].lo && lo < rng[t].hi) issue_s(t, 0);
-          mma_commit(smem_u32(&bars->kv_empty[0]));
+        if (next) {
+          if (t == 0) sync_stage(uk);
+          if (issuer && j + 1 >= rng[t].lo && j + 1 < rng[t].hi) issue_s(t, uk);
+          __syncwarp();
         }
       }
-      for (int jj = 0; ok && jj < n_kv; ++jj) {
-        const int j = lo + jj;
-        const int uv = 2 * jj + 1, uk = 2 * jj + 2;
-        const bool next = jj + 1 < n_kv;
-        if (!mbar_wait(smem_u32(&bars->kv_full[uv % kStages]), (uv / kStages) & 1, wc)) break;
-        bool k_ready = false;
-#pragma unroll
-        for (int t = 0; t < kQTiles; ++t) {
-          if (j >= rng[t].lo && j < rng[t].hi) {
-            if (!mbar_wait(smem_u32(&bars->p_full[t]), np[t] & 1, wc)) { ok = false; break; }
-            tc_fence_after_sync();
-            issue_pv(t, uv);
-            ++np[t];
-          }
-          if (next) {
-            if (!k_ready) {
-              if (!mbar_wait(smem_u32(&bars->kv_full[uk % kStages]), (uk / kStages) & 1, wc)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after_sync();
-              k_ready = true;
-            }
-            if (j + 1 >= rng[t].lo && j + 1 < rng[t].hi) issue_s(t, uk);
-          }
-        }
-        if (!ok) break;
+      if (issuer) {
         mma_commit(smem_u32(&bars->kv_empty[uv % kStages]));
         if (next) mma_commit(smem_u32(&bars->kv_empty[uk % kStages]));
       }
+      __syncwarp();
+    }
+    if (issuer) {
 #pragma unroll
       for (int t = 0; t < kQTiles; ++t) mma_commit(smem_u32(&bars->o_full[t]));
     }
@@ -277,9 +295,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int last_key = (p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1));
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0;
+    bool live = true;
     for (int j = rng[t].lo; j < rng[t].hi; ++j, ++n) {
       // Keep every decision warp-uniform: tcgen05.ld/st are warp-collective.
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[t]), n & 1, wc))) break;
+      if (live) live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[t]), n & 1, wc));
+      if (!live) {  // aborted: keep the barrier schedule with the MMA warp, do nothing else
+        nb_sync(kNbP + t, kNbPCount);
+        continue;
+      }
       tc_fence_after_sync();
       uint32_t r[4][32];
 #pragma unroll
@@ -362,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(smem_u32(&bars->p_full[t]));
+      nb_arrive(kNbP + t, kNbPCount);
     }
     // ---------------------------------------------------------- epilogue
     bool have_o = n > 0;  // O_t holds at least one P V product

@@ -90,6 +90,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// ---------------------------------------------------------------- named barriers
+// Hardware CTA barriers 1..15 (0 is __syncthreads). Waiting on one touches no shared
+// memory, so a thread that issues tcgen05.mma can wait on it without stalling the
+// tensor pipe (a shared-memory access from that thread costs about 480 cycles while
+// the pipe streams operands from shared memory). `count` is in threads, a multiple of
+// 32, and every warp that takes part executes the instruction converged.
+// Producers arrive (non-blocking); the consumer syncs. A producer may arrive again
+// only after the consumer has synced the previous phase; the kernels guarantee this
+// through their data dependencies, and after an abort they switch to nb_sync so that
+// every arrival pairs with one consumer sync.
+__device__ __forceinline__ void nb_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void nb_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
