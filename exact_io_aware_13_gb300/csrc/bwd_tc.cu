@@ -21,7 +21,9 @@
 // Warps 0-15 do the element-wise work in two pairs of warpgroups: pair p takes the
 // sub-steps u with u % 2 == p (buffer p); inside a pair, warpgroup w takes columns
 // [32w, 32w+32) (one thread per TMEM lane = row). Warp 16 loads with TMA, warp 17
-// owns tensor memory and issues the MMAs.
+// owns tensor memory and issues the MMAs, warp 18 relays TMA completions. The MMA warp
+// waits only on hardware named barriers: a shared-memory access from the thread that
+// issues MMAs stalls the tensor pipe (see nb_sync in ptx.cuh).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -31,9 +33,15 @@ namespace {
 constexpr int BT = 128;          // rows of the tile a CTA owns
 constexpr int SUB = 64;          // rows (columns of S) per sub-step
 constexpr int kEwWarps = 16;     // element-wise warps: two pairs of warpgroups
-constexpr int kThreads = (kEwWarps + 2) * 32;
+constexpr int kThreads = (kEwWarps + 3) * 32;
 constexpr int kLoadWarp = kEwWarps;
 constexpr int kMmaWarp = kEwWarps + 1;
+constexpr int kRelayWarp = kEwWarps + 2;  // turns TMA completions into barrier arrivals
+// Named barriers (the MMA warp waits only on these; see nb_sync in ptx.cuh):
+//   kNbP + x      P_x / dS_x written to TMEM: pair x (256 threads) + MMA warp (32)
+//   kNbStage + s  ring stage s loaded: relay warp (32) + MMA warp (32)
+constexpr uint32_t kNbP = 1, kNbPCount = 288;
+constexpr uint32_t kNbStage = 3, kNbStageCount = 64;
 constexpr int kStages = 4;       // ring depth, in sub-steps
 constexpr int kHeadGroup = 4;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -104,7 +112,6 @@ struct BwdBars {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t s_full[2];              // S_x and dP_x in TMEM
-  uint64_t p_full[2];              // P_x / dS_x written back to TMEM
   uint64_t acc_full;               // accumulators final
   uint32_t tmem_base;
   int abort_flag;
@@ -140,10 +147,7 @@ __device__ __forceinline__ void setup_common(BwdBars* bars, uint32_t stage_full_
     mbar_init(smem_u32(&bars->full[s]), stage_full_count);
     mbar_init(smem_u32(&bars->empty[s]), stage_empty_count);
   }
-  for (int x = 0; x < 2; ++x) {
-    mbar_init(smem_u32(&bars->s_full[x]), 1);
-    mbar_init(smem_u32(&bars->p_full[x]), 8);  // one arrival per warp of pair x
-  }
+  for (int x = 0; x < 2; ++x) mbar_init(smem_u32(&bars->s_full[x]), 1);
   mbar_init(smem_u32(&bars->acc_full), 1);
   bars->abort_flag = 0;
   fence_barrier_init();
@@ -153,14 +157,14 @@ __device__ __forceinline__ void setup_common(BwdBars* bars, uint32_t stage_full_
 // a 64-row K-major stage slice (both written by TMA with 128-byte swizzle). The
 // descriptors are built once; each K step adds its byte offset (in 16-byte units).
 template <int D>
-__device__ __forceinline__ void mma_128x64(uint32_t d_tmem, uint32_t a, uint32_t b) {
+__device__ __forceinline__ void mma_128x64(bool pred, uint32_t d_tmem, uint32_t a, uint32_t b) {
   constexpr uint32_t id = idesc_bf16_f32(BT, SUB, false, false);
   const uint64_t da = smem_desc_sw128(a, 16, 1024), db = smem_desc_sw128(b, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t oa = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
     const uint32_t ob = ((kk >> 2) * (SUB * 128) + (kk & 3) * 32) >> 4;
-    mma_ss(d_tmem, da + oa, db + ob, id, kk > 0 ? 1u : 0u);
+    mma_ss_if(pred, d_tmem, da + oa, db + ob, id, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -168,14 +172,14 @@ __device__ __forceinline__ void mma_128x64(uint32_t d_tmem, uint32_t a, uint32_t
 // two element-wise warpgroups of a pair at columns [0,16) and [32,48) of a_tmem;
 // B = a 64-row stage slice used MN-major (its 64-column slabs 8 KB apart).
 template <int D>
-__device__ __forceinline__ void mma_tmem64_x_slice(uint32_t d_tmem, uint32_t a_tmem, uint32_t b,
-                                                   bool accumulate) {
+__device__ __forceinline__ void mma_tmem64_x_slice(bool pred, uint32_t d_tmem, uint32_t a_tmem,
+                                                   uint32_t b, bool accumulate) {
   constexpr uint32_t id = idesc_bf16_f32(BT, D, false, true);
   const uint64_t db = smem_desc_sw128(b, SUB * 128, 1024);
 #pragma unroll
   for (int kk = 0; kk < SUB / 16; ++kk) {
     const uint32_t acol = (kk < 2) ? kk * 8 : 32 + (kk - 2) * 8;
-    mma_ts(d_tmem, a_tmem + acol, db + ((kk * 16 * 128) >> 4), id,
+    mma_ts_if(pred, d_tmem, a_tmem + acol, db + ((kk * 16 * 128) >> 4), id,
            (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -262,6 +266,19 @@ __device__ __forceinline__ void load_loop(uint8_t* smem, BwdBars* bars, const Wa
   }
 }
 
+// Relay warp: after the bytes of ring use u land (full[u % kStages]), arrive on that
+// stage's named barrier for the MMA warp; after an abort, rendezvous instead.
+__device__ __forceinline__ void relay_loop(BwdBars* bars, const WaitCtx& wc, int subs) {
+  bool live = true;
+  for (int u = 0; u < subs; ++u) {
+    const int s = u % kStages;
+    if (live)
+      live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc));
+    if (live) nb_arrive(kNbStage + s, kNbStageCount);
+    else nb_sync(kNbStage + s, kNbStageCount);
+  }
+}
+
 // ============================================================================ dK, dV
 template <int D, bool kAlibi, bool kSoftcap>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -335,37 +352,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     load_loop<D>(smem, bars, wc, lane, &maps.k128, &maps.v128, k0, bg, &maps.q64, &maps.do64,
                  subs, slice, rows, true);
+  } else if (warp == kRelayWarp) {
+    relay_loop(bars, wc, subs);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t sK = smem_u32(smem + L::kFixA), sV = smem_u32(smem + L::kFixB);
-      const uint32_t ring = smem_u32(smem + L::kRing);
-      bool ok = mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
-      // S^T and dP^T of sub-step u into buffer u & 1
-      auto issue_sdp = [&](int u) -> bool {
-        const int s = u % kStages, x = u & 1;
-        if (!mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc)) return false;
-        tc_fence_after_sync();
-        const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
-        mma_128x64<D>(tmem + col_s(x), sK, sQ);    // S^T = K Q^T
-        mma_128x64<D>(tmem + col_dp(x), sV, sDO);  // dP^T = V dO^T
-        mma_commit(smem_u32(&bars->s_full[x]));
-        return true;
-      };
-      if (ok) ok = issue_sdp(0);
-      if (ok && subs > 1) ok = issue_sdp(1);
-      for (int u = 0; ok && u < subs; ++u) {
-        const int s = u % kStages, x = u & 1;
-        if (!mbar_wait(smem_u32(&bars->p_full[x]), (u >> 1) & 1, wc)) break;
-        tc_fence_after_sync();
-        const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
-        mma_tmem64_x_slice<D>(tmem + colDV, tmem + col_s(x), sDO, u > 0);   // dV += P^T dO
-        mma_tmem64_x_slice<D>(tmem + colDK, tmem + col_dp(x), sQ, u > 0);   // dK += dS^T Q
-        mma_commit(smem_u32(&bars->empty[s]));  // stage consumed once these complete
-        if (u + 2 < subs) ok = issue_sdp(u + 2);
-      }
-      mma_commit(smem_u32(&bars->acc_full));
+    // The whole warp walks the schedule and waits on named barriers; every lane executes
+    // the MMA instructions predicated on `issuer` (lane 0), so the warp never diverges.
+    // After an abort the warp keeps every barrier operation and issues nothing.
+    const uint32_t sK = smem_u32(smem + L::kFixA), sV = smem_u32(smem + L::kFixB);
+    const uint32_t ring = smem_u32(smem + L::kRing);
+    const bool issuer =
+        __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc)) && lane == 0;
+    // S^T and dP^T of sub-step u into buffer u & 1
+    auto issue_sdp = [&](int u) {
+      const int s = u % kStages, x = u & 1;
+      nb_sync(kNbStage + s, kNbStageCount);
+      tc_fence_after_sync();
+      const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
+      mma_128x64<D>(issuer, tmem + col_s(x), sK, sQ);    // S^T = K Q^T
+      mma_128x64<D>(issuer, tmem + col_dp(x), sV, sDO);  // dP^T = V dO^T
+      mma_commit_if(issuer, smem_u32(&bars->s_full[x]));
+    };
+    issue_sdp(0);
+    if (subs > 1) issue_sdp(1);
+    for (int u = 0; u < subs; ++u) {
+      const int s = u % kStages, x = u & 1;
+      nb_sync(kNbP + x, kNbPCount);
+      tc_fence_after_sync();
+      const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
+      mma_tmem64_x_slice<D>(issuer, tmem + colDV, tmem + col_s(x), sDO, u > 0);  // dV += P^T dO
+      mma_tmem64_x_slice<D>(issuer, tmem + colDK, tmem + col_dp(x), sQ, u > 0);  // dK += dS^T Q
+      mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage consumed once these complete
+      if (u + 2 < subs) issue_sdp(u + 2);
     }
+    mma_commit_if(issuer, smem_u32(&bars->acc_full));
   } else {
     // ------------------------------------------------------------ element-wise
     const int pair = warp >> 3;                // sub-steps u with u % 2 == pair
@@ -384,14 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = bh - b * p.Hq;
       const int qs = qrow + c0;                  // query of this thread's column 0
       const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc))) {
-        ok_all = false;
-        break;
-      }
+      if (ok_all)
+        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc));
       // the row data were written before full[s] completed; observe them
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc))) {
-        ok_all = false;
-        break;
+      if (ok_all)
+        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc));
+      if (!ok_all) {  // aborted: keep the barrier schedule with the MMA warp
+        nb_sync(kNbP + x, kNbPCount);
+        continue;
       }
       tc_fence_after_sync();
       const float* lse2 = reinterpret_cast<const float*>(smem + L::kRows + s * L::kRowStage) + c0;
@@ -444,11 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st16(tDP, dd);  // dS^T
       tmem_wait_st();
       tc_fence_before_sync();
+      nb_arrive(kNbP + x, kNbPCount);
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&bars->p_full[x]));
-        mbar_arrive(smem_u32(&bars->empty[s]));  // done with the stage's row data
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&bars->empty[s]));  // done with the stage's row data
     }
     // ---------------------------------------------------------- epilogue
     // pair 0 writes dV, pair 1 writes dK (times the softmax scale); warpgroup wg of
@@ -520,35 +538,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto no_rows = [](int, float*, int, int) {};
     load_loop<D>(smem, bars, wc, lane, &maps.q128, &maps.do128, q0, bh, &maps.k64, &maps.v64,
                  subs, slice, no_rows, false);
+  } else if (warp == kRelayWarp) {
+    relay_loop(bars, wc, subs);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem + L::kFixA), sDO = smem_u32(smem + L::kFixB);
-      const uint32_t ring = smem_u32(smem + L::kRing);
-      bool ok = mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
-      // S and dP of sub-step u into buffer u & 1
-      auto issue_sdp = [&](int u) -> bool {
-        const int s = u % kStages, x = u & 1;
-        if (!mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc)) return false;
-        tc_fence_after_sync();
-        const uint32_t sK = ring + s * L::kStage, sV = sK + L::kSubTile;
-        mma_128x64<D>(tmem + col_s(x), sQ, sK);     // S = Q K^T
-        mma_128x64<D>(tmem + col_dp(x), sDO, sV);   // dP = dO V^T
-        mma_commit(smem_u32(&bars->s_full[x]));
-        return true;
-      };
-      if (ok) ok = issue_sdp(0);
-      if (ok && subs > 1) ok = issue_sdp(1);
-      for (int u = 0; ok && u < subs; ++u) {
-        const int s = u % kStages, x = u & 1;
-        if (!mbar_wait(smem_u32(&bars->p_full[x]), (u >> 1) & 1, wc)) break;
-        tc_fence_after_sync();
-        const uint32_t sK = ring + s * L::kStage;
-        mma_tmem64_x_slice<D>(tmem + kColAcc, tmem + col_s(x), sK, u > 0);  // dQ += dS K
-        mma_commit(smem_u32(&bars->empty[s]));  // stage consumed once this completes
-        if (u + 2 < subs) ok = issue_sdp(u + 2);
-      }
-      mma_commit(smem_u32(&bars->acc_full));
+    // The whole warp walks the schedule and waits on named barriers; every lane executes
+    // the MMA instructions predicated on `issuer` (lane 0), so the warp never diverges.
+    const uint32_t sQ = smem_u32(smem + L::kFixA), sDO = smem_u32(smem + L::kFixB);
+    const uint32_t ring = smem_u32(smem + L::kRing);
+    const bool issuer =
+        __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc)) && lane == 0;
+    // S and dP of sub-step u into buffer u & 1
+    auto issue_sdp = [&](int u) {
+      const int s = u % kStages, x = u & 1;
+      nb_sync(kNbStage + s, kNbStageCount);
+      tc_fence_after_sync();
+      const uint32_t sK = ring + s * L::kStage, sV = sK + L::kSubTile;
+      mma_128x64<D>(issuer, tmem + col_s(x), sQ, sK);     // S = Q K^T
+      mma_128x64<D>(issuer, tmem + col_dp(x), sDO, sV);   // dP = dO V^T
+      mma_commit_if(issuer, smem_u32(&bars->s_full[x]));
+    };
+    issue_sdp(0);
+    if (subs > 1) issue_sdp(1);
+    for (int u = 0; u < subs; ++u) {
+      const int s = u % kStages, x = u & 1;
+      nb_sync(kNbP + x, kNbPCount);
+      tc_fence_after_sync();
+      const uint32_t sK = ring + s * L::kStage;
+      mma_tmem64_x_slice<D>(issuer, tmem + kColAcc, tmem + col_s(x), sK, u > 0);  // dQ += dS K
+      mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage consumed once this completes
+      if (u + 2 < subs) issue_sdp(u + 2);
     }
+    mma_commit_if(issuer, smem_u32(&bars->acc_full));
   } else {
     const int pair = warp >> 3;                // sub-steps u with u % 2 == pair
     const int wg = (warp >> 2) & 1;            // which 32 key columns of a sub-step
@@ -573,9 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = pair; u < subs; u += 2) {
       const int kt0 = (kr.lo + (u >> 1)) * BT;
       const int ks = kr.lo * BT + u * SUB + c0;  // key of this thread's column 0
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc))) {
-        ok_all = false;
-        break;
+      if (ok_all)
+        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc));
+      if (!ok_all) {  // aborted: keep the barrier schedule with the MMA warp
+        nb_sync(kNbP + x, kNbPCount);
+        continue;
       }
       tc_fence_after_sync();
       const uint32_t tS = tmem + lane_base + col_s(x) + c0;
@@ -614,8 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st16(tS, dd);  // dS, bf16 pairs
       tmem_wait_st();
       tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[x]));
+      nb_arrive(kNbP + x, kNbPCount);
     }
     // pair 0 writes dQ: warpgroup wg writes columns [wg * D/2, (wg + 1) * D/2)
     const bool have =

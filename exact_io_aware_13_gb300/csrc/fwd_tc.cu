@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp walks the schedule and waits on named barriers; lane 0 issues.
+    // The whole warp walks the schedule and waits on named barriers; every lane executes
+    // the MMA instructions predicated on `issuer` (lane 0), so the warp never diverges.
     // After an abort the warp keeps every barrier operation and issues nothing.
     constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
     constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
@@ -221,9 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
-        mma_ss(tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
+        mma_ss_if(issuer, tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
       }
-      mma_commit(smem_u32(&bars->s_full[t]));
+      mma_commit_if(issuer, smem_u32(&bars->s_full[t]));
     };
     auto issue_pv = [&](int t, int u) {  // O_t += P_t V with V in ring use u
       const uint32_t vb = ring + (u % kStages) * L::kTile;
@@ -232,18 +233,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t colO = t == 0 ? L::kColO0 : L::kColO1;
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
-        mma_ts(tmem + colO, tmem + colS + kk * 8, dv + ((kk * 16 * 128) >> 4), idO,
+        mma_ts_if(issuer, tmem + colO, tmem + colS + kk * 8, dv + ((kk * 16 * 128) >> 4), idO,
                (np[t] > 0 || kk > 0) ? 1u : 0u);
     };
 
     sync_stage(0);
-    if (issuer) {
 #pragma unroll
-      for (int t = 0; t < kQTiles; ++t)
-        if (lo >= rng[t].lo && lo < rng[t].hi) issue_s(t, 0);
-      mma_commit(smem_u32(&bars->kv_empty[0]));
-    }
-    __syncwarp();
+    for (int t = 0; t < kQTiles; ++t)
+      if (lo >= rng[t].lo && lo < rng[t].hi) issue_s(t, 0);
+    mma_commit_if(issuer, smem_u32(&bars->kv_empty[0]));
     for (int jj = 0; jj < n_kv; ++jj) {
       const int j = lo + jj;
       const int uv = 2 * jj + 1, uk = 2 * jj + 2;
@@ -254,26 +252,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= rng[t].lo && j < rng[t].hi) {
           nb_sync(kNbP + t, kNbPCount);
           tc_fence_after_sync();
-          if (issuer) issue_pv(t, uv);
-          __syncwarp();
+          issue_pv(t, uv);
           ++np[t];
         }
         if (next) {
           if (t == 0) sync_stage(uk);
-          if (issuer && j + 1 >= rng[t].lo && j + 1 < rng[t].hi) issue_s(t, uk);
-          __syncwarp();
+          if (j + 1 >= rng[t].lo && j + 1 < rng[t].hi) issue_s(t, uk);
         }
       }
-      if (issuer) {
-        mma_commit(smem_u32(&bars->kv_empty[uv % kStages]));
-        if (next) mma_commit(smem_u32(&bars->kv_empty[uk % kStages]));
-      }
-      __syncwarp();
+      mma_commit_if(issuer, smem_u32(&bars->kv_empty[uv % kStages]));
+      if (next) mma_commit_if(issuer, smem_u32(&bars->kv_empty[uk % kStages]));
     }
-    if (issuer) {
 #pragma unroll
-      for (int t = 0; t < kQTiles; ++t) mma_commit(smem_u32(&bars->o_full[t]));
-    }
+    for (int t = 0; t < kQTiles; ++t) mma_commit_if(issuer, smem_u32(&bars->o_full[t]));
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;                 // query tile of this warpgroup
