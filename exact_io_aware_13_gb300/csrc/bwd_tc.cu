@@ -357,18 +357,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp walks the schedule and waits on named barriers; every lane executes
-    // the MMA instructions predicated on `issuer` (lane 0), so the warp never diverges.
-    // After an abort the warp keeps every barrier operation and issues nothing.
+    // the MMA instructions predicated on `issuer`, the one lane elect.sync picks, so the
+    // warp never diverges (an elect.sync predicate issues an MMA in about 47 cycles, a
+    // predicate computed from the lane index in about 82). If the fixed tiles never
+    // arrive (`ok` false) the warp keeps every barrier operation and issues nothing.
     const uint32_t sK = smem_u32(smem + L::kFixA), sV = smem_u32(smem + L::kFixB);
     const uint32_t ring = smem_u32(smem + L::kRing);
-    const bool issuer =
-        __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc)) && lane == 0;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc));
+    const bool issuer = elect_one();
     // S^T and dP^T of sub-step u into buffer u & 1
     auto issue_sdp = [&](int u) {
       const int s = u % kStages, x = u & 1;
       nb_sync(kNbStage + s, kNbStageCount);
       tc_fence_after_sync();
       const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
+      if (!ok) return;
       mma_128x64<D>(issuer, tmem + col_s(x), sK, sQ);    // S^T = K Q^T
       mma_128x64<D>(issuer, tmem + col_dp(x), sV, sDO);  // dP^T = V dO^T
       mma_commit_if(issuer, smem_u32(&bars->s_full[x]));
@@ -380,12 +383,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       nb_sync(kNbP + x, kNbPCount);
       tc_fence_after_sync();
       const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
-      mma_tmem64_x_slice<D>(issuer, tmem + colDV, tmem + col_s(x), sDO, u > 0);  // dV += P^T dO
-      mma_tmem64_x_slice<D>(issuer, tmem + colDK, tmem + col_dp(x), sQ, u > 0);  // dK += dS^T Q
-      mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage consumed once these complete
+      if (ok) {
+        mma_tmem64_x_slice<D>(issuer, tmem + colDV, tmem + col_s(x), sDO, u > 0);  // dV += P^T dO
+        mma_tmem64_x_slice<D>(issuer, tmem + colDK, tmem + col_dp(x), sQ, u > 0);  // dK += dS^T Q
+        mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage consumed once these complete
+      }
       if (u + 2 < subs) issue_sdp(u + 2);
     }
-    mma_commit_if(issuer, smem_u32(&bars->acc_full));
+    if (ok) mma_commit_if(issuer, smem_u32(&bars->acc_full));
   } else {
     // ------------------------------------------------------------ element-wise
     const int pair = warp >> 3;                // sub-steps u with u % 2 == pair
@@ -541,18 +546,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kRelayWarp) {
     relay_loop(bars, wc, subs);
   } else if (warp == kMmaWarp) {
-    // The whole warp walks the schedule and waits on named barriers; every lane executes
-    // the MMA instructions predicated on `issuer` (lane 0), so the warp never diverges.
+    // Same issue scheme as the dK/dV kernel: named barriers only, MMAs predicated on the
+    // elect.sync lane, nothing issued if the fixed tiles never arrive.
     const uint32_t sQ = smem_u32(smem + L::kFixA), sDO = smem_u32(smem + L::kFixB);
     const uint32_t ring = smem_u32(smem + L::kRing);
-    const bool issuer =
-        __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc)) && lane == 0;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc));
+    const bool issuer = elect_one();
     // S and dP of sub-step u into buffer u & 1
     auto issue_sdp = [&](int u) {
       const int s = u % kStages, x = u & 1;
       nb_sync(kNbStage + s, kNbStageCount);
       tc_fence_after_sync();
       const uint32_t sK = ring + s * L::kStage, sV = sK + L::kSubTile;
+      if (!ok) return;
       mma_128x64<D>(issuer, tmem + col_s(x), sQ, sK);     // S = Q K^T
       mma_128x64<D>(issuer, tmem + col_dp(x), sDO, sV);   // dP = dO V^T
       mma_commit_if(issuer, smem_u32(&bars->s_full[x]));
@@ -564,11 +570,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       nb_sync(kNbP + x, kNbPCount);
       tc_fence_after_sync();
       const uint32_t sK = ring + s * L::kStage;
-      mma_tmem64_x_slice<D>(issuer, tmem + kColAcc, tmem + col_s(x), sK, u > 0);  // dQ += dS K
-      mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage consumed once this completes
+      if (ok) {
+        mma_tmem64_x_slice<D>(issuer, tmem + kColAcc, tmem + col_s(x), sK, u > 0);  // dQ += dS K
+        mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage consumed once this completes
+      }
       if (u + 2 < subs) issue_sdp(u + 2);
     }
-    mma_commit_if(issuer, smem_u32(&bars->acc_full));
+    if (ok) mma_commit_if(issuer, smem_u32(&bars->acc_full));
   } else {
     const int pair = warp >> 3;                // sub-steps u with u % 2 == pair
     const int wg = (warp >> 2) & 1;            // which 32 key columns of a sub-step

@@ -200,21 +200,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp walks the schedule and waits on named barriers; every lane executes
-    // the MMA instructions predicated on `issuer` (lane 0), so the warp never diverges.
-    // After an abort the warp keeps every barrier operation and issues nothing.
+    // the MMA instructions predicated on `issuer`, the one lane elect.sync picks, so the
+    // warp never diverges (an elect.sync predicate issues an MMA in about 47 cycles, a
+    // predicate computed from the lane index in about 82). If the Q tiles never arrive
+    // (`ok` false) the warp keeps every barrier operation and issues nothing.
     constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
     constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
     const uint32_t q_base = smem_u32(smem + L::kQ);
     const uint32_t ring = smem_u32(smem + L::kRing);
     int np[kQTiles] = {0, 0};  // P tiles consumed per query tile
     const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->q_full), 0, wc));
-    const bool issuer = ok && lane == 0;
+    const bool issuer = elect_one();
+    auto commit = [&](uint64_t* bar) {
+      if (ok) mma_commit_if(issuer, smem_u32(bar));
+    };
 
     auto sync_stage = [&](int u) {
       nb_sync(kNbKv + u % kStages, kNbKvCount);
       tc_fence_after_sync();
     };
     auto issue_s = [&](int t, int u) {  // S_t = Q_t K^T with K in ring use u
+      if (!ok) return;
       const uint32_t kb = ring + (u % kStages) * L::kTile;
       const uint32_t qt = q_base + t * L::kTile;
       const uint64_t dq = smem_desc_sw128(qt, 16, 1024), dk = smem_desc_sw128(kb, 16, 1024);
@@ -227,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_if(issuer, smem_u32(&bars->s_full[t]));
     };
     auto issue_pv = [&](int t, int u) {  // O_t += P_t V with V in ring use u
+      if (!ok) return;
       const uint32_t vb = ring + (u % kStages) * L::kTile;
       const uint64_t dv = smem_desc_sw128(vb, L::kChunk, 1024);
       const uint32_t colS = t == 0 ? L::kColS0 : L::kColS1;
@@ -241,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int t = 0; t < kQTiles; ++t)
       if (lo >= rng[t].lo && lo < rng[t].hi) issue_s(t, 0);
-    mma_commit_if(issuer, smem_u32(&bars->kv_empty[0]));
+    commit(&bars->kv_empty[0]);
     for (int jj = 0; jj < n_kv; ++jj) {
       const int j = lo + jj;
       const int uv = 2 * jj + 1, uk = 2 * jj + 2;
@@ -260,11 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j + 1 >= rng[t].lo && j + 1 < rng[t].hi) issue_s(t, uk);
         }
       }
-      mma_commit_if(issuer, smem_u32(&bars->kv_empty[uv % kStages]));
-      if (next) mma_commit_if(issuer, smem_u32(&bars->kv_empty[uk % kStages]));
+      commit(&bars->kv_empty[uv % kStages]);
+      if (next) commit(&bars->kv_empty[uk % kStages]);
     }
 #pragma unroll
-    for (int t = 0; t < kQTiles; ++t) mma_commit_if(issuer, smem_u32(&bars->o_full[t]));
+    for (int t = 0; t < kQTiles; ++t) commit(&bars->o_full[t]);
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;                 // query tile of this warpgroup
