@@ -73,19 +73,83 @@ __device__ __forceinline__ ScoreK score_consts(const Problem& p, int h) {
   return s;
 }
 
-// P and dS of one element from the pre-cap score in log2 units (or in 2 log2e / c
-// units under the soft-cap); lse2 = L * log2e (+inf for a row with no key).
-template <bool kSoftcap>
-__device__ __forceinline__ void p_and_ds(float pre, float lse2, float dp, float delta,
-                                         float capA, bool ok, float& pr, float& ds) {
-  float s2 = pre, dcap = 1.f;
+// P and dS of one element. xs = raw score q.k; `alibi` = kb (j - i) (0 without ALiBi);
+// lse2 = L log2e (+inf for a row with no key). Under the soft-cap the pre-cap score is
+// in 2 log2e / c units and the tanh derivative scales dS. A masked element (ok false)
+// takes the exponent -inf, so P = dS = 0 with no branch: a per-lane condition around
+// the exponential would make the compiler branch on every element.
+template <bool kAlibi, bool kSoftcap>
+__device__ __forceinline__ void p_and_ds(float xs, const ScoreK& sk, float alibi, float lse2,
+                                         float dp, float delta, bool ok, float& pr, float& ds) {
+  float arg, dcap = 1.f;
   if (kSoftcap) {
+    const float pre = kAlibi ? fmaf(xs, sk.k1, alibi) : xs * sk.k1;
     const float t = 1.0f - 2.0f * rcp_approx(1.0f + ex2_approx(pre));  // tanh(pre_cap / c)
-    s2 = capA * t;
+    arg = sk.capA * t - lse2;
     dcap = 1.0f - t * t;
+  } else if (kAlibi) {
+    arg = fmaf(xs, sk.k1, alibi) - lse2;
+  } else {
+    arg = fmaf(xs, sk.k1, -lse2);
   }
-  pr = ok ? ex2_approx(s2 - lse2) : 0.f;
-  ds = pr * (dp - delta) * dcap;
+  pr = ex2_approx(ok ? arg : -INFINITY);
+  ds = kSoftcap ? pr * (dp - delta) * dcap : pr * (dp - delta);
+}
+
+// dkdv element-wise step for one thread: key row j, 32 query columns starting at qs.
+// Writes P^T and dS^T (bf16 pairs). kMasked adds the per-element mask test; the
+// caller picks the variant by a warp-uniform tile test.
+template <bool kAlibi, bool kSoftcap, bool kMasked>
+__device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
+                                         const float* lse2, const float* dl, const int* fk,
+                                         const ScoreK& sk, float base, int j, int qs,
+                                         bool key_ok, bool causal_type, uint32_t (&pp)[16],
+                                         uint32_t (&dd)[16]) {
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    const float4 lv = reinterpret_cast<const float4*>(lse2)[e4];
+    const float4 dv = reinterpret_cast<const float4*>(dl)[e4];
+    const float lvs[4] = {lv.x, lv.y, lv.z, lv.w};
+    const float dvs[4] = {dv.x, dv.y, dv.z, dv.w};
+    float pv[4], dsv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int col = e4 * 4 + q;
+      bool ok = true;
+      if (kMasked) {
+        const int i = qs + col;
+        ok = key_ok && (!causal_type || (i >= j && fk[col] <= j));
+      }
+      p_and_ds<kAlibi, kSoftcap>(__uint_as_float(sr[col]), sk,
+                                 kAlibi ? fmaf(-(float)col, sk.kb, base) : 0.f, lvs[q],
+                                 __uint_as_float(dr[col]), dvs[q], ok, pv[q], dsv[q]);
+    }
+    pp[2 * e4] = pack_bf16x2(pv[0], pv[1]);
+    pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
+    dd[2 * e4] = pack_bf16x2(dsv[0], dsv[1]);
+    dd[2 * e4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+  }
+}
+
+// dq element-wise step for one thread: query row with (lse2, delta), 32 key columns;
+// allowed columns are [c_lo, c_hi] when kMasked. Writes dS (bf16 pairs).
+template <bool kAlibi, bool kSoftcap, bool kMasked>
+__device__ __forceinline__ void dq_ds(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
+                                      const ScoreK& sk, float base, float lse2, float delta,
+                                      int c_lo, int c_hi, uint32_t (&dd)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    float pr[2], ds[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int col = 2 * e + q;
+      const bool ok = !kMasked || (col >= c_lo && col <= c_hi);
+      p_and_ds<kAlibi, kSoftcap>(__uint_as_float(sr[col]), sk,
+                                 kAlibi ? fmaf((float)col, sk.kb, base) : 0.f, lse2,
+                                 __uint_as_float(dr[col]), delta, ok, pr[q], ds[q]);
+    }
+    dd[e] = pack_bf16x2(ds[0], ds[1]);
+  }
 }
 
 // Shared-memory layout shared by both kernels: two fixed 128-row tiles, then a ring
@@ -430,41 +494,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       reg_fence32(sr);
       reg_fence32(dr);
-      const bool masked = tile_needs_mask(p.mask, qrow & ~(BT - 1), k0, BT);
       const float base = kAlibi ? sk.kb * (float)(j - qs) : 0.f;  // kb*(j - i) at column 0
       uint32_t pp[16], dd[16];
-#pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 lv = reinterpret_cast<const float4*>(lse2)[e4];
-        const float4 dv = reinterpret_cast<const float4*>(dl)[e4];
-        const float lvs[4] = {lv.x, lv.y, lv.z, lv.w};
-        const float dvs[4] = {dv.x, dv.y, dv.z, dv.w};
-        float pv[4], dsv[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int col = e4 * 4 + q;
-          const float xs = __uint_as_float(sr[col]);
-          bool ok = true;
-          if (masked) {
-            const int i = qs + col;
-            ok = j < p.Nkv && (!causal_type || (i >= j && fk[col] <= j));
-          }
-          if (!kAlibi && !kSoftcap) {
-            const float pr = ok ? ex2_approx(fmaf(xs, sk.k1, -lvs[q])) : 0.f;
-            pv[q] = pr;
-            dsv[q] = pr * (__uint_as_float(dr[col]) - dvs[q]);
-          } else {
-            const float pre =
-                kAlibi ? fmaf(xs, sk.k1, fmaf(-(float)col, sk.kb, base)) : xs * sk.k1;
-            p_and_ds<kSoftcap>(pre, lvs[q], __uint_as_float(dr[col]), dvs[q], sk.capA, ok,
-                               pv[q], dsv[q]);
-          }
-        }
-        pp[2 * e4] = pack_bf16x2(pv[0], pv[1]);
-        pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
-        dd[2 * e4] = pack_bf16x2(dsv[0], dsv[1]);
-        dd[2 * e4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
-      }
+      if (tile_needs_mask(p.mask, qrow & ~(BT - 1), k0, BT))  // warp-uniform
+        dkdv_pds<kAlibi, kSoftcap, true>(sr, dr, lse2, dl, fk, sk, base, j, qs, j < p.Nkv,
+                                         causal_type, pp, dd);
+      else
+        dkdv_pds<kAlibi, kSoftcap, false>(sr, dr, lse2, dl, fk, sk, base, j, qs, true,
+                                          causal_type, pp, dd);
       tmem_st16(tS, pp);   // P^T, bf16 pairs, in this warpgroup's first 16 columns
       tmem_st16(tDP, dd);  // dS^T
       tmem_wait_st();
@@ -596,7 +633,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       fk = first_key(p.mask, i);
     }
     const int last_key = (p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1));
-    const float nlse2 = -lse2;
     bool ok_all = true;
     for (int u = pair; u < subs; u += 2) {
       const int kt0 = (kr.lo + (u >> 1)) * BT;
@@ -616,31 +652,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       reg_fence32(sr);
       reg_fence32(dr);
-      const bool masked = tile_needs_mask(p.mask, q0, kt0, BT);
-      const int c_lo = fk - ks, c_hi = last_key - ks;  // allowed columns of this row
       const float base = kAlibi ? sk.kb * (float)(ks - i) : 0.f;  // kb*(j - i) at column 0
       uint32_t dd[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        float dsv[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int col = 2 * e + q;
-          const float xs = __uint_as_float(sr[col]);
-          const bool ok = !masked || (col >= c_lo && col <= c_hi);
-          if (!kAlibi && !kSoftcap) {
-            const float pr = ok ? ex2_approx(fmaf(xs, sk.k1, nlse2)) : 0.f;
-            dsv[q] = pr * (__uint_as_float(dr[col]) - dlt);
-          } else {
-            const float pre =
-                kAlibi ? fmaf(xs, sk.k1, fmaf((float)col, sk.kb, base)) : xs * sk.k1;
-            float pr;
-            p_and_ds<kSoftcap>(pre, lse2, __uint_as_float(dr[col]), dlt, sk.capA, ok, pr,
-                               dsv[q]);
-          }
-        }
-        dd[e] = pack_bf16x2(dsv[0], dsv[1]);
-      }
+      if (tile_needs_mask(p.mask, q0, kt0, BT))  // warp-uniform
+        dq_ds<kAlibi, kSoftcap, true>(sr, dr, sk, base, lse2, dlt, fk - ks, last_key - ks, dd);
+      else
+        dq_ds<kAlibi, kSoftcap, false>(sr, dr, sk, base, lse2, dlt, 0, 0, dd);
       tmem_st16(tS, dd);  // dS, bf16 pairs
       tmem_wait_st();
       tc_fence_before_sync();
