@@ -92,6 +92,7 @@ attn_status check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float 
   p->mask.kind = mask_kind;
   p->mask.nq = Nq;
   p->mask.nkv = Nkv;
+  p->nq_pad = (int)(((long long)Nq + 127) / 128 * 128);
   if (score_kind & ATTN_SCORE_SOFTCAP) {
     if (!sp || !(sp->softcap > 0.f) || !std::isfinite(sp->softcap)) return ATTN_ERR_ARG;
     p->softcap = sp->softcap;
@@ -156,6 +157,18 @@ attn_status fwd_common(bool simt, const void* q, const void* k, const void* v, v
   return from_cuda(launch_fwd_tc(p, tq, tk, tv, ob, lse, st));
 }
 
+// Workspace of the backward: the three row-term arrays of RowTerms, each starting on
+// a 256-byte boundary. rows = B * Hq * nq_pad.
+size_t row_terms_bytes(long long rows, int nq_pad) {
+  return 2 * round256((size_t)rows * sizeof(float)) + round256((size_t)nq_pad * sizeof(int));
+}
+RowTerms row_terms(int B, int Hq, int nq_pad, void* workspace) {
+  const size_t plane = round256((size_t)B * Hq * nq_pad * sizeof(float));
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  return RowTerms{reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + plane),
+                  reinterpret_cast<int*>(base + 2 * plane)};
+}
+
 attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                        int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int mask_kind,
@@ -193,7 +206,7 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
       return ATTN_ERR_LAUNCH;
     return ATTN_OK;
   }
-  float* delta = static_cast<float*>(workspace);
+  const RowTerms rt = row_terms(B, Hq, p.nq_pad, workspace);
   const auto* qb = static_cast<const __nv_bfloat16*>(q);
   const auto* kb = static_cast<const __nv_bfloat16*>(k);
   const auto* vb = static_cast<const __nv_bfloat16*>(v);
@@ -214,24 +227,25 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
     if ((s = make_map(&maps.v64, v, B * Hkv, Nkv, d, 64)) != ATTN_OK) return s;
   }
   if ((phases & ATTN_BWD_ROWDOT) &&
-      (s = from_cuda(launch_bwd_rowdot(p, static_cast<const __nv_bfloat16*>(o), dob, delta,
+      (s = from_cuda(launch_bwd_rowdot(p, static_cast<const __nv_bfloat16*>(o), dob, lse, rt,
                                        st))) != ATTN_OK)
     return s;
   if (simt) {
     if ((phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ)) != (ATTN_BWD_DKDV | ATTN_BWD_DQ))
       return phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ) ? ATTN_ERR_ARG : ATTN_OK;
-    return from_cuda(launch_bwd_simt(p, qb, kb, vb, lse, dob, delta, dqb, dkb, dvb, st));
+    return from_cuda(launch_bwd_simt(p, qb, kb, vb, lse, dob, rt.delta, dqb, dkb, dvb, st));
   }
   if (!(phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ))) return ATTN_OK;
-  return from_cuda(launch_bwd_tc(p, maps, lse, delta, dqb, dkb, dvb,
-                                 (phases & ATTN_BWD_DKDV) != 0, (phases & ATTN_BWD_DQ) != 0, st));
+  return from_cuda(launch_bwd_tc(p, maps, rt, dqb, dkb, dvb, (phases & ATTN_BWD_DKDV) != 0,
+                                 (phases & ATTN_BWD_DQ) != 0, st));
 }
 
 // ---------------------------------------------------------------- static workspace
-// Scratch of attn_bwd_static_workspace: the backward's row term D (one float per
-// query row) for callers that cannot allocate. One copy per device, shared by every
-// call on that device.
-static __device__ __align__(256) float g_static_workspace[ATTN_STATIC_WORKSPACE_ROWS];
+// Scratch of attn_bwd_static_workspace: the backward's row terms (three 4-byte words
+// per padded query row) for callers that cannot allocate. One copy per device, shared
+// by every call on that device.
+constexpr size_t kStaticWords = 3 * (size_t)ATTN_STATIC_WORKSPACE_ROWS;
+static __device__ __align__(256) float g_static_workspace[kStaticWords];
 
 std::mutex g_static_mu;
 float* g_static_ptr[kMaxDevices];  // device address of g_static_workspace, per device
@@ -279,7 +293,8 @@ attn_status attn_fwd_simt(const void* q, const void* k, const void* v, void* o, 
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d) {
   (void)Hkv; (void)Nkv; (void)d;
   if (B <= 0 || Hq <= 0 || Nq <= 0) return 0;
-  return round256((size_t)B * Hq * Nq * sizeof(float));  // D, one float per query row
+  const int nq_pad = (int)(((long long)Nq + 127) / 128 * 128);
+  return row_terms_bytes((long long)B * Hq * nq_pad, nq_pad);
 }
 
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -322,7 +337,7 @@ attn_status attn_bwd_static_workspace(const void* q, const void* k, const void* 
                                       const attn_mask_params* mask_params, int score_kind,
                                       const attn_score_params* score_params, void* stream) {
   if (B < 0 || Hq < 0 || Nq < 0) return ATTN_ERR_SHAPE;
-  const long long rows = (long long)B * Hq * Nq;
+  const long long rows = (long long)B * Hq * ((Nq + 127LL) / 128 * 128);
   if (rows > ATTN_STATIC_WORKSPACE_ROWS) return ATTN_ERR_WORKSPACE;
   float* ws = nullptr;
   if (rows > 0) {
@@ -333,7 +348,7 @@ attn_status attn_bwd_static_workspace(const void* q, const void* k, const void* 
   }
   return bwd_common(false, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale,
                     mask_kind, mask_params, score_kind, score_params, ws,
-                    ws ? (size_t)ATTN_STATIC_WORKSPACE_ROWS * sizeof(float) : 0, stream);
+                    ws ? kStaticWords * sizeof(float) : 0, stream);
 }
 
 attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_params, int Nq,

@@ -2,8 +2,8 @@
 //
 // "FlashAttention/es" ("Paso hacia atrás y recomputación") rebuilds S and P tile
 // by tile from the saved log-sum-exp L instead of storing P. With
-// P_ij = exp(s_ij - L_i) and D_i = rowsum(dO_i o O_i) (computed by a separate
-// row-dot kernel), the gradients are
+// P_ij = exp(s_ij - L_i) and D_i = rowsum(dO_i o O_i) (computed, with L log2 e and
+// each row's first key, by a separate row kernel into padded arrays), the gradients are
 //     dV = P^T dO,   dP = dO V^T,   dS = P o (dP - D) [x soft-cap derivative],
 //     dK = scale dS^T Q,   dQ = scale dS K.
 // Two kernels, both deterministic (fixed summation order, no atomics):
@@ -15,15 +15,19 @@
 //     keys at a time: S = Q K^T and dP = dO V^T, dS back into tensor memory, then
 //     dQ += dS K.
 // Each sub-step streams its own 64-row slice of the two operands it walks (Q and dO,
-// or K and V) through a 4-deep shared-memory ring, so loads run three sub-steps
-// ahead. S and dP are double-buffered in tensor memory (two 64-column buffers each),
-// so the MMAs of one sub-step run while the element-wise warps work on another.
-// Warps 0-15 do the element-wise work in two pairs of warpgroups: pair p takes the
-// sub-steps u with u % 2 == p (buffer p); inside a pair, warpgroup w takes columns
-// [32w, 32w+32) (one thread per TMEM lane = row). Warp 16 loads with TMA, warp 17
-// owns tensor memory and issues the MMAs, warp 18 relays TMA completions. The MMA warp
-// waits only on hardware named barriers: a shared-memory access from the thread that
-// issues MMAs stalls the tensor pipe (see nb_sync in ptx.cuh).
+// or K and V; for dkdv also the 64 rows' L log2 e, D and first key) through a 4-deep
+// shared-memory ring, so loads run ahead of the MMAs. Warp 16 loads with TMA, warp 17
+// owns tensor memory and issues the MMAs, warp 18 relays TMA completions; warps 0-15
+// do the element-wise work, one thread per TMEM lane (= row of the CTA's tile). The
+// MMA warp waits only on hardware named barriers: a shared-memory access from the
+// thread that issues MMAs stalls the tensor pipe (see nb_sync in ptx.cuh).
+//   dkdv: every element-wise warp works on every sub-step (warpgroup w takes 16 of
+//     its 64 query columns). S^T / dP^T have one TMEM buffer: the warps release it as
+//     soon as they hold their columns in registers, so the next sub-step's S^T / dP^T
+//     MMAs start while they compute; P^T / dS^T go to one of two separate buffers.
+//   dq: two pairs of warpgroups alternate sub-steps (pair p takes u % 2 == p, warpgroup
+//     w of the pair 32 key columns); S / dP are double-buffered and dS is written back
+//     over S.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -38,18 +42,25 @@ constexpr int kLoadWarp = kEwWarps;
 constexpr int kMmaWarp = kEwWarps + 1;
 constexpr int kRelayWarp = kEwWarps + 2;  // turns TMA completions into barrier arrivals
 // Named barriers (the MMA warp waits only on these; see nb_sync in ptx.cuh):
-//   kNbP + x      P_x / dS_x written to TMEM: pair x (256 threads) + MMA warp (32)
-//   kNbStage + s  ring stage s loaded: relay warp (32) + MMA warp (32)
+//   kNbStage + s   ring stage s loaded: relay warp (32) + MMA warp (32)
+//   dq:   kNbP + x     dS_x written to TMEM: pair x (256 threads) + MMA warp (32)
+//   dkdv: kNbKvRel     S^T / dP^T of the sub-step read: element-wise warps + MMA warp
+//         kNbKvP + x   P^T / dS^T of a sub-step u (x = u % 2) written: same threads
 constexpr uint32_t kNbP = 1, kNbPCount = 288;
 constexpr uint32_t kNbStage = 3, kNbStageCount = 64;
+constexpr uint32_t kNbKvRel = 7, kNbKvP = 8, kNbKvCount = (kEwWarps + 1) * 32;
 constexpr int kStages = 4;       // ring depth, in sub-steps
 constexpr int kHeadGroup = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Tensor memory columns: S buffers, dP buffers (64 each), then the accumulators.
+// Tensor memory columns of dq: S buffers, dP buffers (64 each), then dQ.
 __device__ __forceinline__ uint32_t col_s(int x) { return x * 64; }
 __device__ __forceinline__ uint32_t col_dp(int x) { return 128 + x * 64; }
 constexpr uint32_t kColAcc = 256;
+// Tensor memory columns of dkdv: S^T, dP^T (64 each, one buffer), two P^T / dS^T
+// buffers (bf16 pairs: P^T in the first 32 columns, dS^T in the next 32), dV, dK.
+constexpr uint32_t kKvColS = 0, kKvColDP = 64, kKvColAcc = 256;
+__device__ __forceinline__ uint32_t kv_col_pd(int x) { return 128 + x * 64; }
 
 // Element-wise constants: s2 = x*k1 + kb*(j - i) (log2 units), then the soft-cap.
 struct ScoreK {
@@ -96,17 +107,17 @@ __device__ __forceinline__ void p_and_ds(float xs, const ScoreK& sk, float alibi
   ds = kSoftcap ? pr * (dp - delta) * dcap : pr * (dp - delta);
 }
 
-// dkdv element-wise step for one thread: key row j, 32 query columns starting at qs.
-// Writes P^T and dS^T (bf16 pairs). kMasked adds the per-element mask test; the
-// caller picks the variant by a warp-uniform tile test.
+// dkdv element-wise step for one thread: key row j, 16 query columns starting at qs,
+// with their lse2 / delta / first key. Writes P^T and dS^T (bf16 pairs). kMasked adds
+// the per-element mask test; the caller picks the variant by a warp-uniform tile test.
 template <bool kAlibi, bool kSoftcap, bool kMasked>
-__device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
+__device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_t (&dr)[16],
                                          const float* lse2, const float* dl, const int* fk,
                                          const ScoreK& sk, float base, int j, int qs,
-                                         bool key_ok, bool causal_type, uint32_t (&pp)[16],
-                                         uint32_t (&dd)[16]) {
+                                         bool key_ok, bool causal_type, uint32_t (&pp)[8],
+                                         uint32_t (&dd)[8]) {
 #pragma unroll
-  for (int e4 = 0; e4 < 8; ++e4) {
+  for (int e4 = 0; e4 < 4; ++e4) {
     const float4 lv = reinterpret_cast<const float4*>(lse2)[e4];
     const float4 dv = reinterpret_cast<const float4*>(dl)[e4];
     const float lvs[4] = {lv.x, lv.y, lv.z, lv.w};
@@ -152,9 +163,9 @@ __device__ __forceinline__ void dq_ds(const uint32_t (&sr)[32], const uint32_t (
   }
 }
 
-// Shared-memory layout shared by both kernels: two fixed 128-row tiles, then a ring
-// of kStages stages, each holding a 64-row slice of two operands (and, for dkdv, the
-// per-row data of those 64 query rows).
+// Shared-memory layout shared by both kernels: two fixed 128-row tiles, a ring of
+// kStages stages, each holding a 64-row slice of two operands, and (dkdv only) the
+// row terms of each stage's 64 query rows: lse2, delta, first key, 256 bytes each.
 template <int D>
 struct Layout {
   static constexpr int kFixChunk = BT * 128;        // 64-column slab of a fixed tile
@@ -175,7 +186,8 @@ struct BwdBars {
   uint64_t fixed_full;             // the two fixed tiles
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t s_full[2];              // S_x and dP_x in TMEM
+  uint64_t s_full[2];              // S_x and dP_x in TMEM (dkdv: buffer 0 only)
+  uint64_t pd_free[2];             // dkdv: P^T / dS^T buffer x read by its MMAs
   uint64_t acc_full;               // accumulators final
   uint32_t tmem_base;
   int abort_flag;
@@ -183,8 +195,7 @@ struct BwdBars {
 
 struct BwdArgs {
   Problem p;
-  const float* lse;
-  const float* delta;
+  RowTerms rt;
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -211,7 +222,10 @@ __device__ __forceinline__ void setup_common(BwdBars* bars, uint32_t stage_full_
     mbar_init(smem_u32(&bars->full[s]), stage_full_count);
     mbar_init(smem_u32(&bars->empty[s]), stage_empty_count);
   }
-  for (int x = 0; x < 2; ++x) mbar_init(smem_u32(&bars->s_full[x]), 1);
+  for (int x = 0; x < 2; ++x) {
+    mbar_init(smem_u32(&bars->s_full[x]), 1);
+    mbar_init(smem_u32(&bars->pd_free[x]), 1);
+  }
   mbar_init(smem_u32(&bars->acc_full), 1);
   bars->abort_flag = 0;
   fence_barrier_init();
@@ -248,6 +262,19 @@ __device__ __forceinline__ void mma_tmem64_x_slice(bool pred, uint32_t d_tmem, u
   }
 }
 
+// D[128 x D] (+)= A_tmem[128 x 64] B[64 x D] with A stored contiguously: k-step kk
+// (16 rows of B) reads A columns [8 kk, 8 kk + 8). B as in mma_tmem64_x_slice.
+template <int D>
+__device__ __forceinline__ void mma_pd_x_slice(bool pred, uint32_t d_tmem, uint32_t a_tmem,
+                                               uint32_t b, bool accumulate) {
+  constexpr uint32_t id = idesc_bf16_f32(BT, D, false, true);
+  const uint64_t db = smem_desc_sw128(b, SUB * 128, 1024);
+#pragma unroll
+  for (int kk = 0; kk < SUB / 16; ++kk)
+    mma_ts_if(pred, d_tmem, a_tmem + kk * 8, db + ((kk * 16 * 128) >> 4), id,
+              (accumulate || kk > 0) ? 1u : 0u);
+}
+
 // Write one accumulator row (D fp32 columns at TMEM `t`) times `mul` as bf16.
 // tcgen05.ld is warp-collective: every lane of the warp must call this with the same
 // `live`; `store` (per lane) only decides whether the row is written.
@@ -282,13 +309,14 @@ __device__ __forceinline__ void store_acc_row(uint32_t t, float mul, __nv_bfloat
 
 // Loads the two fixed tiles (rows r0.. of head z) and then, for every sub-step u,
 // the 64-row slices of the two streamed operands into stage u % kStages. `slice`
-// gives (row, head) of sub-step u. `rows` (dkdv only) fills the stage's row data.
-template <int D, typename SliceFn, typename RowsFn>
+// gives (row, head) of sub-step u. With `rt` (dkdv) it also copies the row terms of
+// those 64 query rows into the stage's row block; all of it completes full[s].
+template <int D, typename SliceFn>
 __device__ __forceinline__ void load_loop(uint8_t* smem, BwdBars* bars, const WaitCtx& wc,
                                           int lane, const CUtensorMap* fa, const CUtensorMap* fb,
                                           int r0, int z, const CUtensorMap* sa,
                                           const CUtensorMap* sb, int subs, SliceFn slice,
-                                          RowsFn rows, bool with_rows) {
+                                          const RowTerms* rt, int nq_pad) {
   using L = Layout<D>;
   if (lane == 0) {
     tma_prefetch_desc(sa);
@@ -308,19 +336,22 @@ __device__ __forceinline__ void load_loop(uint8_t* smem, BwdBars* bars, const Wa
     bool ok = true;
     if (lane == 0) ok = mbar_wait(smem_u32(&bars->empty[s]), (use & 1) ^ 1, wc);
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-    const uint32_t full = smem_u32(&bars->full[s]);
     if (lane == 0) {
-      mbar_arrive_expect_tx(full, L::kStage);
+      const uint32_t full = smem_u32(&bars->full[s]);
+      mbar_arrive_expect_tx(full, L::kStage + (rt ? L::kRowStage : 0));
       uint8_t* stg = smem + L::kRing + s * L::kStage;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         tma_load_3d(smem_u32(stg + c * L::kSubChunk), sa, full, c * 64, row, head);
         tma_load_3d(smem_u32(stg + L::kSubTile + c * L::kSubChunk), sb, full, c * 64, row, head);
       }
-    }
-    if (with_rows) {
-      rows(u, reinterpret_cast<float*>(smem + L::kRows + s * L::kRowStage), row, head);
-      mbar_arrive(full);
+      if (rt) {  // rows row .. row + 63 of query head `head` (row + 64 <= nq_pad)
+        const uint32_t rs = smem_u32(smem + L::kRows + s * L::kRowStage);
+        const size_t off = (size_t)head * nq_pad + row;
+        bulk_load(rs, rt->lse2 + off, SUB * 4, full);
+        bulk_load(rs + SUB * 4, rt->delta + off, SUB * 4, full);
+        bulk_load(rs + 2 * SUB * 4, rt->first + row, SUB * 4, full);
+      }
     }
   }
   if (lane == 0) {  // let in-flight copies land before the CTA can exit
@@ -381,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   WaitCtx wc{&bars->abort_flag, p.status};
-  if (threadIdx.x == 0) setup_common(bars, 1 + 32, 1 + 8);
+  if (threadIdx.x == 0) setup_common(bars, 1, 1);
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
     tmem_relinquish();
@@ -390,32 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t colDV = kColAcc, colDK = kColAcc + D;
+  const uint32_t colDV = kKvColAcc, colDK = kKvColAcc + D;
 
   if (warp == kLoadWarp) {
-    // Row data of the 64 query rows of a sub-step: L * log2e (+inf for a row with no
-    // key, so that exp2(s - lse2) = 0), D, and the row's first allowed key.
-    auto rows = [&](int, float* lse2, int q0, int bh) {
-      float* dl = lse2 + SUB;
-      int* fk = reinterpret_cast<int*>(dl + SUB);
-#pragma unroll
-      for (int e = 0; e < SUB / 32; ++e) {
-        const int r = e * 32 + lane, i = q0 + r;
-        float lv = INFINITY, dv = 0.f;
-        int f = 0x7fffffff;  // rows past Nq see no key
-        if (i < p.Nq) {
-          const float l = a.lse[(size_t)bh * p.Nq + i];
-          lv = l == -INFINITY ? INFINITY : l * kLog2e;
-          dv = a.delta[(size_t)bh * p.Nq + i];
-          f = first_key(p.mask, i);
-        }
-        lse2[r] = lv;
-        dl[r] = dv;
-        fk[r] = f;
-      }
-    };
     load_loop<D>(smem, bars, wc, lane, &maps.k128, &maps.v128, k0, bg, &maps.q64, &maps.do64,
-                 subs, slice, rows, true);
+                 subs, slice, &a.rt, p.nq_pad);
   } else if (warp == kRelayWarp) {
     relay_loop(bars, wc, subs);
   } else if (warp == kMmaWarp) {
@@ -425,101 +435,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp never diverges (an elect.sync predicate issues an MMA in about 47 cycles, a
     // predicate computed from the lane index in about 82). If the fixed tiles never
     // arrive (`ok` false) the warp keeps every barrier operation and issues nothing.
+    // Issue order: S^T/dP^T(0), then per sub-step u: S^T/dP^T(u+1) as soon as the
+    // element-wise warps have read S^T/dP^T(u), and dV/dK(u) once P^T/dS^T(u) are
+    // written. The tensor pipe thus runs S^T/dP^T(u+1) and dV/dK(u-1) while the
+    // element-wise warps work on u.
     const uint32_t sK = smem_u32(smem + L::kFixA), sV = smem_u32(smem + L::kFixB);
     const uint32_t ring = smem_u32(smem + L::kRing);
     const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc));
     const bool issuer = elect_one();
-    // S^T and dP^T of sub-step u into buffer u & 1
-    auto issue_sdp = [&](int u) {
-      const int s = u % kStages, x = u & 1;
+    auto issue_sdp = [&](int v) {  // S^T and dP^T of sub-step v
+      const int s = v % kStages;
       nb_sync(kNbStage + s, kNbStageCount);
       tc_fence_after_sync();
-      const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
       if (!ok) return;
-      mma_128x64<D>(issuer, tmem + col_s(x), sK, sQ);    // S^T = K Q^T
-      mma_128x64<D>(issuer, tmem + col_dp(x), sV, sDO);  // dP^T = V dO^T
-      mma_commit_if(issuer, smem_u32(&bars->s_full[x]));
+      const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
+      mma_128x64<D>(issuer, tmem + kKvColS, sK, sQ);    // S^T = K Q^T
+      mma_128x64<D>(issuer, tmem + kKvColDP, sV, sDO);  // dP^T = V dO^T
+      mma_commit_if(issuer, smem_u32(&bars->s_full[0]));
     };
     issue_sdp(0);
-    if (subs > 1) issue_sdp(1);
     for (int u = 0; u < subs; ++u) {
       const int s = u % kStages, x = u & 1;
-      nb_sync(kNbP + x, kNbPCount);
-      tc_fence_after_sync();
-      const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
-      if (ok) {
-        mma_tmem64_x_slice<D>(issuer, tmem + colDV, tmem + col_s(x), sDO, u > 0);  // dV += P^T dO
-        mma_tmem64_x_slice<D>(issuer, tmem + colDK, tmem + col_dp(x), sQ, u > 0);  // dK += dS^T Q
-        mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage consumed once these complete
+      if (u + 1 < subs) {
+        nb_sync(kNbKvRel, kNbKvCount);  // S^T / dP^T(u) are in registers
+        issue_sdp(u + 1);
       }
-      if (u + 2 < subs) issue_sdp(u + 2);
+      nb_sync(kNbKvP + x, kNbKvCount);  // P^T / dS^T(u) in buffer x
+      tc_fence_after_sync();
+      if (ok) {
+        const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
+        mma_pd_x_slice<D>(issuer, tmem + colDV, tmem + kv_col_pd(x), sDO, u > 0);       // dV += P^T dO
+        mma_pd_x_slice<D>(issuer, tmem + colDK, tmem + kv_col_pd(x) + 32, sQ, u > 0);  // dK += dS^T Q
+        mma_commit_if(issuer, smem_u32(&bars->empty[s]));    // stage (and its row terms) free
+        mma_commit_if(issuer, smem_u32(&bars->pd_free[x]));  // buffer x free
+      }
     }
     if (ok) mma_commit_if(issuer, smem_u32(&bars->acc_full));
   } else {
     // ------------------------------------------------------------ element-wise
-    const int pair = warp >> 3;                // sub-steps u with u % 2 == pair
-    const int wg = (warp >> 2) & 1;            // which 32 columns of a sub-step
-    const int row = (warp & 3) * 32 + lane;    // key row in the tile
+    const int q4 = warp & 3;                   // TMEM lane quarter: key rows 32 q4 ..
+    const int wg = warp >> 2;                  // query columns [16 wg, 16 wg + 16)
+    const int row = q4 * 32 + lane;            // key row in the tile
     const int j = k0 + row;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int c0 = wg * 32;
-    const int x = pair;                        // TMEM buffer of this pair
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const int c0 = wg * 16;
     const bool causal_type = p.mask.kind != ATTN_MASK_NONE;
     bool ok_all = true;
-    for (int u = pair; u < subs; u += 2) {
-      const int s = u % kStages;
+    for (int u = 0; u < subs; ++u) {
+      const int s = u % kStages, x = u & 1;
+      const bool rel = u + 1 < subs;  // the MMA warp waits for this release before u + 1
       int qrow, bh;
       slice(u, qrow, bh);
       const int h = bh - b * p.Hq;
       const int qs = qrow + c0;                  // query of this thread's column 0
       const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
       if (ok_all)
-        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc));
-      // the row data were written before full[s] completed; observe them
+        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[0]), u & 1, wc));
+      // the stage's row terms arrived with full[s]; observe them
       if (ok_all)
         ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc));
       if (!ok_all) {  // aborted: keep the barrier schedule with the MMA warp
-        nb_sync(kNbP + x, kNbPCount);
+        if (rel) nb_sync(kNbKvRel, kNbKvCount);
+        nb_sync(kNbKvP + x, kNbKvCount);
         continue;
       }
       tc_fence_after_sync();
+      uint32_t sr[16], dr[16];
+      tmem_ld16(tmem + lane_base + kKvColS + c0, sr);
+      tmem_ld16(tmem + lane_base + kKvColDP + c0, dr);
+      tmem_wait_ld();
+      reg_fence16(sr);
+      reg_fence16(dr);
+      tc_fence_before_sync();
+      if (rel) nb_arrive(kNbKvRel, kNbKvCount);
       const float* lse2 = reinterpret_cast<const float*>(smem + L::kRows + s * L::kRowStage) + c0;
       const float* dl = lse2 + SUB;
       const int* fk = reinterpret_cast<const int*>(dl + SUB);
-      const uint32_t tS = tmem + lane_base + col_s(x) + c0;
-      const uint32_t tDP = tmem + lane_base + col_dp(x) + c0;
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tS, sr);
-      tmem_ld32(tDP, dr);
-      tmem_wait_ld();
-      reg_fence32(sr);
-      reg_fence32(dr);
       const float base = kAlibi ? sk.kb * (float)(j - qs) : 0.f;  // kb*(j - i) at column 0
-      uint32_t pp[16], dd[16];
+      uint32_t pp[8], dd[8];
       if (tile_needs_mask(p.mask, qrow & ~(BT - 1), k0, BT))  // warp-uniform
         dkdv_pds<kAlibi, kSoftcap, true>(sr, dr, lse2, dl, fk, sk, base, j, qs, j < p.Nkv,
                                          causal_type, pp, dd);
       else
         dkdv_pds<kAlibi, kSoftcap, false>(sr, dr, lse2, dl, fk, sk, base, j, qs, true,
                                           causal_type, pp, dd);
-      tmem_st16(tS, pp);   // P^T, bf16 pairs, in this warpgroup's first 16 columns
-      tmem_st16(tDP, dd);  // dS^T
+      // buffer x was last read by the dV / dK MMAs of sub-step u - 2
+      if (u >= 2)
+        ok_all = __all_sync(0xffffffffu,
+                            mbar_wait(smem_u32(&bars->pd_free[x]), ((u >> 1) - 1) & 1, wc));
+      if (!ok_all) {
+        nb_sync(kNbKvP + x, kNbKvCount);
+        continue;
+      }
+      tmem_st8(tmem + lane_base + kv_col_pd(x) + wg * 8, pp);       // P^T, k-step wg
+      tmem_st8(tmem + lane_base + kv_col_pd(x) + 32 + wg * 8, dd);  // dS^T
       tmem_wait_st();
       tc_fence_before_sync();
-      nb_arrive(kNbP + x, kNbPCount);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->empty[s]));  // done with the stage's row data
+      nb_arrive(kNbKvP + x, kNbKvCount);
     }
     // ---------------------------------------------------------- epilogue
-    // pair 0 writes dV, pair 1 writes dK (times the softmax scale); warpgroup wg of
-    // the pair writes columns [wg * D/2, (wg + 1) * D/2)
+    // warpgroups 0 and 1 write the two halves of dV, 2 and 3 those of dK (times the
+    // softmax scale)
     const bool have =
         __all_sync(0xffffffffu, ok_all && mbar_wait(smem_u32(&bars->acc_full), 0, wc));
     tc_fence_after_sync();
+    const int which = wg >> 1, half = wg & 1;
     const size_t krow = (size_t)bg * p.Nkv + (j < p.Nkv ? j : 0);
-    const uint32_t tacc = tmem + lane_base + (pair == 0 ? colDV : colDK) + wg * (D / 2);
-    __nv_bfloat16* dst = (pair == 0 ? a.dv : a.dk) + krow * D + wg * (D / 2);
-    store_acc_row<D / 2>(tacc, pair == 0 ? 1.f : p.scale, dst, have, j < p.Nkv);
+    const uint32_t tacc = tmem + lane_base + (which ? colDK : colDV) + half * (D / 2);
+    __nv_bfloat16* dst = (which ? a.dk : a.dv) + krow * D + half * (D / 2);
+    store_acc_row<D / 2>(tacc, which ? p.scale : 1.f, dst, have, j < p.Nkv);
   }
   __syncwarp();
   tc_fence_before_sync();
@@ -577,9 +601,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == kLoadWarp) {
-    auto no_rows = [](int, float*, int, int) {};
     load_loop<D>(smem, bars, wc, lane, &maps.q128, &maps.do128, q0, bh, &maps.k64, &maps.v64,
-                 subs, slice, no_rows, false);
+                 subs, slice, nullptr, p.nq_pad);
   } else if (warp == kRelayWarp) {
     relay_loop(bars, wc, subs);
   } else if (warp == kMmaWarp) {
@@ -626,11 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
     float lse2 = INFINITY, dlt = 0.f;
     int fk = 0;
-    if (row_ok) {
-      const float l = a.lse[(size_t)bh * p.Nq + i];
-      lse2 = l == -INFINITY ? INFINITY : l * kLog2e;
-      dlt = a.delta[(size_t)bh * p.Nq + i];
-      fk = first_key(p.mask, i);
+    if (row_ok) {  // row terms of the row kernel (lse2 is already L log2 e, +inf if empty)
+      lse2 = a.rt.lse2[(size_t)bh * p.nq_pad + i];
+      dlt = a.rt.delta[(size_t)bh * p.nq_pad + i];
+      fk = a.rt.first[i];
     }
     const int last_key = (p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1));
     bool ok_all = true;
@@ -710,11 +732,11 @@ cudaError_t launch_d(const BwdArgs& ka, const BwdArgs& qa, const BwdMaps& maps, 
 
 }  // namespace
 
-cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const float* lse,
-                          const float* delta, __nv_bfloat16* dq, __nv_bfloat16* dk,
-                          __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st) {
-  BwdArgs ka{p, lse, delta, dq, dk, dv, ceil_div(p.Nkv, BT)};
-  BwdArgs qa{p, lse, delta, dq, dk, dv, ceil_div(p.Nq, BT)};
+cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
+                          __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
+                          bool run_dkdv, bool run_dq, cudaStream_t st) {
+  BwdArgs ka{p, rt, dq, dk, dv, ceil_div(p.Nkv, BT)};
+  BwdArgs qa{p, rt, dq, dk, dv, ceil_div(p.Nq, BT)};
   const long long gk = run_dkdv ? (long long)ka.n_tiles * p.B * p.Hkv : 0;
   const long long gq = run_dq ? (long long)qa.n_tiles * p.B * p.Hq : 0;
   if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;

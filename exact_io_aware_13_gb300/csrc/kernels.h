@@ -19,6 +19,20 @@ struct Problem {
   float softcap;      // c of the soft-cap
   MaskSpec mask;      // mask kind and parameters (doc offsets in device memory)
   int* status;        // device status word (bounded waits write DEV_TIMEOUT)
+  int nq_pad;         // Nq rounded up to a multiple of 128: row stride of the row terms
+};
+
+// Per-query-row terms of the backward, computed once by the row kernel and read by
+// the gradient kernels. Rows are padded per head to nq_pad, so that any 64-row chunk
+// of a 128-row query tile lies inside the arrays (the dK/dV kernel copies them in
+// 256-byte chunks); padding rows hold lse2 = +inf, delta = 0, first = INT_MAX.
+//   lse2[bh * nq_pad + i]  = L_i log2(e)  (+inf for a row that sees no key)
+//   delta[bh * nq_pad + i] = D_i = sum_c dO_ic O_ic
+//   first[i]               = first key row i may see (the mask's lower bound)
+struct RowTerms {
+  float* lse2;
+  float* delta;
+  int* first;
 };
 
 // ALiBi slope of query head h: 2^(-8 (h+1) / Hq).
@@ -33,10 +47,11 @@ cudaError_t launch_fwd_simt(const Problem& p, const __nv_bfloat16* q, const __nv
 cudaError_t launch_bwd_simt(const Problem& p, const __nv_bfloat16* q, const __nv_bfloat16* k,
                             const __nv_bfloat16* v, const float* lse, const __nv_bfloat16* dout,
                             const float* delta, __nv_bfloat16* dq, __nv_bfloat16* dk,
-                            __nv_bfloat16* dv, cudaStream_t st);
-// D_i = sum_c dO_ic * O_ic over every query row (fp32), the backward's row term.
+                            __nv_bfloat16* dv, cudaStream_t st);  // delta: RowTerms::delta
+// The row terms above for every (padded) query row, from O, dO and the forward's L.
 cudaError_t launch_bwd_rowdot(const Problem& p, const __nv_bfloat16* o,
-                              const __nv_bfloat16* dout, float* delta, cudaStream_t st);
+                              const __nv_bfloat16* dout, const float* lse, const RowTerms& rt,
+                              cudaStream_t st);
 // O = 0 and lse = -inf for `rows` rows (the answer when there are no keys).
 cudaError_t launch_fill_masked(long long rows, int d, __nv_bfloat16* o, float* lse,
                                cudaStream_t st);
@@ -51,8 +66,8 @@ cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtenso
 struct BwdMaps {
   CUtensorMap q128, do128, k128, v128, q64, do64, k64, v64;
 };
-cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const float* lse,
-                          const float* delta, __nv_bfloat16* dq, __nv_bfloat16* dk,
-                          __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st);
+cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
+                          __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
+                          bool run_dkdv, bool run_dq, cudaStream_t st);
 
 }  // namespace attn

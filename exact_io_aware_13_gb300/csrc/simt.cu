@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kRows) dq_simt_kernel(Problem p, const __nv_bf
     dof[c] = __bfloat162float(dout[row * D + c]);
     acc[c] = 0.f;
   }
-  const float L = lse[row], Di = delta[row];
+  const float L = lse[row], Di = delta[(size_t)bh * p.nq_pad + (row_ok ? i : 0)];
   const float slope = alibi_slope(h, p.Hq);
   const int fk = row_ok ? first_key(p.mask, i) : 0;
   const TileRange tr = kv_tiles_for_rows(p.mask, r0, kRows);
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kRows) dkdv_simt_kernel(Problem p, const __nv_
       if (threadIdx.x < kKeys) {
         const int i = i0 + threadIdx.x;
         ls[threadIdx.x] = i < p.Nq ? lse[qh + i] : -INFINITY;
-        dls[threadIdx.x] = i < p.Nq ? delta[qh + i] : 0.f;
+        dls[threadIdx.x] = i < p.Nq ? delta[(size_t)(b * p.Hq + h) * p.nq_pad + i] : 0.f;
       }
       __syncthreads();
       if (!key_ok) continue;
@@ -217,38 +217,52 @@ __global__ void __launch_bounds__(kRows) dkdv_simt_kernel(Problem p, const __nv_
   }
 }
 
-// D_i = sum_c dO_ic O_ic: one warp per row, 16-byte loads, fixed reduction order.
+// Row terms of the backward (see RowTerms): one warp per padded query row. D_i is the
+// dot product of the row's dO and O in a fixed order (16-byte loads, butterfly sum).
 template <int D>
-__global__ void __launch_bounds__(256) rowdot_kernel(long long rows, const __nv_bfloat16* o,
-                                                     const __nv_bfloat16* dout, float* delta) {
+__global__ void __launch_bounds__(256) rowdot_kernel(Problem p, long long rows,
+                                                     const __nv_bfloat16* o,
+                                                     const __nv_bfloat16* dout,
+                                                     const float* lse, RowTerms rt) {
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  constexpr int kPer = D / 32;  // elements per lane: 2 (d=64) or 4 (d=128)
-  const __nv_bfloat16* a = o + row * D + lane * kPer;
-  const __nv_bfloat16* bptr = dout + row * D + lane * kPer;
-  float s = 0.f;
-  if constexpr (kPer == 4) {
-    const uint2 av = *reinterpret_cast<const uint2*>(a);
-    const uint2 bv = *reinterpret_cast<const uint2*>(bptr);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+  const long long bh = row / p.nq_pad;
+  const int i = (int)(row - bh * p.nq_pad);
+  float s = 0.f, l2 = INFINITY;
+  if (i < p.Nq) {
+    const long long src = bh * p.Nq + i;
+    constexpr int kPer = D / 32;  // elements per lane: 2 (d=64) or 4 (d=128)
+    const __nv_bfloat16* a = o + src * D + lane * kPer;
+    const __nv_bfloat16* bptr = dout + src * D + lane * kPer;
+    if constexpr (kPer == 4) {
+      const uint2 av = *reinterpret_cast<const uint2*>(a);
+      const uint2 bv = *reinterpret_cast<const uint2*>(bptr);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const float2 x = __bfloat1622float2(a2[t]), y = __bfloat1622float2(b2[t]);
+      for (int t = 0; t < 2; ++t) {
+        const float2 x = __bfloat1622float2(a2[t]), y = __bfloat1622float2(b2[t]);
+        s = fmaf(x.x, y.x, s);
+        s = fmaf(x.y, y.y, s);
+      }
+    } else {
+      const __nv_bfloat162 av = *reinterpret_cast<const __nv_bfloat162*>(a);
+      const __nv_bfloat162 bv = *reinterpret_cast<const __nv_bfloat162*>(bptr);
+      const float2 x = __bfloat1622float2(av), y = __bfloat1622float2(bv);
       s = fmaf(x.x, y.x, s);
       s = fmaf(x.y, y.y, s);
     }
-  } else {
-    const __nv_bfloat162 av = *reinterpret_cast<const __nv_bfloat162*>(a);
-    const __nv_bfloat162 bv = *reinterpret_cast<const __nv_bfloat162*>(bptr);
-    const float2 x = __bfloat1622float2(av), y = __bfloat1622float2(bv);
-    s = fmaf(x.x, y.x, s);
-    s = fmaf(x.y, y.y, s);
-  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) delta[row] = s;
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    const float L = lse[src];
+    l2 = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
+  }
+  if (lane == 0) {
+    rt.delta[row] = s;
+    rt.lse2[row] = l2;
+    if (bh == 0) rt.first[i] = i < p.Nq ? first_key(p.mask, i) : 0x7fffffff;
+  }
 }
 
 // Rows with no key at all: O = 0, lse = -inf.
@@ -301,12 +315,14 @@ cudaError_t launch_bwd_simt(const Problem& p, const __nv_bfloat16* q, const __nv
 }
 
 cudaError_t launch_bwd_rowdot(const Problem& p, const __nv_bfloat16* o,
-                              const __nv_bfloat16* dout, float* delta, cudaStream_t st) {
-  const long long rows = (long long)p.B * p.Hq * p.Nq;
+                              const __nv_bfloat16* dout, const float* lse, const RowTerms& rt,
+                              cudaStream_t st) {
+  const long long rows = (long long)p.B * p.Hq * p.nq_pad;
   if (rows == 0) return cudaSuccess;
-  const unsigned blocks = (unsigned)((rows + 7) / 8);
-  if (p.d == 64) rowdot_kernel<64><<<blocks, 256, 0, st>>>(rows, o, dout, delta);
-  else rowdot_kernel<128><<<blocks, 256, 0, st>>>(rows, o, dout, delta);
+  const long long blocks = (rows + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (p.d == 64) rowdot_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
+  else rowdot_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
   return cudaGetLastError();
 }
 

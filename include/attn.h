@@ -110,7 +110,14 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      int score_kind, const attn_score_params* score_params,
                      void* stream);
 
-/* Bytes of device workspace attn_bwd needs for these sizes (a multiple of 256). */
+/*
+ * Bytes of device workspace attn_bwd needs for these sizes (a multiple of 256): the
+ * backward's per-query-row terms, computed by its first kernel. With
+ * Nq128 = Nq rounded up to a multiple of 128 and R = B * Hq * Nq128, that is
+ * 2 * round256(4 R) + round256(4 Nq128): L log2 e and D_i (one float each per padded
+ * row) and each row's first allowed key (one int32 per padded row position).
+ * 0 when B, Hq or Nq is 0.
+ */
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d);
 
 /*
@@ -132,16 +139,17 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
 
 /* Kernels of the backward pass, for attn_bwd_phases. */
 enum {
-  ATTN_BWD_ROWDOT = 1,   /* D = rowsum(dO o O) into the workspace */
-  ATTN_BWD_DKDV = 2,     /* dK and dV (reads D) */
-  ATTN_BWD_DQ = 4,       /* dQ (reads D) */
+  ATTN_BWD_ROWDOT = 1,   /* row terms into the workspace: D = rowsum(dO o O), L log2 e,
+                            first allowed key */
+  ATTN_BWD_DKDV = 2,     /* dK and dV (reads the row terms) */
+  ATTN_BWD_DQ = 4,       /* dQ (reads the row terms) */
   ATTN_BWD_ALL = 7
 };
 
 /*
  * attn_bwd split into its kernels: runs the ones named in `phases`, in the order
- * ROWDOT, DKDV, DQ, with attn_bwd's arguments and checks. DKDV and DQ read D from
- * the workspace, so ROWDOT must have run on the same workspace and inputs before
+ * ROWDOT, DKDV, DQ, with attn_bwd's arguments and checks. DKDV and DQ read the row
+ * terms from the workspace, so ROWDOT must have run on the same workspace and inputs before
  * them (in this call or an earlier one in stream order). DKDV and DQ do not depend
  * on each other: a caller may time them separately or put them on two streams.
  * attn_bwd(...) is attn_bwd_phases(ATTN_BWD_ALL, ...).
@@ -161,13 +169,15 @@ attn_status attn_bwd_phases(int phases, const void* q, const void* k, const void
  * for example a host program whose device memory is already handed out in full to
  * another allocator, or a runtime that forbids new allocations once it has started.
  * Such a caller still owns and passes every input and output, exactly as for
- * attn_bwd; only the backward's scratch (one fp32 row term per query row) lives in
- * a fixed array inside this library instead of a caller workspace.
+ * attn_bwd; only the backward's scratch (the per-query-row terms that
+ * attn_bwd_workspace_size counts) lives in a fixed array inside this library instead
+ * of a caller workspace.
  *
- * - The array holds ATTN_STATIC_WORKSPACE_ROWS floats (8 MiB) on every device that
- *   loads the library, for the life of the process. B * Hq * Nq must not exceed
- *   ATTN_STATIC_WORKSPACE_ROWS; larger problems return ATTN_ERR_WORKSPACE and
- *   launch nothing (use attn_bwd with a workspace for them).
+ * - The array holds 3 * ATTN_STATIC_WORKSPACE_ROWS 4-byte words (24 MiB) on every
+ *   device that loads the library, for the life of the process. B * Hq * Nq128 (Nq
+ *   rounded up to a multiple of 128) must not exceed ATTN_STATIC_WORKSPACE_ROWS;
+ *   larger problems return ATTN_ERR_WORKSPACE and launch nothing (use attn_bwd with a
+ *   workspace for them).
  * - The first call on a device looks up the array's device address with that device
  *   current (a one-time set-up per device); make that first call before any stream
  *   capture on the device.

@@ -64,10 +64,20 @@ def test_empty_problems_are_a_no_op(lib):
     assert lib.attn_bwd_workspace_size(0, 4, 4, 128, 128, 64) == 0
 
 
+def _round256(x):
+    return (x + 255) // 256 * 256
+
+
 def test_workspace_size(lib):
-    # one fp32 row term per query row, rounded up to 256 bytes
-    assert lib.attn_bwd_workspace_size(2, 16, 16, 8192, 8192, 128) == 2 * 16 * 8192 * 4
-    assert lib.attn_bwd_workspace_size(1, 1, 1, 3, 3, 64) == 256
+    # L log2 e and D per row padded to 128 rows per head, plus one first-key int per
+    # padded row position; each array rounded up to 256 bytes
+    def expect(B, Hq, Nq):
+        nq128 = (Nq + 127) // 128 * 128
+        return 2 * _round256(4 * B * Hq * nq128) + _round256(4 * nq128)
+    assert lib.attn_bwd_workspace_size(2, 16, 16, 8192, 8192, 128) == expect(2, 16, 8192)
+    assert expect(2, 16, 8192) == 2 * 2 * 16 * 8192 * 4 + 8192 * 4
+    assert lib.attn_bwd_workspace_size(1, 1, 1, 3, 3, 64) == 3 * 512
+    assert lib.attn_bwd_workspace_size(3, 5, 5, 700, 700, 64) == expect(3, 5, 700)
     rc = lib.attn_bwd(*([ctypes.c_void_p(4096)] * 9), 1, 1, 1, 128, 128, 64,
                       ctypes.c_float(0.1), 0, None, 0, None, None, 0, None)
     assert rc == 5  # ATTN_ERR_WORKSPACE

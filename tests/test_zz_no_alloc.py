@@ -74,9 +74,9 @@ def test_static_workspace_rejects_oversized_problems(lib):
     from exact_io_aware_13_gb300 import _lib
     rows_max = 1 << 21
     dummy = ctypes.c_void_p(256)
-    # B * Hq * Nq = 2 * 16 * 65537 > 2^21: refused before any pointer is touched
+    # B * Hq * Nq128 = 2 * 16 * 65664 > 2^21: refused before any pointer is touched
     rc = lib.attn_bwd_static_workspace(*([dummy] * 9), 2, 16, 16, 65537, 65537, 128,
                                        ctypes.c_float(0.1), 0, None, 0, None, None)
-    assert rc == 5 and 2 * 16 * 65537 > rows_max  # ATTN_ERR_WORKSPACE
+    assert rc == 5 and 2 * 16 * 65664 > rows_max  # ATTN_ERR_WORKSPACE
     assert "workspace" in lib.attn_strerror(rc).decode()
     assert _lib.header_functions().count("attn_bwd_static_workspace") == 1
