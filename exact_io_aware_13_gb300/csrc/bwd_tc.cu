@@ -46,10 +46,17 @@ constexpr int kRelayWarp = kEwWarps + 2;  // turns TMA completions into barrier 
 //   dq:   kNbP + x     dS_x written to TMEM: pair x (256 threads) + MMA warp (32)
 //   dkdv: kNbKvRel     S^T / dP^T of the sub-step read: element-wise warps + MMA warp
 //         kNbKvP + x   P^T / dS^T of a sub-step u (x = u % 2) written: same threads
+//         kNbKvK       K tile written to tensor memory: same threads
 constexpr uint32_t kNbP = 1, kNbPCount = 288;
 constexpr uint32_t kNbStage = 3, kNbStageCount = 64;
-constexpr uint32_t kNbKvRel = 7, kNbKvP = 8, kNbKvCount = (kEwWarps + 1) * 32;
-constexpr int kStages = 4;       // ring depth, in sub-steps
+constexpr uint32_t kNbKvRel = 8, kNbKvP = 9, kNbKvK = 11, kNbKvCount = (kEwWarps + 1) * 32;
+constexpr int kStagesQ = 4;      // dq ring depth, in sub-steps
+constexpr int kStagesKv = 5;     // dkdv ring depth
+constexpr int kMaxStages = 5;
+// Stage barriers take IDs kNbStage .. kNbStage + kMaxStages - 1; the others must not
+// overlap them (one hardware barrier, one thread count), and IDs end at 15.
+static_assert(kNbStage + kMaxStages <= kNbKvRel && kNbP + 2 <= kNbStage && kNbKvK < 16,
+              "named barrier IDs");
 constexpr int kHeadGroup = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -57,10 +64,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 __device__ __forceinline__ uint32_t col_s(int x) { return x * 64; }
 __device__ __forceinline__ uint32_t col_dp(int x) { return 128 + x * 64; }
 constexpr uint32_t kColAcc = 256;
-// Tensor memory columns of dkdv: S^T, dP^T (64 each, one buffer), two P^T / dS^T
-// buffers (bf16 pairs: P^T in the first 32 columns, dS^T in the next 32), dV, dK.
-constexpr uint32_t kKvColS = 0, kKvColDP = 64, kKvColAcc = 256;
-__device__ __forceinline__ uint32_t kv_col_pd(int x) { return 128 + x * 64; }
+// Tensor memory columns of dkdv: S^T, dP^T (64 each), P^T / dS^T (bf16 pairs: P^T in
+// the first 32 columns, dS^T in the next 32), the K tile (bf16 pairs, A operand of
+// S^T = K Q^T), then dV and dK.
+constexpr uint32_t kKvColS = 0, kKvColDP = 64, kKvColPD = 128, kKvColK = 192, kKvColAcc = 256;
 
 // Element-wise constants: s2 = x*k1 + kb*(j - i) (log2 units), then the soft-cap.
 struct ScoreK {
@@ -163,31 +170,37 @@ __device__ __forceinline__ void dq_ds(const uint32_t (&sr)[32], const uint32_t (
   }
 }
 
-// Shared-memory layout shared by both kernels: two fixed 128-row tiles, a ring of
-// kStages stages, each holding a 64-row slice of two operands, and (dkdv only) the
-// row terms of each stage's 64 query rows: lse2, delta, first key, 256 bytes each.
-template <int D>
+// Shared-memory layouts. dq: the CTA's Q and dO tiles (fixed), then a ring of kS
+// stages, each holding a 64-row slice of K and V. dkdv: the V tile (fixed; K lives in
+// tensor memory), a ring of 64-row slices of Q and dO, and each stage's row terms of
+// those 64 query rows (lse2, delta, first key: 256 bytes each).
+template <int D, int kS, int kFixTiles, bool kRowTerms>
 struct Layout {
+  static constexpr int kStageCount = kS;
   static constexpr int kFixChunk = BT * 128;        // 64-column slab of a fixed tile
   static constexpr int kFixTile = BT * D * 2;
   static constexpr int kSubChunk = SUB * 128;       // 64-column slab of a stage slice
   static constexpr int kSubTile = SUB * D * 2;
   static constexpr int kFixA = 0;
-  static constexpr int kFixB = kFixTile;
-  static constexpr int kRing = 2 * kFixTile;
+  static constexpr int kFixB = kFixTile;            // dq only
+  static constexpr int kRing = kFixTiles * kFixTile;
   static constexpr int kStage = 2 * kSubTile;
-  static constexpr int kRows = kRing + kStages * kStage;  // per stage: lse2, delta, first key
+  static constexpr int kRows = kRing + kS * kStage;
   static constexpr int kRowStage = 3 * SUB * 4;
-  static constexpr int kBars = kRows + kStages * kRowStage;
+  static constexpr int kBars = kRows + (kRowTerms ? kS * kRowStage : 0);
   static constexpr int kAlloc = kBars + 256 + 1024;
 };
+template <int D> using LayoutQ = Layout<D, kStagesQ, 2, false>;
+template <int D> using LayoutKv = Layout<D, kStagesKv, 1, true>;
+static_assert(LayoutKv<128>::kAlloc <= 232448 && LayoutQ<128>::kAlloc <= 232448,
+              "shared memory per CTA");
 
 struct BwdBars {
   uint64_t fixed_full;             // the two fixed tiles
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t s_full[2];              // S_x and dP_x in TMEM (dkdv: buffer 0 only)
-  uint64_t pd_free[2];             // dkdv: P^T / dS^T buffer x read by its MMAs
+  uint64_t pd_free[2];             // dkdv: P^T / dS^T read by their MMAs (entry 0)
   uint64_t acc_full;               // accumulators final
   uint32_t tmem_base;
   int abort_flag;
@@ -196,6 +209,7 @@ struct BwdBars {
 struct BwdArgs {
   Problem p;
   RowTerms rt;
+  const __nv_bfloat16* k;  // K [B, Hkv, Nkv, d] (dkdv copies its tile into tensor memory)
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -215,12 +229,11 @@ __device__ __forceinline__ void cta_tile(int heads, int n_tiles, bool reverse, i
   head = grp * kHeadGroup + rem % gh;
 }
 
-__device__ __forceinline__ void setup_common(BwdBars* bars, uint32_t stage_full_count,
-                                             uint32_t stage_empty_count) {
+__device__ __forceinline__ void setup_common(BwdBars* bars, int stages) {
   mbar_init(smem_u32(&bars->fixed_full), 1);
-  for (int s = 0; s < kStages; ++s) {
-    mbar_init(smem_u32(&bars->full[s]), stage_full_count);
-    mbar_init(smem_u32(&bars->empty[s]), stage_empty_count);
+  for (int s = 0; s < stages; ++s) {
+    mbar_init(smem_u32(&bars->full[s]), 1);   // the loader's arrive + transaction bytes
+    mbar_init(smem_u32(&bars->empty[s]), 1);  // one MMA commit
   }
   for (int x = 0; x < 2; ++x) {
     mbar_init(smem_u32(&bars->s_full[x]), 1);
@@ -259,6 +272,21 @@ __device__ __forceinline__ void mma_tmem64_x_slice(bool pred, uint32_t d_tmem, u
     const uint32_t acol = (kk < 2) ? kk * 8 : 32 + (kk - 2) * 8;
     mma_ts_if(pred, d_tmem, a_tmem + acol, db + ((kk * 16 * 128) >> 4), id,
            (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// D[128 x 64] = A_tmem[128 x D] B^T with A in tensor memory as bf16 pairs (k-step kk,
+// 16 of the head dimension, in columns [8 kk, 8 kk + 8)) and B a 64-row K-major stage
+// slice.
+template <int D>
+__device__ __forceinline__ void mma_tmem_x64(bool pred, uint32_t d_tmem, uint32_t a_tmem,
+                                             uint32_t b) {
+  constexpr uint32_t id = idesc_bf16_f32(BT, SUB, false, false);
+  const uint64_t db = smem_desc_sw128(b, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t ob = ((kk >> 2) * (SUB * 128) + (kk & 3) * 32) >> 4;
+    mma_ts_if(pred, d_tmem, a_tmem + kk * 8, db + ob, id, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -307,30 +335,31 @@ __device__ __forceinline__ void store_acc_row(uint32_t t, float mul, __nv_bfloat
   }
 }
 
-// Loads the two fixed tiles (rows r0.. of head z) and then, for every sub-step u,
-// the 64-row slices of the two streamed operands into stage u % kStages. `slice`
+// Loads the fixed tiles (fa, and fb if given; rows r0.. of head z) and then, for
+// every sub-step u, the 64-row slices of the two streamed operands into stage
+// u % L::kStageCount. `slice`
 // gives (row, head) of sub-step u. With `rt` (dkdv) it also copies the row terms of
 // those 64 query rows into the stage's row block; all of it completes full[s].
-template <int D, typename SliceFn>
+template <int D, class L, typename SliceFn>
 __device__ __forceinline__ void load_loop(uint8_t* smem, BwdBars* bars, const WaitCtx& wc,
                                           int lane, const CUtensorMap* fa, const CUtensorMap* fb,
                                           int r0, int z, const CUtensorMap* sa,
                                           const CUtensorMap* sb, int subs, SliceFn slice,
                                           const RowTerms* rt, int nq_pad) {
-  using L = Layout<D>;
+  constexpr int kS = L::kStageCount;
   if (lane == 0) {
     tma_prefetch_desc(sa);
     tma_prefetch_desc(sb);
     const uint32_t bar = smem_u32(&bars->fixed_full);
-    mbar_arrive_expect_tx(bar, 2 * L::kFixTile);
+    mbar_arrive_expect_tx(bar, (fb ? 2 : 1) * L::kFixTile);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
       tma_load_3d(smem_u32(smem + L::kFixA + c * L::kFixChunk), fa, bar, c * 64, r0, z);
-      tma_load_3d(smem_u32(smem + L::kFixB + c * L::kFixChunk), fb, bar, c * 64, r0, z);
+      if (fb) tma_load_3d(smem_u32(smem + L::kFixB + c * L::kFixChunk), fb, bar, c * 64, r0, z);
     }
   }
   for (int u = 0; u < subs; ++u) {
-    const int s = u % kStages, use = u / kStages;
+    const int s = u % kS, use = u / kS;
     int row, head;
     slice(u, row, head);
     bool ok = true;
@@ -356,19 +385,20 @@ __device__ __forceinline__ void load_loop(uint8_t* smem, BwdBars* bars, const Wa
   }
   if (lane == 0) {  // let in-flight copies land before the CTA can exit
     mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
-    for (int u = imax(0, subs - kStages); u < subs; ++u)
-      mbar_wait(smem_u32(&bars->full[u % kStages]), (u / kStages) & 1, wc);
+    for (int u = imax(0, subs - kS); u < subs; ++u)
+      mbar_wait(smem_u32(&bars->full[u % kS]), (u / kS) & 1, wc);
   }
 }
 
-// Relay warp: after the bytes of ring use u land (full[u % kStages]), arrive on that
+// Relay warp: after the bytes of ring use u land (full[u % kS]), arrive on that
 // stage's named barrier for the MMA warp; after an abort, rendezvous instead.
+template <int kS>
 __device__ __forceinline__ void relay_loop(BwdBars* bars, const WaitCtx& wc, int subs) {
   bool live = true;
   for (int u = 0; u < subs; ++u) {
-    const int s = u % kStages;
+    const int s = u % kS;
     if (live)
-      live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc));
+      live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (u / kS) & 1, wc));
     if (live) nb_arrive(kNbStage + s, kNbStageCount);
     else nb_sync(kNbStage + s, kNbStageCount);
   }
@@ -378,7 +408,7 @@ __device__ __forceinline__ void relay_loop(BwdBars* bars, const WaitCtx& wc, int
 template <int D, bool kAlibi, bool kSoftcap>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
-  using L = Layout<D>;
+  using L = LayoutKv<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -412,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   WaitCtx wc{&bars->abort_flag, p.status};
-  if (threadIdx.x == 0) setup_common(bars, 1, 1);
+  if (threadIdx.x == 0) setup_common(bars, L::kStageCount);
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
     tmem_relinquish();
@@ -424,10 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t colDV = kKvColAcc, colDK = kKvColAcc + D;
 
   if (warp == kLoadWarp) {
-    load_loop<D>(smem, bars, wc, lane, &maps.k128, &maps.v128, k0, bg, &maps.q64, &maps.do64,
-                 subs, slice, &a.rt, p.nq_pad);
+    load_loop<D, L>(smem, bars, wc, lane, &maps.v128, nullptr, k0, bg, &maps.q64, &maps.do64,
+                    subs, slice, &a.rt, p.nq_pad);
   } else if (warp == kRelayWarp) {
-    relay_loop(bars, wc, subs);
+    relay_loop<L::kStageCount>(bars, wc, subs);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp walks the schedule and waits on named barriers; every lane executes
@@ -439,35 +469,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // element-wise warps have read S^T/dP^T(u), and dV/dK(u) once P^T/dS^T(u) are
     // written. The tensor pipe thus runs S^T/dP^T(u+1) and dV/dK(u-1) while the
     // element-wise warps work on u.
-    const uint32_t sK = smem_u32(smem + L::kFixA), sV = smem_u32(smem + L::kFixB);
+    const uint32_t sV = smem_u32(smem + L::kFixA);
     const uint32_t ring = smem_u32(smem + L::kRing);
     const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc));
     const bool issuer = elect_one();
+    nb_sync(kNbKvK, kNbKvCount);  // K tile in tensor memory
     auto issue_sdp = [&](int v) {  // S^T and dP^T of sub-step v
-      const int s = v % kStages;
+      const int s = v % L::kStageCount;
       nb_sync(kNbStage + s, kNbStageCount);
       tc_fence_after_sync();
       if (!ok) return;
       const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
-      mma_128x64<D>(issuer, tmem + kKvColS, sK, sQ);    // S^T = K Q^T
-      mma_128x64<D>(issuer, tmem + kKvColDP, sV, sDO);  // dP^T = V dO^T
+      mma_tmem_x64<D>(issuer, tmem + kKvColS, tmem + kKvColK, sQ);  // S^T = K Q^T
+      mma_128x64<D>(issuer, tmem + kKvColDP, sV, sDO);              // dP^T = V dO^T
       mma_commit_if(issuer, smem_u32(&bars->s_full[0]));
     };
     issue_sdp(0);
     for (int u = 0; u < subs; ++u) {
-      const int s = u % kStages, x = u & 1;
+      const int s = u % L::kStageCount, x = u & 1;
       if (u + 1 < subs) {
         nb_sync(kNbKvRel, kNbKvCount);  // S^T / dP^T(u) are in registers
         issue_sdp(u + 1);
       }
-      nb_sync(kNbKvP + x, kNbKvCount);  // P^T / dS^T(u) in buffer x
+      nb_sync(kNbKvP + x, kNbKvCount);  // P^T / dS^T(u) written
       tc_fence_after_sync();
       if (ok) {
         const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
-        mma_pd_x_slice<D>(issuer, tmem + colDV, tmem + kv_col_pd(x), sDO, u > 0);       // dV += P^T dO
-        mma_pd_x_slice<D>(issuer, tmem + colDK, tmem + kv_col_pd(x) + 32, sQ, u > 0);  // dK += dS^T Q
+        mma_pd_x_slice<D>(issuer, tmem + colDV, tmem + kKvColPD, sDO, u > 0);       // dV += P^T dO
+        mma_pd_x_slice<D>(issuer, tmem + colDK, tmem + kKvColPD + 32, sQ, u > 0);  // dK += dS^T Q
         mma_commit_if(issuer, smem_u32(&bars->empty[s]));    // stage (and its row terms) free
-        mma_commit_if(issuer, smem_u32(&bars->pd_free[x]));  // buffer x free
+        mma_commit_if(issuer, smem_u32(&bars->pd_free[0]));  // P^T / dS^T free
       }
     }
     if (ok) mma_commit_if(issuer, smem_u32(&bars->acc_full));
@@ -480,9 +511,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const int c0 = wg * 16;
     const bool causal_type = p.mask.kind != ATTN_MASK_NONE;
+    {
+      // K rows of the tile into tensor memory (A operand of S^T = K Q^T): this thread's
+      // key row, head-dimension columns [wg D/4, (wg + 1) D/4) as bf16 pairs.
+      constexpr int kW = D / 8;  // 32-bit words per thread
+      uint32_t kr[kW];
+      if (j < p.Nkv) {
+        const uint4* src =
+            reinterpret_cast<const uint4*>(a.k + ((size_t)bg * p.Nkv + j) * D + wg * (D / 4));
+#pragma unroll
+        for (int e = 0; e < kW / 4; ++e) {
+          const uint4 w = src[e];
+          kr[4 * e] = w.x; kr[4 * e + 1] = w.y; kr[4 * e + 2] = w.z; kr[4 * e + 3] = w.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kW; ++e) kr[e] = 0u;
+      }
+      if constexpr (kW == 16) tmem_st16(tmem + lane_base + kKvColK + wg * kW, kr);
+      else tmem_st8(tmem + lane_base + kKvColK + wg * kW, kr);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      nb_arrive(kNbKvK, kNbKvCount);
+    }
     bool ok_all = true;
     for (int u = 0; u < subs; ++u) {
-      const int s = u % kStages, x = u & 1;
+      const int s = u % L::kStageCount, x = u & 1;
       const bool rel = u + 1 < subs;  // the MMA warp waits for this release before u + 1
       int qrow, bh;
       slice(u, qrow, bh);
@@ -493,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[0]), u & 1, wc));
       // the stage's row terms arrived with full[s]; observe them
       if (ok_all)
-        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (u / kStages) & 1, wc));
+        ok_all = __all_sync(0xffffffffu,
+                            mbar_wait(smem_u32(&bars->full[s]), (u / L::kStageCount) & 1, wc));
       if (!ok_all) {  // aborted: keep the barrier schedule with the MMA warp
         if (rel) nb_sync(kNbKvRel, kNbKvCount);
         nb_sync(kNbKvP + x, kNbKvCount);
@@ -519,16 +574,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         dkdv_pds<kAlibi, kSoftcap, false>(sr, dr, lse2, dl, fk, sk, base, j, qs, true,
                                           causal_type, pp, dd);
-      // buffer x was last read by the dV / dK MMAs of sub-step u - 2
-      if (u >= 2)
-        ok_all = __all_sync(0xffffffffu,
-                            mbar_wait(smem_u32(&bars->pd_free[x]), ((u >> 1) - 1) & 1, wc));
+      // P^T / dS^T of sub-step u - 1 must have been read by their MMAs
+      if (u >= 1)
+        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pd_free[0]), (u - 1) & 1, wc));
       if (!ok_all) {
         nb_sync(kNbKvP + x, kNbKvCount);
         continue;
       }
-      tmem_st8(tmem + lane_base + kv_col_pd(x) + wg * 8, pp);       // P^T, k-step wg
-      tmem_st8(tmem + lane_base + kv_col_pd(x) + 32 + wg * 8, dd);  // dS^T
+      tmem_st8(tmem + lane_base + kKvColPD + wg * 8, pp);       // P^T, k-step wg
+      tmem_st8(tmem + lane_base + kKvColPD + 32 + wg * 8, dd);  // dS^T
       tmem_wait_st();
       tc_fence_before_sync();
       nb_arrive(kNbKvP + x, kNbKvCount);
@@ -558,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool kAlibi, bool kSoftcap>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
-  using L = Layout<D>;
+  using L = LayoutQ<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -590,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   WaitCtx wc{&bars->abort_flag, p.status};
-  if (threadIdx.x == 0) setup_common(bars, 1, 1);
+  if (threadIdx.x == 0) setup_common(bars, L::kStageCount);
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
     tmem_relinquish();
@@ -601,10 +655,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == kLoadWarp) {
-    load_loop<D>(smem, bars, wc, lane, &maps.q128, &maps.do128, q0, bh, &maps.k64, &maps.v64,
+    load_loop<D, L>(smem, bars, wc, lane, &maps.q128, &maps.do128, q0, bh, &maps.k64, &maps.v64,
                  subs, slice, nullptr, p.nq_pad);
   } else if (warp == kRelayWarp) {
-    relay_loop(bars, wc, subs);
+    relay_loop<L::kStageCount>(bars, wc, subs);
   } else if (warp == kMmaWarp) {
     // Same issue scheme as the dK/dV kernel: named barriers only, MMAs predicated on the
     // elect.sync lane, nothing issued if the fixed tiles never arrive.
@@ -614,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool issuer = elect_one();
     // S and dP of sub-step u into buffer u & 1
     auto issue_sdp = [&](int u) {
-      const int s = u % kStages, x = u & 1;
+      const int s = u % L::kStageCount, x = u & 1;
       nb_sync(kNbStage + s, kNbStageCount);
       tc_fence_after_sync();
       const uint32_t sK = ring + s * L::kStage, sV = sK + L::kSubTile;
@@ -626,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     issue_sdp(0);
     if (subs > 1) issue_sdp(1);
     for (int u = 0; u < subs; ++u) {
-      const int s = u % kStages, x = u & 1;
+      const int s = u % L::kStageCount, x = u & 1;
       nb_sync(kNbP + x, kNbPCount);
       tc_fence_after_sync();
       const uint32_t sK = ring + s * L::kStage;
@@ -709,14 +763,14 @@ cudaError_t launch_variant(const BwdArgs& kv_args, const BwdArgs& q_args, const 
                            int grid_kv, int grid_q, cudaStream_t st) {
   auto k1 = dkdv_kernel<D, kA, kS>;
   auto k2 = dq_kernel<D, kA, kS>;
-  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Layout<D>::kAlloc);
+  constexpr int kSmemKv = LayoutKv<D>::kAlloc, kSmemQ = LayoutQ<D>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKv);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::kAlloc);
+  e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ);
   if (e != cudaSuccess) return e;
-  if (grid_kv > 0) k1<<<grid_kv, kThreads, Layout<D>::kAlloc, st>>>(maps, kv_args);
+  if (grid_kv > 0) k1<<<grid_kv, kThreads, kSmemKv, st>>>(maps, kv_args);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (grid_q > 0) k2<<<grid_q, kThreads, Layout<D>::kAlloc, st>>>(maps, q_args);
+  if (grid_q > 0) k2<<<grid_q, kThreads, kSmemQ, st>>>(maps, q_args);
   return cudaGetLastError();
 }
 
@@ -733,10 +787,11 @@ cudaError_t launch_d(const BwdArgs& ka, const BwdArgs& qa, const BwdMaps& maps, 
 }  // namespace
 
 cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
-                          __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
+                          const __nv_bfloat16* k, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                          __nv_bfloat16* dv,
                           bool run_dkdv, bool run_dq, cudaStream_t st) {
-  BwdArgs ka{p, rt, dq, dk, dv, ceil_div(p.Nkv, BT)};
-  BwdArgs qa{p, rt, dq, dk, dv, ceil_div(p.Nq, BT)};
+  BwdArgs ka{p, rt, k, dq, dk, dv, ceil_div(p.Nkv, BT)};
+  BwdArgs qa{p, rt, k, dq, dk, dv, ceil_div(p.Nq, BT)};
   const long long gk = run_dkdv ? (long long)ka.n_tiles * p.B * p.Hkv : 0;
   const long long gq = run_dq ? (long long)qa.n_tiles * p.B * p.Hq : 0;
   if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;

@@ -61,13 +61,13 @@ cudaError_t launch_classify(const MaskSpec& m, int32_t* classes, cudaStream_t st
 cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, __nv_bfloat16* o, float* lse,
                           cudaStream_t st);
-// Tensor maps of the backward: 128-row boxes (tiles a CTA loads once) and 64-row
-// boxes (tiles it streams), for q, dout, k and v.
+// Tensor maps of the backward: 128-row boxes (tiles a CTA loads once: Q and dO for dq,
+// V for dK/dV) and 64-row boxes (tiles it streams).
 struct BwdMaps {
-  CUtensorMap q128, do128, k128, v128, q64, do64, k64, v64;
+  CUtensorMap q128, do128, v128, q64, do64, k64, v64;
 };
 cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
-                          __nv_bfloat16* dq, __nv_bfloat16* dk, __nv_bfloat16* dv,
-                          bool run_dkdv, bool run_dq, cudaStream_t st);
+                          const __nv_bfloat16* k, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                          __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st);
 
 }  // namespace attn
