@@ -3,11 +3,14 @@ online softmax, backward rebuilding P from the LSE) on the causal fwd+bwd worklo
 (B=2, H=16, N=8192, d=128, bf16), timed with CUDA events.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload fwd_bwd|causal_fwd|gqa_window_fwd|docs_fwd|tiny_fwd]
 
 Prints one JSON line. `value` is useful TFLOP/s (masked-out work excluded) summed
 over ranks; with N > 1 each rank runs its own replica of the workload (the heads
 are independent, so there is no data-path collective). --impl reference times the
 float64 CPU oracle on a bounded sample of the same workload on the host cores.
+--workload picks one of the other workloads; those are forward-only, so a step is
+one forward pass and the line reports the forward's useful TFLOP/s.
 """
 from __future__ import annotations
 
@@ -26,7 +29,11 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import CAUSAL_FWD_BWD, make_inputs  # noqa: E402
+from workloads import (CAUSAL, CAUSAL_FWD_BWD, DOCS, GQA_WINDOW, MASK_NAMES, TINY,  # noqa: E402
+                       make_inputs)
+
+FWD_WORKLOADS = {"causal_fwd": CAUSAL, "gqa_window_fwd": GQA_WINDOW, "docs_fwd": DOCS,
+                 "tiny_fwd": TINY}
 
 METRIC = "attention fwd/bwd TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 peak"
 UNIT = "TFLOP/s"
@@ -148,9 +155,11 @@ def dist_env():
 
 
 def workload_config(w, extra=None):
+    n_in = 4 if w.backward else 3  # q, k, v (and dO)
+    mib = (n_in - 2) * w.B * w.Hq * w.Nq * w.d * 2 + 2 * w.B * w.Hkv * w.Nkv * w.d * 2
     cfg = {"workload": w.describe(), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.Nq, "d": w.d,
-           "mask": "causal", "seed": w.seed,
-           "l2": "flushed between steps (256 MiB write); inputs 256 MiB > L2"}
+           "mask": MASK_NAMES[w.mask_kind], "seed": w.seed,
+           "l2": f"flushed between steps (256 MiB write); inputs {mib >> 20} MiB"}
     if extra:
         cfg.update(extra)
     return cfg
@@ -257,7 +266,8 @@ def run_ours(args):
     algo = {"fwd_tc_kernel": (4 * w.d * units, "TFLOP/s"),
             "dkdv_kernel": (8 * w.d * units, "TFLOP/s"),
             "dq_kernel": (6 * w.d * units, "TFLOP/s"),
-            "rowdot_kernel": (w.B * w.Hq * w.Nq * (4 * w.d + 4), "GB/s")}
+            # reads O, dO and L; writes L log2 e and D
+            "rowdot_kernel": (w.B * w.Hq * w.Nq * (4 * w.d + 12), "GB/s")}
     kernels = {}
     for n in names:
         ms = statistics.mean(per_kernel[n])
@@ -293,6 +303,101 @@ def run_ours(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_forward(args, w):
+    """Forward-only workloads: a step is one attn_fwd over the whole workload."""
+    from exact_io_aware_13_gb300 import build as libbuild
+    libbuild.build()
+    import exact_io_aware_13_gb300 as ea
+    from exact_io_aware_13_gb300 import flops
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v, _, offs = make_inputs(w, with_dout=False)
+    pairs = flops.allowed_pairs(w.mask_kind, w.Nq, w.Nkv, w.window, offs)
+    f_fwd = flops.attention_flops(w.B, w.Hq, w.d, pairs, backward=False)
+    host = [t.pin_memory() for t in (q, k, v)]
+    qd, kd, vd = (t.to(dev) for t in host)
+    dt = None if offs is None else torch.from_numpy(np.asarray(offs, dtype=np.int32)).to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[:-1], dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    kw = dict(scale=w.scale, mask_kind=w.mask_kind, window=w.window, doc_offsets=dt,
+              score_kind=w.score_kind, softcap=w.softcap)
+    for _ in range(args.warmup):
+        ea.fwd_into(qd, kd, vd, o, lse, **kw)
+    torch.cuda.synchronize()
+    if ea.device_status() != 0:
+        raise RuntimeError("a kernel gave up a bounded wait during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(args.steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            ea.fwd_into(qd, kd, vd, o, lse, **kw)
+            ev[s][1].record(stream)
+        torch.cuda.synchronize()
+    if ea.device_status() != 0:
+        raise RuntimeError("a kernel gave up a bounded wait during the timed steps")
+    times = [e[0].elapsed_time(e[1]) for e in ev]
+    t_all = sum(times)
+    if world > 1:
+        t_all = max_over_ranks(t_all, dev)
+    ms_step = t_all / args.steps
+    value = world * f_fwd / (ms_step * 1e-3) / 1e12
+    outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in outs_host)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for dst, src in zip((qd, kd, vd), host):
+            dst.copy_(src, non_blocking=True)
+        ea.fwd_into(qd, kd, vd, o, lse, **kw)
+        for dst, src in zip(outs_host, (o, lse)):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    pk = peaks()
+    ach = f_fwd / (statistics.mean(times) * 1e-3) / 1e12
+    line = {
+        "metric": "attention forward TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 peak",
+        "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded randn rounded to bf16)",
+        "config": workload_config(w, {"parallelism": f"replicas x{world}",
+                                      "pairs_per_head": pairs}),
+        "pct_of_peak": round(100 * value / world / pk["bf16_tflops"], 1),
+        "kernels": {"fwd_tc_kernel": {"ms": round(statistics.mean(times), 4),
+                                      "min_ms": round(min(times), 4),
+                                      "achieved": round(ach, 2), "unit": UNIT,
+                                      "frac": round(ach / pk["bf16_tflops"], 4)}},
+        "roofline": {"bound": "tensor", "kernel": "fwd_tc_kernel", "achieved": round(ach, 2),
+                     "peak": pk["bf16_tflops"], "unit": UNIT,
+                     "frac": round(ach / pk["bf16_tflops"], 4),
+                     "peak_source": pk["source"] + " bf16 burst", "traffic": None},
+        "e2e": {"value": round(world * f_fwd / (ms_e2e * 1e-3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(ms_e2e, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -363,11 +468,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="fwd_bwd", choices=["fwd_bwd", *FWD_WORKLOADS])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "fwd_bwd":
+        run_forward(args, FWD_WORKLOADS[args.workload])
     else:
         run_ours(args)
 
