@@ -113,8 +113,14 @@ KERNEL_SOURCES = {"fwd_tc_kernel": "fwd_tc.cu", "dkdv_kernel": "bwd_tc.cu",
                   "dq_kernel": "bwd_tc.cu", "rowdot_kernel": "simt.cu"}
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 248563712,
-                      "sha256": "8dedac898de439b4b2a60de199fce6479434e8e2a47816336bf850578578c62c"},
+    "fwd_tc_kernel": {"bytes": 201393152 + 47004928,
+                      "sha256": "b9d290e9b09a53967bc19d4269bb7cade7a007bc207c9127828c46cdfca55c5c"},
+    "rowdot_kernel": {"bytes": 135274752 + 4241152,
+                      "sha256": "1f69db384bac8bffc2176c6223a7b5940c03f66c7127ea38ad82fbe219446ef5"},
+    "dkdv_kernel": {"bytes": 270715904 + 103128576,
+                    "sha256": "fa2ce09954fdb9647e03ffeb2e218c17e81523980982ff6494f8e47ca66e8c96"},
+    "dq_kernel": {"bytes": 270680576 + 52014592,
+                  "sha256": "fa2ce09954fdb9647e03ffeb2e218c17e81523980982ff6494f8e47ca66e8c96"},
 }
 
 
