@@ -217,51 +217,60 @@ __global__ void __launch_bounds__(kRows) dkdv_simt_kernel(Problem p, const __nv_
   }
 }
 
-// Row terms of the backward (see RowTerms): one warp per padded query row. D_i is the
-// dot product of the row's dO and O in a fixed order (16-byte loads, butterfly sum).
+// Row terms of the backward (see RowTerms), one padded query row per group of D/8
+// lanes: each lane reads 16 bytes (8 elements) of the row's O and dO, and the group
+// sums its products with a fixed butterfly, so D_i does not depend on the launch.
+// A warp handles kUnroll rows per lane group at once to keep enough loads in flight.
 template <int D>
 __global__ void __launch_bounds__(256) rowdot_kernel(Problem p, long long rows,
                                                      const __nv_bfloat16* o,
                                                      const __nv_bfloat16* dout,
                                                      const float* lse, RowTerms rt) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const long long bh = row / p.nq_pad;
-  const int i = (int)(row - bh * p.nq_pad);
-  float s = 0.f, l2 = INFINITY;
-  if (i < p.Nq) {
-    const long long src = bh * p.Nq + i;
-    constexpr int kPer = D / 32;  // elements per lane: 2 (d=64) or 4 (d=128)
-    const __nv_bfloat16* a = o + src * D + lane * kPer;
-    const __nv_bfloat16* bptr = dout + src * D + lane * kPer;
-    if constexpr (kPer == 4) {
-      const uint2 av = *reinterpret_cast<const uint2*>(a);
-      const uint2 bv = *reinterpret_cast<const uint2*>(bptr);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+  constexpr int kLanes = D / 8;             // lanes per row
+  constexpr int kGroups = 32 / kLanes;      // rows per warp and pass
+  constexpr int kUnroll = 4;
+  constexpr long long kRowsPerWarp = (long long)kGroups * kUnroll;
+  const int lane = threadIdx.x & 31, grp = lane / kLanes, sub = lane % kLanes;
+  const long long warp0 = ((long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kRowsPerWarp;
+  uint4 av[kUnroll], bv[kUnroll];
+  long long src[kUnroll];
+  bool real[kUnroll];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const float2 x = __bfloat1622float2(a2[t]), y = __bfloat1622float2(b2[t]);
-        s = fmaf(x.x, y.x, s);
-        s = fmaf(x.y, y.y, s);
-      }
-    } else {
-      const __nv_bfloat162 av = *reinterpret_cast<const __nv_bfloat162*>(a);
-      const __nv_bfloat162 bv = *reinterpret_cast<const __nv_bfloat162*>(bptr);
-      const float2 x = __bfloat1622float2(av), y = __bfloat1622float2(bv);
+  for (int r = 0; r < kUnroll; ++r) {  // issue every load first
+    const long long row = warp0 + r * kGroups + grp;
+    const long long bh = row / p.nq_pad;
+    const int i = (int)(row - bh * p.nq_pad);
+    real[r] = row < rows && i < p.Nq;
+    src[r] = bh * p.Nq + i;
+    av[r] = real[r] ? reinterpret_cast<const uint4*>(o + src[r] * D)[sub] : make_uint4(0, 0, 0, 0);
+    bv[r] = real[r] ? reinterpret_cast<const uint4*>(dout + src[r] * D)[sub] : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int r = 0; r < kUnroll; ++r) {
+    const long long row = warp0 + r * kGroups + grp;
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av[r]);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv[r]);
+    float s = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float2 x = __bfloat1622float2(a2[t]), y = __bfloat1622float2(b2[t]);
       s = fmaf(x.x, y.x, s);
       s = fmaf(x.y, y.y, s);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    const float L = lse[src];
-    l2 = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
-  }
-  if (lane == 0) {
-    rt.delta[row] = s;
-    rt.lse2[row] = l2;
-    if (bh == 0) rt.first[i] = i < p.Nq ? first_key(p.mask, i) : 0x7fffffff;
+    for (int off = kLanes / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (sub == 0 && row < rows) {
+      const long long bh = row / p.nq_pad;
+      const int i = (int)(row - bh * p.nq_pad);
+      float l2 = INFINITY;
+      if (real[r]) {
+        const float L = lse[src[r]];
+        l2 = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
+      }
+      rt.delta[row] = real[r] ? s : 0.f;
+      rt.lse2[row] = l2;
+      if (bh == 0) rt.first[i] = i < p.Nq ? first_key(p.mask, i) : 0x7fffffff;
+    }
   }
 }
 
@@ -319,7 +328,8 @@ cudaError_t launch_bwd_rowdot(const Problem& p, const __nv_bfloat16* o,
                               cudaStream_t st) {
   const long long rows = (long long)p.B * p.Hq * p.nq_pad;
   if (rows == 0) return cudaSuccess;
-  const long long blocks = (rows + 7) / 8;
+  const long long per_block = 8LL * (32 / (p.d / 8)) * 4;  // warps x rows per warp
+  const long long blocks = (rows + per_block - 1) / per_block;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (p.d == 64) rowdot_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
   else rowdot_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
