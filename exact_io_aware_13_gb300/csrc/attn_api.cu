@@ -217,8 +217,6 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
   BwdMaps maps;  // built before the first launch: errors launch nothing
   if (!simt && (phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ))) {
     // 128-row boxes for the tiles a CTA loads once, 64-row boxes for the streamed ones
-    if ((s = make_map(&maps.q128, q, B * Hq, Nq, d)) != ATTN_OK) return s;
-    if ((s = make_map(&maps.do128, dout, B * Hq, Nq, d)) != ATTN_OK) return s;
     if ((s = make_map(&maps.v128, v, B * Hkv, Nkv, d)) != ATTN_OK) return s;
     if ((s = make_map(&maps.q64, q, B * Hq, Nq, d, 64)) != ATTN_OK) return s;
     if ((s = make_map(&maps.do64, dout, B * Hq, Nq, d, 64)) != ATTN_OK) return s;
@@ -235,7 +233,7 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
     return from_cuda(launch_bwd_simt(p, qb, kb, vb, lse, dob, rt.delta, dqb, dkb, dvb, st));
   }
   if (!(phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ))) return ATTN_OK;
-  return from_cuda(launch_bwd_tc(p, maps, rt, kb, dqb, dkb, dvb, (phases & ATTN_BWD_DKDV) != 0,
+  return from_cuda(launch_bwd_tc(p, maps, rt, qb, dob, kb, dqb, dkb, dvb, (phases & ATTN_BWD_DKDV) != 0,
                                  (phases & ATTN_BWD_DQ) != 0, st));
 }
 

@@ -47,23 +47,28 @@ constexpr int kRelayWarp = kEwWarps + 2;  // turns TMA completions into barrier 
 //   dkdv: kNbKvRel     S^T / dP^T of the sub-step read: element-wise warps + MMA warp
 //         kNbKvP + x   P^T / dS^T of a sub-step u (x = u % 2) written: same threads
 //         kNbKvK       K tile written to tensor memory: same threads
+//   dq:   kNbQL        Q and dO tiles written to tensor memory: element-wise warps + MMA warp
 constexpr uint32_t kNbP = 1, kNbPCount = 288;
 constexpr uint32_t kNbStage = 3, kNbStageCount = 64;
-constexpr uint32_t kNbKvRel = 8, kNbKvP = 9, kNbKvK = 11, kNbKvCount = (kEwWarps + 1) * 32;
+constexpr uint32_t kNbKvRel = 8, kNbKvP = 9, kNbKvK = 11, kNbQL = 12;
+constexpr uint32_t kNbKvCount = (kEwWarps + 1) * 32;
 constexpr int kStagesQ = 4;      // dq ring depth, in sub-steps
 constexpr int kStagesKv = 5;     // dkdv ring depth
 constexpr int kMaxStages = 5;
 // Stage barriers take IDs kNbStage .. kNbStage + kMaxStages - 1; the others must not
 // overlap them (one hardware barrier, one thread count), and IDs end at 15.
-static_assert(kNbStage + kMaxStages <= kNbKvRel && kNbP + 2 <= kNbStage && kNbKvK < 16,
+static_assert(kNbStage + kMaxStages <= kNbKvRel && kNbP + 2 <= kNbStage && kNbKvK < kNbQL &&
+                  kNbQL < 16,
               "named barrier IDs");
 constexpr int kHeadGroup = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Tensor memory columns of dq: S buffers, dP buffers (64 each), then dQ.
+// Tensor memory columns of dq: S buffers, dP buffers (64 each), dQ, then the Q and dO
+// tiles as bf16 pairs (A operands of S = Q K^T and dP = dO V^T; D/2 columns each).
 __device__ __forceinline__ uint32_t col_s(int x) { return x * 64; }
 __device__ __forceinline__ uint32_t col_dp(int x) { return 128 + x * 64; }
-constexpr uint32_t kColAcc = 256;
+constexpr uint32_t kColAcc = 256, kColQ = 384;
+template <int D> constexpr uint32_t col_do() { return kColQ + D / 2; }
 // Tensor memory columns of dkdv: S^T, dP^T (64 each), P^T / dS^T (bf16 pairs: P^T in
 // the first 32 columns, dS^T in the next 32), the K tile (bf16 pairs, A operand of
 // S^T = K Q^T), then dV and dK.
@@ -170,10 +175,10 @@ __device__ __forceinline__ void dq_ds(const uint32_t (&sr)[32], const uint32_t (
   }
 }
 
-// Shared-memory layouts. dq: the CTA's Q and dO tiles (fixed), then a ring of kS
-// stages, each holding a 64-row slice of K and V. dkdv: the V tile (fixed; K lives in
-// tensor memory), a ring of 64-row slices of Q and dO, and each stage's row terms of
-// those 64 query rows (lse2, delta, first key: 256 bytes each).
+// Shared-memory layouts. dq: a ring of kS stages, each holding a 64-row slice of K and
+// V (Q and dO live in tensor memory). dkdv: the V tile (fixed; K lives in tensor
+// memory), a ring of 64-row slices of Q and dO, and each stage's row terms of those 64
+// query rows (lse2, delta, first key: 256 bytes each).
 template <int D, int kS, int kFixTiles, bool kRowTerms>
 struct Layout {
   static constexpr int kStageCount = kS;
@@ -182,7 +187,6 @@ struct Layout {
   static constexpr int kSubChunk = SUB * 128;       // 64-column slab of a stage slice
   static constexpr int kSubTile = SUB * D * 2;
   static constexpr int kFixA = 0;
-  static constexpr int kFixB = kFixTile;            // dq only
   static constexpr int kRing = kFixTiles * kFixTile;
   static constexpr int kStage = 2 * kSubTile;
   static constexpr int kRows = kRing + kS * kStage;
@@ -190,7 +194,7 @@ struct Layout {
   static constexpr int kBars = kRows + (kRowTerms ? kS * kRowStage : 0);
   static constexpr int kAlloc = kBars + 256 + 1024;
 };
-template <int D> using LayoutQ = Layout<D, kStagesQ, 2, false>;
+template <int D> using LayoutQ = Layout<D, kStagesQ, 0, false>;
 template <int D> using LayoutKv = Layout<D, kStagesKv, 1, true>;
 static_assert(LayoutKv<128>::kAlloc <= 232448 && LayoutQ<128>::kAlloc <= 232448,
               "shared memory per CTA");
@@ -209,7 +213,9 @@ struct BwdBars {
 struct BwdArgs {
   Problem p;
   RowTerms rt;
-  const __nv_bfloat16* k;  // K [B, Hkv, Nkv, d] (dkdv copies its tile into tensor memory)
+  const __nv_bfloat16* q;     // Q, dO [B, Hq, Nq, d] and K [B, Hkv, Nkv, d]: the tiles the
+  const __nv_bfloat16* dout;  // kernels keep in tensor memory are copied from here
+  const __nv_bfloat16* k;
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -335,27 +341,27 @@ __device__ __forceinline__ void store_acc_row(uint32_t t, float mul, __nv_bfloat
   }
 }
 
-// Loads the fixed tiles (fa, and fb if given; rows r0.. of head z) and then, for
-// every sub-step u, the 64-row slices of the two streamed operands into stage
+// Loads the fixed tile fa if given (rows r0.. of head z) and then, for every
+// sub-step u, the 64-row slices of the two streamed operands into stage
 // u % L::kStageCount. `slice`
 // gives (row, head) of sub-step u. With `rt` (dkdv) it also copies the row terms of
 // those 64 query rows into the stage's row block; all of it completes full[s].
 template <int D, class L, typename SliceFn>
 __device__ __forceinline__ void load_loop(uint8_t* smem, BwdBars* bars, const WaitCtx& wc,
-                                          int lane, const CUtensorMap* fa, const CUtensorMap* fb,
-                                          int r0, int z, const CUtensorMap* sa,
+                                          int lane, const CUtensorMap* fa, int r0, int z,
+                                          const CUtensorMap* sa,
                                           const CUtensorMap* sb, int subs, SliceFn slice,
                                           const RowTerms* rt, int nq_pad) {
   constexpr int kS = L::kStageCount;
   if (lane == 0) {
     tma_prefetch_desc(sa);
     tma_prefetch_desc(sb);
-    const uint32_t bar = smem_u32(&bars->fixed_full);
-    mbar_arrive_expect_tx(bar, (fb ? 2 : 1) * L::kFixTile);
+    if (fa) {
+      const uint32_t bar = smem_u32(&bars->fixed_full);
+      mbar_arrive_expect_tx(bar, L::kFixTile);
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      tma_load_3d(smem_u32(smem + L::kFixA + c * L::kFixChunk), fa, bar, c * 64, r0, z);
-      if (fb) tma_load_3d(smem_u32(smem + L::kFixB + c * L::kFixChunk), fb, bar, c * 64, r0, z);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(smem_u32(smem + L::kFixA + c * L::kFixChunk), fa, bar, c * 64, r0, z);
     }
   }
   for (int u = 0; u < subs; ++u) {
@@ -384,7 +390,7 @@ __device__ __forceinline__ void load_loop(uint8_t* smem, BwdBars* bars, const Wa
     }
   }
   if (lane == 0) {  // let in-flight copies land before the CTA can exit
-    mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
+    if (fa) mbar_wait(smem_u32(&bars->fixed_full), 0, wc);
     for (int u = imax(0, subs - kS); u < subs; ++u)
       mbar_wait(smem_u32(&bars->full[u % kS]), (u / kS) & 1, wc);
   }
@@ -454,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t colDV = kKvColAcc, colDK = kKvColAcc + D;
 
   if (warp == kLoadWarp) {
-    load_loop<D, L>(smem, bars, wc, lane, &maps.v128, nullptr, k0, bg, &maps.q64, &maps.do64,
-                    subs, slice, &a.rt, p.nq_pad);
+    load_loop<D, L>(smem, bars, wc, lane, &maps.v128, k0, bg, &maps.q64, &maps.do64, subs,
+                    slice, &a.rt, p.nq_pad);
   } else if (warp == kRelayWarp) {
     relay_loop<L::kStageCount>(bars, wc, subs);
   } else if (warp == kMmaWarp) {
@@ -655,26 +661,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == kLoadWarp) {
-    load_loop<D, L>(smem, bars, wc, lane, &maps.q128, &maps.do128, q0, bh, &maps.k64, &maps.v64,
-                 subs, slice, nullptr, p.nq_pad);
+    load_loop<D, L>(smem, bars, wc, lane, nullptr, q0, bh, &maps.k64, &maps.v64, subs, slice,
+                    nullptr, p.nq_pad);
   } else if (warp == kRelayWarp) {
     relay_loop<L::kStageCount>(bars, wc, subs);
   } else if (warp == kMmaWarp) {
     // Same issue scheme as the dK/dV kernel: named barriers only, MMAs predicated on the
-    // elect.sync lane, nothing issued if the fixed tiles never arrive.
-    const uint32_t sQ = smem_u32(smem + L::kFixA), sDO = smem_u32(smem + L::kFixB);
+    // elect.sync lane.
     const uint32_t ring = smem_u32(smem + L::kRing);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc));
     const bool issuer = elect_one();
+    nb_sync(kNbQL, kNbKvCount);  // Q and dO in tensor memory
     // S and dP of sub-step u into buffer u & 1
     auto issue_sdp = [&](int u) {
       const int s = u % L::kStageCount, x = u & 1;
       nb_sync(kNbStage + s, kNbStageCount);
       tc_fence_after_sync();
       const uint32_t sK = ring + s * L::kStage, sV = sK + L::kSubTile;
-      if (!ok) return;
-      mma_128x64<D>(issuer, tmem + col_s(x), sQ, sK);     // S = Q K^T
-      mma_128x64<D>(issuer, tmem + col_dp(x), sDO, sV);   // dP = dO V^T
+      mma_tmem_x64<D>(issuer, tmem + col_s(x), tmem + kColQ, sK);         // S = Q K^T
+      mma_tmem_x64<D>(issuer, tmem + col_dp(x), tmem + col_do<D>(), sV);  // dP = dO V^T
       mma_commit_if(issuer, smem_u32(&bars->s_full[x]));
     };
     issue_sdp(0);
@@ -684,13 +688,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       nb_sync(kNbP + x, kNbPCount);
       tc_fence_after_sync();
       const uint32_t sK = ring + s * L::kStage;
-      if (ok) {
-        mma_tmem64_x_slice<D>(issuer, tmem + kColAcc, tmem + col_s(x), sK, u > 0);  // dQ += dS K
-        mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage consumed once this completes
-      }
+      mma_tmem64_x_slice<D>(issuer, tmem + kColAcc, tmem + col_s(x), sK, u > 0);  // dQ += dS K
+      mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage consumed once this completes
       if (u + 2 < subs) issue_sdp(u + 2);
     }
-    if (ok) mma_commit_if(issuer, smem_u32(&bars->acc_full));
+    mma_commit_if(issuer, smem_u32(&bars->acc_full));
   } else {
     const int pair = warp >> 3;                // sub-steps u with u % 2 == pair
     const int wg = (warp >> 2) & 1;            // which 32 key columns of a sub-step
@@ -709,6 +711,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       fk = a.rt.first[i];
     }
     const int last_key = (p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1));
+    {
+      // Q and dO rows of the tile into tensor memory: warpgroups 0 and 1 copy the two
+      // halves of this thread's Q row, 2 and 3 those of its dO row (zeros past Nq).
+      const int wq = warp >> 2, half = wq & 1;
+      constexpr int kW = D / 4;  // 32-bit words (bf16 pairs) per thread
+      uint32_t wv[kW];
+      const uint4* src = reinterpret_cast<const uint4*>(
+          (wq < 2 ? a.q : a.dout) + ((size_t)bh * p.Nq + (row_ok ? i : 0)) * D + half * (D / 2));
+#pragma unroll
+      for (int e = 0; e < kW / 4; ++e) {
+        const uint4 v = row_ok ? src[e] : make_uint4(0, 0, 0, 0);
+        wv[4 * e] = v.x; wv[4 * e + 1] = v.y; wv[4 * e + 2] = v.z; wv[4 * e + 3] = v.w;
+      }
+      const uint32_t dst = tmem + lane_base + (wq < 2 ? kColQ : col_do<D>()) + half * (D / 4);
+      if constexpr (kW == 32) tmem_st32(dst, wv);
+      else tmem_st16(dst, wv);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      nb_arrive(kNbQL, kNbKvCount);
+    }
     bool ok_all = true;
     for (int u = pair; u < subs; u += 2) {
       const int kt0 = (kr.lo + (u >> 1)) * BT;
@@ -787,11 +809,12 @@ cudaError_t launch_d(const BwdArgs& ka, const BwdArgs& qa, const BwdMaps& maps, 
 }  // namespace
 
 cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
+                          const __nv_bfloat16* q, const __nv_bfloat16* dout,
                           const __nv_bfloat16* k, __nv_bfloat16* dq, __nv_bfloat16* dk,
                           __nv_bfloat16* dv,
                           bool run_dkdv, bool run_dq, cudaStream_t st) {
-  BwdArgs ka{p, rt, k, dq, dk, dv, ceil_div(p.Nkv, BT)};
-  BwdArgs qa{p, rt, k, dq, dk, dv, ceil_div(p.Nq, BT)};
+  BwdArgs ka{p, rt, q, dout, k, dq, dk, dv, ceil_div(p.Nkv, BT)};
+  BwdArgs qa{p, rt, q, dout, k, dq, dk, dv, ceil_div(p.Nq, BT)};
   const long long gk = run_dkdv ? (long long)ka.n_tiles * p.B * p.Hkv : 0;
   const long long gq = run_dq ? (long long)qa.n_tiles * p.B * p.Hq : 0;
   if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;

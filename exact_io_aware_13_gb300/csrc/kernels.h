@@ -61,12 +61,13 @@ cudaError_t launch_classify(const MaskSpec& m, int32_t* classes, cudaStream_t st
 cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, __nv_bfloat16* o, float* lse,
                           cudaStream_t st);
-// Tensor maps of the backward: 128-row boxes (tiles a CTA loads once: Q and dO for dq,
-// V for dK/dV) and 64-row boxes (tiles it streams).
+// Tensor maps of the backward: the 128-row V box (the tile a dK/dV CTA loads once) and
+// 64-row boxes (the slices both kernels stream).
 struct BwdMaps {
-  CUtensorMap q128, do128, v128, q64, do64, k64, v64;
+  CUtensorMap v128, q64, do64, k64, v64;
 };
 cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
+                          const __nv_bfloat16* q, const __nv_bfloat16* dout,
                           const __nv_bfloat16* k, __nv_bfloat16* dq, __nv_bfloat16* dk,
                           __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st);
 
