@@ -3,14 +3,16 @@ online softmax, backward rebuilding P from the LSE) on the causal fwd+bwd worklo
 (B=2, H=16, N=8192, d=128, bf16), timed with CUDA events.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload fwd_bwd|causal_fwd|gqa_window_fwd|docs_fwd|tiny_fwd]
+                [--workload fwd_bwd|causal_fwd|gqa_window_fwd|docs_fwd|tiny_fwd|fp8_causal_fwd]
 
 Prints one JSON line. `value` is useful TFLOP/s (masked-out work excluded) summed
 over ranks; with N > 1 each rank runs its own replica of the workload (the heads
 are independent, so there is no data-path collective). --impl reference times the
 float64 CPU oracle on a bounded sample of the same workload on the host cores.
 --workload picks one of the other workloads; those are forward-only, so a step is
-one forward pass and the line reports the forward's useful TFLOP/s.
+one forward pass and the line reports the forward's useful TFLOP/s. fp8_causal_fwd
+runs the FP8 forward (e4m3 inputs with block scales, quantised once before the timed
+steps; the end-to-end number includes the quantisation).
 """
 from __future__ import annotations
 
@@ -33,7 +35,7 @@ from workloads import (CAUSAL, CAUSAL_FWD_BWD, DOCS, GQA_WINDOW, MASK_NAMES, TIN
                        make_inputs)
 
 FWD_WORKLOADS = {"causal_fwd": CAUSAL, "gqa_window_fwd": GQA_WINDOW, "docs_fwd": DOCS,
-                 "tiny_fwd": TINY}
+                 "tiny_fwd": TINY, "fp8_causal_fwd": CAUSAL}
 
 METRIC = "attention fwd/bwd TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 peak"
 UNIT = "TFLOP/s"
@@ -315,8 +317,9 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
-def run_forward(args, w):
-    """Forward-only workloads: a step is one attn_fwd over the whole workload."""
+def run_forward(args, w, fp8=False):
+    """Forward-only workloads: a step is one attn_fwd (or attn_fwd_fp8) over the whole
+    workload."""
     from exact_io_aware_13_gb300 import build as libbuild
     libbuild.build()
     import exact_io_aware_13_gb300 as ea
@@ -339,8 +342,21 @@ def run_forward(args, w):
     stream = torch.cuda.current_stream()
     kw = dict(scale=w.scale, mask_kind=w.mask_kind, window=w.window, doc_offsets=dt,
               score_kind=w.score_kind, softcap=w.softcap)
+    if fp8:
+        (q8, sq), (k8, sk), (v8t, sv) = ea.fp8_inputs(qd, kd, vd)
+
+        def fwd():
+            ea.fwd_fp8_into(q8, sq, k8, sk, v8t, sv, o, lse, Nkv=w.Nkv, **kw)
+
+        def fwd_e2e():  # the public FP8 call: quantise, then the FP8 forward
+            (a8, a_s), (b8, b_s), (c8, c_s) = ea.fp8_inputs(qd, kd, vd)
+            ea.fwd_fp8_into(a8, a_s, b8, b_s, c8, c_s, o, lse, Nkv=w.Nkv, **kw)
+    else:
+        def fwd():
+            ea.fwd_into(qd, kd, vd, o, lse, **kw)
+        fwd_e2e = fwd
     for _ in range(args.warmup):
-        ea.fwd_into(qd, kd, vd, o, lse, **kw)
+        fwd()
     torch.cuda.synchronize()
     if ea.device_status() != 0:
         raise RuntimeError("a kernel gave up a bounded wait during warm-up")
@@ -352,7 +368,7 @@ def run_forward(args, w):
         for s in range(args.steps):
             flush.zero_()
             ev[s][0].record(stream)
-            ea.fwd_into(qd, kd, vd, o, lse, **kw)
+            fwd()
             ev[s][1].record(stream)
         torch.cuda.synchronize()
     if ea.device_status() != 0:
@@ -373,7 +389,7 @@ def run_forward(args, w):
     for _ in range(args.steps):
         for dst, src in zip((qd, kd, vd), host):
             dst.copy_(src, non_blocking=True)
-        ea.fwd_into(qd, kd, vd, o, lse, **kw)
+        fwd_e2e()
         for dst, src in zip(outs_host, (o, lse)):
             dst.copy_(src, non_blocking=True)
     e1.record(stream)
@@ -381,23 +397,27 @@ def run_forward(args, w):
     ms_e2e = e0.elapsed_time(e1) / args.steps
     pk = peaks()
     ach = f_fwd / (statistics.mean(times) * 1e-3) / 1e12
+    peak = pk["bf16_tflops"] * (2 if fp8 else 1)  # FP8 dense rate: 2x bf16 (nominal ratio)
     line = {
-        "metric": "attention forward TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 peak",
+        "metric": ("attention FP8 forward TFLOP/s (unmasked FLOPs) and % of GB300 dense FP8 peak"
+                   if fp8 else
+                   "attention forward TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 peak"),
         "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded randn rounded to bf16)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "data": "synthetic (seeded randn rounded to bf16" + (", quantised to e4m3)" if fp8 else ")"),
         "config": workload_config(w, {"parallelism": f"replicas x{world}",
                                       "pairs_per_head": pairs}),
-        "pct_of_peak": round(100 * value / world / pk["bf16_tflops"], 1),
+        "pct_of_peak": round(100 * value / world / peak, 1),
         "kernels": {"fwd_tc_kernel": {"ms": round(statistics.mean(times), 4),
                                       "min_ms": round(min(times), 4),
                                       "achieved": round(ach, 2), "unit": UNIT,
-                                      "frac": round(ach / pk["bf16_tflops"], 4)}},
+                                      "frac": round(ach / peak, 4)}},
         "roofline": {"bound": "tensor", "kernel": "fwd_tc_kernel", "achieved": round(ach, 2),
-                     "peak": pk["bf16_tflops"], "unit": UNIT,
-                     "frac": round(ach / pk["bf16_tflops"], 4),
-                     "peak_source": pk["source"] + " bf16 burst", "traffic": None},
+                     "peak": peak, "unit": UNIT, "frac": round(ach / peak, 4),
+                     "peak_source": pk["source"] + (" bf16 burst x 2 (nominal fp8/bf16 ratio)"
+                                                    if fp8 else " bf16 burst"),
+                     "traffic": None},
         "e2e": {"value": round(world * f_fwd / (ms_e2e * 1e-3) / 1e12, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 4)},
@@ -481,7 +501,7 @@ def main():
     if args.impl == "reference":
         run_reference(args)
     elif args.workload != "fwd_bwd":
-        run_forward(args, FWD_WORKLOADS[args.workload])
+        run_forward(args, FWD_WORKLOADS[args.workload], fp8=args.workload.startswith("fp8"))
     else:
         run_ours(args)
 

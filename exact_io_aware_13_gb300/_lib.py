@@ -47,6 +47,9 @@ SIGNATURES = {
     "attn_bwd_static_workspace": (_I, _BWD_ARGS[:20] + [_P]),
     "attn_bwd_phases": (_I, [_I] + _BWD_ARGS),
     "attn_classify_tiles": (_I, [_I, _MP, _I, _I, _P, _P]),
+    "attn_fwd_fp8": (_I, [_P] * 8 + [_I, _I, _I, _I, _I, _I, _F, _I, _MP, _I, _SP, _P]),
+    "attn_fp8_v_row_bytes": (ctypes.c_size_t, [_I]),
+    "attn_quantize_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "attn_device_status": (_I, [_P]),
     "attn_strerror": (ctypes.c_char_p, [_I]),
 }

@@ -163,3 +163,66 @@ def classify_tiles(mask_kind: int, Nq: int, Nkv: int, *, window: int = 0, doc_of
 def device_status(stream=None) -> int:
     """Synchronise and return the library's device status (0 = no kernel gave up)."""
     return int(_lib.load().attn_device_status(_stream(stream)))
+
+
+# ---------------------------------------------------------------- FP8
+FP8_TILES, FP8_V_TRANSPOSED = 0, 1
+
+
+def quantize_fp8(x: torch.Tensor, layout: int = FP8_TILES, stream=None):
+    """bf16 x [B, H, N, d] -> (e4m3 codes as uint8, fp32 scales) via attn_quantize_fp8.
+    FP8_TILES: codes [B, H, N, d], scales [B*H, ceil(N/128)];
+    FP8_V_TRANSPOSED: codes [B, H, d, attn_fp8_v_row_bytes(N)], scales [B*H]."""
+    _check_tensors(x)
+    lib = _lib.load()
+    B, H, N, d = x.shape
+    if layout == FP8_TILES:
+        codes = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+        scales = torch.empty((B * H, (N + 127) // 128), dtype=torch.float32, device=x.device)
+    else:
+        codes = torch.empty((B, H, d, int(lib.attn_fp8_v_row_bytes(N))), dtype=torch.uint8,
+                            device=x.device)
+        scales = torch.empty((B * H,), dtype=torch.float32, device=x.device)
+    st = lib.attn_quantize_fp8(_ptr(x), _ptr(codes), _ptr(scales), B * H, N, d, layout,
+                               _stream(stream))
+    _lib.check(st, "attn_quantize_fp8")
+    return codes, scales
+
+
+def fp8_inputs(q, k, v, stream=None):
+    """Quantise bf16 q, k, v for forward_fp8: ((q8, sq), (k8, sk), (v8t, sv))."""
+    return (quantize_fp8(q, FP8_TILES, stream), quantize_fp8(k, FP8_TILES, stream),
+            quantize_fp8(v, FP8_V_TRANSPOSED, stream))
+
+
+def fwd_fp8_into(q8, sq, k8, sk, v8t, sv, o, lse, *, Nkv: int, scale: float,
+                 mask_kind: int = MASK_NONE, window: int = 0, doc_offsets=None,
+                 score_kind: int = SCORE_NONE, softcap: float = 0.0, stream=None) -> None:
+    """Run attn_fwd_fp8 into o (bf16 [B,Hq,Nq,128]) and lse."""
+    _check_tensors(q8, sq, k8, sk, v8t, sv, o, lse, doc_offsets)
+    lib = _lib.load()
+    B, Hq, Nq, d = q8.shape
+    Hkv = k8.shape[1]
+    mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap)
+    st = lib.attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8t), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
+                          _ptr(lse), B, Hq, Hkv, Nq, Nkv, d, ctypes.c_float(scale), mask_kind, mp,
+                          score_kind, sp, _stream(stream))
+    del keep
+    _lib.check(st, "attn_fwd_fp8")
+
+
+def forward_fp8(q, k, v, *, scale: Optional[float] = None, mask_kind: int = MASK_NONE,
+                window: int = 0, doc_offsets=None, score_kind: int = SCORE_NONE,
+                softcap: float = 0.0, stream=None):
+    """Quantise bf16 q, k, v to e4m3 with block scales and run the FP8 forward.
+    Returns (o, lse, ((q8, sq), (k8, sk), (v8t, sv)))."""
+    d = q.shape[-1]
+    if scale is None:
+        scale = float(torch.tensor(d, dtype=torch.float32).rsqrt())
+    (q8, sq), (k8, sk), (v8t, sv) = quant = fp8_inputs(q, k, v, stream)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    fwd_fp8_into(q8, sq, k8, sk, v8t, sv, o, lse, Nkv=k.shape[2], scale=scale,
+                 mask_kind=mask_kind, window=window, doc_offsets=doc_offsets,
+                 score_kind=score_kind, softcap=softcap, stream=stream)
+    return o, lse, quant

@@ -264,6 +264,24 @@ attn_status static_workspace_ptr(float** out) {
   return ATTN_OK;
 }
 
+// ---------------------------------------------------------------- FP8
+// Tensor map over bytes [dz][dy][dx] with rows of row_bytes, box 128 x 128 x 1,
+// 128-byte swizzle (e4m3 tiles: 128 values of the innermost dimension per row).
+attn_status make_map8(CUtensorMap* map, const void* base, int dx, int dy, int dz,
+                      size_t row_bytes) {
+  cuuint64_t dims[3] = {(cuuint64_t)dx, (cuuint64_t)dy, (cuuint64_t)dz};
+  cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)row_bytes * dy};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
 }  // namespace
 }  // namespace attn
 
@@ -346,6 +364,57 @@ attn_status attn_bwd_static_workspace(const void* q, const void* k, const void* 
   return bwd_common(false, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, scale,
                     mask_kind, mask_params, score_kind, score_params, ws,
                     ws ? kStaticWords * sizeof(float) : 0, stream);
+}
+
+size_t attn_fp8_v_row_bytes(int Nkv) { return Nkv <= 0 ? 0 : (size_t)(Nkv + 15) / 16 * 16; }
+
+attn_status attn_quantize_fp8(const void* x, void* out, float* scales, int BH, int N, int d,
+                              int layout, void* stream) {
+  if (BH < 0 || N < 0 || (d != 64 && d != 128)) return ATTN_ERR_SHAPE;
+  if (layout != ATTN_FP8_TILES && layout != ATTN_FP8_V_TRANSPOSED) return ATTN_ERR_ARG;
+  if ((long long)BH * N == 0 && layout == ATTN_FP8_TILES) return ATTN_OK;
+  if (BH == 0) return ATTN_OK;
+  if (!out || !scales || (N > 0 && !x)) return ATTN_ERR_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned4(scales)) return ATTN_ERR_ALIGN;
+  if (layout == ATTN_FP8_TILES && BH > 65535) return ATTN_ERR_SHAPE;
+  DeviceInfo* dev = nullptr;
+  attn_status s = current_device(&dev);
+  if (s != ATTN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  auto* ob = static_cast<uint8_t*>(out);
+  if (layout == ATTN_FP8_TILES) return from_cuda(launch_quantize_tiles(xb, ob, scales, BH, N, d, st));
+  return from_cuda(launch_quantize_v_transposed(xb, ob, scales, BH, N, d, st));
+}
+
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale,
+                         const float* k_scale, const float* v_scale, void* o, float* lse, int B,
+                         int Hq, int Hkv, int Nq, int Nkv, int d, float scale, int mask_kind,
+                         const attn_mask_params* mask_params, int score_kind,
+                         const attn_score_params* score_params, void* stream) {
+  Problem p;
+  attn_status s = check_problem(B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind, mask_params,
+                                score_kind, score_params, &p);
+  if (s != ATTN_OK) return s;
+  if (d != 128) return ATTN_ERR_SHAPE;
+  const long long rows_q = (long long)B * Hq * Nq;
+  if (rows_q == 0) return ATTN_OK;
+  if (!q8 || !q_scale || !o || !lse) return ATTN_ERR_ARG;
+  if (Nkv > 0 && (!k8 || !v8t || !k_scale || !v_scale)) return ATTN_ERR_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(o) || !aligned16(lse) ||
+      !aligned4(q_scale) || !aligned4(k_scale) || !aligned4(v_scale))
+    return ATTN_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if ((s = current_device(&dev)) != ATTN_OK) return s;
+  p.status = dev->status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto* ob = static_cast<__nv_bfloat16*>(o);
+  if (Nkv == 0) return from_cuda(launch_fill_masked(rows_q, d, ob, lse, st));
+  CUtensorMap tq, tk, tvt;
+  if ((s = make_map8(&tq, q8, d, Nq, B * Hq, d)) != ATTN_OK) return s;
+  if ((s = make_map8(&tk, k8, d, Nkv, B * Hkv, d)) != ATTN_OK) return s;
+  if ((s = make_map8(&tvt, v8t, Nkv, d, B * Hkv, attn_fp8_v_row_bytes(Nkv))) != ATTN_OK) return s;
+  return from_cuda(launch_fwd_fp8_tc(p, tq, tk, tvt, q_scale, k_scale, v_scale, ob, lse, st));
 }
 
 attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_params, int Nq,

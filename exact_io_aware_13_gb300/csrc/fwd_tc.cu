@@ -24,6 +24,15 @@
 //     score columns, and rescales its O row in TMEM when the max has grown by more
 //     than 2^8 (a stale max is exact: O and l share it until the final division).
 // Tensor memory: S0 cols [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d).
+//
+// FP8 variant (kFp8, d = 128): Q and K are e4m3 with one scale per 128-row tile, V is
+// e4m3 stored transposed ([d, keys] per head, keys contiguous) with one scale per head,
+// so both MMAs read K-major 8-bit operands (kind::f8f6f4, K = 32 per instruction). The
+// score of a tile pair is scale * s_q * s_k * (Q8 K8^T); P is multiplied by 2^7 and
+// rounded to e4m3 before P V (so values down to 2^-16 keep a relative error of 2^-4 and
+// smaller ones an absolute error of at most 2^-17); the row sums l use the unrounded P,
+// and the epilogue multiplies O by s_v 2^-7 / l. The running max may lag the true max
+// by at most 2^1 here (not 2^8), so P <= 2 and P 2^7 <= 256 stays below e4m3's 448.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -46,11 +55,15 @@ constexpr uint32_t kNbKv = 3, kNbKvCount = 64;
 constexpr int kHeadGroup = 4;  // heads whose CTAs are scheduled together (L2 reuse)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr float kRescaleLog2Fp8 = 1.0f;  // FP8: P = exp2(s - m) <= 2, so P 2^7 fits e4m3
+constexpr float kPScaleFp8 = 128.0f;     // P is scaled by 2^7 before rounding to e4m3
 
-template <int D>
+template <int D, bool kFp8>
 struct Layout {
-  static constexpr int kChunk = BM * 128;               // one 64-column slab: 16 KB
-  static constexpr int kTile = BM * D * 2;              // one Q/K/V tile
+  static constexpr int kElem = kFp8 ? 1 : 2;           // bytes per element
+  static constexpr int kChunk = BM * 128;               // one 128-byte-wide slab: 16 KB
+  static constexpr int kSlabs = D * kElem / 128;        // slabs per tile
+  static constexpr int kTile = BM * D * kElem;          // one Q/K/V tile (fp8: V^T tile)
   static constexpr int kQ = 0;
   static constexpr int kRing = kQ + kQTiles * kTile;
   static constexpr int kBars = kRing + kStages * kTile;
@@ -75,6 +88,11 @@ struct FwdArgs {
   __nv_bfloat16* o;
   float* lse;
   int num_qblocks;  // ceil(Nq / 256)
+  // FP8 only: dequantisation scales of Q [B*Hq, nqt], K [B*Hkv, nkt], V [B*Hkv]
+  const float* sq;
+  const float* sk;
+  const float* sv;
+  int nqt, nkt;     // 128-row tiles per head of Q and K
 };
 
 // CTA -> (batch*head, 256-row query block). Heads are taken kHeadGroup at a time
@@ -90,11 +108,12 @@ __device__ __forceinline__ void cta_work(const FwdArgs& a, int& bh, int& qb) {
   bh = grp * kHeadGroup + rem % gh;
 }
 
-template <int D, bool kAlibi, bool kSoftcap>
+template <int D, bool kAlibi, bool kSoftcap, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
-  using L = Layout<D>;
+  using L = Layout<D, kFp8>;
+  static_assert(!kFp8 || D == 128, "the FP8 path is built for d = 128");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -165,9 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int t = 0; t < kQTiles; ++t)
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem_u32(smem + L::kQ + t * L::kTile + c * L::kChunk), &tm_q, qbar, c * 64,
-                      q0 + t * BM, bh);
+        for (int c = 0; c < L::kSlabs; ++c)
+          tma_load_3d(smem_u32(smem + L::kQ + t * L::kTile + c * L::kChunk), &tm_q, qbar,
+                      c * (128 / L::kElem), q0 + t * BM, bh);
       for (int u = 0; u < 2 * n_kv; ++u) {
         const int s = u % kStages, use = u / kStages;
         if (!mbar_wait(smem_u32(&bars->kv_empty[s]), (use & 1) ^ 1, wc)) break;
@@ -175,10 +194,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(fb, L::kTile);
         const CUtensorMap* map = (u & 1) ? &tm_v : &tm_k;
         const int krow = (lo + (u >> 1)) * BN;
+        if (kFp8 && (u & 1)) {  // V^T tile: keys krow.. (x), all d rows (y)
+          tma_load_3d(smem_u32(smem + L::kRing + s * L::kTile), map, fb, krow, 0, bg);
+        } else {
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem_u32(smem + L::kRing + s * L::kTile + c * L::kChunk), map, fb, c * 64,
-                      krow, bg);
+          for (int c = 0; c < L::kSlabs; ++c)
+            tma_load_3d(smem_u32(smem + L::kRing + s * L::kTile + c * L::kChunk), map, fb,
+                        c * (128 / L::kElem), krow, bg);
+        }
       }
       // Do not leave while copies into this CTA's shared memory are in flight.
       mbar_wait(qbar, 0, wc);
@@ -204,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp never diverges (an elect.sync predicate issues an MMA in about 47 cycles, a
     // predicate computed from the lane index in about 82). If the Q tiles never arrive
     // (`ok` false) the warp keeps every barrier operation and issues nothing.
-    constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
-    constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
+    constexpr uint32_t idS = kFp8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false, false);
+    constexpr uint32_t idO = kFp8 ? idesc_e4m3_f32(BM, D) : idesc_bf16_f32(BM, D, false, true);
     const uint32_t q_base = smem_u32(smem + L::kQ);
     const uint32_t ring = smem_u32(smem + L::kRing);
     int np[kQTiles] = {0, 0};  // P tiles consumed per query tile
@@ -225,23 +248,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t qt = q_base + t * L::kTile;
       const uint64_t dq = smem_desc_sw128(qt, 16, 1024), dk = smem_desc_sw128(kb, 16, 1024);
       const uint32_t col = t == 0 ? L::kColS0 : L::kColS1;
+      // 32 bytes of the head dimension per instruction (16 bf16 or 32 e4m3 values)
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < D * L::kElem / 32; ++kk) {
         const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
-        mma_ss_if(issuer, tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
+        if (kFp8) mma_f8_ss_if(issuer, tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
+        else mma_ss_if(issuer, tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
       }
       mma_commit_if(issuer, smem_u32(&bars->s_full[t]));
     };
     auto issue_pv = [&](int t, int u) {  // O_t += P_t V with V in ring use u
       if (!ok) return;
       const uint32_t vb = ring + (u % kStages) * L::kTile;
-      const uint64_t dv = smem_desc_sw128(vb, L::kChunk, 1024);
       const uint32_t colS = t == 0 ? L::kColS0 : L::kColS1;
       const uint32_t colO = t == 0 ? L::kColO0 : L::kColO1;
+      if (kFp8) {  // P (e4m3, 4 per column) x V^T tile (K-major): 32 keys per instruction
+        const uint64_t dv = smem_desc_sw128(vb, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
-        mma_ts_if(issuer, tmem + colO, tmem + colS + kk * 8, dv + ((kk * 16 * 128) >> 4), idO,
-               (np[t] > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BN / 32; ++kk)
+          mma_f8_ts_if(issuer, tmem + colO, tmem + colS + kk * 8, dv + ((kk * 32) >> 4), idO,
+                       (np[t] > 0 || kk > 0) ? 1u : 0u);
+      } else {  // P (bf16 pairs) x V tile used MN-major: 16 keys per instruction
+        const uint64_t dv = smem_desc_sw128(vb, L::kChunk, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts_if(issuer, tmem + colO, tmem + colS + kk * 8, dv + ((kk * 16 * 128) >> 4), idO,
+                    (np[t] > 0 || kk > 0) ? 1u : 0u);
+      }
     };
 
     sync_stage(0);
@@ -290,11 +323,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The common case (no score mod, positive scale, tile fully allowed) works on the
     // raw scores x: max over x, then p = exp2(x * k1 - m) in one FFMA + ex2.
     const bool raw_ok = !kAlibi && !kSoftcap && k1 > 0.f;
+    // FP8: the tile pair's dequantisation factor s_q s_k scales k1 (and kb stays)
+    const int qtile = q0 / BM + t;  // may lie past the last tile (then no key tile runs)
+    const float sqv = (kFp8 && qtile < a.nqt) ? a.sq[(size_t)bh * a.nqt + qtile] : 1.f;
     const int last_key = (p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1));
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0;
     bool live = true;
     for (int j = rng[t].lo; j < rng[t].hi; ++j, ++n) {
+      const float k1j = kFp8 ? k1 * sqv * a.sk[(size_t)bg * a.nkt + j] : k1;
       // Keep every decision warp-uniform: tcgen05.ld/st are warp-collective.
       if (live) live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[t]), n & 1, wc));
       if (!live) {  // aborted: keep the barrier schedule with the MMA warp, do nothing else
@@ -330,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e) {
             const int col = c * 32 + e;
             const float x = __uint_as_float(r[c][e]);
-            float s2 = kAlibi ? fmaf(x, k1, fmaf((float)col, kb, base)) : x * k1;
+            float s2 = kAlibi ? fmaf(x, k1j, fmaf((float)col, kb, base)) : x * k1j;
             if (kSoftcap) s2 = capA - 2.0f * capA * rcp_approx(1.0f + ex2_approx(s2));
             if (masked) s2 = (col >= c_lo && col <= c_hi) ? s2 : -INFINITY;
             mx[e & 7] = fmaxf(mx[e & 7], s2);
@@ -339,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                        fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      if (fast) mt *= k1;  // into log2 units
+      if (fast) mt *= k1j;  // into log2 units
       const float m_new = fmaxf(m_run, mt);
-      const bool grow = m_new > m_run + kRescaleLog2;
+      const bool grow = m_new > m_run + (kFp8 ? kRescaleLog2Fp8 : kRescaleLog2);
       const bool warp_grow = __any_sync(0xffffffffu, grow);
       float corr = 1.f;
       if (warp_grow) {
@@ -351,22 +388,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run *= corr;
       }
       const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-      const float mul = fast ? k1 : 1.f;  // p = exp2(v * mul - m)
+      const float mul = fast ? k1j : 1.f;  // p = exp2(v * mul - m)
       float acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+        if (kFp8) {  // P 2^7 as e4m3, four per column: 32 keys in 8 columns
+          uint32_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), mul, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
-          acc[(2 * e) & 7] += p0;
-          acc[(2 * e + 1) & 7] += p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 8; ++e) {
+            float pv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              pv[q] = ex2_approx(fmaf(__uint_as_float(r[c][4 * e + q]), mul, neg_m));
+              acc[(4 * e + q) & 7] += pv[q];
+            }
+            pk[e] = pack_e4m3x2(pv[0] * kPScaleFp8, pv[1] * kPScaleFp8) |
+                    (pack_e4m3x2(pv[2] * kPScaleFp8, pv[3] * kPScaleFp8) << 16);
+          }
+          tmem_st8(tS + c * 8, pk);
+        } else {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), mul, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
+            acc[(2 * e) & 7] += p0;
+            acc[(2 * e + 1) & 7] += p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + c * 16, pk);
         }
-        tmem_st16(tS + c * 16, pk);
       }
       l_run += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       if (warp_grow && n > 0) {  // O_t already holds P V of earlier tiles: rescale it
@@ -389,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool have_o = n > 0;  // O_t holds at least one P V product
     if (have_o) have_o = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full[t]), 0, wc));
     tc_fence_after_sync();
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    if (kFp8) inv *= a.sv[bg] * (1.f / kPScaleFp8);
     uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * p.Nq + (i < p.Nq ? i : 0)) * D);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
@@ -428,11 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kAlibi, bool kSoftcap>
+template <int D, bool kAlibi, bool kSoftcap, bool kFp8 = false>
 cudaError_t launch_variant(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int grid, cudaStream_t st) {
-  auto kern = fwd_tc_kernel<D, kAlibi, kSoftcap>;
-  const int smem = Layout<D>::kAlloc;
+  auto kern = fwd_tc_kernel<D, kAlibi, kSoftcap, kFp8>;
+  const int smem = Layout<D, kFp8>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
@@ -454,7 +508,7 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
 cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, __nv_bfloat16* o, float* lse,
                           cudaStream_t st) {
-  FwdArgs a;
+  FwdArgs a{};
   a.p = p;
   a.o = o;
   a.lse = lse;
@@ -464,6 +518,33 @@ cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtenso
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (p.d == 64) return launch_d<64>(a, tq, tk, tv, (int)grid, st);
   return launch_d<128>(a, tq, tk, tv, (int)grid, st);
+}
+
+}  // namespace attn
+
+namespace attn {
+
+cudaError_t launch_fwd_fp8_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tvt, const float* sq, const float* sk,
+                              const float* sv, __nv_bfloat16* o, float* lse, cudaStream_t st) {
+  FwdArgs a{};
+  a.p = p;
+  a.o = o;
+  a.lse = lse;
+  a.num_qblocks = ceil_div(p.Nq, kQTiles * BM);
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  a.nqt = ceil_div(p.Nq, BM);
+  a.nkt = ceil_div(p.Nkv, BN);
+  const long long grid = (long long)a.num_qblocks * p.B * p.Hq;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL || p.d != 128) return cudaErrorInvalidValue;
+  const bool al = p.score_kind & ATTN_SCORE_ALIBI, sc = p.score_kind & ATTN_SCORE_SOFTCAP;
+  if (al && sc) return launch_variant<128, true, true, true>(a, tq, tk, tvt, (int)grid, st);
+  if (al) return launch_variant<128, true, false, true>(a, tq, tk, tvt, (int)grid, st);
+  if (sc) return launch_variant<128, false, true, true>(a, tq, tk, tvt, (int)grid, st);
+  return launch_variant<128, false, false, true>(a, tq, tk, tvt, (int)grid, st);
 }
 
 }  // namespace attn

@@ -61,6 +61,19 @@ cudaError_t launch_classify(const MaskSpec& m, int32_t* classes, cudaStream_t st
 cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, __nv_bfloat16* o, float* lse,
                           cudaStream_t st);
+// FP8 forward (d = 128): tq, tk over e4m3 Q, K [B*H, N, 128]; tvt over e4m3 V^T
+// [B*Hkv, 128, Nkv rounded up to 16]; sq [B*Hq, ceil(Nq/128)], sk [B*Hkv, ceil(Nkv/128)],
+// sv [B*Hkv] dequantisation scales (device).
+cudaError_t launch_fwd_fp8_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tvt, const float* sq, const float* sk,
+                              const float* sv, __nv_bfloat16* o, float* lse, cudaStream_t st);
+// Quantisation to e4m3: tiles (one scale per 128 rows of [BH, N, d]) or, for V, one
+// scale per head with the output transposed to [BH, d, ceil16(N)] (zero padded).
+cudaError_t launch_quantize_tiles(const __nv_bfloat16* x, uint8_t* out, float* scales, int BH,
+                                  int N, int d, cudaStream_t st);
+cudaError_t launch_quantize_v_transposed(const __nv_bfloat16* x, uint8_t* out, float* scales,
+                                         int BH, int N, int d, cudaStream_t st);
+
 // Tensor maps of the backward: the 128-row V box (the tile a dK/dV CTA loads once) and
 // 64-row boxes (the slices both kernels stream).
 struct BwdMaps {

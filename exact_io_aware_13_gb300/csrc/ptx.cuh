@@ -362,6 +362,35 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// ---------------------------------------------------------------- 8-bit (e4m3) MMAs
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0), f32 D,
+// both operands K-major (8-bit operands are only used K-major here).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                       // D format f32
+         | (0u << 7) | (0u << 10)        // A, B format e4m3
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+// D (+)= A B^T, K = 32 per instruction, A and B in shared memory.
+__device__ __forceinline__ void mma_f8_ss_if(bool pred, uint32_t d_tmem, uint64_t adesc,
+                                             uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+      " @q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"((uint32_t)pred)
+      : "memory");
+}
+// Same with A in tensor memory: four e4m3 values per 32-bit column, the lowest byte
+// holding the lowest K index, so K = 32 spans 8 columns.
+__device__ __forceinline__ void mma_f8_ts_if(bool pred, uint32_t d_tmem, uint32_t a_tmem,
+                                             uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+      " @q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc), "r"((uint32_t)pred)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -377,6 +406,14 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two floats to two e4m3 bytes, round to nearest even, saturating at +-448; `lo` lands
+// in bits 7..0.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

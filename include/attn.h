@@ -196,6 +196,47 @@ attn_status attn_bwd_static_workspace(const void* q, const void* k, const void* 
                                       const attn_score_params* score_params, void* stream);
 
 /*
+ * FP8 forward with block scales ("FlashAttention/es", "Variantes y sucesores", and
+ * "FlashAttention-3 y torch.compile", section 2, name FP8 inputs for FlashAttention-3).
+ * The inputs are e4m3 codes plus fp32 dequantisation scales, as written by
+ * attn_quantize_fp8:
+ *   q8   e4m3 [B, Hq, Nq, 128],  q_scale [B*Hq, ceil(Nq/128)]  (one per 128-row tile)
+ *   k8   e4m3 [B, Hkv, Nkv, 128], k_scale [B*Hkv, ceil(Nkv/128)]
+ *   v8t  e4m3 [B, Hkv, 128, attn_fp8_v_row_bytes(Nkv)] (V transposed, keys contiguous,
+ *        zero padded), v_scale [B*Hkv] (one per head)
+ * so that Q = q8 * q_scale etc. The result is attention (same masks and score mods as
+ * attn_fwd) of those dequantised inputs, with P rounded to e4m3 (after a factor 2^7)
+ * for the P V product: per element |O_ic - O_exact_ic| <= 2^-4 sum_j P_ij |V_jc|
+ * + 2^-17 sum_j |V_jc| (over the row's allowed keys), plus bf16 rounding of O; lse is
+ * exact up to fp32 rounding. d must be 128.
+ * o: bf16 [B, Hq, Nq, 128]; lse: fp32 [B, Hq, Nq]. All pointers are DEVICE memory,
+ * tensors 16-byte aligned, scales 4-byte aligned. Allocates nothing.
+ */
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale,
+                         const float* k_scale, const float* v_scale, void* o, float* lse,
+                         int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale,
+                         int mask_kind, const attn_mask_params* mask_params, int score_kind,
+                         const attn_score_params* score_params, void* stream);
+
+/* Layouts of attn_quantize_fp8. */
+enum {
+  ATTN_FP8_TILES = 0,          /* Q, K: out [BH, N, d], scales [BH, ceil(N/128)] */
+  ATTN_FP8_V_TRANSPOSED = 1    /* V: out [BH, d, attn_fp8_v_row_bytes(N)], scales [BH] */
+};
+
+/* Row length in bytes of the transposed e4m3 V: Nkv rounded up to 16 (0 if Nkv <= 0). */
+size_t attn_fp8_v_row_bytes(int Nkv);
+
+/*
+ * bf16 x [BH, N, d] (d = 64 or 128, DEVICE) to e4m3 codes and fp32 scales: each
+ * block (a 128-row tile for ATTN_FP8_TILES, a whole head for ATTN_FP8_V_TRANSPOSED)
+ * gets s = amax / 448 (1 for an all-zero block) and code = e4m3(x / s), an IEEE fp32
+ * division rounded to nearest even. Deterministic. x and out 16-byte aligned.
+ */
+attn_status attn_quantize_fp8(const void* x, void* out, float* scales, int BH, int N, int d,
+                              int layout, void* stream);
+
+/*
  * Block-sparsity classifier ("El FlexAttention de PyTorch con FlashAttention-4 es
  * un cambio radical", "Limitaciones actuales", names block sparsity): writes
  * classes[r * ceil(Nkv/128) + c] = EMPTY / PARTIAL / FULL for query tile r and key
