@@ -28,11 +28,12 @@
 // FP8 variant (kFp8, d = 128): Q and K are e4m3 with one scale per 128-row tile, V is
 // e4m3 stored transposed ([d, keys] per head, keys contiguous) with one scale per head,
 // so both MMAs read K-major 8-bit operands (kind::f8f6f4, K = 32 per instruction). The
-// score of a tile pair is scale * s_q * s_k * (Q8 K8^T); P is multiplied by 2^7 and
-// rounded to e4m3 before P V (so values down to 2^-16 keep a relative error of 2^-4 and
-// smaller ones an absolute error of at most 2^-17); the row sums l use the unrounded P,
-// and the epilogue multiplies O by s_v 2^-7 / l. The running max may lag the true max
-// by at most 2^1 here (not 2^8), so P <= 2 and P 2^7 <= 256 stays below e4m3's 448.
+// score of a tile pair is scale * s_q * s_k * (Q8 K8^T); P is computed as
+// exp2(s - m + 7) = 2^7 P and rounded to e4m3 before P V (so values down to 2^-16 keep a
+// relative error of 2^-4 and smaller ones an absolute error of at most 2^-17); the row
+// sums l add up the unrounded 2^7 P, and the epilogue multiplies O by s_v / l (the 2^7
+// cancels) and subtracts 7 from log2 l for the LSE. The running max may lag the true
+// max by at most 2^1 here (not 2^8), so 2^7 P <= 256 stays below e4m3's 448.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -56,7 +57,7 @@ constexpr int kHeadGroup = 4;  // heads whose CTAs are scheduled together (L2 re
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 constexpr float kRescaleLog2Fp8 = 1.0f;  // FP8: P = exp2(s - m) <= 2, so P 2^7 fits e4m3
-constexpr float kPScaleFp8 = 128.0f;     // P is scaled by 2^7 before rounding to e4m3
+constexpr float kPScaleLog2Fp8 = 7.0f;  // P is scaled by 2^7 before rounding to e4m3
 
 template <int D, bool kFp8>
 struct Layout {
@@ -387,14 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_new;
         l_run *= corr;
       }
-      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+      // FP8: exp2(s - m + 7) = 2^7 p, the scale e4m3 rounding wants, at no extra cost
+      const float neg_m = (m_run == -INFINITY ? 0.f : -m_run) + (kFp8 ? kPScaleLog2Fp8 : 0.f);
       const float mul = fast ? k1j : 1.f;  // p = exp2(v * mul - m)
       float acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        if (kFp8) {  // P 2^7 as e4m3, four per column: 32 keys in 8 columns
+        if (kFp8) {  // 2^7 P as e4m3, four per column: 32 keys in 8 columns
           uint32_t pk[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -404,8 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pv[q] = ex2_approx(fmaf(__uint_as_float(r[c][4 * e + q]), mul, neg_m));
               acc[(4 * e + q) & 7] += pv[q];
             }
-            pk[e] = pack_e4m3x2(pv[0] * kPScaleFp8, pv[1] * kPScaleFp8) |
-                    (pack_e4m3x2(pv[2] * kPScaleFp8, pv[3] * kPScaleFp8) << 16);
+            pk[e] = pack_e4m3x2(pv[0], pv[1]) | (pack_e4m3x2(pv[2], pv[3]) << 16);
           }
           tmem_st8(tS + c * 8, pk);
         } else {
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (have_o) have_o = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full[t]), 0, wc));
     tc_fence_after_sync();
     float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    if (kFp8) inv *= a.sv[bg] * (1.f / kPScaleFp8);
+    if (kFp8) inv *= a.sv[bg];  // l holds 2^7 times the row sum, like O
     uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * p.Nq + (i < p.Nq ? i : 0)) * D);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
@@ -470,7 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (i < p.Nq)
       a.lse[(size_t)bh * p.Nq + i] =
-          l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+          l_run > 0.f ? (m_run + log2f(l_run) - (kFp8 ? kPScaleLog2Fp8 : 0.f)) *
+                            0.69314718055994531f
+                      : -INFINITY;
   }
   __syncwarp();
 
