@@ -143,3 +143,113 @@ def make_inputs(w: Workload, *, with_dout: Optional[bool] = None):
 def random_doc_offsets(total: int, seed: int, lo: int, hi: int) -> np.ndarray:
     """Offsets for a small packed sequence (test sizes), same drawing rule."""
     return document_offsets(total, seed, lo, hi)
+
+
+# ---------------------------------------------------------------- paged decode
+# Inference side of the pages: the KV cache is cut into fixed-size pages ("FlashAttention/es",
+# "Variantes y sucesores", names PagedAttention's segmented KV cache for serving many
+# sequences at once), and each step attends the newest Nq query tokens of every sequence
+# to all of its cached keys. Shapes follow the GQA workload (Hq = 32, Hkv = 8, d = 128).
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    seed: int
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int            # new query tokens per sequence (1 = one decode step)
+    d: int
+    len_min: int       # cached keys per sequence, drawn uniformly from [len_min, len_max]
+    len_max: int
+    page_size: int
+    mask_kind: int = MASK_NONE
+    window: int = 0
+    score_kind: int = SCORE_NONE
+    softcap: float = 0.0
+    lengths: Optional[tuple] = None  # explicit lengths (override the draw)
+    spare_pages: int = 3             # pool pages no sequence uses
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.d)))
+
+    def replace(self, **kw) -> "DecodeWorkload":
+        return dataclasses.replace(self, **kw)
+
+    def describe(self) -> str:
+        s = (f"{self.name}: B={self.B} Hq={self.Hq} Hkv={self.Hkv} Nq={self.Nq} d={self.d} "
+             f"len=[{self.len_min},{self.len_max}] page={self.page_size} "
+             f"mask={MASK_NAMES[self.mask_kind]}")
+        if self.mask_kind == MASK_SLIDING_WINDOW:
+            s += f" W={self.window}"
+        if self.score_kind & SCORE_ALIBI:
+            s += " +alibi"
+        if self.score_kind & SCORE_SOFTCAP:
+            s += f" +softcap{self.softcap:g}"
+        return s
+
+
+PAGED_DECODE = DecodeWorkload("paged decode", 5, B=64, Hq=32, Hkv=8, Nq=1, d=128,
+                              len_min=512, len_max=8192, page_size=64)
+
+_PAGE_BLOCK = 1024  # pages drawn per randn call (bounds the float32 temporaries)
+
+
+def decode_lengths(w: DecodeWorkload) -> np.ndarray:
+    if w.lengths is not None:
+        return np.asarray(w.lengths, dtype=np.int32)
+    rng = np.random.default_rng(w.seed)
+    return rng.integers(w.len_min, w.len_max, size=w.B, endpoint=True).astype(np.int32)
+
+
+def make_decode_inputs(w: DecodeWorkload, *, poison_unused: bool = False):
+    """Seeded paged-decode inputs (CPU):
+
+    q          bf16 [B, Hq, Nq, d]
+    k_cache    bf16 [num_pages, Hkv, page_size, d]   (a page holds page_size tokens
+    v_cache    bf16 [num_pages, Hkv, page_size, d]    of one sequence, per kv head)
+    page_table int32 [B, max_pages]  (page of token t of sequence b: page_table[b, t // page_size];
+                                      entries past the sequence hold -1)
+    seq_lens   int32 [B]
+
+    Recipe: lengths from ``numpy.random.default_rng(seed).integers(len_min, len_max,
+    endpoint=True, size=B)``; each sequence takes ceil(len / page_size) pages, and the pool
+    (those plus ``spare_pages``) is shuffled by ``rng.permutation`` of the same generator;
+    values from ``torch.Generator('cpu').manual_seed(seed)``: q, then K pages and V pages
+    in blocks of 1024 pages, float32 ``randn`` rounded to bf16. ``poison_unused`` writes NaN
+    into every cache slot no sequence owns (the unused tail of a last page, the spare
+    pages), which no correct kernel may let into a result.
+    """
+    lens = decode_lengths(w)
+    rng = np.random.default_rng(w.seed)
+    if w.lengths is None:
+        rng.integers(w.len_min, w.len_max, size=w.B, endpoint=True)  # same stream position
+    ps = w.page_size
+    need = [(int(n) + ps - 1) // ps for n in lens]
+    num_pages = int(sum(need)) + w.spare_pages
+    perm = rng.permutation(num_pages).astype(np.int32)
+    max_pages = max(1, (int(w.len_max) + ps - 1) // ps, max(need, default=0))
+    table = np.full((w.B, max_pages), -1, dtype=np.int32)
+    at = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[at:at + n]
+        at += n
+    g = torch.Generator("cpu").manual_seed(w.seed)
+    q = torch.randn((w.B, w.Hq, w.Nq, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    caches = []
+    for _ in range(2):
+        c = torch.empty((num_pages, w.Hkv, ps, w.d), dtype=torch.bfloat16)
+        for p0 in range(0, num_pages, _PAGE_BLOCK):
+            p1 = min(num_pages, p0 + _PAGE_BLOCK)
+            c[p0:p1] = torch.randn((p1 - p0, w.Hkv, ps, w.d), generator=g, dtype=torch.float32)
+        caches.append(c)
+    k_cache, v_cache = caches
+    if poison_unused:
+        owned = np.zeros((num_pages, ps), dtype=bool)
+        for b, n in enumerate(lens):
+            t = np.arange(int(n))
+            owned[table[b, t // ps], t % ps] = True
+        bad = torch.from_numpy(~owned)[:, None, :, None].expand(-1, w.Hkv, -1, w.d)
+        k_cache[bad] = float("nan")
+        v_cache[bad] = float("nan")
+    return q, k_cache, v_cache, torch.from_numpy(table), torch.from_numpy(lens.copy())
