@@ -3,7 +3,8 @@ online softmax, backward rebuilding P from the LSE) on the causal fwd+bwd worklo
 (B=2, H=16, N=8192, d=128, bf16), timed with CUDA events.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload fwd_bwd|causal_fwd|gqa_window_fwd|docs_fwd|tiny_fwd|fp8_causal_fwd]
+                [--workload fwd_bwd|causal_fwd|gqa_window_fwd|docs_fwd|tiny_fwd|fp8_causal_fwd
+                            |paged_decode]
 
 Prints one JSON line. `value` is useful TFLOP/s (masked-out work excluded) summed
 over ranks; with N > 1 each rank runs its own replica of the workload (the heads
@@ -12,7 +13,8 @@ float64 CPU oracle on a bounded sample of the same workload on the host cores.
 --workload picks one of the other workloads; those are forward-only, so a step is
 one forward pass and the line reports the forward's useful TFLOP/s. fp8_causal_fwd
 runs the FP8 forward (e4m3 inputs with block scales, quantised once before the timed
-steps; the end-to-end number includes the quantisation).
+steps; the end-to-end number includes the quantisation). paged_decode times one decode
+step over a paged KV cache and reports GB/s against the HBM roofline.
 """
 from __future__ import annotations
 
@@ -31,8 +33,8 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import (CAUSAL, CAUSAL_FWD_BWD, DOCS, GQA_WINDOW, MASK_NAMES, TINY,  # noqa: E402
-                       make_inputs)
+from workloads import (CAUSAL, CAUSAL_FWD_BWD, DOCS, GQA_WINDOW, MASK_NAMES,  # noqa: E402
+                       PAGED_DECODE, TINY, make_decode_inputs, make_inputs)
 
 FWD_WORKLOADS = {"causal_fwd": CAUSAL, "gqa_window_fwd": GQA_WINDOW, "docs_fwd": DOCS,
                  "tiny_fwd": TINY, "fp8_causal_fwd": CAUSAL}
@@ -430,6 +432,121 @@ def run_forward(args, w, fp8=False):
         print(json.dumps(line), flush=True)
 
 
+def run_decode(args, w):
+    """Paged decode: a step is one attn_decode_paged call (the decode kernel and, when the
+    keys are split, the combine kernel) over every sequence of the workload. The KV cache
+    is resident state (uploaded once, like weights); a step's inputs are the new queries,
+    the page table and the lengths."""
+    from exact_io_aware_13_gb300 import build as libbuild
+    libbuild.build()
+    import exact_io_aware_13_gb300 as ea
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, kc, vc, table, lens = make_decode_inputs(w)
+    host = [t.pin_memory() for t in (q, table, lens)]
+    qd, td, ld = (t.to(dev) for t in host)
+    kcd, vcd = kc.to(dev), vc.to(dev)
+    del kc, vc
+    total = int(lens.sum())
+    kv_bytes = total * w.Hkv * w.d * 2 * 2
+    io_bytes = kv_bytes + q.numel() * 2 * 2 + q.numel() // w.d * 4  # + Q in, O out, LSE out
+    pairs = total * w.Hq * w.Nq  # every query sees every cached key (one decode token)
+    f_step = 4 * w.d * pairs
+    split = ea.decode_split_keys(w.B, w.Hq, w.Hkv, w.Nq, total)
+    msl = w.len_max
+    o = torch.empty((w.B, w.Hq, w.Nq, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+    nws = ea.decode_workspace_size(w.B, w.Hq, w.Nq, w.d, msl, split)
+    ws = torch.empty((max(nws, 256),), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    kw = dict(max_seq_len=msl, split_keys=split, scale=w.scale, mask_kind=w.mask_kind,
+              window=w.window, score_kind=w.score_kind, softcap=w.softcap)
+
+    def step():
+        ea.decode_paged_into(qd, kcd, vcd, td, ld, o, lse, ws if nws else None, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ea.device_status() != 0:
+        raise RuntimeError("a kernel reported a device error during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(args.steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            step()
+            ev[s][1].record(stream)
+        torch.cuda.synchronize()
+    if ea.device_status() != 0:
+        raise RuntimeError("a kernel reported a device error during the timed steps")
+    times = [e[0].elapsed_time(e[1]) for e in ev]
+    t_all = sum(times)
+    if world > 1:
+        t_all = max_over_ranks(t_all, dev)
+    ms_step = t_all / args.steps
+    gbs = world * io_bytes / (ms_step * 1e-3) / 1e9
+    outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in outs_host)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for dst, src in zip((qd, td, ld), host):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(outs_host, (o, lse)):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    pk = peaks()
+    ms_mean = statistics.mean(times)
+    ach = io_bytes / (ms_mean * 1e-3) / 1e9
+    launches = 1 if nws == 0 else 2
+    line = {
+        "metric": "attention paged decode: GB/s of KV cache, queries and outputs moved, and % "
+                  "of measured GB300 HBM copy bandwidth",
+        "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded randn rounded to bf16; seeded lengths and shuffled pages)",
+        "config": {"workload": w.describe(), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq,
+                   "d": w.d, "page_size": w.page_size, "kv_tokens": total,
+                   "split_keys": split, "seed": w.seed,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"flushed between steps (256 MiB write); KV cache {kv_bytes >> 20} MiB"},
+        "pct_of_peak": round(100 * gbs / world / pk["hbm_gbs"], 1),
+        "tflops": round(world * f_step / (ms_step * 1e-3) / 1e12, 2),
+        "kernels": {"decode_tc_kernel+decode_combine_kernel": {
+            "ms": round(ms_mean, 4), "min_ms": round(min(times), 4), "achieved": round(ach, 1),
+            "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4)}},
+        "roofline": {"bound": "hbm", "kernel": "decode_tc_kernel (+ combine, timed together)",
+                     "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(ach / pk["hbm_gbs"], 4),
+                     "peak_source": pk["source"] + " HBM copy", "traffic": None},
+        "e2e": {"value": round(world * io_bytes / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(ms_e2e, 4)},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+    }
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def cpu_baseline(w, seconds: float = 20.0, heads: int = 1):
     """Time the float64 oracle (forward + backward) on `heads` (b, h) heads of the
     workload, full sequence, on the host cores."""
@@ -494,12 +611,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="fwd_bwd", choices=["fwd_bwd", *FWD_WORKLOADS])
+    ap.add_argument("--workload", default="fwd_bwd",
+                    choices=["fwd_bwd", *FWD_WORKLOADS, "paged_decode"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "paged_decode":
+        run_decode(args, PAGED_DECODE)
     elif args.workload != "fwd_bwd":
         run_forward(args, FWD_WORKLOADS[args.workload], fp8=args.workload.startswith("fp8"))
     else:

@@ -16,7 +16,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "attn.h")
 ATTN_OK = 0
 STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_ARG", 2: "ATTN_ERR_SHAPE", 3: "ATTN_ERR_ALIGN",
                 4: "ATTN_ERR_ARCH", 5: "ATTN_ERR_WORKSPACE", 6: "ATTN_ERR_LAUNCH",
-                7: "ATTN_ERR_DEVICE_TIMEOUT"}
+                7: "ATTN_ERR_DEVICE_TIMEOUT", 8: "ATTN_ERR_DEVICE_INPUT"}
 
 
 class MaskParams(ctypes.Structure):
@@ -50,6 +50,10 @@ SIGNATURES = {
     "attn_fwd_fp8": (_I, [_P] * 8 + [_I, _I, _I, _I, _I, _I, _F, _I, _MP, _I, _SP, _P]),
     "attn_fp8_v_row_bytes": (ctypes.c_size_t, [_I]),
     "attn_quantize_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    "attn_decode_paged": (_I, [_P] * 7 + [_I] * 10 + [_F, _I, _MP, _I, _SP, _P, ctypes.c_size_t,
+                                                     _P]),
+    "attn_decode_workspace_size": (ctypes.c_size_t, [_I] * 6),
+    "attn_decode_split_keys": (_I, [_I, _I, _I, _I, ctypes.c_longlong, _I]),
     "attn_device_status": (_I, [_P]),
     "attn_strerror": (ctypes.c_char_p, [_I]),
 }
@@ -61,7 +65,8 @@ def header_functions() -> list[str]:
     """Names of the functions include/attn.h declares."""
     with open(HEADER) as f:
         text = f.read()
-    return re.findall(r"^\s*(?:attn_status|size_t|const char\*)\s+(attn_\w+)\s*\(", text, re.M)
+    return re.findall(r"^\s*(?:attn_status|size_t|int|const char\*)\s+(attn_\w+)\s*\(", text,
+                      re.M)
 
 
 def load() -> ctypes.CDLL:

@@ -226,3 +226,72 @@ def forward_fp8(q, k, v, *, scale: Optional[float] = None, mask_kind: int = MASK
                  mask_kind=mask_kind, window=window, doc_offsets=doc_offsets,
                  score_kind=score_kind, softcap=softcap, stream=stream)
     return o, lse, quant
+
+
+# ---------------------------------------------------------------- paged decode
+def decode_split_keys(B: int, Hq: int, Hkv: int, Nq: int, total_kv_tokens: int,
+                      num_sms: Optional[int] = None) -> int:
+    """The library's split size for a decode call (keys per chunk)."""
+    if num_sms is None:
+        num_sms = (torch.cuda.get_device_properties(torch.cuda.current_device())
+                   .multi_processor_count if torch.cuda.is_available() else 0)
+    return int(_lib.load().attn_decode_split_keys(int(B), int(Hq), int(Hkv), int(Nq),
+                                                  int(total_kv_tokens), int(num_sms)))
+
+
+def decode_workspace_size(B: int, Hq: int, Nq: int, d: int, max_seq_len: int,
+                          split_keys: int) -> int:
+    return int(_lib.load().attn_decode_workspace_size(int(B), int(Hq), int(Nq), int(d),
+                                                      int(max_seq_len), int(split_keys)))
+
+
+def decode_paged_into(q, k_cache, v_cache, page_table, seq_lens, o, lse, workspace, *,
+                      max_seq_len: int, split_keys: int, scale: float,
+                      mask_kind: int = MASK_NONE, window: int = 0, score_kind: int = SCORE_NONE,
+                      softcap: float = 0.0, stream=None) -> None:
+    """attn_decode_paged on caller-owned tensors (see include/attn.h for the layouts):
+    q [B, Hq, Nq, d], caches [pages, Hkv, page_size, d], page_table int32 [B, max_pages],
+    seq_lens int32 [B]; writes o and lse."""
+    _check_tensors(q, k_cache, v_cache, page_table, seq_lens, o, lse, workspace)
+    B, Hq, Nq, d = q.shape
+    num_pages, Hkv, page_size, dk = k_cache.shape
+    if dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must be [pages, Hkv, page_size, d]")
+    if page_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("page_table and seq_lens must be int32")
+    if page_table.dim() != 2 or page_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("page_table must be [B, max_pages] and seq_lens [B]")
+    mp, sp, _keep = _params(mask_kind, window, None, softcap)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.load().attn_decode_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seq_lens), _ptr(o),
+        _ptr(lse), B, Hq, Hkv, Nq, d, num_pages, page_size, page_table.shape[1],
+        int(max_seq_len), int(split_keys), ctypes.c_float(scale), mask_kind, mp, score_kind, sp,
+        _ptr(workspace), ctypes.c_size_t(ws_bytes), _stream(stream))
+    _lib.check(st, "attn_decode_paged")
+
+
+def decode_paged(q, k_cache, v_cache, page_table, seq_lens, *, max_seq_len: Optional[int] = None,
+                 split_keys: Optional[int] = None, total_kv_tokens: Optional[int] = None,
+                 scale: Optional[float] = None, mask_kind: int = MASK_NONE, window: int = 0,
+                 score_kind: int = SCORE_NONE, softcap: float = 0.0, stream=None):
+    """Allocating wrapper of decode_paged_into: returns (o, lse). max_seq_len defaults to
+    the page table's capacity; split_keys to the library's choice for total_kv_tokens
+    (default B * max_seq_len)."""
+    B, Hq, Nq, d = q.shape
+    Hkv, page_size = k_cache.shape[1], k_cache.shape[2]
+    if max_seq_len is None:
+        max_seq_len = page_table.shape[1] * page_size
+    if split_keys is None:
+        split_keys = decode_split_keys(B, Hq, Hkv, Nq, total_kv_tokens or B * max_seq_len)
+    if scale is None:
+        scale = float(d) ** -0.5
+    o = torch.empty((B, Hq, Nq, d), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    nbytes = decode_workspace_size(B, Hq, Nq, d, max_seq_len, split_keys)
+    ws = torch.empty((nbytes,), dtype=torch.uint8, device=q.device) if nbytes else None
+    decode_paged_into(q, k_cache, v_cache, page_table, seq_lens, o, lse, ws,
+                      max_seq_len=max_seq_len, split_keys=split_keys, scale=scale,
+                      mask_kind=mask_kind, window=window, score_kind=score_kind, softcap=softcap,
+                      stream=stream)
+    return o, lse

@@ -19,6 +19,9 @@ namespace {
 __device__ int g_device_status;
 
 constexpr int kMaxDevices = 64;
+// Bit of the device status word that bounded waits set (DEV_TIMEOUT in the kernels);
+// any other set bit reports an out-of-range device input.
+constexpr int DEV_TIMEOUT_BIT = 1;
 
 struct DeviceInfo {
   bool probed = false;
@@ -282,6 +285,20 @@ attn_status make_map8(CUtensorMap* map, const void* base, int dx, int dy, int dz
 
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+// ---------------------------------------------------------------- paged decode
+// Page sizes whose 64-key tiles never straddle a page: 8, 16, 32 (several pages per
+// tile) or any multiple of 64.
+bool decode_page_size_ok(int ps) { return ps == 8 || ps == 16 || ps == 32 || (ps > 0 && ps % 64 == 0); }
+
+long long decode_chunks(int max_seq_len, int split_keys) {
+  return max_seq_len <= 0 ? 1 : ((long long)max_seq_len + split_keys - 1) / split_keys;
+}
+
+// Split-mode scratch: L2 of every (chunk, row), then O of every (chunk, row).
+size_t decode_lse_plane(long long n_chunks, long long rows) {
+  return round256((size_t)(n_chunks * rows) * sizeof(float));
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -417,6 +434,109 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const 
   return from_cuda(launch_fwd_fp8_tc(p, tq, tk, tvt, q_scale, k_scale, v_scale, ob, lse, st));
 }
 
+int attn_decode_split_keys(int B, int Hq, int Hkv, int Nq, long long total_kv_tokens,
+                           int num_sms) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || total_kv_tokens <= 0 || Hq % Hkv != 0)
+    return 256;
+  const long long rows = (long long)(Hq / Hkv) * Nq;
+  const long long row_tiles = (rows + 127) / 128;
+  // about sixteen waves of two resident CTAs per SM
+  const long long target = 32LL * (num_sms > 0 ? num_sms : 148);
+  const long long work = total_kv_tokens * Hkv * row_tiles;
+  long long keys = (work + target - 1) / target;
+  keys = (keys + 63) / 64 * 64;
+  if (keys < 256) keys = 256;
+  if (keys > (1 << 24)) keys = 1 << 24;
+  return (int)keys;
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int Nq, int d, int max_seq_len, int split_keys) {
+  if (B <= 0 || Hq <= 0 || Nq <= 0 || d <= 0 || split_keys <= 0) return 0;
+  const long long n = decode_chunks(max_seq_len, split_keys);
+  if (n <= 1) return 0;
+  const long long rows = (long long)B * Hq * Nq;
+  return decode_lse_plane(n, rows) + round256((size_t)(n * rows) * d * sizeof(float));
+}
+
+attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* page_table, const int32_t* seq_lens, void* o,
+                              float* lse, int B, int Hq, int Hkv, int Nq, int d, int num_pages,
+                              int page_size, int max_pages_per_seq, int max_seq_len,
+                              int split_keys, float scale, int mask_kind,
+                              const attn_mask_params* mask_params, int score_kind,
+                              const attn_score_params* score_params, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || Nq < 0 || num_pages < 0 || max_pages_per_seq < 0 ||
+      max_seq_len < 0)
+    return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_SHAPE;
+  if (Hkv == 0 ? Hq != 0 : (Hq % Hkv) != 0) return ATTN_ERR_SHAPE;
+  if (!decode_page_size_ok(page_size)) return ATTN_ERR_SHAPE;
+  if ((long long)max_seq_len > (long long)max_pages_per_seq * page_size) return ATTN_ERR_SHAPE;
+  if (split_keys <= 0 || split_keys % 64 != 0) return ATTN_ERR_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_ARG;
+  if (mask_kind != ATTN_MASK_NONE && mask_kind != ATTN_MASK_CAUSAL &&
+      mask_kind != ATTN_MASK_SLIDING_WINDOW)
+    return ATTN_ERR_ARG;
+  if (score_kind & ~(ATTN_SCORE_ALIBI | ATTN_SCORE_SOFTCAP)) return ATTN_ERR_ARG;
+  DecodeProblem p{};
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Nq = Nq; p.d = d;
+  p.page_size = page_size; p.max_pages = max_pages_per_seq; p.num_pages = num_pages;
+  p.max_seq_len = max_seq_len;
+  p.chunk = split_keys;
+  p.scale = scale;
+  p.score_kind = score_kind;
+  p.mask_kind = mask_kind;
+  if (score_kind & ATTN_SCORE_SOFTCAP) {
+    if (!score_params || !(score_params->softcap > 0.f) || !std::isfinite(score_params->softcap))
+      return ATTN_ERR_ARG;
+    p.softcap = score_params->softcap;
+  }
+  if (mask_kind == ATTN_MASK_SLIDING_WINDOW) {
+    if (!mask_params || mask_params->window < 0) return ATTN_ERR_ARG;
+    p.window = mask_params->window;
+  }
+  const long long rows_total = (long long)B * Hq * Nq;
+  if (rows_total == 0) return ATTN_OK;
+  const long long n_chunks = decode_chunks(max_seq_len, split_keys);
+  const long long row_tiles = ((long long)(Hq / Hkv) * Nq + 127) / 128;
+  if (rows_total > 0x7fffffffLL || (long long)B * Hkv * row_tiles > 65535 ||
+      (long long)num_pages * Hkv * page_size > 0x7fffffffLL || n_chunks > 0x7fffffffLL)
+    return ATTN_ERR_SHAPE;
+  p.n_chunks = (int)n_chunks;
+  if (!q || !o || !lse || !seq_lens) return ATTN_ERR_ARG;
+  if (max_seq_len > 0 && (!k_cache || !v_cache || !page_table || num_pages == 0))
+    return ATTN_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      !aligned16(lse) || !aligned4(page_table) || !aligned4(seq_lens))
+    return ATTN_ERR_ALIGN;
+  const size_t need = attn_decode_workspace_size(B, Hq, Nq, d, max_seq_len, split_keys);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  attn_status s = current_device(&dev);
+  if (s != ATTN_OK) return s;
+  p.status = dev->status;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto* ob = static_cast<__nv_bfloat16*>(o);
+  if (max_seq_len == 0) return from_cuda(launch_fill_masked(rows_total, d, ob, lse, st));
+  DecodeOut out{ob, lse, nullptr, nullptr};
+  if (need > 0) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    out.part_lse = reinterpret_cast<float*>(ws);
+    out.part_o = reinterpret_cast<float*>(ws + decode_lse_plane(n_chunks, rows_total));
+  }
+  CUtensorMap tq, tk, tv;
+  const int kv_rows = num_pages * Hkv * page_size;
+  const unsigned box = page_size < 64 ? (unsigned)page_size : 64u;
+  if ((s = make_map(&tq, q, 1, (int)rows_total, d, 128)) != ATTN_OK) return s;
+  if ((s = make_map(&tk, k_cache, 1, kv_rows, d, box)) != ATTN_OK) return s;
+  if ((s = make_map(&tv, v_cache, 1, kv_rows, d, box)) != ATTN_OK) return s;
+  return from_cuda(launch_decode_tc(p, tq, tk, tv, out, st));
+}
+
 attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_params, int Nq,
                                 int Nkv, int32_t* classes, void* stream) {
   Problem p;
@@ -443,7 +563,7 @@ attn_status attn_device_status(void* stream) {
     const int zero = 0;
     if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
       return ATTN_ERR_LAUNCH;
-    return ATTN_ERR_DEVICE_TIMEOUT;
+    return (value & DEV_TIMEOUT_BIT) ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_ERR_DEVICE_INPUT;
   }
   return ATTN_OK;
 }
@@ -458,6 +578,8 @@ const char* attn_strerror(attn_status status) {
     case ATTN_ERR_WORKSPACE: return "workspace missing or smaller than attn_bwd_workspace_size";
     case ATTN_ERR_LAUNCH: return "CUDA launch or driver call failed";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    case ATTN_ERR_DEVICE_INPUT:
+      return "a kernel met an out-of-range device input (sequence length or page index)";
   }
   return "unknown status";
 }

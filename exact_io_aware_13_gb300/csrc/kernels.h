@@ -84,4 +84,41 @@ cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms&
                           const __nv_bfloat16* k, __nv_bfloat16* dq, __nv_bfloat16* dk,
                           __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st);
 
+// ---- Paged decode.
+// Keys [lo, hi) that query i of the Nq newest tokens of a sequence with L cached tokens
+// may see: query i sits at position L - Nq + i; causal stops at that position, the
+// sliding window also starts `window - 1` keys before it. hi == lo when none.
+ATTN_HD void decode_row_keys(int mask_kind, int window, int L, int Nq, int i, int& lo, int& hi) {
+  const int pos = L - Nq + i;
+  lo = 0;
+  hi = L;
+  if (mask_kind != ATTN_MASK_NONE) hi = imin(L, pos + 1);
+  if (mask_kind == ATTN_MASK_SLIDING_WINDOW) lo = window > pos ? 0 : pos - window + 1;
+  if (hi < lo) hi = lo;
+}
+
+struct DecodeProblem {
+  int B, Hq, Hkv, Nq, d;
+  int page_size, max_pages, num_pages;
+  int max_seq_len;           // bound on seq_lens (<= max_pages * page_size)
+  int chunk;                 // keys per split (a multiple of 64)
+  int n_chunks;              // ceil(max_seq_len / chunk): grid x; 1 = no combine
+  float scale, softcap;
+  int score_kind, mask_kind, window;
+  const int32_t* page_table;  // [B, max_pages] device
+  const int32_t* seq_lens;    // [B] device
+  int* status;
+};
+struct DecodeOut {
+  __nv_bfloat16* o;  // [B, Hq, Nq, d]
+  float* lse;        // [B, Hq, Nq], natural log
+  float* part_o;     // split mode: [n_chunks, B*Hq*Nq, d] fp32, O_c / l_c
+  float* part_lse;   // split mode: [n_chunks, B*Hq*Nq], m_c + log2 l_c
+};
+// tq: [B*Hq*Nq, d] bf16, box 64 x 128; tk, tv: [pages*Hkv*page_size, d] bf16, box
+// 64 x min(page_size, 64). Launches the decode kernel and, with n_chunks > 1, the
+// combine kernel.
+cudaError_t launch_decode_tc(const DecodeProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                             const CUtensorMap& tv, const DecodeOut& out, cudaStream_t st);
+
 }  // namespace attn

@@ -8,8 +8,8 @@
 
 namespace attn {
 
-// Device-side error codes written to the library's status word.
-enum : int { DEV_OK = 0, DEV_TIMEOUT = 1 };
+// Device-side status bits, OR-ed into the library's status word.
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INPUT = 2 };
 
 // A wait gives up after this many nanoseconds of %globaltimer (each wait in these
 // kernels is on work of the same CTA and normally lasts microseconds).
@@ -83,7 +83,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
       if (*w.abort_smem) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
         *w.abort_smem = 1;
-        atomicExch(w.status_gmem, DEV_TIMEOUT);
+        atomicOr(w.status_gmem, DEV_TIMEOUT);
         return false;
       }
     }

@@ -65,7 +65,9 @@ typedef enum {
   ATTN_ERR_ARCH = 4,           /* the current device is not compute capability 10.3 */
   ATTN_ERR_WORKSPACE = 5,      /* workspace NULL or smaller than attn_bwd_workspace_size */
   ATTN_ERR_LAUNCH = 6,         /* a CUDA runtime/driver call or a launch failed */
-  ATTN_ERR_DEVICE_TIMEOUT = 7  /* a kernel's bounded wait expired (attn_device_status) */
+  ATTN_ERR_DEVICE_TIMEOUT = 7, /* a kernel's bounded wait expired (attn_device_status) */
+  ATTN_ERR_DEVICE_INPUT = 8    /* a kernel met an out-of-range DEVICE input: a decode
+                                  sequence length or page index (attn_device_status) */
 } attn_status;
 
 enum {
@@ -237,6 +239,66 @@ attn_status attn_quantize_fp8(const void* x, void* out, float* scales, int BH, i
                               int layout, void* stream);
 
 /*
+ * Decode over a paged KV cache ("FlashAttention/es", "Variantes y sucesores", names
+ * PagedAttention, which cuts the inference KV cache into fixed-size pages shared by
+ * many sequences). One call attends the Nq newest query tokens of each of B sequences
+ * to every cached token of that sequence.
+ *
+ *   q          bf16 [B, Hq, Nq, d]  query i of sequence b sits at position
+ *                                   seq_lens[b] - Nq + i (its own K/V are already in
+ *                                   the cache)
+ *   k_cache,   bf16 [num_pages, Hkv, page_size, d]: page p, kv head g, slot s
+ *   v_cache
+ *   page_table int32 [B, max_pages_per_seq]: token t of sequence b is in page
+ *              page_table[b][t / page_size], slot t % page_size
+ *   seq_lens   int32 [B]: cached tokens per sequence, 0 <= seq_lens[b] <= max_seq_len
+ *   o          bf16 [B, Hq, Nq, d];  lse fp32 [B, Hq, Nq] (natural log)
+ * All pointers are DEVICE memory; tensors 16-byte aligned, page_table and seq_lens
+ * 4-byte aligned. page_table and seq_lens are read on the device only; a length
+ * outside [0, max_seq_len] or a page index outside [0, num_pages) for a token the call
+ * reads makes attn_device_status report ATTN_ERR_DEVICE_INPUT (the results of that
+ * call are then unspecified; nothing outside the given buffers is touched).
+ *
+ * Masks use the positions above (aligned at the bottom right): ATTN_MASK_NONE (every
+ * cached token), ATTN_MASK_CAUSAL (j <= position of the query), ATTN_MASK_SLIDING_WINDOW
+ * (also position - j < window). ALiBi uses the signed distance position - j; soft-cap as
+ * in attn_fwd. Document masking is not accepted (ATTN_ERR_ARG). Slots of a page past
+ * the end of its sequence are never part of a result, whatever they hold.
+ *
+ * page_size: 8, 16, 32 or a multiple of 64. max_seq_len (<= max_pages_per_seq *
+ * page_size) bounds seq_lens. split_keys (a positive multiple of 64, see
+ * attn_decode_split_keys) cuts each sequence into chunks of that many keys, computed by
+ * separate CTAs and merged by their log-sum-exp; with a single chunk
+ * (max_seq_len <= split_keys) no merge runs and no workspace is needed. workspace:
+ * DEVICE memory of attn_decode_workspace_size bytes, 256-byte aligned, not shared with
+ * a concurrent call. Deterministic for fixed split_keys. Allocates nothing.
+ */
+attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* page_table, const int32_t* seq_lens, void* o,
+                              float* lse, int B, int Hq, int Hkv, int Nq, int d, int num_pages,
+                              int page_size, int max_pages_per_seq, int max_seq_len,
+                              int split_keys, float scale, int mask_kind,
+                              const attn_mask_params* mask_params, int score_kind,
+                              const attn_score_params* score_params, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes of attn_decode_paged: with n = ceil(max_seq_len / split_keys) chunks
+ * and R = B * Hq * Nq rows, round256(4 n R) + round256(4 n R d) when n > 1 (each chunk's
+ * per-row log2-sum-exp and normalised fp32 output), else 0.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int Nq, int d, int max_seq_len,
+                                  int split_keys);
+
+/*
+ * A split_keys for attn_decode_paged: about sixteen waves of two CTAs per SM over
+ * total_kv_tokens (the sum of seq_lens, or B * max_seq_len when unknown), a multiple of
+ * 64 and at least 256. Pure function of its arguments.
+ */
+int attn_decode_split_keys(int B, int Hq, int Hkv, int Nq, long long total_kv_tokens,
+                           int num_sms);
+
+/*
  * Block-sparsity classifier ("El FlexAttention de PyTorch con FlashAttention-4 es
  * un cambio radical", "Limitaciones actuales", names block sparsity): writes
  * classes[r * ceil(Nkv/128) + c] = EMPTY / PARTIAL / FULL for query tile r and key
@@ -267,7 +329,8 @@ attn_status attn_bwd_simt(const void* q, const void* k, const void* v, const voi
 /*
  * Synchronises `stream` and reports whether a kernel of this library on the
  * current device gave up a bounded wait since the last call (ATTN_ERR_DEVICE_TIMEOUT),
- * or whether the stream itself failed (ATTN_ERR_LAUNCH). Clears the flag.
+ * met an out-of-range device input (ATTN_ERR_DEVICE_INPUT), or whether the stream
+ * itself failed (ATTN_ERR_LAUNCH). Clears the flags.
  */
 attn_status attn_device_status(void* stream);
 

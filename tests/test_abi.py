@@ -24,7 +24,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_strerror_texts(lib):
-    for code in range(8):
+    for code in range(9):
         assert lib.attn_strerror(code).decode()
     assert lib.attn_strerror(99).decode() == "unknown status"
 
@@ -86,3 +86,54 @@ def test_workspace_size(lib):
 def test_classify_rejects_bad_kind(lib):
     assert lib.attn_classify_tiles(9, None, 10, 10, None, None) == 1
     assert lib.attn_classify_tiles(0, None, 0, 10, None, None) == 0
+
+
+def _decode(lib, **kw):
+    a = dict(q=None, k=None, v=None, table=None, lens=None, o=None, lse=None, B=2, Hq=8, Hkv=2,
+             Nq=1, d=128, pages=10, ps=16, maxp=8, msl=100, split=64, scale=0.125, mask=0,
+             mp=None, score=0, sp=None, ws=None, wsb=0)
+    a.update(kw)
+    return lib.attn_decode_paged(a["q"], a["k"], a["v"], a["table"], a["lens"], a["o"], a["lse"],
+                                 a["B"], a["Hq"], a["Hkv"], a["Nq"], a["d"], a["pages"], a["ps"],
+                                 a["maxp"], a["msl"], a["split"], ctypes.c_float(a["scale"]),
+                                 a["mask"], a["mp"], a["score"], a["sp"], a["ws"], a["wsb"], None)
+
+
+def test_decode_argument_errors_return_before_any_device_call(lib):
+    assert _decode(lib, d=96) == 2                    # ATTN_ERR_SHAPE
+    assert _decode(lib, Hq=3) == 2
+    for ps in (0, 4, 12, 48, 96):                     # page sizes that straddle 64-key tiles
+        assert _decode(lib, ps=ps, maxp=64) == 2, ps
+    assert _decode(lib, msl=8 * 16 + 1) == 2          # above the page table's capacity
+    assert _decode(lib, split=0) == 1                 # ATTN_ERR_ARG
+    assert _decode(lib, split=96) == 1
+    assert _decode(lib, mask=3) == 1                  # no document masking in decode
+    assert _decode(lib, mask=2) == 1                  # window without params
+    assert _decode(lib, scale=float("inf")) == 1
+    assert _decode(lib) == 1                          # null tensors
+    good = {n: ctypes.c_void_p(0x10000 * (i + 1)) for i, n in
+            enumerate(("q", "k", "v", "table", "lens", "o", "lse"))}
+    assert _decode(lib, **dict(good, q=ctypes.c_void_p(0x10008))) == 3   # misaligned q
+    assert _decode(lib, **dict(good, table=ctypes.c_void_p(0x30002))) == 3
+    assert _decode(lib, **good) == 5                  # two chunks need a workspace
+    assert _decode(lib, **good, ws=ctypes.c_void_p(0x100000), wsb=10) == 5
+    assert _decode(lib, B=0) == 0                     # nothing to do
+    assert _decode(lib, Nq=0) == 0
+
+
+def test_decode_workspace_size_and_split_keys(lib):
+    # one chunk: no workspace; n chunks: per-row log2-sum-exp plane + fp32 O plane
+    assert lib.attn_decode_workspace_size(4, 32, 1, 128, 8192, 8192) == 0
+    assert lib.attn_decode_workspace_size(4, 32, 1, 128, 0, 256) == 0
+    n, rows = 16, 4 * 32 * 1
+    assert lib.attn_decode_workspace_size(4, 32, 1, 128, 8192, 512) == \
+        _round256(4 * n * rows) + _round256(4 * n * rows * 128)
+    assert lib.attn_decode_workspace_size(3, 5, 7, 64, 1000, 192) == \
+        _round256(4 * 6 * 105) + _round256(4 * 6 * 105 * 64)
+    # split keys: a multiple of 64, at least 256, about 32 CTAs of work per SM
+    for args in [(64, 32, 8, 1, 64 * 4352, 152), (1, 8, 8, 1, 100, 152),
+                 (8, 64, 8, 40, 8 * 100000, 148), (2, 4, 4, 1, 0, 0)]:
+        keys = lib.attn_decode_split_keys(*args)
+        assert keys >= 256 and keys % 64 == 0, args
+    assert lib.attn_decode_split_keys(64, 32, 8, 1, 64 * 4352, 152) == 512
+    assert lib.attn_decode_split_keys(1, 8, 8, 1, 100, 152) == 256
