@@ -460,7 +460,7 @@ def run_decode(args, w):
     msl = w.len_max
     o = torch.empty((w.B, w.Hq, w.Nq, w.d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
-    nws = ea.decode_workspace_size(w.B, w.Hq, w.Nq, w.d, msl, split)
+    nws = ea.decode_workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.d, msl, split)
     ws = torch.empty((max(nws, 256),), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()

@@ -52,7 +52,7 @@ SIGNATURES = {
     "attn_quantize_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "attn_decode_paged": (_I, [_P] * 7 + [_I] * 10 + [_F, _I, _MP, _I, _SP, _P, ctypes.c_size_t,
                                                      _P]),
-    "attn_decode_workspace_size": (ctypes.c_size_t, [_I] * 6),
+    "attn_decode_workspace_size": (ctypes.c_size_t, [_I] * 7),
     "attn_decode_split_keys": (_I, [_I, _I, _I, _I, ctypes.c_longlong, _I]),
     "attn_device_status": (_I, [_P]),
     "attn_strerror": (ctypes.c_char_p, [_I]),

@@ -239,9 +239,9 @@ def decode_split_keys(B: int, Hq: int, Hkv: int, Nq: int, total_kv_tokens: int,
                                                   int(total_kv_tokens), int(num_sms)))
 
 
-def decode_workspace_size(B: int, Hq: int, Nq: int, d: int, max_seq_len: int,
+def decode_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, d: int, max_seq_len: int,
                           split_keys: int) -> int:
-    return int(_lib.load().attn_decode_workspace_size(int(B), int(Hq), int(Nq), int(d),
+    return int(_lib.load().attn_decode_workspace_size(int(B), int(Hq), int(Hkv), int(Nq), int(d),
                                                       int(max_seq_len), int(split_keys)))
 
 
@@ -288,7 +288,7 @@ def decode_paged(q, k_cache, v_cache, page_table, seq_lens, *, max_seq_len: Opti
         scale = float(d) ** -0.5
     o = torch.empty((B, Hq, Nq, d), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
-    nbytes = decode_workspace_size(B, Hq, Nq, d, max_seq_len, split_keys)
+    nbytes = decode_workspace_size(B, Hq, Hkv, Nq, d, max_seq_len, split_keys)
     ws = torch.empty((nbytes,), dtype=torch.uint8, device=q.device) if nbytes else None
     decode_paged_into(q, k_cache, v_cache, page_table, seq_lens, o, lse, ws,
                       max_seq_len=max_seq_len, split_keys=split_keys, scale=scale,

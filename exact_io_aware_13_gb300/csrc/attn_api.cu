@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -27,6 +28,7 @@ struct DeviceInfo {
   bool probed = false;
   bool is_sm103 = false;
   int* status = nullptr;  // device address of g_device_status on this device
+  int num_sms = 0;
 };
 
 std::mutex g_mu;
@@ -50,6 +52,8 @@ attn_status current_device(DeviceInfo** out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return ATTN_ERR_LAUNCH;
     d.is_sm103 = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
     if (d.is_sm103) {
       void* ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return ATTN_ERR_LAUNCH;
@@ -439,9 +443,9 @@ int attn_decode_split_keys(int B, int Hq, int Hkv, int Nq, long long total_kv_to
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || total_kv_tokens <= 0 || Hq % Hkv != 0)
     return 256;
   const long long rows = (long long)(Hq / Hkv) * Nq;
-  const long long row_tiles = (rows + 127) / 128;
-  // about sixteen waves of two resident CTAs per SM
-  const long long target = 32LL * (num_sms > 0 ? num_sms : 148);
+  const long long row_tiles = (rows + 63) / 64;
+  // about twelve work items per SM for the persistent kernel (one CTA per SM)
+  const long long target = 12LL * (num_sms > 0 ? num_sms : 148);
   const long long work = total_kv_tokens * Hkv * row_tiles;
   long long keys = (work + target - 1) / target;
   keys = (keys + 63) / 64 * 64;
@@ -450,10 +454,13 @@ int attn_decode_split_keys(int B, int Hq, int Hkv, int Nq, long long total_kv_to
   return (int)keys;
 }
 
-size_t attn_decode_workspace_size(int B, int Hq, int Nq, int d, int max_seq_len, int split_keys) {
-  if (B <= 0 || Hq <= 0 || Nq <= 0 || d <= 0 || split_keys <= 0) return 0;
-  const long long n = decode_chunks(max_seq_len, split_keys);
-  if (n <= 1) return 0;
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int d, int max_seq_len,
+                                  int split_keys) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || d <= 0 || split_keys <= 0 || Hq % Hkv != 0)
+    return 0;
+  const long long copies = decode_row_copies((int)std::min<long long>((long long)(Hq / Hkv) * Nq, 1 << 30));
+  const long long n = decode_chunks(max_seq_len, split_keys) * copies;
+  if (n <= 1 || max_seq_len <= 0) return 0;
   const long long rows = (long long)B * Hq * Nq;
   return decode_lse_plane(n, rows) + round256((size_t)(n * rows) * d * sizeof(float));
 }
@@ -499,8 +506,8 @@ attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_
   const long long rows_total = (long long)B * Hq * Nq;
   if (rows_total == 0) return ATTN_OK;
   const long long n_chunks = decode_chunks(max_seq_len, split_keys);
-  const long long row_tiles = ((long long)(Hq / Hkv) * Nq + 127) / 128;
-  if (rows_total > 0x7fffffffLL || (long long)B * Hkv * row_tiles > 65535 ||
+  const long long row_tiles = ((long long)(Hq / Hkv) * Nq + 63) / 64;
+  if (rows_total > 0x7fffffffLL || (long long)B * Hkv * row_tiles * n_chunks > (1LL << 40) ||
       (long long)num_pages * Hkv * page_size > 0x7fffffffLL || n_chunks > 0x7fffffffLL)
     return ATTN_ERR_SHAPE;
   p.n_chunks = (int)n_chunks;
@@ -510,7 +517,7 @@ attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
       !aligned16(lse) || !aligned4(page_table) || !aligned4(seq_lens))
     return ATTN_ERR_ALIGN;
-  const size_t need = attn_decode_workspace_size(B, Hq, Nq, d, max_seq_len, split_keys);
+  const size_t need = attn_decode_workspace_size(B, Hq, Hkv, Nq, d, max_seq_len, split_keys);
   if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_ALIGN;
   DeviceInfo* dev = nullptr;
@@ -526,15 +533,17 @@ attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_
   if (need > 0) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     out.part_lse = reinterpret_cast<float*>(ws);
-    out.part_o = reinterpret_cast<float*>(ws + decode_lse_plane(n_chunks, rows_total));
+    const long long parts =
+        n_chunks * decode_row_copies((int)std::min<long long>((long long)(Hq / Hkv) * Nq, 1 << 30));
+    out.part_o = reinterpret_cast<float*>(ws + decode_lse_plane(parts, rows_total));
   }
   CUtensorMap tq, tk, tv;
   const int kv_rows = num_pages * Hkv * page_size;
   const unsigned box = page_size < 64 ? (unsigned)page_size : 64u;
-  if ((s = make_map(&tq, q, 1, (int)rows_total, d, 128)) != ATTN_OK) return s;
+  if ((s = make_map(&tq, q, 1, (int)rows_total, d, 32)) != ATTN_OK) return s;
   if ((s = make_map(&tk, k_cache, 1, kv_rows, d, box)) != ATTN_OK) return s;
   if ((s = make_map(&tv, v_cache, 1, kv_rows, d, box)) != ATTN_OK) return s;
-  return from_cuda(launch_decode_tc(p, tq, tk, tv, out, st));
+  return from_cuda(launch_decode_tc(p, tq, tk, tv, out, dev->num_sms, st));
 }
 
 attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_params, int Nq,

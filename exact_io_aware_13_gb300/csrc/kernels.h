@@ -97,6 +97,12 @@ ATTN_HD void decode_row_keys(int mask_kind, int window, int L, int Nq, int i, in
   if (hi < lo) hi = lo;
 }
 
+// Copies of an item's packed rows (G * Nq per kv head) that the decode kernel keeps in
+// tensor memory, so that two warps on two SM sub-partitions share the softmax of at
+// most 32 rows: 2 for up to 32 rows, else 1. Each copy of a chunk is a separate partial
+// result.
+ATTN_HD int decode_row_copies(int rows) { return rows <= 32 ? 2 : 1; }
+
 struct DecodeProblem {
   int B, Hq, Hkv, Nq, d;
   int page_size, max_pages, num_pages;
@@ -112,13 +118,14 @@ struct DecodeProblem {
 struct DecodeOut {
   __nv_bfloat16* o;  // [B, Hq, Nq, d]
   float* lse;        // [B, Hq, Nq], natural log
-  float* part_o;     // split mode: [n_chunks, B*Hq*Nq, d] fp32, O_c / l_c
-  float* part_lse;   // split mode: [n_chunks, B*Hq*Nq], m_c + log2 l_c
+  float* part_o;     // partials: [n_chunks * copies, B*Hq*Nq, d] fp32, O_c / l_c
+  float* part_lse;   // partials: [n_chunks * copies, B*Hq*Nq], m_c + log2 l_c
 };
-// tq: [B*Hq*Nq, d] bf16, box 64 x 128; tk, tv: [pages*Hkv*page_size, d] bf16, box
-// 64 x min(page_size, 64). Launches the decode kernel and, with n_chunks > 1, the
-// combine kernel.
+// tq: [B*Hq*Nq, d] bf16, box 64 x 32; tk, tv: [pages*Hkv*page_size, d] bf16, box
+// 64 x min(page_size, 64). Launches the persistent decode kernel on num_ctas CTAs (one
+// per SM) and, unless there is one chunk and one row copy, the combine kernel.
 cudaError_t launch_decode_tc(const DecodeProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                             const CUtensorMap& tv, const DecodeOut& out, cudaStream_t st);
+                             const CUtensorMap& tv, const DecodeOut& out, int num_ctas,
+                             cudaStream_t st);
 
 }  // namespace attn

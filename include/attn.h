@@ -269,7 +269,8 @@ attn_status attn_quantize_fp8(const void* x, void* out, float* scales, int BH, i
  * page_size) bounds seq_lens. split_keys (a positive multiple of 64, see
  * attn_decode_split_keys) cuts each sequence into chunks of that many keys, computed by
  * separate CTAs and merged by their log-sum-exp; with a single chunk
- * (max_seq_len <= split_keys) no merge runs and no workspace is needed. workspace:
+ * (max_seq_len <= split_keys) and more than 32 rows per query group no merge runs and no
+ * workspace is needed. workspace:
  * DEVICE memory of attn_decode_workspace_size bytes, 256-byte aligned, not shared with
  * a concurrent call. Deterministic for fixed split_keys. Allocates nothing.
  */
@@ -283,17 +284,21 @@ attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_
                               size_t workspace_bytes, void* stream);
 
 /*
- * Workspace bytes of attn_decode_paged: with n = ceil(max_seq_len / split_keys) chunks
- * and R = B * Hq * Nq rows, round256(4 n R) + round256(4 n R d) when n > 1 (each chunk's
- * per-row log2-sum-exp and normalised fp32 output), else 0.
+ * Workspace bytes of attn_decode_paged. The kernel keeps c copies of the rows of a kv
+ * head's query group (G * Nq rows, G = Hq / Hkv) so that the softmax of a few rows is
+ * spread over the SM: c = 2 for up to 32 rows, else 1. With
+ * n = ceil(max_seq_len / split_keys) * c partial results per row and R = B * Hq * Nq
+ * rows: round256(4 n R) + round256(4 n R d) (each partial's log2-sum-exp and normalised
+ * fp32 output) when n > 1 and max_seq_len > 0, else 0.
  */
-size_t attn_decode_workspace_size(int B, int Hq, int Nq, int d, int max_seq_len,
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int d, int max_seq_len,
                                   int split_keys);
 
 /*
- * A split_keys for attn_decode_paged: about sixteen waves of two CTAs per SM over
- * total_kv_tokens (the sum of seq_lens, or B * max_seq_len when unknown), a multiple of
- * 64 and at least 256. Pure function of its arguments.
+ * A split_keys for attn_decode_paged: about twelve work items (key chunks of one kv head
+ * and 64-row query tile) per SM over total_kv_tokens (the sum of seq_lens, or
+ * B * max_seq_len when unknown), a multiple of 64 and at least 256. Pure function of its
+ * arguments.
  */
 int attn_decode_split_keys(int B, int Hq, int Hkv, int Nq, long long total_kv_tokens,
                            int num_sms);

@@ -122,18 +122,24 @@ def test_decode_argument_errors_return_before_any_device_call(lib):
 
 
 def test_decode_workspace_size_and_split_keys(lib):
-    # one chunk: no workspace; n chunks: per-row log2-sum-exp plane + fp32 O plane
-    assert lib.attn_decode_workspace_size(4, 32, 1, 128, 8192, 8192) == 0
-    assert lib.attn_decode_workspace_size(4, 32, 1, 128, 0, 256) == 0
-    n, rows = 16, 4 * 32 * 1
-    assert lib.attn_decode_workspace_size(4, 32, 1, 128, 8192, 512) == \
-        _round256(4 * n * rows) + _round256(4 * n * rows * 128)
-    assert lib.attn_decode_workspace_size(3, 5, 7, 64, 1000, 192) == \
-        _round256(4 * 6 * 105) + _round256(4 * 6 * 105 * 64)
+    # n partials per row (chunks x row copies): log2-sum-exp plane + fp32 O plane
+    ws = lib.attn_decode_workspace_size
+    # 128 rows per group (one copy), one chunk: results written in place
+    assert ws(4, 32, 1, 4, 128, 8192, 8192) == 0
+    assert ws(4, 32, 8, 1, 128, 0, 256) == 0            # no cached key at all
+    # G * Nq = 4 rows: 2 copies, even with one chunk
+    rows = 4 * 32 * 1
+    assert ws(4, 32, 8, 1, 128, 8192, 8192) == _round256(4 * 2 * rows) + _round256(4 * 2 * rows * 128)
+    assert ws(4, 32, 8, 1, 128, 8192, 512) == _round256(4 * 32 * rows) + _round256(4 * 32 * rows * 128)
+    # 32 rows: 2 copies; 35 and 105 rows: 1 copy
+    assert ws(3, 4, 1, 8, 64, 1000, 192) == _round256(4 * 12 * 96) + _round256(4 * 12 * 96 * 64)
+    assert ws(3, 5, 1, 7, 64, 1000, 192) == _round256(4 * 6 * 105) + _round256(4 * 6 * 105 * 64)
+    assert ws(3, 35, 7, 7, 64, 1000, 192) == _round256(4 * 6 * 735) + _round256(4 * 6 * 735 * 64)
+    assert ws(3, 5, 1, 21, 64, 1000, 192) == _round256(4 * 6 * 315) + _round256(4 * 6 * 315 * 64)
     # split keys: a multiple of 64, at least 256, about 32 CTAs of work per SM
     for args in [(64, 32, 8, 1, 64 * 4352, 152), (1, 8, 8, 1, 100, 152),
                  (8, 64, 8, 40, 8 * 100000, 148), (2, 4, 4, 1, 0, 0)]:
         keys = lib.attn_decode_split_keys(*args)
         assert keys >= 256 and keys % 64 == 0, args
-    assert lib.attn_decode_split_keys(64, 32, 8, 1, 64 * 4352, 152) == 512
+    assert lib.attn_decode_split_keys(64, 32, 8, 1, 64 * 4352, 152) == 1280  # ceil64(1222)
     assert lib.attn_decode_split_keys(1, 8, 8, 1, 100, 152) == 256
