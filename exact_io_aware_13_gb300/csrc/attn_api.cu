@@ -537,13 +537,13 @@ attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_
         n_chunks * decode_row_copies((int)std::min<long long>((long long)(Hq / Hkv) * Nq, 1 << 30));
     out.part_o = reinterpret_cast<float*>(ws + decode_lse_plane(parts, rows_total));
   }
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tk, tv;
   const int kv_rows = num_pages * Hkv * page_size;
   const unsigned box = page_size < 64 ? (unsigned)page_size : 64u;
-  if ((s = make_map(&tq, q, 1, (int)rows_total, d, 32)) != ATTN_OK) return s;
   if ((s = make_map(&tk, k_cache, 1, kv_rows, d, box)) != ATTN_OK) return s;
   if ((s = make_map(&tv, v_cache, 1, kv_rows, d, box)) != ATTN_OK) return s;
-  return from_cuda(launch_decode_tc(p, tq, tk, tv, out, dev->num_sms, st));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  return from_cuda(launch_decode_tc(p, tk, tv, out, dev->num_sms, st));
 }
 
 attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_params, int Nq,

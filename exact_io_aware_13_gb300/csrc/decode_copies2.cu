@@ -5,9 +5,9 @@
 namespace attn {
 namespace dec {
 
-cudaError_t launch_decode_copies2(const Args& a, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_decode_copies2(const Args& a, const CUtensorMap& tk,
                                   const CUtensorMap& tv, int grid, cudaStream_t st) {
-  return launch_decode_copies<2>(a, tq, tk, tv, grid, st);
+  return launch_decode_copies<2>(a, tk, tv, grid, st);
 }
 
 }  // namespace dec

@@ -65,9 +65,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const Args a) {
 
 }  // namespace dec
 
-cudaError_t launch_decode_tc(const DecodeProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                             const CUtensorMap& tv, const DecodeOut& out, int num_ctas,
-                             cudaStream_t st) {
+cudaError_t launch_decode_tc(const DecodeProblem& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const DecodeOut& out, int num_ctas, cudaStream_t st) {
   using namespace dec;
   Args a{};
   a.p = p;
@@ -81,8 +80,8 @@ cudaError_t launch_decode_tc(const DecodeProblem& p, const CUtensorMap& tq, cons
   a.direct = p.n_chunks == 1 && a.rep == 1;
   if (a.rows_total == 0 || num_ctas <= 0) return cudaSuccess;
   if ((a.rows_total + 7) / 8 > 0x7fffffffLL) return cudaErrorInvalidValue;
-  cudaError_t e = a.rep == 2 ? launch_decode_copies2(a, tq, tk, tv, num_ctas, st)
-                             : launch_decode_copies<1>(a, tq, tk, tv, num_ctas, st);
+  cudaError_t e = a.rep == 2 ? launch_decode_copies2(a, tk, tv, num_ctas, st)
+                             : launch_decode_copies<1>(a, tk, tv, num_ctas, st);
   if (e != cudaSuccess || a.direct) return e;
   const long long blocks = (a.rows_total + 7) / 8;
   if (p.d == 64) decode_combine_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(a);

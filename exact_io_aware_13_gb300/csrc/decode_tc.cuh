@@ -55,6 +55,8 @@
 
 #pragma once
 
+#include <climits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -65,7 +67,7 @@ namespace dec {
 constexpr int BM = 128;      // MMA M (TMEM lanes)
 constexpr int kItemRows = 64;  // packed query rows per item: TMEM quadrants 0 and 2
 constexpr int BN = 64;       // keys per tile (MMA N of S, K of P V)
-constexpr int kStages = 5;   // K/V ring depth
+constexpr int kStages = 7;   // K/V ring depth
 // A warp runs on SM sub-partition warp % 4, and a softmax or epilogue warp may only
 // address the TMEM lanes of quadrant warp % 4. An item's rows live in quadrants 0 and 2
 // (rows 0-31 and 32-63, or two copies of rows 0-31), so the softmax and epilogue warps
@@ -80,13 +82,13 @@ __device__ __forceinline__ bool is_softmax_warp(int w) { return w == 4 || w == 6
 __device__ __forceinline__ bool is_epilogue_warp(int w) { return w == 0 || w == 2; }
 // Named barriers (the MMA warp waits only on these):
 //   kNbP + (u & 1)   P of tile u in TMEM: the n_part softmax warps + MMA warp
-//   kNbQ + b         Q buffer b loaded: relay (32) + MMA (32)
-//   kNbK + s, kNbV + s   K / V of ring stage s landed: relay (32) + MMA (32)
+//   kNbQ + b         Q buffer b written to TMEM: the n_part epilogue warps + MMA warp
+//   kNbKV + s        K and V of ring stage s landed: relay (32) + MMA (32)
 constexpr uint32_t kNbP = 1;
-constexpr uint32_t kNbQ = 3, kNbK = 5, kNbV = kNbK + kStages, kNbPairCount = 64;
-constexpr uint32_t kNbX = kNbV + kStages;  // row-max exchange between the two row copies
+constexpr uint32_t kNbQ = 3, kNbX = 5;  // kNbX: row-max exchange between the two row copies
+constexpr uint32_t kNbKV = 6, kNbPairCount = 64;
 constexpr uint32_t kNbXCount = 64;
-static_assert(kNbX <= 15, "named barrier IDs");
+static_assert(kNbKV + kStages - 1 <= 15, "named barrier IDs");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr unsigned long long kDrainLimitNs = 200000000ull;  // waits for own copies at exit
@@ -94,32 +96,30 @@ constexpr unsigned long long kDrainLimitNs = 200000000ull;  // waits for own cop
 template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;           // 128-byte column blocks
-  static constexpr int kQHalf = BM * 128;          // 16 KB
   static constexpr int kKvHalf = BN * 128;         // 8 KB
-  static constexpr int kQBuf = kHalves * kQHalf;
-  static constexpr int kQ = 0;                     // two Q buffers
-  static constexpr int kRing = kQ + 2 * kQBuf;
+  static constexpr int kRing = 0;
   static constexpr int kTileBytes = kHalves * kKvHalf;  // one K or V tile
   static constexpr int kStage = 2 * kTileBytes;          // K then V
   static constexpr int kBars = kRing + kStages * kStage;
   static constexpr int kXchg = kBars + 512;             // row maxima [2][2][32] floats
-  static constexpr int kBytes = kXchg + 2 * 2 * 32 * 4;
+  static constexpr int kStats = kXchg + 2 * 2 * 32 * 4;  // m, l [O buffer][copy][lane][2]
+  static constexpr int kBytes = kStats + 2 * 2 * 32 * 2 * 4;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128;  // O buffers at kColO + b * D
-  static constexpr uint32_t kColStats = 384;  // m, l of O buffer b at kColStats + 2 b
+  static constexpr uint32_t kColQ = kColO + 2 * D;  // Q buffers (bf16 pairs) at kColQ + b * D / 2
 };
+static_assert(Layout<128>::kAlloc <= 232448, "shared memory");
 
 struct Bars {
-  uint64_t q_full[2];
-  uint64_t q_empty[2];
+  uint64_t q_empty[2];     // Q buffer b no longer read by S MMAs (MMA commit)
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
   uint64_t empty[kStages];
   uint64_t s_full[2];
   uint64_t pv_done;
   uint64_t o_full[2];      // O buffer b holds an item's P V sums (MMA commit)
-  uint64_t stats_full[2];  // its rows' m and l are in TMEM (softmax warps)
+  uint64_t stats_full[2];  // its rows' m and l are in shared memory (softmax warps)
   uint64_t o_empty[2];     // its result has been written out (epilogue warps)
   uint64_t tail[kStages];
   uint64_t mma_done;
@@ -174,51 +174,6 @@ struct Item {
   bool live;            // processed: has tiles, or (single-chunk launch) owns its rows
 };
 
-// Items of this CTA: [start, end) of the list, and the cursor at `start`.
-__device__ inline void cta_items(const Args& a, int lane, long long& start, long long& end,
-                          Cursor& cu) {
-  const DecodeProblem& p = a.p;
-  const long long per_b = (long long)p.Hkv * a.row_tiles;
-  long long total = 0;
-  for (int b0 = 0; b0 < p.B; b0 += 32) {
-    const int b = b0 + lane;
-    long long n = b < p.B ? chunks_of(a, seq_len(a, b)) * per_b : 0;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
-    total += n;
-  }
-  start = total * blockIdx.x / gridDim.x;
-  end = total * (blockIdx.x + 1) / gridDim.x;
-  cu = Cursor{p.B, 0, 0, 0, 0, 0};
-  if (start >= end) return;
-  long long base = 0;
-  for (int b0 = 0; b0 < p.B; b0 += 32) {
-    const int b = b0 + lane;
-    const long long n = b < p.B ? chunks_of(a, seq_len(a, b)) * per_b : 0;
-    long long incl = n;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const long long v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    const long long group = __shfl_sync(0xffffffffu, incl, 31);
-    if (base + group > start) {
-      const uint32_t m = __ballot_sync(0xffffffffu, base + incl > start);
-      const int l = __ffs(m) - 1;
-      const long long before = base + __shfl_sync(0xffffffffu, incl - n, l);
-      cu.b = b0 + l;
-      cu.Lb = seq_len(a, cu.b);
-      cu.nb = chunks_of(a, cu.Lb);
-      const long long rem = start - before;
-      cu.hk = (int)(rem / ((long long)a.row_tiles * cu.nb));
-      cu.rt = (int)((rem / cu.nb) % a.row_tiles);
-      cu.c = (int)(rem % cu.nb);
-      return;
-    }
-    base += group;
-  }
-}
-
 __device__ __forceinline__ void advance(const Args& a, Cursor& cu) {
   if (++cu.c < cu.nb) return;
   cu.c = 0;
@@ -233,6 +188,85 @@ __device__ __forceinline__ void advance(const Args& a, Cursor& cu) {
     cu.nb = chunks_of(a, cu.Lb);
   } while (cu.nb == 0);
 }
+
+// The CTAs split the item list by key tiles, not by item count (items differ in size:
+// the last chunk of a sequence is short). An item's cost is its tiles without the mask,
+// and items are laid end to end in list order, so item i starts at tile position f_i;
+// CTA k takes the items with S_k <= f_i < S_{k+1}, S_k = floor(total * k / CTAs) (the
+// last CTA takes the rest, items without tiles included).
+__device__ __forceinline__ int item_tiles(const Args& a, int L, int c) {
+  const int c0 = a.direct ? 0 : c * a.p.chunk;
+  const int c1 = a.direct ? L : imin(c0 + a.p.chunk, L);
+  return ceil_div(c1 - c0, BN);  // c0 is a multiple of 64
+}
+
+// The cursor at this CTA's first item (b = B when it has none), that item's tile
+// position, and the position where the next CTA's items start.
+__device__ inline void cta_items(const Args& a, int lane, Cursor& cu, long long& pos,
+                                 long long& end_pos) {
+  const DecodeProblem& p = a.p;
+  const long long blocks = (long long)p.Hkv * a.row_tiles;  // (kv head, row tile) per sequence
+  long long total = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    const int L = b < p.B ? seq_len(a, b) : 0;
+    long long t = (b < p.B && chunks_of(a, L) > 0) ? blocks * ceil_div(L, BN) : 0;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    total += t;
+  }
+  const long long S = total * blockIdx.x / gridDim.x;
+  end_pos = blockIdx.x + 1 == gridDim.x ? LLONG_MAX : total * (blockIdx.x + 1) / gridDim.x;
+  cu = Cursor{p.B, 0, 0, 0, 0, 0};
+  pos = S;
+  if (S >= end_pos) return;
+  long long base = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    const int L = b < p.B ? seq_len(a, b) : 0;
+    const bool has = b < p.B && chunks_of(a, L) > 0;
+    const long long t = has ? blocks * ceil_div(L, BN) : 0;
+    long long incl = t;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    // sequence b holds an item at or after S: S lies inside its tiles, or it has only
+    // items without tiles, all at position base_b >= S
+    const bool cond = has && (base + incl > S || (t == 0 && base + incl - t >= S));
+    const uint32_t m = __ballot_sync(0xffffffffu, cond);
+    if (m) {
+      const int l = __ffs(m) - 1;
+      const long long bbase = base + __shfl_sync(0xffffffffu, incl - t, l);
+      cu.b = b0 + l;
+      cu.Lb = seq_len(a, cu.b);
+      cu.nb = chunks_of(a, cu.Lb);
+      const long long T = ceil_div(cu.Lb, BN);                     // tiles of one block
+      const long long CT = a.direct ? (T > 0 ? T : 1) : p.chunk / BN;  // tiles of a full chunk
+      long long rem = S - bbase, blk = 0, c = 0;
+      if (rem > 0) {
+        blk = rem / T;
+        const long long off = rem - blk * T;
+        c = (off + CT - 1) / CT;
+        if (c >= cu.nb) { c = 0; ++blk; }
+      }
+      pos = bbase + blk * T + c * CT;
+      if (blk >= blocks) {  // past this sequence's last item: the next sequence's first
+        cu.hk = p.Hkv - 1; cu.rt = a.row_tiles - 1; cu.c = cu.nb - 1;
+        advance(a, cu);
+        pos = bbase + blocks * T;
+      } else {
+        cu.hk = (int)(blk / a.row_tiles);
+        cu.rt = (int)(blk % a.row_tiles);
+        cu.c = (int)c;
+      }
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+}
+
 
 __device__ __forceinline__ int warp_min(int v) {
 #pragma unroll
@@ -270,33 +304,39 @@ __device__ inline Item make_item(const Args& a, const Cursor& cu, int lane) {
   return it;
 }
 
-// Walks this CTA's items, calling f(item, new_q, run, u0, next) for each live item:
-// new_q when its Q tile differs from the previous item with tiles (run = index of that Q
-// tile, in buffer run & 1), u0 = index of its first key tile in the CTA's tile
-// sequence, next = the following live item (next.live false at the end).
-template <typename F>
+// Walks this CTA's items that have key tiles (with kWithEmpty, only those without: the
+// single-chunk launch writes their results up front), calling
+// f(item, new_q, run, u0, next, next_new_q): new_q when its Q tile differs from the
+// previous item's (run = index of that Q tile, in buffer run & 1), u0 = index of its
+// first key tile in the CTA's tile sequence, next = the following item (next.live false
+// at the end) and next_new_q whether it starts a new Q tile.
+template <bool kWithEmpty = false, typename F>
 __device__ __forceinline__ void for_each_item(const Args& a, int lane, F&& f) {
-  long long start, end;
+  long long pos, end_pos;
   Cursor cu;
-  cta_items(a, lane, start, end, cu);
+  cta_items(a, lane, cu, pos, end_pos);
   int run = -1, pb = -1, phk = -1, prt = -1;
   int u = 0;
   Item held{};
   held.live = false;
   bool held_new_q = false;
   int held_run = 0, held_u = 0;
-  for (long long idx = start; idx <= end; ++idx) {
+  for (;;) {
     Item it{};
     it.live = false;
-    if (idx < end) {
+    const bool more = cu.b < a.p.B && pos < end_pos;
+    if (more) {
       it = make_item(a, cu, lane);
+      pos += item_tiles(a, cu.Lb, cu.c);
       advance(a, cu);
+      it.live = kWithEmpty ? (it.live && it.n_t == 0) : it.n_t > 0;
       if (!it.live) continue;
     }
-    if (held.live) f(held, held_new_q, held_run, held_u, it);
+    const bool next_new_q = it.live && (it.b != pb || it.hk != phk || it.rt != prt);
+    if (held.live) f(held, held_new_q, held_run, held_u, it, next_new_q);
     if (!it.live) break;
     bool new_q = false;
-    if (it.n_t > 0 && (it.b != pb || it.hk != phk || it.rt != prt)) {
+    if (!kWithEmpty && (it.b != pb || it.hk != phk || it.rt != prt)) {
       new_q = true;
       ++run;
       pb = it.b; phk = it.hk; prt = it.rt;
@@ -312,8 +352,7 @@ __device__ __forceinline__ void for_each_item(const Args& a, int lane, F&& f) {
 // kRep: copies of the item's rows in TMEM (2 when they fit in one 32-row block, else 1).
 template <int D, bool kAlibi, bool kSoftcap, int kRep>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-                     const __grid_constant__ CUtensorMap tm_k,
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const Args a) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -332,7 +371,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (L0 < 0 || L0 > p.max_seq_len) { atomicOr(p.status, DEV_BAD_INPUT); break; }
       }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(smem_u32(&bars->q_full[t]), 1);
       mbar_init(smem_u32(&bars->q_empty[t]), 1);
       mbar_init(smem_u32(&bars->s_full[t]), 1);
     }
@@ -368,12 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int R = imin(ps, BN);       // rows per box (a piece of one page)
     const int pieces = BN / R;        // boxes per tile and tensor (<= 8)
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
     }
     bool live = true;
-    int issued = 0, q_loads = 0;
+    int issued = 0;
     // First page-table window of the next item, fetched one item ahead (a dependent
     // global load at the start of every item would stall the ring).
     auto fetch_for = [&](const Item& it, int base) {
@@ -383,28 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool have_pre = false;
     int pre_cur = -1, pre_nxt = -1;
-    for_each_item(a, lane, [&](const Item& it, bool new_q, int run, int u0, const Item& next) {
-      if (!live || it.n_t == 0) return;
-      if (new_q) {
-        const int qb = run & 1;
-        if (run >= 2)  // the previous Q tile in this buffer is no longer read
-          live = __all_sync(0xffffffffu,
-                            mbar_wait(smem_u32(&bars->q_empty[qb]), ((run >> 1) - 1) & 1, wc));
-        if (!live) return;
-        const long long row0 =
-            ((long long)it.b * p.Hq + (long long)it.hk * a.G) * p.Nq + (long long)it.rt * kItemRows;
-        const uint32_t qbar = smem_u32(&bars->q_full[qb]);
-        if (lane == 0) {  // quadrants 0, 1: rows 0-31; 2, 3: rows 32-63 (copies of 0-31)
-          mbar_arrive_expect_tx(qbar, L::kQBuf);
-#pragma unroll
-          for (int hf = 0; hf < L::kHalves; ++hf)
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              tma_load_3d(smem_u32(smem + L::kQ + qb * L::kQBuf + hf * L::kQHalf + q * 32 * 128),
-                          &tm_q, qbar, hf * 64, (int)(row0 + (kRep == 1 && q >= 2 ? 32 : 0)), 0);
-        }
-        ++q_loads;
-      }
+    for_each_item(a, lane, [&](const Item& it, bool, int, int u0, const Item& next, bool) {
+      if (!live) return;
       int wbase = (it.tb * BN) / ps;  // page index held by lane 0 of `cur`
       int cur = have_pre ? pre_cur : fetch_for(it, wbase);
       int nxt = have_pre ? pre_nxt : fetch_for(it, wbase + 32);
@@ -466,16 +483,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     });
     // Do not leave while copies into this CTA's shared memory are in flight.
-    for (int r = imax(0, q_loads - 2); r < q_loads; ++r)
-      drain_wait(smem_u32(&bars->q_full[r & 1]), (r >> 1) & 1);
     for (int u = imax(0, issued - kStages); u < issued; ++u) {
       drain_wait(smem_u32(&bars->k_full[u % kStages]), (u / kStages) & 1);
       drain_wait(smem_u32(&bars->v_full[u % kStages]), (u / kStages) & 1);
     }
   } else if (warp == kRelayWarp) {
     // ------------------------------------------------------------ relay
-    // After each TMA completion, arrive on the matching named barrier for the MMA warp.
-    // After an abort, rendezvous (bar.sync) instead, so every barrier phase still pairs.
+    // Once K and V of a stage have landed (and the unused V rows of a sequence's last
+    // tile are cleared), arrive on the stage's named barrier for the MMA warp. After an
+    // abort, rendezvous (bar.sync) instead, so every barrier phase still pairs.
     bool live = true;
     auto pass = [&](uint32_t bar, uint32_t parity, uint32_t id) {
       if (live) live = __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
@@ -483,11 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       else nb_sync(id, kNbPairCount);
     };
     uint32_t tail_parity = 0;  // bit s: phase parity of tail[s]
-    for_each_item(a, lane, [&](const Item& it, bool new_q, int run, int u0, const Item&) {
-      if (new_q) pass(smem_u32(&bars->q_full[run & 1]), (run >> 1) & 1, kNbQ + (run & 1));
+    for_each_item(a, lane, [&](const Item& it, bool, int, int u0, const Item&, bool) {
       for (int t = 0; t < it.n_t; ++t) {
         const int u = u0 + t, s = u % kStages;
-        pass(smem_u32(&bars->k_full[s]), (u / kStages) & 1, kNbK + s);
+        if (live)
+          live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->k_full[s]), (u / kStages) & 1, wc));
         const int t0 = (it.tb + t) * BN;
         const int valid = imin(BN, it.Lb - t0);
         if (valid < BN) {
@@ -512,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&bars->v_full[s]));
           }
         }
-        pass(smem_u32(&bars->v_full[s]), (u / kStages) & 1, kNbV + s);
+        pass(smem_u32(&bars->v_full[s]), (u / kStages) & 1, kNbKV + s);
       }
     });
   } else if (warp == kMmaWarp) {
@@ -532,7 +548,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto pv = [&]() {  // O += P V of tile prev_u
       const int s = prev_u % kStages;
       nb_sync(kNbP + (prev_u & 1), p_count);
-      nb_sync(kNbV + s, kNbPairCount);
       tc_fence_after_sync();
       const uint32_t vb = ring + s * L::kStage + L::kTileBytes;
       const uint64_t dv = smem_desc_sw128(vb, L::kKvHalf, 1024);
@@ -545,25 +560,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_if(issuer, smem_u32(&bars->pv_done));
       if (prev_last) mma_commit_if(issuer, smem_u32(&bars->o_full[prev_ob]));
     };
-    for_each_item(a, lane, [&](const Item& it, bool new_q, int run, int u0, const Item&) {
+    for_each_item(a, lane, [&](const Item& it, bool new_q, int run, int u0, const Item&, bool) {
       const int qb = run & 1;
       if (new_q) {
-        nb_sync(kNbQ + qb, kNbPairCount);
+        nb_sync(kNbQ + qb, p_count);
         tc_fence_after_sync();
       }
-      const uint32_t q_base = smem_u32(smem + L::kQ + qb * L::kQBuf);
+      const uint32_t tq = tmem + L::kColQ + qb * (D / 2);
       for (int t = 0; t < it.n_t; ++t) {
         const int u = u0 + t, s = u % kStages;
-        nb_sync(kNbK + s, kNbPairCount);
+        nb_sync(kNbKV + s, kNbPairCount);
         tc_fence_after_sync();
         const uint32_t kb = ring + s * L::kStage;
-        const uint64_t dq = smem_desc_sw128(q_base, 16, 1024), dk = smem_desc_sw128(kb, 16, 1024);
+        const uint64_t dk = smem_desc_sw128(kb, 16, 1024);
         const uint32_t col = (u & 1) ? L::kColS1 : L::kColS0;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // 16 head dims per instruction
-          const uint32_t offq = ((kk >> 2) * L::kQHalf + (kk & 3) * 32) >> 4;
+        for (int kk = 0; kk < D / 16; ++kk) {  // 16 head dims per instruction; Q in TMEM
           const uint32_t offk = ((kk >> 2) * L::kKvHalf + (kk & 3) * 32) >> 4;
-          mma_ss_if(issuer, tmem + col, dq + offq, dk + offk, idS, kk > 0 ? 1u : 0u);
+          mma_ts_if(issuer, tmem + col, tq + kk * 8, dk + offk, idS, kk > 0 ? 1u : 0u);
         }
         mma_commit_if(issuer, smem_u32(&bars->s_full[u & 1]));
         // every S of the previous Q tile was issued before this one
@@ -601,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool raw_ok = !kAlibi && !kSoftcap && k1 > 0.f;
     bool live = true;
     int items_with_tiles = 0;
-    for_each_item(a, lane, [&](const Item& it, bool, int, int u0, const Item&) {
-      if (it.n_t == 0) return;  // no key for any row: the epilogue warps write the result
+    float* stats = reinterpret_cast<float*>(smem + L::kStats);  // [2][2][32][2]
+    for_each_item(a, lane, [&](const Item& it, bool, int, int u0, const Item&, bool) {
       const int row = rb * 32 + lane;  // packed row of the item
       const bool active = rb * 32 < it.rows_here;  // warp-uniform
       const bool valid_row = row < it.rows_here;
@@ -739,64 +753,85 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before_sync();
         nb_arrive(kNbP + (u & 1), p_count);
       }
-      // Row max and sum for the epilogue warps, next to O in tensor memory.
-      if (active) {
-        uint32_t ml[2] = {__float_as_uint(m_run), __float_as_uint(l_run)};
-        __syncwarp();
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(
-                         tmem + lane_base + L::kColStats + 2 * ob),
-                     "r"(ml[0]), "r"(ml[1])
-                     : "memory");
-        tmem_wait_st();
-      }
-      tc_fence_before_sync();
+      // Row max and sum for the epilogue warps (the mbarrier arrival releases them).
+      if (active)
+        *reinterpret_cast<float2*>(stats + ((ob * 2 + j) * 32 + lane) * 2) = make_float2(m_run, l_run);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->stats_full[ob]));
     });
   } else if (is_epilogue_warp(warp) && (warp & 3) / 2 < a.n_part) {
-    // ------------------------------------------------------------ item results
+    // ------------------------------------------------------------ Q tiles and results
     // Quadrant 2 j writes the result of its rows: rows 32 j .. without copies; with two
-    // copies of rows 0-31, partial result j of the item's chunk.
+    // copies of rows 0-31, partial result j of the item's chunk. The same warps put each
+    // run's Q rows into tensor memory (bf16 pairs, the A operand of S = Q K^T) one item
+    // ahead: the MMA warp issues the last P V of an item only after the first S of the
+    // next, so that Q must be in place before this item's result is awaited.
     const int quad = warp & 3, j = quad >> 1;
     const int rb = kRep == 1 ? j : 0, ci = kRep == 1 ? 0 : j;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t p_count = 32u * (a.n_part + 1);
+    const float* stats = reinterpret_cast<const float*>(smem + L::kStats);
+    const int row = rb * 32 + lane;
     bool live = true;
-    int items_with_tiles = 0;
-    for_each_item(a, lane, [&](const Item& it, bool, int, int, const Item&) {
-      const int row = rb * 32 + lane;
+    auto grow_of = [&](const Item& it) {
+      return ((long long)it.b * p.Hq + (long long)it.hk * a.G) * p.Nq +
+             (long long)it.rt * kItemRows + row;
+    };
+    auto prep_q = [&](const Item& it, int run) {
+      const int qb = run & 1;
+      if (run >= 2 && live)  // the S MMAs of Q tile run - 2 have completed
+        live = __all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&bars->q_empty[qb]), ((run >> 1) - 1) & 1, wc));
+      tc_fence_after_sync();
+      const bool ok = live && row < it.rows_here;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + grow_of(it) * D);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {  // 32 columns (64 values) per store
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 v = ok ? __ldg(src + c * 8 + e) : make_uint4(0, 0, 0, 0);
+          w[4 * e] = v.x; w[4 * e + 1] = v.y; w[4 * e + 2] = v.z; w[4 * e + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_base + L::kColQ + qb * (D / 2) + c * 32, w);
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      if (live) nb_arrive(kNbQ + qb, p_count);
+      else nb_sync(kNbQ + qb, p_count);
+    };
+    // Items without any key (single-chunk launches only): O = 0, LSE = -inf.
+    if (ci == 0)
+      for_each_item<true>(a, lane, [&](const Item& it, bool, int, int, const Item&, bool) {
+        if (row >= it.rows_here) return;
+        const long long r = grow_of(it);
+        uint4* orow = reinterpret_cast<uint4*>(a.out.o + r * D);
+#pragma unroll
+        for (int e = 0; e < D / 8; ++e) orow[e] = make_uint4(0, 0, 0, 0);
+        a.out.lse[r] = -INFINITY;
+      });
+    int k = 0;
+    for_each_item(a, lane, [&](const Item& it, bool new_q, int run, int, const Item& next,
+                               bool next_new_q) {
+      if (new_q && run == 0) prep_q(it, 0);
+      if (next_new_q) prep_q(next, run + 1);
       const bool active = rb * 32 < it.rows_here;  // warp-uniform
       const bool valid_row = row < it.rows_here;
-      int ob = 0;
-      bool have_o = false;
-      float m_run = -INFINITY, l_run = 0.f;
-      if (it.n_t > 0) {
-        const int k = items_with_tiles++;
-        ob = k & 1;
-        if (live)
-          live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full[ob]), (k >> 1) & 1, wc));
-        if (live)
-          live = __all_sync(0xffffffffu,
-                            mbar_wait(smem_u32(&bars->stats_full[ob]), (k >> 1) & 1, wc));
-        have_o = live;
-        tc_fence_after_sync();
-        if (have_o && active) {
-          uint32_t ml[2];
-          __syncwarp();
-          asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
-                       : "=r"(ml[0]), "=r"(ml[1])
-                       : "r"(tmem + lane_base + L::kColStats + 2 * ob));
-          tmem_wait_ld();
-          m_run = __uint_as_float(ml[0]);
-          l_run = __uint_as_float(ml[1]);
-        }
-      } else if (ci > 0) {
-        return;  // an item without keys (single-chunk launch only) has one result
-      }
+      const int ob = k & 1;
+      if (live)
+        live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full[ob]), (k >> 1) & 1, wc));
+      if (live)
+        live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->stats_full[ob]), (k >> 1) & 1, wc));
+      ++k;
+      const bool have_o = live;
+      tc_fence_after_sync();
       const uint32_t tO = tmem + lane_base + L::kColO + ob * D;
       if (active) {
+        const float2 ml = have_o ? *reinterpret_cast<const float2*>(stats + ((ob * 2 + j) * 32 + lane) * 2)
+                                 : make_float2(-INFINITY, 0.f);
+        const float m_run = ml.x, l_run = ml.y;
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        const long long grow_row =
-            ((long long)it.b * p.Hq + (long long)it.hk * a.G) * p.Nq + (long long)it.rt * kItemRows + row;
+        const long long grow_row = grow_of(it);
         const size_t part = ((size_t)it.c * a.rep + ci) * a.rows_total + grow_row;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -836,11 +871,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           else a.out.part_lse[part] = l2;
         }
       }
-      if (it.n_t > 0) {  // O buffer ob may take the next item's P V sums
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->o_empty[ob]));
-      }
+      // O buffer ob and its row statistics may take the next item's values
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->o_empty[ob]));
     });
   }
   __syncwarp();
@@ -853,36 +887,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool kAlibi, bool kSoftcap, int kRep>
-cudaError_t launch_variant(const Args& a, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_variant(const Args& a, const CUtensorMap& tk,
                            const CUtensorMap& tv, int grid, cudaStream_t st) {
   auto kern = decode_tc_kernel<D, kAlibi, kSoftcap, kRep>;
   const int smem = Layout<D>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
+  kern<<<grid, kThreads, smem, st>>>(tk, tv, a);
   return cudaGetLastError();
 }
 
 template <int D, int kRep>
-cudaError_t launch_d(const Args& a, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_d(const Args& a, const CUtensorMap& tk,
                      const CUtensorMap& tv, int grid, cudaStream_t st) {
   const bool al = a.p.score_kind & ATTN_SCORE_ALIBI, sc = a.p.score_kind & ATTN_SCORE_SOFTCAP;
-  if (al && sc) return launch_variant<D, true, true, kRep>(a, tq, tk, tv, grid, st);
-  if (al) return launch_variant<D, true, false, kRep>(a, tq, tk, tv, grid, st);
-  if (sc) return launch_variant<D, false, true, kRep>(a, tq, tk, tv, grid, st);
-  return launch_variant<D, false, false, kRep>(a, tq, tk, tv, grid, st);
+  if (al && sc) return launch_variant<D, true, true, kRep>(a, tk, tv, grid, st);
+  if (al) return launch_variant<D, true, false, kRep>(a, tk, tv, grid, st);
+  if (sc) return launch_variant<D, false, true, kRep>(a, tk, tv, grid, st);
+  return launch_variant<D, false, false, kRep>(a, tk, tv, grid, st);
 }
 
 // The decode kernel for kRep copies of the rows (every head dimension and score mod).
 template <int kRep>
-cudaError_t launch_decode_copies(const Args& a, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_decode_copies(const Args& a, const CUtensorMap& tk,
                                  const CUtensorMap& tv, int grid, cudaStream_t st) {
-  if (a.p.d == 64) return launch_d<64, kRep>(a, tq, tk, tv, grid, st);
-  return launch_d<128, kRep>(a, tq, tk, tv, grid, st);
+  if (a.p.d == 64) return launch_d<64, kRep>(a, tk, tv, grid, st);
+  return launch_d<128, kRep>(a, tk, tv, grid, st);
 }
 
 // Defined in decode_copies2.cu (a translation unit of its own, compiled in parallel).
-cudaError_t launch_decode_copies2(const Args& a, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_decode_copies2(const Args& a, const CUtensorMap& tk,
                                   const CUtensorMap& tv, int grid, cudaStream_t st);
 
 }  // namespace dec

@@ -113,6 +113,7 @@ struct DecodeProblem {
   int score_kind, mask_kind, window;
   const int32_t* page_table;  // [B, max_pages] device
   const int32_t* seq_lens;    // [B] device
+  const __nv_bfloat16* q;     // [B, Hq, Nq, d] device
   int* status;
 };
 struct DecodeOut {
@@ -121,11 +122,10 @@ struct DecodeOut {
   float* part_o;     // partials: [n_chunks * copies, B*Hq*Nq, d] fp32, O_c / l_c
   float* part_lse;   // partials: [n_chunks * copies, B*Hq*Nq], m_c + log2 l_c
 };
-// tq: [B*Hq*Nq, d] bf16, box 64 x 32; tk, tv: [pages*Hkv*page_size, d] bf16, box
-// 64 x min(page_size, 64). Launches the persistent decode kernel on num_ctas CTAs (one
-// per SM) and, unless there is one chunk and one row copy, the combine kernel.
-cudaError_t launch_decode_tc(const DecodeProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                             const CUtensorMap& tv, const DecodeOut& out, int num_ctas,
-                             cudaStream_t st);
+// tk, tv: [pages*Hkv*page_size, d] bf16, box 64 x min(page_size, 64). Launches the
+// persistent decode kernel on num_ctas CTAs (one per SM) and, unless there is one chunk
+// and one row copy, the combine kernel.
+cudaError_t launch_decode_tc(const DecodeProblem& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const DecodeOut& out, int num_ctas, cudaStream_t st);
 
 }  // namespace attn
