@@ -113,18 +113,23 @@ class ClockSampler:
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel on this
 # workload, keyed by the SHA-256 of the kernel's sources (its .cu file plus the shared
 # headers) at capture time. A kernel whose sources have changed since reports null.
-KERNEL_SOURCES = {"fwd_tc_kernel": "fwd_tc.cu", "dkdv_kernel": "bwd_tc.cu",
-                  "dq_kernel": "bwd_tc.cu", "rowdot_kernel": "simt.cu"}
+KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu",),
+                  "dq_kernel": ("bwd_tc.cu",), "rowdot_kernel": ("simt.cu",),
+                  "decode_tc_kernel": ("decode_tc.cuh", "decode_tc.cu", "decode_copies2.cu")}
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
+# decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192), read bytes rounded
+# to the kilobyte by ncu's GB figure.
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201393152 + 47004928,
-                      "sha256": "b9d290e9b09a53967bc19d4269bb7cade7a007bc207c9127828c46cdfca55c5c"},
-    "rowdot_kernel": {"bytes": 135274752 + 4241152,
-                      "sha256": "1f69db384bac8bffc2176c6223a7b5940c03f66c7127ea38ad82fbe219446ef5"},
-    "dkdv_kernel": {"bytes": 270715904 + 103128576,
-                    "sha256": "fa2ce09954fdb9647e03ffeb2e218c17e81523980982ff6494f8e47ca66e8c96"},
-    "dq_kernel": {"bytes": 270680576 + 52014592,
-                  "sha256": "fa2ce09954fdb9647e03ffeb2e218c17e81523980982ff6494f8e47ca66e8c96"},
+    "fwd_tc_kernel": {"bytes": 201558016 + 46595328,
+                    "sha256": "b30b83f583d45e7b29c443d6467dc9b4960b460102dca1cdd7827f74313ef806"},
+    "rowdot_kernel": {"bytes": 135309312 + 659968,
+                    "sha256": "3908d9051038efc55b6a5da93c393435ac200bda88cd39900f65cf6aeb34ca8d"},
+    "dkdv_kernel": {"bytes": 270977536 + 99044864,
+                  "sha256": "3e65cfc99061a1d218a89bf7c82e0a5e467fb05018502429f7424dd9e2ad4389"},
+    "dq_kernel": {"bytes": 270628096 + 48471552,
+                "sha256": "3e65cfc99061a1d218a89bf7c82e0a5e467fb05018502429f7424dd9e2ad4389"},
+    "decode_tc_kernel": {"bytes": 1119384000 + 9659904,
+                       "sha256": "b4bab05fdc8dd31bb21608ce17a4108cef894dd9c779738e2cd5c627239968e4"},
 }
 
 
@@ -132,7 +137,7 @@ def kernel_source_sha(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_io_aware_13_gb300", "csrc")
-    for name in (KERNEL_SOURCES[kernel],) + SHARED_HEADERS:
+    for name in KERNEL_SOURCES[kernel] + SHARED_HEADERS:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -534,7 +539,8 @@ def run_decode(args, w):
         "roofline": {"bound": "hbm", "kernel": "decode_tc_kernel (+ combine, timed together)",
                      "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(ach / pk["hbm_gbs"], 4),
-                     "peak_source": pk["source"] + " HBM copy", "traffic": None},
+                     "peak_source": pk["source"] + " HBM copy",
+                     "traffic": ncu_traffic("decode_tc_kernel")},
         "e2e": {"value": round(world * io_bytes / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 4)},

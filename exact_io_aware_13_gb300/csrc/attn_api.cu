@@ -444,8 +444,8 @@ int attn_decode_split_keys(int B, int Hq, int Hkv, int Nq, long long total_kv_to
     return 256;
   const long long rows = (long long)(Hq / Hkv) * Nq;
   const long long row_tiles = (rows + 63) / 64;
-  // about twelve work items per SM for the persistent kernel (one CTA per SM)
-  const long long target = 12LL * (num_sms > 0 ? num_sms : 148);
+  // about ten work items per SM for the persistent kernel (one CTA per SM)
+  const long long target = 10LL * (num_sms > 0 ? num_sms : 148);
   const long long work = total_kv_tokens * Hkv * row_tiles;
   long long keys = (work + target - 1) / target;
   keys = (keys + 63) / 64 * 64;

@@ -295,7 +295,7 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int d, int max
                                   int split_keys);
 
 /*
- * A split_keys for attn_decode_paged: about twelve work items (key chunks of one kv head
+ * A split_keys for attn_decode_paged: about ten work items (key chunks of one kv head
  * and 64-row query tile) per SM over total_kv_tokens (the sum of seq_lens, or
  * B * max_seq_len when unknown), a multiple of 64 and at least 256. Pure function of its
  * arguments.

@@ -141,5 +141,5 @@ def test_decode_workspace_size_and_split_keys(lib):
                  (8, 64, 8, 40, 8 * 100000, 148), (2, 4, 4, 1, 0, 0)]:
         keys = lib.attn_decode_split_keys(*args)
         assert keys >= 256 and keys % 64 == 0, args
-    assert lib.attn_decode_split_keys(64, 32, 8, 1, 64 * 4352, 152) == 1280  # ceil64(1222)
+    assert lib.attn_decode_split_keys(64, 32, 8, 1, 64 * 4352, 152) == 1472  # ceil64(1466.1)
     assert lib.attn_decode_split_keys(1, 8, 8, 1, 100, 152) == 256
