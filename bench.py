@@ -4,7 +4,7 @@ online softmax, backward rebuilding P from the LSE) on the causal fwd+bwd worklo
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload fwd_bwd|causal_fwd|gqa_window_fwd|docs_fwd|tiny_fwd|fp8_causal_fwd
-                            |paged_decode]
+                            |causal_fwd_d256|paged_decode]
 
 Prints one JSON line. `value` is useful TFLOP/s (masked-out work excluded) summed
 over ranks; with N > 1 each rank runs its own replica of the workload (the heads
@@ -33,11 +33,11 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import (CAUSAL, CAUSAL_FWD_BWD, DOCS, GQA_WINDOW, MASK_NAMES,  # noqa: E402
-                       PAGED_DECODE, TINY, make_decode_inputs, make_inputs)
+from workloads import (CAUSAL, CAUSAL_D256, CAUSAL_FWD_BWD, DOCS, GQA_WINDOW,  # noqa: E402
+                       MASK_NAMES, PAGED_DECODE, TINY, make_decode_inputs, make_inputs)
 
 FWD_WORKLOADS = {"causal_fwd": CAUSAL, "gqa_window_fwd": GQA_WINDOW, "docs_fwd": DOCS,
-                 "tiny_fwd": TINY, "fp8_causal_fwd": CAUSAL}
+                 "tiny_fwd": TINY, "fp8_causal_fwd": CAUSAL, "causal_fwd_d256": CAUSAL_D256}
 
 METRIC = "attention fwd/bwd TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 peak"
 UNIT = "TFLOP/s"
@@ -405,6 +405,7 @@ def run_forward(args, w, fp8=False):
     pk = peaks()
     ach = f_fwd / (statistics.mean(times) * 1e-3) / 1e12
     peak = pk["bf16_tflops"] * (2 if fp8 else 1)  # FP8 dense rate: 2x bf16 (nominal ratio)
+    kname = "fwd256_kernel" if w.d == 256 else "fwd_tc_kernel"
     line = {
         "metric": ("attention FP8 forward TFLOP/s (unmasked FLOPs) and % of GB300 dense FP8 peak"
                    if fp8 else
@@ -416,11 +417,11 @@ def run_forward(args, w, fp8=False):
         "config": workload_config(w, {"parallelism": f"replicas x{world}",
                                       "pairs_per_head": pairs}),
         "pct_of_peak": round(100 * value / world / peak, 1),
-        "kernels": {"fwd_tc_kernel": {"ms": round(statistics.mean(times), 4),
+        "kernels": {kname: {"ms": round(statistics.mean(times), 4),
                                       "min_ms": round(min(times), 4),
                                       "achieved": round(ach, 2), "unit": UNIT,
                                       "frac": round(ach / peak, 4)}},
-        "roofline": {"bound": "tensor", "kernel": "fwd_tc_kernel", "achieved": round(ach, 2),
+        "roofline": {"bound": "tensor", "kernel": kname, "achieved": round(ach, 2),
                      "peak": peak, "unit": UNIT, "frac": round(ach / peak, 4),
                      "peak_source": pk["source"] + (" bf16 burst x 2 (nominal fp8/bf16 ratio)"
                                                     if fp8 else " bf16 burst"),

@@ -84,7 +84,7 @@ attn_status check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float 
                           int mask_kind, const attn_mask_params* mp, int score_kind,
                           const attn_score_params* sp, Problem* p) {
   if (B < 0 || Hq < 0 || Hkv < 0 || Nq < 0 || Nkv < 0) return ATTN_ERR_SHAPE;
-  if (d != 64 && d != 128) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_SHAPE;  // 256: tensor-core forward only
   if (Hkv == 0 ? Hq != 0 : (Hq % Hkv) != 0) return ATTN_ERR_SHAPE;
   const long long rows_q = (long long)B * Hq * Nq, rows_k = (long long)B * Hkv * Nkv;
   if (rows_q * d > 0x7fffffffLL * 16 || rows_k * d > 0x7fffffffLL * 16) return ATTN_ERR_SHAPE;
@@ -141,6 +141,7 @@ attn_status fwd_common(bool simt, const void* q, const void* k, const void* v, v
   Problem p;
   attn_status s = check_problem(B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind, mp, score_kind, sp, &p);
   if (s != ATTN_OK) return s;
+  if (simt && d == 256) return ATTN_ERR_SHAPE;
   const long long rows_q = (long long)B * Hq * Nq;
   if (rows_q == 0) return ATTN_OK;
   if (!q || !o || !lse) return ATTN_ERR_ARG;
@@ -158,6 +159,11 @@ attn_status fwd_common(bool simt, const void* q, const void* k, const void* v, v
   const auto* vb = static_cast<const __nv_bfloat16*>(v);
   if (simt) return from_cuda(launch_fwd_simt(p, qb, kb, vb, ob, lse, st));
   CUtensorMap tq, tk, tv;
+  if (d == 256) {
+    if ((s = make_map(&tk, k, B * Hkv, Nkv, d, 64)) != ATTN_OK) return s;
+    if ((s = make_map(&tv, v, B * Hkv, Nkv, d, 64)) != ATTN_OK) return s;
+    return from_cuda(launch_fwd256_tc(p, qb, tk, tv, ob, lse, st));
+  }
   if ((s = make_map(&tq, q, B * Hq, Nq, d)) != ATTN_OK) return s;
   if ((s = make_map(&tk, k, B * Hkv, Nkv, d)) != ATTN_OK) return s;
   if ((s = make_map(&tv, v, B * Hkv, Nkv, d)) != ATTN_OK) return s;
@@ -186,6 +192,7 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
   Problem p;
   attn_status s = check_problem(B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind, mp, score_kind, sp, &p);
   if (s != ATTN_OK) return s;
+  if (d == 256) return ATTN_ERR_SHAPE;  // the backward handles d = 64 and 128
   const long long rows_q = (long long)B * Hq * Nq, rows_k = (long long)B * Hkv * Nkv;
   if (rows_q == 0 && rows_k == 0) return ATTN_OK;
   if (rows_q > 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_ERR_ARG;
@@ -417,7 +424,7 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const 
   attn_status s = check_problem(B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind, mask_params,
                                 score_kind, score_params, &p);
   if (s != ATTN_OK) return s;
-  if (d != 128) return ATTN_ERR_SHAPE;
+  if (d != 128) return ATTN_ERR_SHAPE;  // FP8 forward: d = 128
   const long long rows_q = (long long)B * Hq * Nq;
   if (rows_q == 0) return ATTN_OK;
   if (!q8 || !q_scale || !o || !lse) return ATTN_ERR_ARG;
@@ -581,7 +588,8 @@ const char* attn_strerror(attn_status status) {
   switch (status) {
     case ATTN_OK: return "success";
     case ATTN_ERR_ARG: return "invalid argument (null pointer, unknown kind or bad parameter)";
-    case ATTN_ERR_SHAPE: return "unsupported shape (d must be 64 or 128, Hq a multiple of Hkv)";
+    case ATTN_ERR_SHAPE:
+      return "unsupported shape (d must be 64 or 128, or 256 for attn_fwd; Hq a multiple of Hkv)";
     case ATTN_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
     case ATTN_ERR_ARCH: return "current device is not an sm_103 (GB300) GPU";
     case ATTN_ERR_WORKSPACE: return "workspace missing or smaller than attn_bwd_workspace_size";

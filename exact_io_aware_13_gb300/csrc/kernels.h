@@ -61,6 +61,10 @@ cudaError_t launch_classify(const MaskSpec& m, int32_t* classes, cudaStream_t st
 cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, __nv_bfloat16* o, float* lse,
                           cudaStream_t st);
+// Forward for head dimension 256: q [B*Hq, Nq, 256] bf16 (read by the softmax warps into
+// tensor memory), tk, tv over [B*Hkv, Nkv, 256] with 64 x 64 boxes.
+cudaError_t launch_fwd256_tc(const Problem& p, const __nv_bfloat16* q, const CUtensorMap& tk,
+                             const CUtensorMap& tv, __nv_bfloat16* o, float* lse, cudaStream_t st);
 // FP8 forward (d = 128): tq, tk over e4m3 Q, K [B*H, N, 128]; tvt over e4m3 V^T
 // [B*Hkv, 128, Nkv rounded up to 16]; sq [B*Hq, ceil(Nq/128)], sk [B*Hkv, ceil(Nkv/128)],
 // sv [B*Hkv] dequantisation scales (device).

@@ -2,8 +2,12 @@
 seeded inputs and compare with the stated tolerances.
 
 Tolerances (bf16 inputs, fp32 accumulation):
-  forward : max|O - O_ref| <= 1e-2 ; max|LSE - LSE_ref| <= 1e-3 on finite entries,
-            and -inf exactly where the oracle has -inf;
+  forward : |O - O_ref| <= 1e-2 + half a bf16 ulp of O_ref, per element: O is stored as
+            bf16 (8 significant bits), whose rounding alone reaches 0.008 for |O| in
+            [2, 4) and 0.016 in [4, 8), so the 1e-2 bounds the error before that last
+            rounding;
+            max|LSE - LSE_ref| <= 1e-3 on finite entries, and -inf exactly where the
+            oracle has -inf;
   backward: max|dX - dX_ref| <= 2e-2 * max|dX_ref| + 1e-5 for each of dq, dk, dv.
             The 1e-5 floor only matters where the exact gradient vanishes (one allowed
             key per row: P = 1 and dP - D = 0): there the kernels leave fp32
@@ -41,16 +45,23 @@ def oracle_kwargs(w: Workload, offs):
                 score_kind=w.score_kind, softcap=w.softcap)
 
 
+def bf16_half_ulp(x):
+    """Half the spacing of bf16 numbers at |x| (8 significant bits): 2^(floor(log2|x|) - 8)."""
+    a = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
+    return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
+
+
 def check_forward(o, lse, o_ref, lse_ref, what=""):
     o = np.asarray(o, dtype=np.float64)
     lse = np.asarray(lse, dtype=np.float64)
     assert o.shape == o_ref.shape and lse.shape == lse_ref.shape
+    over = float((np.abs(o - o_ref) - bf16_half_ulp(o_ref)).max()) if o.size else 0.0
     err_o = float(np.abs(o - o_ref).max()) if o.size else 0.0
     ninf_ref = np.isneginf(lse_ref)
     assert (np.isneginf(lse) == ninf_ref).all(), f"{what}: -inf pattern of LSE differs"
     fin = ~ninf_ref
     err_l = float(np.abs(lse[fin] - lse_ref[fin]).max()) if fin.any() else 0.0
-    assert err_o <= O_TOL, f"{what}: max|dO| = {err_o}"
+    assert over <= O_TOL, f"{what}: max(|dO| - bf16 half-ulp) = {over} (max|dO| = {err_o})"
     assert err_l <= LSE_TOL, f"{what}: max|dLSE| = {err_l}"
     return err_o, err_l
 

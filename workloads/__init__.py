@@ -93,6 +93,11 @@ CAUSAL_FWD_BWD = Workload("causal fwd+bwd", 4, B=2, Hq=16, Hkv=16, Nq=8192, Nkv=
 
 WORKLOADS = [TINY, CAUSAL, GQA_WINDOW, DOCS, CAUSAL_FWD_BWD]
 
+# Head dimension 256, the top of the range the pages give ("FlashAttention/es",
+# "Limitaciones"): the causal workload's FLOPs at twice the head size, half the batch.
+CAUSAL_D256 = Workload("causal fwd d=256", 6, B=2, Hq=16, Hkv=16, Nq=8192, Nkv=8192, d=256,
+                       mask_kind=MASK_CAUSAL)
+
 
 def document_lengths(total: int, seed: int, lo: int = 512, hi: int = 4096) -> list[int]:
     """Draw document lengths uniformly from [lo, hi] until they cover ``total``.
