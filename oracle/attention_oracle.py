@@ -37,6 +37,14 @@ G = Hq / Hkv), in float64 from the bf16-rounded inputs:
        dK_g = scale * sum_{h in g} dS^T Q_h
      ALiBi adds a constant, so it passes the gradient through unchanged.
 
+  7. Dropout ("FlashAttention/es", "Variantes y sucesores": FlashAttention-1 supported
+     dropout), when dropout_p > 0: with the keep mask Z of ``philox.keep_mask`` (its
+     docstring states the generator and the counter layout),
+       O = (P * Z / (1 - p)) V,  L unchanged (the softmax is taken before dropout);
+     and in the backward, with dP' = (dO V^T) * Z / (1 - p),
+       dV = (P * Z / (1 - p))^T dO,  D_i = sum_j P_ij dP'_ij = rowsum(dO * O),
+       dS = P * (dP' - D).
+
 Readings where the pages are silent (each listed in the design doc as well):
   * GQA maps query head h to kv head floor(h / G).
   * ALiBi uses the 0-based query-head index and the signed distance (i - j).
@@ -54,6 +62,8 @@ import math
 from typing import Optional, Sequence
 
 import numpy as np
+
+from . import philox
 
 MASK_NONE = 0
 MASK_CAUSAL = 1
@@ -143,7 +153,8 @@ def _head_probs(q_h, k_g, scale, h, Hq, mask_kind, window, doc_offsets, score_ki
 
 def forward(q, k, v, scale: float, mask_kind: int = MASK_NONE, window: int = 0,
             doc_offsets=None, score_kind: int = 0, softcap: float = 0.0,
-            rows: Optional[np.ndarray] = None, heads: Optional[Sequence[tuple]] = None):
+            rows: Optional[np.ndarray] = None, heads: Optional[Sequence[tuple]] = None,
+            dropout_p: float = 0.0, dropout_seed: int = 0):
     """Exact attention forward.
 
     q: [B, Hq, Nq, d], k/v: [B, Hkv, Nkv, d] (any float type; widened to float64).
@@ -163,6 +174,10 @@ def forward(q, k, v, scale: float, mask_kind: int = MASK_NONE, window: int = 0,
         g = h // G
         p, s, _, m, l, live = _head_probs(q[b, h], k[b, g], scale, h, Hq, mask_kind, window,
                                           doc_offsets, score_kind, softcap, rows)
+        if dropout_p > 0:
+            keep = philox.keep_mask(dropout_seed, b * Hq + h, rows, np.arange(k.shape[2]),
+                                    dropout_p)
+            p = p * keep / (1.0 - dropout_p)
         out[b, h] = p @ v[b, g]
         lse[b, h] = np.where(live, m + np.log(np.where(live, l, 1.0)), -np.inf)
     return out, lse
@@ -181,7 +196,8 @@ def probabilities(q, k, scale, h_index: int = 0, b_index: int = 0, mask_kind=MAS
 
 def backward(q, k, v, dout, scale: float, mask_kind: int = MASK_NONE, window: int = 0,
              doc_offsets=None, score_kind: int = 0, softcap: float = 0.0,
-             kv_heads: Optional[Sequence[tuple]] = None):
+             kv_heads: Optional[Sequence[tuple]] = None, dropout_p: float = 0.0,
+             dropout_seed: int = 0):
     """Analytic gradients of sum(dO * O) with respect to q, k, v (float64).
 
     Materialises P per head. ``kv_heads`` restricts the work to a list of (b, g)
@@ -205,8 +221,14 @@ def backward(q, k, v, dout, scale: float, mask_kind: int = MASK_NONE, window: in
                                                   window, doc_offsets, score_kind, softcap,
                                                   rows)
             do_h = dout[b, h]
-            dv_acc += p.T @ do_h
             dp = do_h @ v[b, g].T
+            if dropout_p > 0:
+                zs = philox.keep_mask(dropout_seed, b * Hq + h, rows, np.arange(k.shape[2]),
+                                      dropout_p) / (1.0 - dropout_p)
+                dv_acc += (p * zs).T @ do_h
+                dp = dp * zs
+            else:
+                dv_acc += p.T @ do_h
             D = (p * dp).sum(axis=1)
             ds = p * (dp - D[:, None])
             if score_kind & SCORE_SOFTCAP:
