@@ -33,8 +33,8 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import (CAUSAL, CAUSAL_D256, CAUSAL_FWD_BWD, DOCS, GQA_WINDOW,  # noqa: E402
-                       MASK_NAMES, PAGED_DECODE, TINY, make_decode_inputs, make_inputs)
+from workloads import (CAUSAL, CAUSAL_D256, CAUSAL_FWD_BWD,  # noqa: E402
+                       CAUSAL_FWD_BWD_DROPOUT, DOCS, GQA_WINDOW, MASK_NAMES, PAGED_DECODE, TINY, make_decode_inputs, make_inputs)
 
 FWD_WORKLOADS = {"causal_fwd": CAUSAL, "gqa_window_fwd": GQA_WINDOW, "docs_fwd": DOCS,
                  "tiny_fwd": TINY, "fp8_causal_fwd": CAUSAL, "causal_fwd_d256": CAUSAL_D256}
@@ -175,12 +175,14 @@ def workload_config(w, extra=None):
     cfg = {"workload": w.describe(), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.Nq, "d": w.d,
            "mask": MASK_NAMES[w.mask_kind], "seed": w.seed,
            "l2": f"flushed between steps (256 MiB write); inputs {mib >> 20} MiB"}
+    if w.dropout_p > 0:
+        cfg.update(dropout_p=w.dropout_p, dropout_seed=w.dropout_seed)
     if extra:
         cfg.update(extra)
     return cfg
 
 
-def run_ours(args):
+def run_ours(args, w=CAUSAL_FWD_BWD):
     from exact_io_aware_13_gb300 import build as libbuild
     libbuild.build()  # compiles libattn.so from source if it is missing or stale
     import exact_io_aware_13_gb300 as ea
@@ -191,7 +193,6 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = CAUSAL_FWD_BWD
     pairs = flops.allowed_pairs(w.mask_kind, w.Nq, w.Nkv)
     f_fwd = flops.attention_flops(w.B, w.Hq, w.d, pairs, backward=False)
     f_bwd = flops.attention_flops(w.B, w.Hq, w.d, pairs, backward=True)
@@ -207,6 +208,8 @@ def run_ours(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     kw = dict(scale=w.scale, mask_kind=w.mask_kind)
+    if w.dropout_p > 0:
+        kw.update(dropout_p=w.dropout_p, dropout_seed=w.dropout_seed)
 
     def step():
         ea.fwd_into(qd, kd, vd, o, lse, **kw)
@@ -310,7 +313,8 @@ def run_ours(args):
                      "unit": algo[dom][1], "frac": kernels[dom]["frac"],
                      "peak_source": pk["source"] + (" bf16 burst" if algo[dom][1] == "TFLOP/s"
                                                     else " HBM copy"),
-                     "traffic": ncu_traffic(dom)},
+                     # counters were taken on the kernels without dropout
+                     "traffic": ncu_traffic(dom) if w.dropout_p == 0 else None},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
         "gpu_launches": 4 * args.steps,
@@ -565,8 +569,9 @@ def cpu_baseline(w, seconds: float = 20.0, heads: int = 1):
     while done < heads or (time.perf_counter() - t0 < seconds and done < w.B * w.Hq):
         b, h = divmod(done, w.Hq)
         sl = (slice(b, b + 1), slice(h, h + 1))
-        oracle.forward(q[sl], k[sl], v[sl], w.scale, mask_kind=w.mask_kind)
-        oracle.backward(q[sl], k[sl], v[sl], do[sl], w.scale, mask_kind=w.mask_kind)
+        drop = dict(dropout_p=w.dropout_p, dropout_seed=w.dropout_seed)
+        oracle.forward(q[sl], k[sl], v[sl], w.scale, mask_kind=w.mask_kind, **drop)
+        oracle.backward(q[sl], k[sl], v[sl], do[sl], w.scale, mask_kind=w.mask_kind, **drop)
         done += 1
         if time.perf_counter() - t0 > seconds:
             break
@@ -619,7 +624,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="fwd_bwd",
-                    choices=["fwd_bwd", *FWD_WORKLOADS, "paged_decode"])
+                    choices=["fwd_bwd", "fwd_bwd_dropout", *FWD_WORKLOADS, "paged_decode"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -627,6 +632,8 @@ def main():
         run_reference(args)
     elif args.workload == "paged_decode":
         run_decode(args, PAGED_DECODE)
+    elif args.workload == "fwd_bwd_dropout":
+        run_ours(args, CAUSAL_FWD_BWD_DROPOUT)
     elif args.workload != "fwd_bwd":
         run_forward(args, FWD_WORKLOADS[args.workload], fp8=args.workload.startswith("fp8"))
     else:

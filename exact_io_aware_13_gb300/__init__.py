@@ -2,7 +2,7 @@
 FlexAttention-style score/mask modifications, as a C-ABI CUDA library with a thin
 Python binding."""
 from .attention import (MASK_CAUSAL, MASK_DOCUMENT_CAUSAL, MASK_NONE,  # noqa: F401
-                        MASK_SLIDING_WINDOW, SCORE_ALIBI, SCORE_NONE, SCORE_SOFTCAP,
+                        MASK_SLIDING_WINDOW, SCORE_ALIBI, SCORE_DROPOUT, SCORE_NONE, SCORE_SOFTCAP,
                         TILE_EMPTY, TILE_FULL, TILE_PARTIAL, BWD_ALL, BWD_DKDV, BWD_DQ,
                         BWD_ROWDOT, backward, bwd_into, bwd_phases_into,
                         bwd_workspace_size, classify_tiles, device_status, forward, fwd_into,

@@ -25,7 +25,8 @@ class MaskParams(ctypes.Structure):
 
 
 class ScoreParams(ctypes.Structure):
-    _fields_ = [("softcap", ctypes.c_float)]
+    _fields_ = [("softcap", ctypes.c_float), ("dropout_p", ctypes.c_float),
+                ("dropout_seed", ctypes.c_uint64)]
 
 
 _P = ctypes.c_void_p

@@ -13,7 +13,7 @@ import torch
 from . import _lib
 
 MASK_NONE, MASK_CAUSAL, MASK_SLIDING_WINDOW, MASK_DOCUMENT_CAUSAL = 0, 1, 2, 3
-SCORE_NONE, SCORE_ALIBI, SCORE_SOFTCAP = 0, 1, 2
+SCORE_NONE, SCORE_ALIBI, SCORE_SOFTCAP, SCORE_DROPOUT = 0, 1, 2, 4
 TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 BWD_ROWDOT, BWD_DKDV, BWD_DQ, BWD_ALL = 1, 2, 4, 7
 TILE = 128
@@ -30,15 +30,20 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def _params(mask_kind: int, window: int, doc_offsets: Optional[torch.Tensor],
-            softcap: float):
+            softcap: float, dropout_p: float = 0.0, dropout_seed: int = 0):
     mp = _lib.MaskParams(int(window), None, 0)
     if doc_offsets is not None:
         if doc_offsets.dtype != torch.int32 or not doc_offsets.is_cuda:
             raise ValueError("doc_offsets must be an int32 CUDA tensor")
         mp.doc_offsets = doc_offsets.data_ptr()
         mp.n_docs = doc_offsets.numel() - 1
-    sp = _lib.ScoreParams(float(softcap))
+    sp = _lib.ScoreParams(float(softcap), float(dropout_p), int(dropout_seed) & (2**64 - 1))
     return ctypes.byref(mp), ctypes.byref(sp), (mp, sp)
+
+
+def _score_kind(score_kind: int, dropout_p: float) -> int:
+    """Dropout is switched on by a positive drop probability."""
+    return int(score_kind) | (SCORE_DROPOUT if dropout_p > 0 else 0)
 
 
 def _dims(q: torch.Tensor, k: torch.Tensor):
@@ -59,32 +64,37 @@ def _check_tensors(*ts):
 
 def fwd_into(q, k, v, o, lse, *, scale: float, mask_kind: int = MASK_NONE, window: int = 0,
              doc_offsets=None, score_kind: int = SCORE_NONE, softcap: float = 0.0,
-             stream=None, impl: str = "tc") -> None:
-    """Run attn_fwd (impl="tc") or attn_fwd_simt (impl="simt") into o and lse."""
+             dropout_p: float = 0.0, dropout_seed: int = 0, stream=None,
+             impl: str = "tc") -> None:
+    """Run attn_fwd (impl="tc") or attn_fwd_simt (impl="simt") into o and lse. A positive
+    dropout_p drops elements of P by the Philox4x32-10 mask of dropout_seed."""
     _check_tensors(q, k, v, o, lse, doc_offsets)
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
-    mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap)
+    mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap, dropout_p, dropout_seed)
     fn = lib.attn_fwd if impl == "tc" else lib.attn_fwd_simt
     st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nkv, d,
-            ctypes.c_float(scale), mask_kind, mp, score_kind, sp, _stream(stream))
+            ctypes.c_float(scale), mask_kind, mp, _score_kind(score_kind, dropout_p), sp,
+            _stream(stream))
     del keep
     _lib.check(st, fn.__name__)
 
 
 def forward(q, k, v, *, scale: Optional[float] = None, mask_kind: int = MASK_NONE,
             window: int = 0, doc_offsets=None, score_kind: int = SCORE_NONE,
-            softcap: float = 0.0, stream=None, impl: str = "tc"):
+            softcap: float = 0.0, dropout_p: float = 0.0, dropout_seed: int = 0,
+            stream=None, impl: str = "tc"):
     """Exact attention forward. q: bf16 [B,Hq,Nq,d], k/v: bf16 [B,Hkv,Nkv,d] on CUDA.
-    Returns (o bf16 [B,Hq,Nq,d], lse fp32 [B,Hq,Nq])."""
+    Returns (o bf16 [B,Hq,Nq,d], lse fp32 [B,Hq,Nq]); lse is that of the undropped
+    softmax when dropout_p > 0."""
     d = q.shape[-1]
     if scale is None:
         scale = float(torch.tensor(d, dtype=torch.float32).rsqrt())
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     fwd_into(q, k, v, o, lse, scale=scale, mask_kind=mask_kind, window=window,
-             doc_offsets=doc_offsets, score_kind=score_kind, softcap=softcap, stream=stream,
-             impl=impl)
+             doc_offsets=doc_offsets, score_kind=score_kind, softcap=softcap,
+             dropout_p=dropout_p, dropout_seed=dropout_seed, stream=stream, impl=impl)
     return o, lse
 
 
@@ -95,35 +105,39 @@ def bwd_workspace_size(q, k) -> int:
 
 def bwd_into(q, k, v, o, lse, dout, dq, dk, dv, workspace, *, scale: float,
              mask_kind: int = MASK_NONE, window: int = 0, doc_offsets=None,
-             score_kind: int = SCORE_NONE, softcap: float = 0.0, stream=None,
-             impl: str = "tc") -> None:
-    """Run attn_bwd (impl="tc") or attn_bwd_simt into dq, dk, dv."""
+             score_kind: int = SCORE_NONE, softcap: float = 0.0, dropout_p: float = 0.0,
+             dropout_seed: int = 0, stream=None, impl: str = "tc") -> None:
+    """Run attn_bwd (impl="tc") or attn_bwd_simt into dq, dk, dv; dropout_p and
+    dropout_seed must be those of the forward."""
     _check_tensors(q, k, v, o, lse, dout, dq, dk, dv, workspace, doc_offsets)
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
-    mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap)
+    mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap, dropout_p, dropout_seed)
     fn = lib.attn_bwd if impl == "tc" else lib.attn_bwd_simt
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
             _ptr(dv), B, Hq, Hkv, Nq, Nkv, d, ctypes.c_float(scale), mask_kind, mp,
-            score_kind, sp, _ptr(workspace), ctypes.c_size_t(ws_bytes), _stream(stream))
+            _score_kind(score_kind, dropout_p), sp, _ptr(workspace),
+            ctypes.c_size_t(ws_bytes), _stream(stream))
     del keep
     _lib.check(st, fn.__name__)
 
 
 def bwd_phases_into(phases: int, q, k, v, o, lse, dout, dq, dk, dv, workspace, *, scale: float,
                     mask_kind: int = MASK_NONE, window: int = 0, doc_offsets=None,
-                    score_kind: int = SCORE_NONE, softcap: float = 0.0, stream=None) -> None:
+                    score_kind: int = SCORE_NONE, softcap: float = 0.0,
+                    dropout_p: float = 0.0, dropout_seed: int = 0, stream=None) -> None:
     """Run some of the backward's kernels (BWD_ROWDOT | BWD_DKDV | BWD_DQ) via
     attn_bwd_phases; BWD_ROWDOT must have run on the same workspace first."""
     _check_tensors(q, k, v, o, lse, dout, dq, dk, dv, workspace, doc_offsets)
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
-    mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap)
+    mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap, dropout_p, dropout_seed)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib.attn_bwd_phases(int(phases), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                              _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nkv, d,
-                             ctypes.c_float(scale), mask_kind, mp, score_kind, sp,
+                             ctypes.c_float(scale), mask_kind, mp,
+                             _score_kind(score_kind, dropout_p), sp,
                              _ptr(workspace), ctypes.c_size_t(ws_bytes), _stream(stream))
     del keep
     _lib.check(st, "attn_bwd_phases")
@@ -131,9 +145,10 @@ def bwd_phases_into(phases: int, q, k, v, o, lse, dout, dq, dk, dv, workspace, *
 
 def backward(q, k, v, o, lse, dout, *, scale: Optional[float] = None,
              mask_kind: int = MASK_NONE, window: int = 0, doc_offsets=None,
-             score_kind: int = SCORE_NONE, softcap: float = 0.0, stream=None,
-             impl: str = "tc"):
-    """Gradients (dq, dk, dv) of sum(dout * o), rebuilding P from lse."""
+             score_kind: int = SCORE_NONE, softcap: float = 0.0, dropout_p: float = 0.0,
+             dropout_seed: int = 0, stream=None, impl: str = "tc"):
+    """Gradients (dq, dk, dv) of sum(dout * o), rebuilding P from lse (and the dropout
+    mask from dropout_seed when dropout_p > 0)."""
     d = q.shape[-1]
     if scale is None:
         scale = float(torch.tensor(d, dtype=torch.float32).rsqrt())
@@ -143,7 +158,7 @@ def backward(q, k, v, o, lse, dout, *, scale: Optional[float] = None,
     ws = torch.empty(max(bwd_workspace_size(q, k), 256), dtype=torch.uint8, device=q.device)
     bwd_into(q, k, v, o, lse, dout, dq, dk, dv, ws, scale=scale, mask_kind=mask_kind,
              window=window, doc_offsets=doc_offsets, score_kind=score_kind, softcap=softcap,
-             stream=stream, impl=impl)
+             dropout_p=dropout_p, dropout_seed=dropout_seed, stream=stream, impl=impl)
     return dq, dk, dv
 
 

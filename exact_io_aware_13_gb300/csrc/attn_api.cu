@@ -91,7 +91,8 @@ attn_status check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float 
   if ((long long)B * Hq > 0x7fffffff / 2) return ATTN_ERR_SHAPE;
   if (!std::isfinite(scale)) return ATTN_ERR_ARG;
   if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_DOCUMENT_CAUSAL) return ATTN_ERR_ARG;
-  if (score_kind & ~(ATTN_SCORE_ALIBI | ATTN_SCORE_SOFTCAP)) return ATTN_ERR_ARG;
+  if (score_kind & ~(ATTN_SCORE_ALIBI | ATTN_SCORE_SOFTCAP | ATTN_SCORE_DROPOUT))
+    return ATTN_ERR_ARG;
   std::memset(p, 0, sizeof(*p));
   p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->Nq = Nq; p->Nkv = Nkv; p->d = d;
   p->scale = scale;
@@ -103,6 +104,13 @@ attn_status check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float 
   if (score_kind & ATTN_SCORE_SOFTCAP) {
     if (!sp || !(sp->softcap > 0.f) || !std::isfinite(sp->softcap)) return ATTN_ERR_ARG;
     p->softcap = sp->softcap;
+  }
+  if (score_kind & ATTN_SCORE_DROPOUT) {
+    if (!sp || !(sp->dropout_p >= 0.f && sp->dropout_p < 1.f)) return ATTN_ERR_ARG;
+    p->drop_thr = std::min(255, (int)std::floor(sp->dropout_p * 256.0f));
+    p->drop_scale = 1.0f / (1.0f - sp->dropout_p);
+    p->drop_seed_lo = (uint32_t)(sp->dropout_seed & 0xFFFFFFFFull);
+    p->drop_seed_hi = (uint32_t)(sp->dropout_seed >> 32);
   }
   if (mask_kind == ATTN_MASK_SLIDING_WINDOW) {
     if (!mp || mp->window < 0) return ATTN_ERR_ARG;
@@ -142,6 +150,8 @@ attn_status fwd_common(bool simt, const void* q, const void* k, const void* v, v
   attn_status s = check_problem(B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind, mp, score_kind, sp, &p);
   if (s != ATTN_OK) return s;
   if (simt && d == 256) return ATTN_ERR_SHAPE;
+  // dropout: tensor-core path with d <= 128 only
+  if ((score_kind & ATTN_SCORE_DROPOUT) && (simt || d == 256)) return ATTN_ERR_ARG;
   const long long rows_q = (long long)B * Hq * Nq;
   if (rows_q == 0) return ATTN_OK;
   if (!q || !o || !lse) return ATTN_ERR_ARG;
@@ -193,6 +203,7 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
   attn_status s = check_problem(B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind, mp, score_kind, sp, &p);
   if (s != ATTN_OK) return s;
   if (d == 256) return ATTN_ERR_SHAPE;  // the backward handles d = 64 and 128
+  if (simt && (score_kind & ATTN_SCORE_DROPOUT)) return ATTN_ERR_ARG;
   const long long rows_q = (long long)B * Hq * Nq, rows_k = (long long)B * Hkv * Nkv;
   if (rows_q == 0 && rows_k == 0) return ATTN_OK;
   if (rows_q > 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_ERR_ARG;
@@ -425,6 +436,7 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const 
                                 score_kind, score_params, &p);
   if (s != ATTN_OK) return s;
   if (d != 128) return ATTN_ERR_SHAPE;  // FP8 forward: d = 128
+  if (score_kind & ATTN_SCORE_DROPOUT) return ATTN_ERR_ARG;
   const long long rows_q = (long long)B * Hq * Nq;
   if (rows_q == 0) return ATTN_OK;
   if (!q8 || !q_scale || !o || !lse) return ATTN_ERR_ARG;

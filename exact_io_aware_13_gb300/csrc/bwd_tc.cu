@@ -97,13 +97,15 @@ __device__ __forceinline__ ScoreK score_consts(const Problem& p, int h) {
 }
 
 // P and dS of one element. xs = raw score q.k; `alibi` = kb (j - i) (0 without ALiBi);
-// lse2 = L log2e (+inf for a row with no key). Under the soft-cap the pre-cap score is
-// in 2 log2e / c units and the tanh derivative scales dS. A masked element (ok false)
-// takes the exponent -inf, so P = dS = 0 with no branch: a per-lane condition around
-// the exponential would make the compiler branch on every element.
+// lse2 = L log2e (+inf for a row with no key); zs = the dropout factor of the element
+// (keep / (1 - p), 1 without dropout), so dS = P (dP zs - D). Under the soft-cap the
+// pre-cap score is in 2 log2e / c units and the tanh derivative scales dS. A masked
+// element (ok false) takes the exponent -inf, so P = dS = 0 with no branch: a per-lane
+// condition around the exponential would make the compiler branch on every element.
 template <bool kAlibi, bool kSoftcap>
 __device__ __forceinline__ void p_and_ds(float xs, const ScoreK& sk, float alibi, float lse2,
-                                         float dp, float delta, bool ok, float& pr, float& ds) {
+                                         float dp, float delta, bool ok, float zs, float& pr,
+                                         float& ds) {
   float arg, dcap = 1.f;
   if (kSoftcap) {
     const float pre = kAlibi ? fmaf(xs, sk.k1, alibi) : xs * sk.k1;
@@ -116,7 +118,43 @@ __device__ __forceinline__ void p_and_ds(float xs, const ScoreK& sk, float alibi
     arg = fmaf(xs, sk.k1, -lse2);
   }
   pr = ex2_approx(ok ? arg : -INFINITY);
-  ds = kSoftcap ? pr * (dp - delta) * dcap : pr * (dp - delta);
+  const float dpz = dp * zs;
+  ds = kSoftcap ? pr * (dpz - delta) * dcap : pr * (dpz - delta);
+}
+
+// Dropout factors (keep / (1 - p) or 0) of the 16 query columns qs .. qs + 15 of one key
+// row j, for the dK/dV layout (lane = key). One Philox call covers 16 keys of one query
+// row, so lane L draws the call of query qs + L / 2 and key block (j - lane) / 16 + L % 2,
+// and the warp passes each call's bytes to the 16 lanes (keys) that own them.
+__device__ __forceinline__ void dropout_cols_dkdv(const Problem& p, int j, int lane, int qs,
+                                                  int bh, float (&zs)[16]) {
+  const int jw = j - lane;  // first key of the warp, a multiple of 32
+  const uint4 w = philox4x32_10((uint32_t)((jw >> 4) + (lane & 1)), (uint32_t)(qs + (lane >> 1)),
+                                (uint32_t)bh, 0u, p.drop_seed_lo, p.drop_seed_hi);
+  const int sel = (lane & 15) >> 2, sh = 8 * (lane & 3);
+  const uint32_t thr = (uint32_t)p.drop_thr;
+#pragma unroll
+  for (int col = 0; col < 16; ++col) {
+    const int src = 2 * col + (lane >> 4);
+    const uint32_t a0 = __shfl_sync(0xffffffffu, w.x, src), a1 = __shfl_sync(0xffffffffu, w.y, src);
+    const uint32_t a2 = __shfl_sync(0xffffffffu, w.z, src), a3 = __shfl_sync(0xffffffffu, w.w, src);
+    const uint32_t word = sel == 0 ? a0 : sel == 1 ? a1 : sel == 2 ? a2 : a3;
+    zs[col] = ((word >> sh) & 0xFFu) >= thr ? p.drop_scale : 0.f;
+  }
+}
+
+// Dropout factors of the 32 key columns ks .. ks + 31 (ks a multiple of 16) of query row
+// i, for the dQ layout (thread = query row): two Philox calls.
+__device__ __forceinline__ void dropout_cols_dq(const Problem& p, int i, int ks, int bh,
+                                                float (&zs)[32]) {
+  const uint32_t thr = (uint32_t)p.drop_thr;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const uint4 w = philox4x32_10((uint32_t)((ks >> 4) + hh), (uint32_t)i, (uint32_t)bh, 0u,
+                                  p.drop_seed_lo, p.drop_seed_hi);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) zs[hh * 16 + e] = philox_byte(w, e) >= thr ? p.drop_scale : 0.f;
+  }
 }
 
 // dkdv element-wise step for one thread: key row j, 16 query columns starting at qs,
@@ -126,8 +164,8 @@ template <bool kAlibi, bool kSoftcap, bool kMasked>
 __device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_t (&dr)[16],
                                          const float* lse2, const float* dl, const int* fk,
                                          const ScoreK& sk, float base, int j, int qs,
-                                         bool key_ok, bool causal_type, uint32_t (&pp)[8],
-                                         uint32_t (&dd)[8]) {
+                                         bool key_ok, bool causal_type, const float (&zs)[16],
+                                         uint32_t (&pp)[8], uint32_t (&dd)[8]) {
 #pragma unroll
   for (int e4 = 0; e4 < 4; ++e4) {
     const float4 lv = reinterpret_cast<const float4*>(lse2)[e4];
@@ -145,7 +183,8 @@ __device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_
       }
       p_and_ds<kAlibi, kSoftcap>(__uint_as_float(sr[col]), sk,
                                  kAlibi ? fmaf(-(float)col, sk.kb, base) : 0.f, lvs[q],
-                                 __uint_as_float(dr[col]), dvs[q], ok, pv[q], dsv[q]);
+                                 __uint_as_float(dr[col]), dvs[q], ok, zs[col], pv[q], dsv[q]);
+      pv[q] *= zs[col];  // dV takes the dropped P
     }
     pp[2 * e4] = pack_bf16x2(pv[0], pv[1]);
     pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
@@ -159,7 +198,8 @@ __device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_
 template <bool kAlibi, bool kSoftcap, bool kMasked>
 __device__ __forceinline__ void dq_ds(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
                                       const ScoreK& sk, float base, float lse2, float delta,
-                                      int c_lo, int c_hi, uint32_t (&dd)[16]) {
+                                      int c_lo, int c_hi, const float (&zs)[32],
+                                      uint32_t (&dd)[16]) {
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     float pr[2], ds[2];
@@ -169,7 +209,7 @@ __device__ __forceinline__ void dq_ds(const uint32_t (&sr)[32], const uint32_t (
       const bool ok = !kMasked || (col >= c_lo && col <= c_hi);
       p_and_ds<kAlibi, kSoftcap>(__uint_as_float(sr[col]), sk,
                                  kAlibi ? fmaf((float)col, sk.kb, base) : 0.f, lse2,
-                                 __uint_as_float(dr[col]), delta, ok, pr[q], ds[q]);
+                                 __uint_as_float(dr[col]), delta, ok, zs[col], pr[q], ds[q]);
     }
     dd[e] = pack_bf16x2(ds[0], ds[1]);
   }
@@ -411,7 +451,7 @@ __device__ __forceinline__ void relay_loop(BwdBars* bars, const WaitCtx& wc, int
 }
 
 // ============================================================================ dK, dV
-template <int D, bool kAlibi, bool kSoftcap>
+template <int D, bool kAlibi, bool kSoftcap, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using L = LayoutKv<D>;
@@ -573,13 +613,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* dl = lse2 + SUB;
       const int* fk = reinterpret_cast<const int*>(dl + SUB);
       const float base = kAlibi ? sk.kb * (float)(j - qs) : 0.f;  // kb*(j - i) at column 0
+      float zs[16];
+      if constexpr (kDrop) {
+        dropout_cols_dkdv(p, j, lane, qs, bh, zs);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) zs[e] = 1.f;
+      }
       uint32_t pp[8], dd[8];
       if (tile_needs_mask(p.mask, qrow & ~(BT - 1), k0, BT))  // warp-uniform
         dkdv_pds<kAlibi, kSoftcap, true>(sr, dr, lse2, dl, fk, sk, base, j, qs, j < p.Nkv,
-                                         causal_type, pp, dd);
+                                         causal_type, zs, pp, dd);
       else
         dkdv_pds<kAlibi, kSoftcap, false>(sr, dr, lse2, dl, fk, sk, base, j, qs, true,
-                                          causal_type, pp, dd);
+                                          causal_type, zs, pp, dd);
       // P^T / dS^T of sub-step u - 1 must have been read by their MMAs
       if (u >= 1)
         ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pd_free[0]), (u - 1) & 1, wc));
@@ -615,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================================ dQ
-template <int D, bool kAlibi, bool kSoftcap>
+template <int D, bool kAlibi, bool kSoftcap, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using L = LayoutQ<D>;
@@ -751,11 +798,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence32(sr);
       reg_fence32(dr);
       const float base = kAlibi ? sk.kb * (float)(ks - i) : 0.f;  // kb*(j - i) at column 0
+      float zs[32];
+      if constexpr (kDrop) {
+        dropout_cols_dq(p, i, ks, bh, zs);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) zs[e] = 1.f;
+      }
       uint32_t dd[16];
       if (tile_needs_mask(p.mask, q0, kt0, BT))  // warp-uniform
-        dq_ds<kAlibi, kSoftcap, true>(sr, dr, sk, base, lse2, dlt, fk - ks, last_key - ks, dd);
+        dq_ds<kAlibi, kSoftcap, true>(sr, dr, sk, base, lse2, dlt, fk - ks, last_key - ks, zs, dd);
       else
-        dq_ds<kAlibi, kSoftcap, false>(sr, dr, sk, base, lse2, dlt, 0, 0, dd);
+        dq_ds<kAlibi, kSoftcap, false>(sr, dr, sk, base, lse2, dlt, 0, 0, zs, dd);
       tmem_st16(tS, dd);  // dS, bf16 pairs
       tmem_wait_st();
       tc_fence_before_sync();
@@ -780,11 +834,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kA, bool kS>
+template <int D, bool kA, bool kS, bool kDrop>
 cudaError_t launch_variant(const BwdArgs& kv_args, const BwdArgs& q_args, const BwdMaps& maps,
                            int grid_kv, int grid_q, cudaStream_t st) {
-  auto k1 = dkdv_kernel<D, kA, kS>;
-  auto k2 = dq_kernel<D, kA, kS>;
+  auto k1 = dkdv_kernel<D, kA, kS, kDrop>;
+  auto k2 = dq_kernel<D, kA, kS, kDrop>;
   constexpr int kSmemKv = LayoutKv<D>::kAlloc, kSmemQ = LayoutQ<D>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKv);
   if (e != cudaSuccess) return e;
@@ -796,14 +850,21 @@ cudaError_t launch_variant(const BwdArgs& kv_args, const BwdArgs& q_args, const 
   return cudaGetLastError();
 }
 
+template <int D, bool kDrop>
+cudaError_t launch_dd(const BwdArgs& ka, const BwdArgs& qa, const BwdMaps& maps, int gk, int gq,
+                      cudaStream_t st) {
+  const bool al = ka.p.score_kind & ATTN_SCORE_ALIBI, sc = ka.p.score_kind & ATTN_SCORE_SOFTCAP;
+  if (al && sc) return launch_variant<D, true, true, kDrop>(ka, qa, maps, gk, gq, st);
+  if (al) return launch_variant<D, true, false, kDrop>(ka, qa, maps, gk, gq, st);
+  if (sc) return launch_variant<D, false, true, kDrop>(ka, qa, maps, gk, gq, st);
+  return launch_variant<D, false, false, kDrop>(ka, qa, maps, gk, gq, st);
+}
+
 template <int D>
 cudaError_t launch_d(const BwdArgs& ka, const BwdArgs& qa, const BwdMaps& maps, int gk, int gq,
                      cudaStream_t st) {
-  const bool al = ka.p.score_kind & ATTN_SCORE_ALIBI, sc = ka.p.score_kind & ATTN_SCORE_SOFTCAP;
-  if (al && sc) return launch_variant<D, true, true>(ka, qa, maps, gk, gq, st);
-  if (al) return launch_variant<D, true, false>(ka, qa, maps, gk, gq, st);
-  if (sc) return launch_variant<D, false, true>(ka, qa, maps, gk, gq, st);
-  return launch_variant<D, false, false>(ka, qa, maps, gk, gq, st);
+  if (ka.p.score_kind & ATTN_SCORE_DROPOUT) return launch_dd<D, true>(ka, qa, maps, gk, gq, st);
+  return launch_dd<D, false>(ka, qa, maps, gk, gq, st);
 }
 
 }  // namespace

@@ -25,6 +25,9 @@
 //     than 2^8 (a stale max is exact: O and l share it until the final division).
 // Tensor memory: S0 cols [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d).
 //
+// Dropout variant (kDrop, bf16 only): P is multiplied by the keep mask / (1 - p) before
+// the P V product; the row sums and the LSE keep the undropped P.
+//
 // FP8 variant (kFp8, d = 128): Q and K are e4m3 with one scale per 128-row tile, V is
 // e4m3 stored transposed ([d, keys] per head, keys contiguous) with one scale per head,
 // so both MMAs read K-major 8-bit operands (kind::f8f6f4, K = 32 per instruction). The
@@ -109,7 +112,7 @@ __device__ __forceinline__ void cta_work(const FwdArgs& a, int& bh, int& qb) {
   bh = grp * kHeadGroup + rem % gh;
 }
 
-template <int D, bool kAlibi, bool kSoftcap, bool kFp8>
+template <int D, bool kAlibi, bool kSoftcap, bool kFp8, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -411,13 +414,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st8(tS + c * 8, pk);
         } else {
           uint32_t pk[16];
+          // Dropout: one Philox call per 16 keys of this row; l sums the undropped P
+          // (the softmax is taken before dropout), P V takes the dropped, rescaled P.
+          uint4 rw[2];
+          if (kDrop) {
+            const uint32_t blk = (uint32_t)((k0 + c * 32) >> 4);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+              rw[hh] = philox4x32_10(blk + hh, (uint32_t)i, (uint32_t)bh, 0u, p.drop_seed_lo,
+                                     p.drop_seed_hi);
+          }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), mul, neg_m));
             const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
             acc[(2 * e) & 7] += p0;
             acc[(2 * e + 1) & 7] += p1;
-            pk[e] = pack_bf16x2(p0, p1);
+            if (kDrop) {
+              const uint32_t thr = (uint32_t)p.drop_thr;
+              const uint4& w = rw[e >> 3];
+              const float d0 = philox_byte(w, (2 * e) & 15) >= thr ? p0 * p.drop_scale : 0.f;
+              const float d1 = philox_byte(w, (2 * e + 1) & 15) >= thr ? p1 * p.drop_scale : 0.f;
+              pk[e] = pack_bf16x2(d0, d1);
+            } else {
+              pk[e] = pack_bf16x2(p0, p1);
+            }
           }
           tmem_st16(tS + c * 16, pk);
         }
@@ -485,10 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kAlibi, bool kSoftcap, bool kFp8 = false>
+template <int D, bool kAlibi, bool kSoftcap, bool kFp8 = false, bool kDrop = false>
 cudaError_t launch_variant(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int grid, cudaStream_t st) {
-  auto kern = fwd_tc_kernel<D, kAlibi, kSoftcap, kFp8>;
+  auto kern = fwd_tc_kernel<D, kAlibi, kSoftcap, kFp8, kDrop>;
   const int smem = Layout<D, kFp8>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -496,14 +517,21 @@ cudaError_t launch_variant(const FwdArgs& a, const CUtensorMap& tq, const CUtens
   return cudaGetLastError();
 }
 
+template <int D, bool kDrop>
+cudaError_t launch_dd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const CUtensorMap& tv, int grid, cudaStream_t st) {
+  const bool al = a.p.score_kind & ATTN_SCORE_ALIBI, sc = a.p.score_kind & ATTN_SCORE_SOFTCAP;
+  if (al && sc) return launch_variant<D, true, true, false, kDrop>(a, tq, tk, tv, grid, st);
+  if (al) return launch_variant<D, true, false, false, kDrop>(a, tq, tk, tv, grid, st);
+  if (sc) return launch_variant<D, false, true, false, kDrop>(a, tq, tk, tv, grid, st);
+  return launch_variant<D, false, false, false, kDrop>(a, tq, tk, tv, grid, st);
+}
+
 template <int D>
 cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, int grid, cudaStream_t st) {
-  const bool al = a.p.score_kind & ATTN_SCORE_ALIBI, sc = a.p.score_kind & ATTN_SCORE_SOFTCAP;
-  if (al && sc) return launch_variant<D, true, true>(a, tq, tk, tv, grid, st);
-  if (al) return launch_variant<D, true, false>(a, tq, tk, tv, grid, st);
-  if (sc) return launch_variant<D, false, true>(a, tq, tk, tv, grid, st);
-  return launch_variant<D, false, false>(a, tq, tk, tv, grid, st);
+  if (a.p.score_kind & ATTN_SCORE_DROPOUT) return launch_dd<D, true>(a, tq, tk, tv, grid, st);
+  return launch_dd<D, false>(a, tq, tk, tv, grid, st);
 }
 
 }  // namespace

@@ -20,6 +20,12 @@ struct Problem {
   MaskSpec mask;      // mask kind and parameters (doc offsets in device memory)
   int* status;        // device status word (bounded waits write DEV_TIMEOUT)
   int nq_pad;         // Nq rounded up to a multiple of 128: row stride of the row terms
+  // Dropout (score_kind & ATTN_SCORE_DROPOUT): element (i, j) of query head bh is kept
+  // iff byte j % 16 of Philox4x32-10((j / 16, i, bh, 0), seed) >= drop_thr; kept values
+  // are multiplied by drop_scale = 1 / (1 - p).
+  int drop_thr;
+  float drop_scale;
+  uint32_t drop_seed_lo, drop_seed_hi;
 };
 
 // Per-query-row terms of the backward, computed once by the row kernel and read by

@@ -391,6 +391,34 @@ __device__ __forceinline__ void mma_f8_ts_if(bool pred, uint32_t d_tmem, uint32_
       : "memory");
 }
 
+// ---------------------------------------------------------------- Philox4x32-10
+// The counter-based generator of Salmon, Moraes, Dror and Shaw ("Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011): ten rounds of
+//   (hi0, lo0) = M0 x0, (hi1, lo1) = M1 x2, (x0, x1, x2, x3) <- (hi1^x1^k0, lo1, hi0^x3^k1, lo0)
+// with the key (k0, k1) advanced by (W0, W1) after each round.
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t x0, uint32_t x1, uint32_t x2,
+                                               uint32_t x3, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(M0, x0), lo0 = M0 * x0;
+    const uint32_t hi1 = __umulhi(M1, x2), lo1 = M1 * x2;
+    x0 = hi1 ^ x1 ^ k0;
+    x1 = lo1;
+    x2 = hi0 ^ x3 ^ k1;
+    x3 = lo0;
+    k0 += W0;
+    k1 += W1;
+  }
+  return make_uint4(x0, x1, x2, x3);
+}
+
+// Byte b (0..15) of a Philox output: word b / 4, bits 8 (b % 4) upward.
+__device__ __forceinline__ uint32_t philox_byte(const uint4& w, int b) {
+  const uint32_t word = (b >> 2) == 0 ? w.x : (b >> 2) == 1 ? w.y : (b >> 2) == 2 ? w.z : w.w;
+  return (word >> (8 * (b & 3))) & 0xFFu;
+}
+
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -82,7 +82,8 @@ enum {
 enum {
   ATTN_SCORE_NONE = 0,
   ATTN_SCORE_ALIBI = 1,
-  ATTN_SCORE_SOFTCAP = 2
+  ATTN_SCORE_SOFTCAP = 2,
+  ATTN_SCORE_DROPOUT = 4   /* dropout on P (attn_fwd / attn_bwd, tensor-core path, d <= 128) */
 };
 
 /* Tile classes written by attn_classify_tiles. */
@@ -99,7 +100,20 @@ typedef struct {
 
 typedef struct {
   float softcap;               /* ATTN_SCORE_SOFTCAP: the cap c > 0 */
+  float dropout_p;             /* ATTN_SCORE_DROPOUT: drop probability, 0 <= p < 1 */
+  uint64_t dropout_seed;       /* ATTN_SCORE_DROPOUT: seed of the keep mask */
 } attn_score_params;
+
+/*
+ * Dropout ("FlashAttention/es", "Variantes y sucesores": FlashAttention-1 supported
+ * dropout). Element (i, j) of query head bh = b * Hq + h is kept iff byte j % 16 of
+ * Philox4x32-10 (Salmon et al., SC 2011; 128-bit counter (j / 16, i, bh, 0), key = the
+ * seed, low word first; byte k = bits 8 (k % 4) .. of word k / 4) is at least
+ * floor(256 p) (capped at 255), so p is taken to 1/256; kept values are scaled by
+ * 1 / (1 - p). The forward computes O = (P Z / (1 - p)) V with lse from the undropped
+ * softmax; attn_bwd, given the same p and seed, regenerates Z: dV = (P Z / (1 - p))^T dO
+ * and dS = P (dP Z / (1 - p) - D). Pass the same score_kind and score_params to both.
+ */
 
 /*
  * Forward pass ("FlashAttention/es", "El algoritmo FlashAttention"): writes

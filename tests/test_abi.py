@@ -49,7 +49,19 @@ def test_argument_errors_return_before_any_device_call(lib):
     assert _fwd(lib, Nq=-1) == 2
     assert _fwd(lib, scale=float("nan")) == 1         # ATTN_ERR_ARG
     assert _fwd(lib, mask=7) == 1
-    assert _fwd(lib, score=4) == 1
+    assert _fwd(lib, score=8) == 1                    # unknown score bit
+    assert _fwd(lib, score=4) == 1                    # dropout without params
+    for p_drop in (-0.1, 1.0, 1.5, float("nan")):
+        sp = _lib.ScoreParams(0.0, p_drop, 7)
+        assert _fwd(lib, score=4, sp=ctypes.byref(sp)) == 1, p_drop
+    sp = _lib.ScoreParams(0.0, 0.1, 7)
+    assert _fwd(lib, score=4, sp=ctypes.byref(sp)) == 1   # valid dropout, null tensors
+    assert _fwd(lib, score=4, sp=ctypes.byref(sp), d=256) == 1  # dropout: d <= 128
+    assert lib.attn_fwd_simt(None, None, None, None, None, 1, 2, 1, 16, 16, 64,
+                             ctypes.c_float(0.125), 0, None, 4, ctypes.byref(sp), None) == 1
+    assert lib.attn_bwd_simt(*([ctypes.c_void_p(4096)] * 9), 1, 1, 1, 128, 128, 64,
+                             ctypes.c_float(0.1), 0, None, 4, ctypes.byref(sp),
+                             ctypes.c_void_p(4096), 1 << 20, None) == 1
     assert _fwd(lib, mask=2, mp=None) == 1            # window without params
     mp = _lib.MaskParams(-1, None, 0)
     assert _fwd(lib, mask=2, mp=ctypes.byref(mp)) == 1

@@ -58,6 +58,8 @@ class Workload:
     backward: bool = False
     doc_min: int = 512
     doc_max: int = 4096
+    dropout_p: float = 0.0
+    dropout_seed: int = 0
 
     @property
     def scale(self) -> float:
@@ -73,6 +75,8 @@ class Workload:
             s += " +alibi"
         if self.score_kind & SCORE_SOFTCAP:
             s += f" +softcap{self.softcap:g}"
+        if self.dropout_p > 0:
+            s += f" +dropout{self.dropout_p:g}"
         return s
 
     def replace(self, **kw) -> "Workload":
@@ -92,6 +96,12 @@ CAUSAL_FWD_BWD = Workload("causal fwd+bwd", 4, B=2, Hq=16, Hkv=16, Nq=8192, Nkv=
                           d=128, mask_kind=MASK_CAUSAL, backward=True)
 
 WORKLOADS = [TINY, CAUSAL, GQA_WINDOW, DOCS, CAUSAL_FWD_BWD]
+
+# Dropout on P ("FlashAttention/es", "Variantes y sucesores"), at the rate usually
+# trained with, on the causal fwd+bwd shapes; the seed has both 32-bit halves set.
+CAUSAL_FWD_BWD_DROPOUT = CAUSAL_FWD_BWD.replace(name="causal fwd+bwd dropout 0.1", seed=7,
+                                                dropout_p=0.1,
+                                                dropout_seed=0x9E3779B97F4A7C15)
 
 # Head dimension 256, the top of the range the pages give ("FlashAttention/es",
 # "Limitaciones"): the causal workload's FLOPs at twice the head size, half the batch.
