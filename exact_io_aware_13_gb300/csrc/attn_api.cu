@@ -105,10 +105,13 @@ attn_status check_problem(int B, int Hq, int Hkv, int Nq, int Nkv, int d, float 
     if (!sp || !(sp->softcap > 0.f) || !std::isfinite(sp->softcap)) return ATTN_ERR_ARG;
     p->softcap = sp->softcap;
   }
+  p->drop_scale = 1.f;
+  p->drop_keep = 1.f;
   if (score_kind & ATTN_SCORE_DROPOUT) {
     if (!sp || !(sp->dropout_p >= 0.f && sp->dropout_p < 1.f)) return ATTN_ERR_ARG;
     p->drop_thr = std::min(255, (int)std::floor(sp->dropout_p * 256.0f));
-    p->drop_scale = 1.0f / (1.0f - sp->dropout_p);
+    p->drop_keep = 1.0f - sp->dropout_p;
+    p->drop_scale = 1.0f / p->drop_keep;
     p->drop_seed_lo = (uint32_t)(sp->dropout_seed & 0xFFFFFFFFull);
     p->drop_seed_hi = (uint32_t)(sp->dropout_seed >> 32);
   }

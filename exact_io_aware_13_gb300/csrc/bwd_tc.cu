@@ -97,15 +97,18 @@ __device__ __forceinline__ ScoreK score_consts(const Problem& p, int h) {
 }
 
 // P and dS of one element. xs = raw score q.k; `alibi` = kb (j - i) (0 without ALiBi);
-// lse2 = L log2e (+inf for a row with no key); zs = the dropout factor of the element
-// (keep / (1 - p), 1 without dropout), so dS = P (dP zs - D). Under the soft-cap the
-// pre-cap score is in 2 log2e / c units and the tanh derivative scales dS. A masked
-// element (ok false) takes the exponent -inf, so P = dS = 0 with no branch: a per-lane
-// condition around the exponential would make the compiler branch on every element.
+// lse2 = L log2e (+inf for a row with no key); zm = the element's dropout keep mask
+// (all ones without dropout, 0 where the element is dropped). With dropout the row term
+// is D' = D (1 - p) and the result dS' = P (dP Z - D') is dS (1 - p); the factor
+// 1 / (1 - p) is applied with the softmax scale in the dK and dQ epilogues. Under the
+// soft-cap the pre-cap score is in 2 log2e / c units and the tanh derivative scales dS. A
+// masked element (ok false) takes the exponent -inf, so P = dS = 0 with no branch: a
+// per-lane condition around the exponential would make the compiler branch on every
+// element.
 template <bool kAlibi, bool kSoftcap>
 __device__ __forceinline__ void p_and_ds(float xs, const ScoreK& sk, float alibi, float lse2,
-                                         float dp, float delta, bool ok, float zs, float& pr,
-                                         float& ds) {
+                                         float dp, float delta, bool ok, uint32_t zm,
+                                         float& pr, float& ds) {
   float arg, dcap = 1.f;
   if (kSoftcap) {
     const float pre = kAlibi ? fmaf(xs, sk.k1, alibi) : xs * sk.k1;
@@ -118,53 +121,53 @@ __device__ __forceinline__ void p_and_ds(float xs, const ScoreK& sk, float alibi
     arg = fmaf(xs, sk.k1, -lse2);
   }
   pr = ex2_approx(ok ? arg : -INFINITY);
-  const float dpz = dp * zs;
+  const float dpz = __uint_as_float(__float_as_uint(dp) & zm);
   ds = kSoftcap ? pr * (dpz - delta) * dcap : pr * (dpz - delta);
 }
 
-// Dropout factors (keep / (1 - p) or 0) of the 16 query columns qs .. qs + 15 of one key
-// row j, for the dK/dV layout (lane = key). One Philox call covers 16 keys of one query
-// row, so lane L draws the call of query qs + L / 2 and key block (j - lane) / 16 + L % 2,
-// and the warp passes each call's bytes to the 16 lanes (keys) that own them.
-__device__ __forceinline__ void dropout_cols_dkdv(const Problem& p, int j, int lane, int qs,
-                                                  int bh, float (&zs)[16]) {
+// Dropout keep flags (keep_flags4 layout: flag of column c in byte c % 4 of word c / 4)
+// of the 16 query columns qs .. qs + 15 of key row j, for the dK/dV layout (lane = key).
+// One Philox call covers 16 keys of one query row, so lane L draws the call of query
+// qs + L % 16 and key block (j - lane) / 16 + L / 16; a byte transpose within each
+// half-warp then hands every lane the bytes of its own key.
+__device__ __forceinline__ void dropout_flags_dkdv(const Problem& p, const DropThr& th, int j,
+                                                   int lane, int qs, int bh,
+                                                   uint32_t (&kf)[4]) {
   const int jw = j - lane;  // first key of the warp, a multiple of 32
-  const uint4 w = philox4x32_10((uint32_t)((jw >> 4) + (lane & 1)), (uint32_t)(qs + (lane >> 1)),
+  const uint4 r = philox4x32_10((uint32_t)((jw >> 4) + (lane >> 4)), (uint32_t)(qs + (lane & 15)),
                                 (uint32_t)bh, 0u, p.drop_seed_lo, p.drop_seed_hi);
-  const int sel = (lane & 15) >> 2, sh = 8 * (lane & 3);
-  const uint32_t thr = (uint32_t)p.drop_thr;
+  kf[0] = r.x;
+  kf[1] = r.y;
+  kf[2] = r.z;
+  kf[3] = r.w;
+  transpose16x16_bytes(kf, lane);
 #pragma unroll
-  for (int col = 0; col < 16; ++col) {
-    const int src = 2 * col + (lane >> 4);
-    const uint32_t a0 = __shfl_sync(0xffffffffu, w.x, src), a1 = __shfl_sync(0xffffffffu, w.y, src);
-    const uint32_t a2 = __shfl_sync(0xffffffffu, w.z, src), a3 = __shfl_sync(0xffffffffu, w.w, src);
-    const uint32_t word = sel == 0 ? a0 : sel == 1 ? a1 : sel == 2 ? a2 : a3;
-    zs[col] = ((word >> sh) & 0xFFu) >= thr ? p.drop_scale : 0.f;
-  }
+  for (int q = 0; q < 4; ++q) kf[q] = keep_flags4(kf[q], th);
 }
 
-// Dropout factors of the 32 key columns ks .. ks + 31 (ks a multiple of 16) of query row
-// i, for the dQ layout (thread = query row): two Philox calls.
-__device__ __forceinline__ void dropout_cols_dq(const Problem& p, int i, int ks, int bh,
-                                                float (&zs)[32]) {
-  const uint32_t thr = (uint32_t)p.drop_thr;
+// Dropout keep flags of the 32 key columns ks .. ks + 31 (ks a multiple of 16) of query
+// row i, for the dQ layout (thread = query row): two Philox calls.
+__device__ __forceinline__ void dropout_flags_dq(const Problem& p, const DropThr& th, int i,
+                                                 int ks, int bh, uint32_t (&kf)[8]) {
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
-    const uint4 w = philox4x32_10((uint32_t)((ks >> 4) + hh), (uint32_t)i, (uint32_t)bh, 0u,
+    const uint4 r = philox4x32_10((uint32_t)((ks >> 4) + hh), (uint32_t)i, (uint32_t)bh, 0u,
                                   p.drop_seed_lo, p.drop_seed_hi);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) zs[hh * 16 + e] = philox_byte(w, e) >= thr ? p.drop_scale : 0.f;
+    kf[4 * hh + 0] = keep_flags4(r.x, th);
+    kf[4 * hh + 1] = keep_flags4(r.y, th);
+    kf[4 * hh + 2] = keep_flags4(r.z, th);
+    kf[4 * hh + 3] = keep_flags4(r.w, th);
   }
 }
 
 // dkdv element-wise step for one thread: key row j, 16 query columns starting at qs,
 // with their lse2 / delta / first key. Writes P^T and dS^T (bf16 pairs). kMasked adds
 // the per-element mask test; the caller picks the variant by a warp-uniform tile test.
-template <bool kAlibi, bool kSoftcap, bool kMasked>
+template <bool kAlibi, bool kSoftcap, bool kMasked, bool kDrop>
 __device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_t (&dr)[16],
                                          const float* lse2, const float* dl, const int* fk,
                                          const ScoreK& sk, float base, int j, int qs,
-                                         bool key_ok, bool causal_type, const float (&zs)[16],
+                                         bool key_ok, bool causal_type, const uint32_t (&kf)[4],
                                          uint32_t (&pp)[8], uint32_t (&dd)[8]) {
 #pragma unroll
   for (int e4 = 0; e4 < 4; ++e4) {
@@ -181,10 +184,11 @@ __device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_
         const int i = qs + col;
         ok = key_ok && (!causal_type || (i >= j && fk[col] <= j));
       }
+      const uint32_t zm = kDrop ? keep_mask_elem(kf[e4], q) : 0xffffffffu;
       p_and_ds<kAlibi, kSoftcap>(__uint_as_float(sr[col]), sk,
                                  kAlibi ? fmaf(-(float)col, sk.kb, base) : 0.f, lvs[q],
-                                 __uint_as_float(dr[col]), dvs[q], ok, zs[col], pv[q], dsv[q]);
-      pv[q] *= zs[col];  // dV takes the dropped P
+                                 __uint_as_float(dr[col]), dvs[q], ok, zm, pv[q], dsv[q]);
+      if (kDrop) pv[q] = __uint_as_float(__float_as_uint(pv[q]) & zm);  // dV takes P Z
     }
     pp[2 * e4] = pack_bf16x2(pv[0], pv[1]);
     pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
@@ -195,10 +199,10 @@ __device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_
 
 // dq element-wise step for one thread: query row with (lse2, delta), 32 key columns;
 // allowed columns are [c_lo, c_hi] when kMasked. Writes dS (bf16 pairs).
-template <bool kAlibi, bool kSoftcap, bool kMasked>
+template <bool kAlibi, bool kSoftcap, bool kMasked, bool kDrop>
 __device__ __forceinline__ void dq_ds(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
                                       const ScoreK& sk, float base, float lse2, float delta,
-                                      int c_lo, int c_hi, const float (&zs)[32],
+                                      int c_lo, int c_hi, const uint32_t (&kf)[8],
                                       uint32_t (&dd)[16]) {
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
@@ -207,9 +211,10 @@ __device__ __forceinline__ void dq_ds(const uint32_t (&sr)[32], const uint32_t (
     for (int q = 0; q < 2; ++q) {
       const int col = 2 * e + q;
       const bool ok = !kMasked || (col >= c_lo && col <= c_hi);
+      const uint32_t zm = kDrop ? keep_mask_elem(kf[col >> 2], col & 3) : 0xffffffffu;
       p_and_ds<kAlibi, kSoftcap>(__uint_as_float(sr[col]), sk,
                                  kAlibi ? fmaf((float)col, sk.kb, base) : 0.f, lse2,
-                                 __uint_as_float(dr[col]), delta, ok, zs[col], pr[q], ds[q]);
+                                 __uint_as_float(dr[col]), delta, ok, zm, pr[q], ds[q]);
     }
     dd[e] = pack_bf16x2(ds[0], ds[1]);
   }
@@ -589,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = bh - b * p.Hq;
       const int qs = qrow + c0;                  // query of this thread's column 0
       const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
+      const DropThr dthr = drop_thr_words(kDrop ? p.drop_thr : 0);
       if (ok_all)
         ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[0]), u & 1, wc));
       // the stage's row terms arrived with full[s]; observe them
@@ -613,20 +619,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* dl = lse2 + SUB;
       const int* fk = reinterpret_cast<const int*>(dl + SUB);
       const float base = kAlibi ? sk.kb * (float)(j - qs) : 0.f;  // kb*(j - i) at column 0
-      float zs[16];
-      if constexpr (kDrop) {
-        dropout_cols_dkdv(p, j, lane, qs, bh, zs);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) zs[e] = 1.f;
-      }
+      uint32_t kf[4];
+      if constexpr (kDrop) dropout_flags_dkdv(p, dthr, j, lane, qs, bh, kf);
       uint32_t pp[8], dd[8];
       if (tile_needs_mask(p.mask, qrow & ~(BT - 1), k0, BT))  // warp-uniform
-        dkdv_pds<kAlibi, kSoftcap, true>(sr, dr, lse2, dl, fk, sk, base, j, qs, j < p.Nkv,
-                                         causal_type, zs, pp, dd);
+        dkdv_pds<kAlibi, kSoftcap, true, kDrop>(sr, dr, lse2, dl, fk, sk, base, j, qs,
+                                                j < p.Nkv, causal_type, kf, pp, dd);
       else
-        dkdv_pds<kAlibi, kSoftcap, false>(sr, dr, lse2, dl, fk, sk, base, j, qs, true,
-                                          causal_type, zs, pp, dd);
+        dkdv_pds<kAlibi, kSoftcap, false, kDrop>(sr, dr, lse2, dl, fk, sk, base, j, qs, true,
+                                                 causal_type, kf, pp, dd);
       // P^T / dS^T of sub-step u - 1 must have been read by their MMAs
       if (u >= 1)
         ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pd_free[0]), (u - 1) & 1, wc));
@@ -650,7 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t krow = (size_t)bg * p.Nkv + (j < p.Nkv ? j : 0);
     const uint32_t tacc = tmem + lane_base + (which ? colDK : colDV) + half * (D / 2);
     __nv_bfloat16* dst = (which ? a.dk : a.dv) + krow * D + half * (D / 2);
-    store_acc_row<D / 2>(tacc, which ? p.scale : 1.f, dst, have, j < p.Nkv);
+    const float dsc = kDrop ? p.drop_scale : 1.f;  // dV = (P Z)^T dO / (1 - p); dK from dS'
+    store_acc_row<D / 2>(tacc, which ? p.scale * dsc : dsc, dst, have, j < p.Nkv);
   }
   __syncwarp();
   tc_fence_before_sync();
@@ -750,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c0 = wg * 32;
     const int x = pair;
     const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
+    const DropThr dthr = drop_thr_words(kDrop ? p.drop_thr : 0);
     float lse2 = INFINITY, dlt = 0.f;
     int fk = 0;
     if (row_ok) {  // row terms of the row kernel (lse2 is already L log2 e, +inf if empty)
@@ -798,18 +801,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence32(sr);
       reg_fence32(dr);
       const float base = kAlibi ? sk.kb * (float)(ks - i) : 0.f;  // kb*(j - i) at column 0
-      float zs[32];
-      if constexpr (kDrop) {
-        dropout_cols_dq(p, i, ks, bh, zs);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) zs[e] = 1.f;
-      }
+      uint32_t kf[8];
+      if constexpr (kDrop) dropout_flags_dq(p, dthr, i, ks, bh, kf);
       uint32_t dd[16];
       if (tile_needs_mask(p.mask, q0, kt0, BT))  // warp-uniform
-        dq_ds<kAlibi, kSoftcap, true>(sr, dr, sk, base, lse2, dlt, fk - ks, last_key - ks, zs, dd);
+        dq_ds<kAlibi, kSoftcap, true, kDrop>(sr, dr, sk, base, lse2, dlt, fk - ks, last_key - ks,
+                                             kf, dd);
       else
-        dq_ds<kAlibi, kSoftcap, false>(sr, dr, sk, base, lse2, dlt, 0, 0, zs, dd);
+        dq_ds<kAlibi, kSoftcap, false, kDrop>(sr, dr, sk, base, lse2, dlt, 0, 0, kf, dd);
       tmem_st16(tS, dd);  // dS, bf16 pairs
       tmem_wait_st();
       tc_fence_before_sync();
@@ -822,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (pair == 0) {  // warp-uniform
       const uint32_t tq = tmem + lane_base + kColAcc + wg * (D / 2);
       __nv_bfloat16* dst = a.dq + ((size_t)bh * p.Nq + (row_ok ? i : 0)) * D + wg * (D / 2);
-      store_acc_row<D / 2>(tq, p.scale, dst, have, row_ok);
+      store_acc_row<D / 2>(tq, kDrop ? p.scale * p.drop_scale : p.scale, dst, have, row_ok);
     }
   }
   __syncwarp();

@@ -394,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // FP8: exp2(s - m + 7) = 2^7 p, the scale e4m3 rounding wants, at no extra cost
       const float neg_m = (m_run == -INFINITY ? 0.f : -m_run) + (kFp8 ? kPScaleLog2Fp8 : 0.f);
       const float mul = fast ? k1j : 1.f;  // p = exp2(v * mul - m)
+      const DropThr dthr = drop_thr_words(kDrop ? p.drop_thr : 0);
       float acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -414,15 +415,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st8(tS + c * 8, pk);
         } else {
           uint32_t pk[16];
-          // Dropout: one Philox call per 16 keys of this row; l sums the undropped P
-          // (the softmax is taken before dropout), P V takes the dropped, rescaled P.
-          uint4 rw[2];
+          // Dropout: one Philox call per 16 keys of this row gives the keep flags of
+          // those keys; l sums the undropped P (the softmax is taken before dropout) and
+          // P V takes the dropped P, whose 1 / (1 - p) is applied with 1 / l at the end.
+          uint32_t kf[8];
           if (kDrop) {
             const uint32_t blk = (uint32_t)((k0 + c * 32) >> 4);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-              rw[hh] = philox4x32_10(blk + hh, (uint32_t)i, (uint32_t)bh, 0u, p.drop_seed_lo,
-                                     p.drop_seed_hi);
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint4 w = philox4x32_10(blk + hh, (uint32_t)i, (uint32_t)bh, 0u,
+                                            p.drop_seed_lo, p.drop_seed_hi);
+              kf[4 * hh + 0] = keep_flags4(w.x, dthr);
+              kf[4 * hh + 1] = keep_flags4(w.y, dthr);
+              kf[4 * hh + 2] = keep_flags4(w.z, dthr);
+              kf[4 * hh + 3] = keep_flags4(w.w, dthr);
+            }
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -430,15 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
             acc[(2 * e) & 7] += p0;
             acc[(2 * e + 1) & 7] += p1;
-            if (kDrop) {
-              const uint32_t thr = (uint32_t)p.drop_thr;
-              const uint4& w = rw[e >> 3];
-              const float d0 = philox_byte(w, (2 * e) & 15) >= thr ? p0 * p.drop_scale : 0.f;
-              const float d1 = philox_byte(w, (2 * e + 1) & 15) >= thr ? p1 * p.drop_scale : 0.f;
-              pk[e] = pack_bf16x2(d0, d1);
-            } else {
-              pk[e] = pack_bf16x2(p0, p1);
-            }
+            pk[e] = pack_bf16x2(p0, p1);
+            if (kDrop)  // keys 2e, 2e + 1: flag bytes (2e) % 4, +1 of word e / 2
+              pk[e] &= keep_mask_pair(kf[e >> 1], 2 * (e & 1));
           }
           tmem_st16(tS + c * 16, pk);
         }
@@ -465,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (have_o) have_o = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full[t]), 0, wc));
     tc_fence_after_sync();
     float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    if (kDrop) inv *= p.drop_scale;  // the kept terms' 1 / (1 - p)
     if (kFp8) inv *= a.sv[bg];  // l holds 2^7 times the row sum, like O
     uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * p.Nq + (i < p.Nq ? i : 0)) * D);
 #pragma unroll

@@ -22,9 +22,11 @@ struct Problem {
   int nq_pad;         // Nq rounded up to a multiple of 128: row stride of the row terms
   // Dropout (score_kind & ATTN_SCORE_DROPOUT): element (i, j) of query head bh is kept
   // iff byte j % 16 of Philox4x32-10((j / 16, i, bh, 0), seed) >= drop_thr; kept values
-  // are multiplied by drop_scale = 1 / (1 - p).
+  // are multiplied by drop_scale = 1 / (1 - p) (drop_keep = 1 - p; both 1 without
+  // dropout). The backward's row term is D (1 - p).
   int drop_thr;
   float drop_scale;
+  float drop_keep;
   uint32_t drop_seed_lo, drop_seed_hi;
 };
 

@@ -401,8 +401,9 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t x0, uint32_t x1, uint32_
   constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(M0, x0), lo0 = M0 * x0;
-    const uint32_t hi1 = __umulhi(M1, x2), lo1 = M1 * x2;
+    const uint64_t p0 = (uint64_t)M0 * x0, p1 = (uint64_t)M1 * x2;  // one wide multiply each
+    const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
     x0 = hi1 ^ x1 ^ k0;
     x1 = lo1;
     x2 = hi0 ^ x3 ^ k1;
@@ -413,10 +414,87 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t x0, uint32_t x1, uint32_
   return make_uint4(x0, x1, x2, x3);
 }
 
-// Byte b (0..15) of a Philox output: word b / 4, bits 8 (b % 4) upward.
-__device__ __forceinline__ uint32_t philox_byte(const uint4& w, int b) {
-  const uint32_t word = (b >> 2) == 0 ? w.x : (b >> 2) == 1 ? w.y : (b >> 2) == 2 ? w.z : w.w;
-  return (word >> (8 * (b & 3))) & 0xFFu;
+// Dropout keep flags of four mask bytes at once. Byte b is kept iff b >= t, i.e. iff
+// b + (255 - t) + 1 carries out of the byte. With y = 255 - t in every byte and
+// ylo = (y & 0x7F7F7F7F) + 0x01010101, the low seven bits of every byte are added with
+// the carry-in in one 32-bit add (at most 0x7F + 0x7F + 1: nothing crosses into the next
+// byte), so bit 7 of the sum is the carry into bit 7, and the carry out of the byte is
+// the majority of that and the two bit-7 inputs. Returns the flags in bit 7 of each byte
+// (the other bits are don't-care).
+struct DropThr {
+  uint32_t y, ylo;
+};
+__host__ __device__ __forceinline__ DropThr drop_thr_words(int t) {
+  const uint32_t y = 0x01010101u * (uint32_t)(255 - t);
+  return {y, (y & 0x7F7F7F7Fu) + 0x01010101u};
+}
+__device__ __forceinline__ uint32_t keep_flags4(uint32_t w, const DropThr& th) {
+  const uint32_t a = (w & 0x7F7F7F7Fu) + th.ylo;
+  return (w & th.y) | ((w | th.y) & a);
+}
+// prmt with a selector: each selector nibble n picks byte n & 7 of {b, a} (a = bytes 0-3)
+// and, when n & 8, replicates that byte's top bit over the whole result byte.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// All-ones iff flag byte k (k = 0..3) of keep_flags4's result is set: an element mask.
+// k is a constant after unrolling, so the selector is too.
+__device__ __forceinline__ uint32_t keep_mask_elem(uint32_t flags, int k) {
+  return prmt(flags, 0u, 0x8888u | (0x1111u * (uint32_t)k));
+}
+// Mask of a bf16 pair: bytes 0-1 from flag byte k, bytes 2-3 from flag byte k + 1.
+__device__ __forceinline__ uint32_t keep_mask_pair(uint32_t flags, int k) {
+  return prmt(flags, 0u, (0x88u | (0x11u * (uint32_t)k)) | ((0x88u | (0x11u * (uint32_t)(k + 1))) << 8));
+}
+
+// 16 x 16 byte transpose within each half-warp: lane s of a half (s = lane % 16) holds
+// row s as w[0..3] (byte b of w[q] = column 4q + b) and ends with column s (byte c of
+// the result = row c). One butterfly stage per bit of the column index: lanes s and
+// s ^ m swap the bytes whose column bit differs from their own lane bit, and the
+// partner's bytes land in the positions just vacated.
+__device__ __forceinline__ void transpose16x16_bytes(uint32_t (&w)[4], int lane) {
+  {  // column bit 3: words 2, 3 against words 0, 1
+    const bool hi = lane & 8;
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, hi ? w[0] : w[2], 8);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, hi ? w[1] : w[3], 8);
+    w[0] = hi ? r0 : w[0];
+    w[1] = hi ? r1 : w[1];
+    w[2] = hi ? w[2] : r0;
+    w[3] = hi ? w[3] : r1;
+  }
+  {  // column bit 2: words 1, 3 against words 0, 2
+    const bool hi = lane & 4;
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, hi ? w[0] : w[1], 4);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, hi ? w[2] : w[3], 4);
+    w[0] = hi ? r0 : w[0];
+    w[2] = hi ? r1 : w[2];
+    w[1] = hi ? w[1] : r0;
+    w[3] = hi ? w[3] : r1;
+  }
+  {  // column bit 1: the high half of each word against the low half
+    const bool hi = lane & 2;
+    const uint32_t ps = hi ? 0x5410u : 0x7632u;
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, prmt(w[0], w[1], ps), 2);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, prmt(w[2], w[3], ps), 2);
+    const uint32_t ue = hi ? 0x3254u : 0x5410u, uo = hi ? 0x3276u : 0x7610u;
+    w[0] = prmt(w[0], r0, ue);
+    w[1] = prmt(w[1], r0, uo);
+    w[2] = prmt(w[2], r1, ue);
+    w[3] = prmt(w[3], r1, uo);
+  }
+  {  // column bit 0: odd bytes against even bytes
+    const bool hi = lane & 1;
+    const uint32_t ps = hi ? 0x6420u : 0x7531u;
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, prmt(w[0], w[1], ps), 1);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, prmt(w[2], w[3], ps), 1);
+    const uint32_t ue = hi ? 0x3514u : 0x5240u, uo = hi ? 0x3716u : 0x7260u;
+    w[0] = prmt(w[0], r0, ue);
+    w[1] = prmt(w[1], r0, uo);
+    w[2] = prmt(w[2], r1, ue);
+    w[3] = prmt(w[3], r1, uo);
+  }
 }
 
 // ---------------------------------------------------------------- math

@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(256) rowdot_kernel(Problem p, long long rows,
         const float L = lse[src[r]];
         l2 = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
       }
-      rt.delta[row] = real[r] ? s : 0.f;
+      rt.delta[row] = real[r] ? s * p.drop_keep : 0.f;  // with dropout D (1 - p)
       rt.lse2[row] = l2;
       if (bh == 0) rt.first[i] = i < p.Nq ? first_key(p.mask, i) : 0x7fffffff;
     }
