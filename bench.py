@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import (CAUSAL, CAUSAL_D256, CAUSAL_FWD_BWD,  # noqa: E402
+from workloads import (CAUSAL, CAUSAL_D256, CAUSAL_D256_FWD_BWD, CAUSAL_FWD_BWD,  # noqa: E402
                        CAUSAL_FWD_BWD_DROPOUT, DOCS, GQA_WINDOW, MASK_NAMES, PAGED_DECODE, TINY, make_decode_inputs, make_inputs)
 
 FWD_WORKLOADS = {"causal_fwd": CAUSAL, "gqa_window_fwd": GQA_WINDOW, "docs_fwd": DOCS,
@@ -113,8 +113,8 @@ class ClockSampler:
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel on this
 # workload, keyed by the SHA-256 of the kernel's sources (its .cu file plus the shared
 # headers) at capture time. A kernel whose sources have changed since reports null.
-KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu",),
-                  "dq_kernel": ("bwd_tc.cu",), "rowdot_kernel": ("simt.cu",),
+KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", "bwd_common.cuh"),
+                  "dq_kernel": ("bwd_tc.cu", "bwd_common.cuh"), "rowdot_kernel": ("simt.cu",),
                   "decode_tc_kernel": ("decode_tc.cuh", "decode_tc.cu", "decode_copies2.cu")}
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192), read bytes rounded
@@ -225,7 +225,9 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
     # Per step: attn_fwd, then the backward's three kernels through attn_bwd_phases
     # (the same launches attn_bwd makes), with an event between kernels so that each
     # kernel's own duration is measured on the stream it runs on.
-    names = ["fwd_tc_kernel", "rowdot_kernel", "dkdv_kernel", "dq_kernel"]
+    # (at d = 256 the dK/dV phase is two kernels, the dV and the dK walk)
+    names = (["fwd256_kernel", "rowdot_kernel", "dkdv256_kernel", "dq256_kernel"] if w.d == 256
+             else ["fwd_tc_kernel", "rowdot_kernel", "dkdv_kernel", "dq_kernel"])
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
@@ -243,7 +245,7 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
     if ea.device_status() != 0:
         raise RuntimeError("a kernel gave up a bounded wait during the timed steps")
     per_kernel = {n: [e[i].elapsed_time(e[i + 1]) for e in ev] for i, n in enumerate(names)}
-    t_fwd = per_kernel["fwd_tc_kernel"]
+    t_fwd = per_kernel[names[0]]
     t_bwd = [sum(per_kernel[n][s] for n in names[1:]) for s in range(args.steps)]
     t_step = sum(a + b for a, b in zip(t_fwd, t_bwd))  # ms over K steps
     if world > 1:
@@ -281,9 +283,10 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
     # Algorithmic work of one launch of each kernel: FLOPs of the
     # contractions it performs per allowed pair, or bytes for the row-dot kernel.
     units = w.B * w.Hq * pairs
-    algo = {"fwd_tc_kernel": (4 * w.d * units, "TFLOP/s"),
-            "dkdv_kernel": (8 * w.d * units, "TFLOP/s"),
-            "dq_kernel": (6 * w.d * units, "TFLOP/s"),
+    # (d = 256: the dV walk runs S^T and dV, the dK walk S^T, dP^T and dK)
+    algo = {names[0]: (4 * w.d * units, "TFLOP/s"),
+            names[2]: ((10 if w.d == 256 else 8) * w.d * units, "TFLOP/s"),
+            names[3]: (6 * w.d * units, "TFLOP/s"),
             # reads O, dO and L; writes L log2 e and D
             "rowdot_kernel": (w.B * w.Hq * w.Nq * (4 * w.d + 12), "GB/s")}
     kernels = {}
@@ -317,7 +320,7 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
                      "traffic": ncu_traffic(dom) if w.dropout_p == 0 else None},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (5 if w.d == 256 else 4) * args.steps,  # d = 256: dV and dK walks
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -624,7 +627,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="fwd_bwd",
-                    choices=["fwd_bwd", "fwd_bwd_dropout", *FWD_WORKLOADS, "paged_decode"])
+                    choices=["fwd_bwd", "fwd_bwd_dropout", "fwd_bwd_d256", *FWD_WORKLOADS,
+                             "paged_decode"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -634,6 +638,8 @@ def main():
         run_decode(args, PAGED_DECODE)
     elif args.workload == "fwd_bwd_dropout":
         run_ours(args, CAUSAL_FWD_BWD_DROPOUT)
+    elif args.workload == "fwd_bwd_d256":
+        run_ours(args, CAUSAL_D256_FWD_BWD)
     elif args.workload != "fwd_bwd":
         run_forward(args, FWD_WORKLOADS[args.workload], fp8=args.workload.startswith("fp8"))
     else:

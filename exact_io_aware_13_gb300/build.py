@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libattn.so")
 
-SOURCES = ["attn_api.cu", "simt.cu", "fwd_tc.cu", "fwd256_tc.cu", "bwd_tc.cu", "fp8.cu", "decode_tc.cu",
+SOURCES = ["attn_api.cu", "simt.cu", "fwd_tc.cu", "fwd256_tc.cu", "bwd_tc.cu", "bwd256_tc.cu", "fp8.cu", "decode_tc.cu",
            "decode_copies2.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

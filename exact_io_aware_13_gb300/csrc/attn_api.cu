@@ -205,8 +205,9 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
   Problem p;
   attn_status s = check_problem(B, Hq, Hkv, Nq, Nkv, d, scale, mask_kind, mp, score_kind, sp, &p);
   if (s != ATTN_OK) return s;
-  if (d == 256) return ATTN_ERR_SHAPE;  // the backward handles d = 64 and 128
-  if (simt && (score_kind & ATTN_SCORE_DROPOUT)) return ATTN_ERR_ARG;
+  if (simt && d == 256) return ATTN_ERR_SHAPE;  // the SIMT backward: d = 64 and 128
+  // dropout: tensor-core path with d <= 128 only (like the forward)
+  if ((score_kind & ATTN_SCORE_DROPOUT) && (simt || d == 256)) return ATTN_ERR_ARG;
   const long long rows_q = (long long)B * Hq * Nq, rows_k = (long long)B * Hkv * Nkv;
   if (rows_q == 0 && rows_k == 0) return ATTN_OK;
   if (rows_q > 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_ERR_ARG;
@@ -250,6 +251,7 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
     if ((s = make_map(&maps.do64, dout, B * Hq, Nq, d, 64)) != ATTN_OK) return s;
     if ((s = make_map(&maps.k64, k, B * Hkv, Nkv, d, 64)) != ATTN_OK) return s;
     if ((s = make_map(&maps.v64, v, B * Hkv, Nkv, d, 64)) != ATTN_OK) return s;
+    if (d == 256 && (s = make_map(&maps.do128, dout, B * Hq, Nq, d)) != ATTN_OK) return s;
   }
   if ((phases & ATTN_BWD_ROWDOT) &&
       (s = from_cuda(launch_bwd_rowdot(p, static_cast<const __nv_bfloat16*>(o), dob, lse, rt,
@@ -261,8 +263,10 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
     return from_cuda(launch_bwd_simt(p, qb, kb, vb, lse, dob, rt.delta, dqb, dkb, dvb, st));
   }
   if (!(phases & (ATTN_BWD_DKDV | ATTN_BWD_DQ))) return ATTN_OK;
-  return from_cuda(launch_bwd_tc(p, maps, rt, qb, dob, kb, dqb, dkb, dvb, (phases & ATTN_BWD_DKDV) != 0,
-                                 (phases & ATTN_BWD_DQ) != 0, st));
+  const bool run_kv = (phases & ATTN_BWD_DKDV) != 0, run_q = (phases & ATTN_BWD_DQ) != 0;
+  if (d == 256)
+    return from_cuda(launch_bwd256_tc(p, maps, rt, qb, dob, kb, dqb, dkb, dvb, run_kv, run_q, st));
+  return from_cuda(launch_bwd_tc(p, maps, rt, qb, dob, kb, dqb, dkb, dvb, run_kv, run_q, st));
 }
 
 // ---------------------------------------------------------------- static workspace

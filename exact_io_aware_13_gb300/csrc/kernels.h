@@ -90,11 +90,17 @@ cudaError_t launch_quantize_v_transposed(const __nv_bfloat16* x, uint8_t* out, f
 // 64-row boxes (the slices both kernels stream).
 struct BwdMaps {
   CUtensorMap v128, q64, do64, k64, v64;
+  CUtensorMap do128;  // head dimension 256 only: the dQ kernel's fixed dO tile
 };
 cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
                           const __nv_bfloat16* q, const __nv_bfloat16* dout,
                           const __nv_bfloat16* k, __nv_bfloat16* dq, __nv_bfloat16* dk,
                           __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st);
+// Head dimension 256: dV, dK (two walks over the key tiles) and dQ.
+cudaError_t launch_bwd256_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
+                             const __nv_bfloat16* q, const __nv_bfloat16* dout,
+                             const __nv_bfloat16* k, __nv_bfloat16* dq, __nv_bfloat16* dk,
+                             __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st);
 
 // ---- Paged decode.
 // Keys [lo, hi) that query i of the Nq newest tokens of a sequence with L cached tokens

@@ -332,7 +332,8 @@ cudaError_t launch_bwd_rowdot(const Problem& p, const __nv_bfloat16* o,
   const long long blocks = (rows + per_block - 1) / per_block;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (p.d == 64) rowdot_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
-  else rowdot_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
+  else if (p.d == 128) rowdot_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
+  else rowdot_kernel<256><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
   return cudaGetLastError();
 }
 

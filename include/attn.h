@@ -21,8 +21,9 @@
  *       lse            : fp32 [B, Hq, Nq]
  *     Every tensor pointer must be 16-byte aligned (ATTN_ERR_ALIGN otherwise).
  *   - Query head h reads kv head h / (Hq / Hkv) (grouped-query attention).
- *   - d must be 64 or 128; attn_fwd also takes d = 256 ("FlashAttention/es",
- *     "Limitaciones": head sizes up to about 256). Hq must be a multiple of Hkv.
+ *   - d must be 64, 128 or 256 ("FlashAttention/es", "Limitaciones": head sizes up to
+ *     about 256); the SIMT entry points, the FP8 forward and dropout take 64 and 128
+ *     only. Hq must be a multiple of Hkv.
  *   - scale multiplies Q K^T (usually 1/sqrt(d)); it must be finite.
  *   - Scores are modified in the order: scale, ALiBi, soft-cap, mask.
  *       ALiBi:    s_ij -= slope_h * (i - j), slope_h = 2^(-8 (h+1) / Hq),
@@ -60,7 +61,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_ARG = 1,            /* null pointer, unknown kind, bad scale/window/softcap */
-  ATTN_ERR_SHAPE = 2,          /* unsupported d (256 outside attn_fwd), Hq % Hkv != 0, negative size,
+  ATTN_ERR_SHAPE = 2,          /* unsupported d (256 on the SIMT/FP8 paths), Hq % Hkv != 0, negative size,
                                   document mask with Nq != Nkv, size over 2^31 */
   ATTN_ERR_ALIGN = 3,          /* a tensor pointer is not 16-byte aligned */
   ATTN_ERR_ARCH = 4,           /* the current device is not compute capability 10.3 */

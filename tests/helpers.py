@@ -13,7 +13,9 @@ Tolerances (bf16 inputs, fp32 accumulation):
   backward: max|dX - dX_ref| <= 2e-2 * max|dX_ref| + 1e-5 for each of dq, dk, dv.
             The 1e-5 floor only matters where the exact gradient vanishes (one allowed
             key per row: P = 1 and dP - D = 0): there the kernels leave fp32
-            accumulation-order residue of |dO||V| * 2^-23 * d, about 1e-6.
+            accumulation-order residue of |dO||V| * 2^-23 * d, about 1e-6 at d = 128.
+            dP and D are d-term sums whose size and rounding both grow as sqrt(d), so
+            the floor is 1e-5 * d / 128 for d > 128.
 """
 from __future__ import annotations
 
@@ -74,15 +76,16 @@ def check_forward(o, lse, o_ref, lse_ref, what="", o_tol=O_TOL):
     return err_o, err_l
 
 
-def check_grads(got, ref, what=""):
+def check_grads(got, ref, what="", d=128):
+    floor = GRAD_ABS_FLOOR * max(1.0, d / 128)
     errs = []
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         g = np.asarray(g, dtype=np.float64)
         assert np.isfinite(g).all(), f"{what}: {name} not finite"
         scale = float(np.abs(r).max()) if r.size else 0.0
         err = float(np.abs(g - r).max()) if r.size else 0.0
-        assert err <= GRAD_REL_TOL * scale + GRAD_ABS_FLOOR, \
-            f"{what}: max|d{name}| = {err} vs {GRAD_REL_TOL} * {scale} + {GRAD_ABS_FLOOR}"
+        assert err <= GRAD_REL_TOL * scale + floor, \
+            f"{what}: max|d{name}| = {err} vs {GRAD_REL_TOL} * {scale} + {floor}"
         errs.append(err / max(scale, 1e-30))
     return errs
 

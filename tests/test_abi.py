@@ -41,10 +41,16 @@ def _fwd(lib, **kw):
 def test_argument_errors_return_before_any_device_call(lib):
     assert _fwd(lib, d=96) == 2                       # ATTN_ERR_SHAPE
     assert _fwd(lib, d=512) == 2
-    # d = 256: the forward takes it, the backward does not
-    rc = lib.attn_bwd(*([ctypes.c_void_p(4096)] * 9), 1, 1, 1, 128, 128, 256,
-                      ctypes.c_float(0.1), 0, None, 0, None, ctypes.c_void_p(4096), 1 << 20, None)
+    # d = 256: the tensor-core forward and backward take it, the SIMT backward does not
+    rc = lib.attn_bwd_simt(*([ctypes.c_void_p(4096)] * 9), 1, 1, 1, 128, 128, 256,
+                           ctypes.c_float(0.1), 0, None, 0, None, ctypes.c_void_p(4096), 1 << 20,
+                           None)
     assert rc == 2
+    sp = _lib.ScoreParams(0.0, 0.1, 7)  # ... and dropout stays at d <= 128
+    rc = lib.attn_bwd(*([ctypes.c_void_p(4096)] * 9), 1, 1, 1, 128, 128, 256,
+                      ctypes.c_float(0.1), 0, None, 4, ctypes.byref(sp), ctypes.c_void_p(4096),
+                      1 << 20, None)
+    assert rc == 1
     assert _fwd(lib, Hq=3, Hkv=2) == 2
     assert _fwd(lib, Nq=-1) == 2
     assert _fwd(lib, scale=float("nan")) == 1         # ATTN_ERR_ARG

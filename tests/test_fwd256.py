@@ -72,7 +72,7 @@ def test_forward256_is_deterministic():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-def test_backward_and_simt_reject_d256():
+def test_simt_and_dropout_reject_d256():
     import exact_io_aware_13_gb300 as ea
     from exact_io_aware_13_gb300 import _lib
     w = H.small_workload("d256rej", MASK_CAUSAL, N=64, d=256)
@@ -83,8 +83,11 @@ def test_backward_and_simt_reject_d256():
     assert e.value.status == 2
     o, lse = ea.forward(q, k, v, scale=w.scale)
     with pytest.raises(_lib.AttnError) as e:
-        ea.backward(q, k, v, o, lse, do, scale=w.scale)
+        ea.backward(q, k, v, o, lse, do, scale=w.scale, impl="simt")
     assert e.value.status == 2
+    with pytest.raises(_lib.AttnError) as e:
+        ea.backward(q, k, v, o, lse, do, scale=w.scale, dropout_p=0.1)
+    assert e.value.status == 1
 
 
 def test_forward256_full_size_sampled():

@@ -107,6 +107,7 @@ CAUSAL_FWD_BWD_DROPOUT = CAUSAL_FWD_BWD.replace(name="causal fwd+bwd dropout 0.1
 # "Limitaciones"): the causal workload's FLOPs at twice the head size, half the batch.
 CAUSAL_D256 = Workload("causal fwd d=256", 6, B=2, Hq=16, Hkv=16, Nq=8192, Nkv=8192, d=256,
                        mask_kind=MASK_CAUSAL)
+CAUSAL_D256_FWD_BWD = CAUSAL_D256.replace(name="causal fwd+bwd d=256", seed=8, backward=True)
 
 
 def document_lengths(total: int, seed: int, lo: int = 512, hi: int = 4096) -> list[int]:
