@@ -45,7 +45,7 @@ G = Hq / Hkv), in float64 from the bf16-rounded inputs:
        dV = (P * Z / (1 - p))^T dO,  D_i = sum_j P_ij dP'_ij = rowsum(dO * O),
        dS = P * (dP' - D).
 
-Readings where the pages are silent (each listed in the design doc as well):
+Readings where the pages are silent:
   * GQA maps query head h to kv head floor(h / G).
   * ALiBi uses the 0-based query-head index and the signed distance (i - j).
   * Causal means j <= i on absolute positions (top-left aligned) even if Nq != Nkv.
