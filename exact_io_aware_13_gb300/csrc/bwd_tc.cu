@@ -224,15 +224,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       nb_arrive(kNbKvK, kNbKvCount);
     }
     bool ok_all = true;
+    // (head, query tile) of sub-step u, its score constants and whether the tile needs
+    // the per-element mask, advanced every second sub-step (the order `slice` gives)
+    int st_q = 0, st_h = 0;
+    ScoreK sk = score_consts<kAlibi, kSoftcap>(p, g * G);
+    bool need_mask = tile_needs_mask(p.mask, qr.lo * BT, k0, BT);
+    const DropThr dthr = drop_thr_words(kDrop ? p.drop_thr : 0);
     for (int u = 0; u < subs; ++u) {
       const int s = u % L::kStageCount, x = u & 1;
       const bool rel = u + 1 < subs;  // the MMA warp waits for this release before u + 1
-      int qrow, bh;
-      slice(u, qrow, bh);
-      const int h = bh - b * p.Hq;
+      if (u > 0 && x == 0) {
+        if (++st_q == n_q) {
+          st_q = 0;
+          ++st_h;
+          sk = score_consts<kAlibi, kSoftcap>(p, g * G + st_h);
+        }
+        need_mask = tile_needs_mask(p.mask, (qr.lo + st_q) * BT, k0, BT);
+      }
+      const int qrow = (qr.lo + st_q) * BT + x * SUB;
+      const int bh = b * p.Hq + g * G + st_h;
       const int qs = qrow + c0;                  // query of this thread's column 0
-      const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
-      const DropThr dthr = drop_thr_words(kDrop ? p.drop_thr : 0);
       if (ok_all)
         ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[0]), u & 1, wc));
       // the stage's row terms arrived with full[s]; observe them
@@ -260,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kf[4];
       if constexpr (kDrop) dropout_flags_dkdv(p, dthr, j, lane, qs, bh, kf);
       uint32_t pp[8], dd[8];
-      if (tile_needs_mask(p.mask, qrow & ~(BT - 1), k0, BT))  // warp-uniform
+      if (need_mask)  // warp-uniform
         dkdv_pds<kAlibi, kSoftcap, true, kDrop>(sr, dr, lse2, dl, fk, sk, base, j, qs,
                                                 j < p.Nkv, causal_type, kf, pp, dd);
       else
