@@ -266,15 +266,29 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
     bufs = [(qd, kd, vd, dod, o, lse, dq, dk, dv),
             tuple(torch.empty_like(t) for t in (qd, kd, vd, dod, o, lse, dq, dk, dv))]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    # one stream per tensor copy, so that several copy engines share each direction
+    s_in_t = [torch.cuda.Stream(device=dev) for _ in range(4)]
+    s_out_t = [torch.cuda.Stream(device=dev) for _ in range(5)]
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def copy_in(x):
-        with torch.cuda.stream(s_in):
-            for dst, src in zip(bufs[x][:4], host):
+    def fan_out(main, subs, pairs, done):
+        """Copies dst <- src, one per stream of `subs`, after what `main` has queued;
+        `done` records on `main` once all of them finished."""
+        start = torch.cuda.Event()
+        start.record(main)
+        for st_, (dst, src) in zip(subs, pairs):
+            st_.wait_event(start)
+            with torch.cuda.stream(st_):
                 dst.copy_(src, non_blocking=True)
-            ev_in[x].record(s_in)
+            fin = torch.cuda.Event()
+            fin.record(st_)
+            main.wait_event(fin)
+        done.record(main)
+
+    def copy_in(x):
+        fan_out(s_in, s_in_t, list(zip(bufs[x][:4], host)), ev_in[x])
 
     if world > 1:
         torch.distributed.barrier()
@@ -298,11 +312,8 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
             if st_i >= 1:
                 s_in.wait_event(ev_done[1 - x])  # step st_i - 1 is done with those inputs
             copy_in(1 - x)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_done[x])
-            for dst, src in zip(outs_host, (bo, blse, bdq, bdk, bdv)):
-                dst.copy_(src, non_blocking=True)
-            ev_out[x].record(s_out)
+        s_out.wait_event(ev_done[x])
+        fan_out(s_out, s_out_t, list(zip(outs_host, (bo, blse, bdq, bdk, bdv))), ev_out[x])
     stream.wait_event(ev_out[(args.steps - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize()
