@@ -124,10 +124,10 @@ NCU_TRAFFIC = {
                     "sha256": "90b9f678428459c176f39d27eb1a508f95b61ff5c3283631d5e51138e17c4975"},
     "rowdot_kernel": {"bytes": 135301120 + 734720,
                     "sha256": "fbbba20f908173e85008c277a58065dfe75f498fb387af7eb3afa15220a4bb28"},
-    "dkdv_kernel": {"bytes": 270854144 + 99784448,
-                  "sha256": "d7772ab275ccd857ac9faad5357848a51ffa091f06b661e02aef17092c1127f2"},
-    "dq_kernel": {"bytes": 270834176 + 48614144,
-                "sha256": "d7772ab275ccd857ac9faad5357848a51ffa091f06b661e02aef17092c1127f2"},
+    "dkdv_kernel": {"bytes": 270628608 + 102324224,
+                  "sha256": "264643858eb43ad224d628c9c80bf4c26b0626a248547a9cf01947101e77a473"},
+    "dq_kernel": {"bytes": 270846464 + 51926272,
+                "sha256": "264643858eb43ad224d628c9c80bf4c26b0626a248547a9cf01947101e77a473"},
     "decode_tc_kernel": {"bytes": 1119384000 + 9659904,
                        "sha256": "b4bab05fdc8dd31bb21608ce17a4108cef894dd9c779738e2cd5c627239968e4"},
 }
