@@ -414,7 +414,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st8(tS + c * 8, pk);
         } else {
-          uint32_t pk[16];
           // Dropout: one Philox call per 16 keys of this row gives the keep flags of
           // those keys; l sums the undropped P (the softmax is taken before dropout) and
           // P V takes the dropped P, whose 1 / (1 - p) is applied with 1 / l at the end.
@@ -431,17 +430,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               kf[4 * hh + 3] = keep_flags4(w.w, dthr);
             }
           }
+          // P goes to tensor memory in two halves of 8 words (fewer live registers than
+          // one 16-word store: the softmax row already holds 128)
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), mul, neg_m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
-            acc[(2 * e) & 7] += p0;
-            acc[(2 * e + 1) & 7] += p1;
-            pk[e] = pack_bf16x2(p0, p1);
-            if (kDrop)  // keys 2e, 2e + 1: flag bytes (2e) % 4, +1 of word e / 2
-              pk[e] &= keep_mask_pair(kf[e >> 1], 2 * (e & 1));
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t ph[8];
+#pragma unroll
+            for (int e8 = 0; e8 < 8; ++e8) {
+              const int e = hf * 8 + e8;
+              const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), mul, neg_m));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
+              acc[(2 * e) & 7] += p0;
+              acc[(2 * e + 1) & 7] += p1;
+              ph[e8] = pack_bf16x2(p0, p1);
+              if (kDrop)  // keys 2e, 2e + 1: flag bytes (2e) % 4, +1 of word e / 2
+                ph[e8] &= keep_mask_pair(kf[e >> 1], 2 * (e & 1));
+            }
+            tmem_st8(tS + c * 16 + hf * 8, ph);
           }
-          tmem_st16(tS + c * 16, pk);
         }
       }
       l_run += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
