@@ -119,8 +119,8 @@ KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", 
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201568256 + 46669056,
-                    "sha256": "90b9f678428459c176f39d27eb1a508f95b61ff5c3283631d5e51138e17c4975"},
+    "fwd_tc_kernel": {"bytes": 201400576 + 46058240,
+                    "sha256": "ec5a2a306f9d9f55e849ff72551a34c13896916fa6d37be006cb211571dedfc3"},
     "rowdot_kernel": {"bytes": 135301120 + 734720,
                     "sha256": "fbbba20f908173e85008c277a58065dfe75f498fb387af7eb3afa15220a4bb28"},
     "dkdv_kernel": {"bytes": 270628608 + 102324224,

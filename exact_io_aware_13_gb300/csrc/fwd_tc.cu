@@ -414,27 +414,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st8(tS + c * 8, pk);
         } else {
-          // Dropout: one Philox call per 16 keys of this row gives the keep flags of
-          // those keys; l sums the undropped P (the softmax is taken before dropout) and
-          // P V takes the dropped P, whose 1 / (1 - p) is applied with 1 / l at the end.
-          uint32_t kf[8];
-          if (kDrop) {
-            const uint32_t blk = (uint32_t)((k0 + c * 32) >> 4);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const uint4 w = philox4x32_10(blk + hh, (uint32_t)i, (uint32_t)bh, 0u,
-                                            p.drop_seed_lo, p.drop_seed_hi);
-              kf[4 * hh + 0] = keep_flags4(w.x, dthr);
-              kf[4 * hh + 1] = keep_flags4(w.y, dthr);
-              kf[4 * hh + 2] = keep_flags4(w.z, dthr);
-              kf[4 * hh + 3] = keep_flags4(w.w, dthr);
-            }
-          }
+          // Dropout: one Philox call per 16 keys of this row (one half below) gives the
+          // keep flags of those keys; l sums the undropped P (the softmax is taken before
+          // dropout) and P V takes the dropped P, whose 1 / (1 - p) is applied with 1 / l
+          // at the end.
           // P goes to tensor memory in two halves of 8 words (fewer live registers than
           // one 16-word store: the softmax row already holds 128)
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-            uint32_t ph[8];
+            uint32_t ph[8], kf[4];
+            if (kDrop) {
+              const uint4 w = philox4x32_10((uint32_t)((k0 + c * 32) >> 4) + hf, (uint32_t)i,
+                                            (uint32_t)bh, 0u, p.drop_seed_lo, p.drop_seed_hi);
+              kf[0] = keep_flags4(w.x, dthr);
+              kf[1] = keep_flags4(w.y, dthr);
+              kf[2] = keep_flags4(w.z, dthr);
+              kf[3] = keep_flags4(w.w, dthr);
+            }
 #pragma unroll
             for (int e8 = 0; e8 < 8; ++e8) {
               const int e = hf * 8 + e8;
@@ -443,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               acc[(2 * e) & 7] += p0;
               acc[(2 * e + 1) & 7] += p1;
               ph[e8] = pack_bf16x2(p0, p1);
-              if (kDrop)  // keys 2e, 2e + 1: flag bytes (2e) % 4, +1 of word e / 2
-                ph[e8] &= keep_mask_pair(kf[e >> 1], 2 * (e & 1));
+              if (kDrop)  // keys 2e8, 2e8 + 1 of the half: flag bytes (2e8) % 4, +1 of word e8 / 2
+                ph[e8] &= keep_mask_pair(kf[e8 >> 1], 2 * (e8 & 1));
             }
             tmem_st8(tS + c * 16 + hf * 8, ph);
           }
