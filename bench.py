@@ -127,25 +127,29 @@ SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
     "fwd_tc_kernel": {"bytes": 201400576 + 46058240,
-                    "sha256": "ec5a2a306f9d9f55e849ff72551a34c13896916fa6d37be006cb211571dedfc3"},
+                    "sha256": "e6f07bb72070c4c545f27501734bc4eeba9a1bfa31e5aff474e7769b7c9f1f5f"},
     "rowdot_kernel": {"bytes": 135301120 + 734720,
-                    "sha256": "fbbba20f908173e85008c277a58065dfe75f498fb387af7eb3afa15220a4bb28"},
+                    "sha256": "75b3397d3eb84e18561f4d87abb9ef7961b5d444a6a2e1441b0fe90db9fefd5a"},
     "dkdv_kernel": {"bytes": 270628608 + 102324224,
-                  "sha256": "264643858eb43ad224d628c9c80bf4c26b0626a248547a9cf01947101e77a473"},
+                  "sha256": "664b695ce2f1a563ae5e1a9f609297351d7469a3fb9655f0175eb58aff7f20ae"},
     "dq_kernel": {"bytes": 270846464 + 51926272,
-                "sha256": "264643858eb43ad224d628c9c80bf4c26b0626a248547a9cf01947101e77a473"},
+                "sha256": "664b695ce2f1a563ae5e1a9f609297351d7469a3fb9655f0175eb58aff7f20ae"},
     "decode_tc_kernel": {"bytes": 1119357952 + 9291264,
-                       "sha256": "8db3d330202db7d9e3ef86bbc6bc58e4a3f12bc56cc32ec8f3fac86db0ed38b4"},
+                       "sha256": "c614a56391ac51ec161b8ae159a4363fbbd3718fa106c1dd3d18ccc8c55fd5a8"},
 }
 
 
 def kernel_source_sha(kernel: str) -> str:
+    """SHA-256 of the kernel's sources with // comments and blank space removed, so that
+    an edit of the comments alone keeps the figures of the unchanged code."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_io_aware_13_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel] + SHARED_HEADERS:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            code = re.sub(r"//[^\n]*", "", f.read())
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()
 
 

@@ -14,6 +14,11 @@
 //   * dq: one CTA per (batch, query head, 128-row tile); it walks the key tiles 64
 //     keys at a time: S = Q K^T and dP = dO V^T, dS back into tensor memory, then
 //     dQ += dS K.
+// Dropout (kDrop): both kernels regenerate the forward's keep mask Z (Philox4x32-10, one
+// call per 16 keys of a query row; the dK/dV warps, one lane per key, get their bytes
+// through a byte transpose within each half-warp). With the row term D (1 - p) from the
+// row kernel, dV takes P o Z and dS' = P o (dP o Z - D (1 - p)) = (1 - p) dS; the
+// epilogues multiply dV, dK and dQ by 1 / (1 - p).
 // Each sub-step streams its own 64-row slice of the two operands it walks (Q and dO,
 // or K and V; for dkdv also the 64 rows' L log2 e, D and first key) through a 4-deep
 // shared-memory ring, so loads run ahead of the MMAs. Warp 16 loads with TMA, warp 17

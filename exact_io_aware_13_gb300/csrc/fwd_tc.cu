@@ -25,8 +25,9 @@
 //     than 2^8 (a stale max is exact: O and l share it until the final division).
 // Tensor memory: S0 cols [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d).
 //
-// Dropout variant (kDrop, bf16 only): P is multiplied by the keep mask / (1 - p) before
-// the P V product; the row sums and the LSE keep the undropped P.
+// Dropout variant (kDrop, bf16 only): the bf16 P is ANDed with the keep mask (one Philox
+// call per 16 keys of a row) before the P V product; the row sums and the LSE keep the
+// undropped P, and the epilogue divides O by l (1 - p).
 //
 // FP8 variant (kFp8, d = 128): Q and K are e4m3 with one scale per 128-row tile, V is
 // e4m3 stored transposed ([d, keys] per head, keys contiguous) with one scale per head,
