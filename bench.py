@@ -130,10 +130,10 @@ NCU_TRAFFIC = {
                     "sha256": "e6f07bb72070c4c545f27501734bc4eeba9a1bfa31e5aff474e7769b7c9f1f5f"},
     "rowdot_kernel": {"bytes": 135301120 + 734720,
                     "sha256": "75b3397d3eb84e18561f4d87abb9ef7961b5d444a6a2e1441b0fe90db9fefd5a"},
-    "dkdv_kernel": {"bytes": 270628608 + 102324224,
-                  "sha256": "664b695ce2f1a563ae5e1a9f609297351d7469a3fb9655f0175eb58aff7f20ae"},
-    "dq_kernel": {"bytes": 270846464 + 51926272,
-                "sha256": "664b695ce2f1a563ae5e1a9f609297351d7469a3fb9655f0175eb58aff7f20ae"},
+    "dkdv_kernel": {"bytes": 270629120 + 102725888,
+                  "sha256": "6557cf33ebd337a424bddea71c23fc32168395b832aed68f25018d28f4a1adf4"},
+    "dq_kernel": {"bytes": 270628864 + 48264448,
+                "sha256": "6557cf33ebd337a424bddea71c23fc32168395b832aed68f25018d28f4a1adf4"},
     "decode_tc_kernel": {"bytes": 1119357952 + 9291264,
                        "sha256": "c614a56391ac51ec161b8ae159a4363fbbd3718fa106c1dd3d18ccc8c55fd5a8"},
 }

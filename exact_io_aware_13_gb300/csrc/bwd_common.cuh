@@ -25,11 +25,11 @@ constexpr int kRelayWarp = kEwWarps + 2;  // turns TMA completions into barrier 
 //   dq:   kNbQL        Q and dO tiles written to tensor memory: element-wise warps + MMA warp
 constexpr uint32_t kNbP = 1, kNbPCount = 288;
 constexpr uint32_t kNbStage = 3, kNbStageCount = 64;
-constexpr uint32_t kNbKvRel = 8, kNbKvP = 9, kNbKvK = 11, kNbQL = 12;
+constexpr uint32_t kNbKvRel = 9, kNbKvP = 10, kNbKvK = 12, kNbQL = 13;
 constexpr uint32_t kNbKvCount = (kEwWarps + 1) * 32;
-constexpr int kStagesQ = 4;      // dq ring depth, in sub-steps
+constexpr int kStagesQ = 6;      // dq ring depth, in sub-steps
 constexpr int kStagesKv = 5;     // dkdv ring depth
-constexpr int kMaxStages = 5;
+constexpr int kMaxStages = 6;
 // Stage barriers take IDs kNbStage .. kNbStage + kMaxStages - 1; the others must not
 // overlap them (one hardware barrier, one thread count), and IDs end at 15.
 static_assert(kNbStage + kMaxStages <= kNbKvRel && kNbP + 2 <= kNbStage && kNbKvK < kNbQL &&

@@ -20,8 +20,8 @@
 // row kernel, dV takes P o Z and dS' = P o (dP o Z - D (1 - p)) = (1 - p) dS; the
 // epilogues multiply dV, dK and dQ by 1 / (1 - p).
 // Each sub-step streams its own 64-row slice of the two operands it walks (Q and dO,
-// or K and V; for dkdv also the 64 rows' L log2 e, D and first key) through a 4-deep
-// shared-memory ring, so loads run ahead of the MMAs. Warp 16 loads with TMA, warp 17
+// or K and V; for dkdv also the 64 rows' L log2 e, D and first key) through a
+// shared-memory ring (5 stages for dkdv, 6 for dq), so loads run ahead of the MMAs. Warp 16 loads with TMA, warp 17
 // owns tensor memory and issues the MMAs, warp 18 relays TMA completions; warps 0-15
 // do the element-wise work, one thread per TMEM lane (= row of the CTA's tile). The
 // MMA warp waits only on hardware named barriers: a shared-memory access from the
