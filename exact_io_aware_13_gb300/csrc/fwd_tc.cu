@@ -419,31 +419,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           // keep flags of those keys; l sums the undropped P (the softmax is taken before
           // dropout) and P V takes the dropped P, whose 1 / (1 - p) is applied with 1 / l
           // at the end.
-          // P goes to tensor memory in two halves of 8 words (fewer live registers than
-          // one 16-word store: the softmax row already holds 128)
+          // P goes to tensor memory in two halves of 8 words where that measured faster
+          // (no score mod: fewer live registers beside the 128 scores; dropout: one Philox
+          // call per half), else in one 16-word store (with ALiBi / soft-cap the halves
+          // ran slower on the document workload, 329 against 370 TFLOP/s).
+          constexpr bool kHalves = kDrop || (!kAlibi && !kSoftcap);
+          if constexpr (kHalves) {
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t ph[8], kf[4];
-            if (kDrop) {
-              const uint4 w = philox4x32_10((uint32_t)((k0 + c * 32) >> 4) + hf, (uint32_t)i,
-                                            (uint32_t)bh, 0u, p.drop_seed_lo, p.drop_seed_hi);
-              kf[0] = keep_flags4(w.x, dthr);
-              kf[1] = keep_flags4(w.y, dthr);
-              kf[2] = keep_flags4(w.z, dthr);
-              kf[3] = keep_flags4(w.w, dthr);
+            for (int hf = 0; hf < 2; ++hf) {
+              uint32_t ph[8], kf[4];
+              if (kDrop) {
+                const uint4 w = philox4x32_10((uint32_t)((k0 + c * 32) >> 4) + hf, (uint32_t)i,
+                                              (uint32_t)bh, 0u, p.drop_seed_lo, p.drop_seed_hi);
+                kf[0] = keep_flags4(w.x, dthr);
+                kf[1] = keep_flags4(w.y, dthr);
+                kf[2] = keep_flags4(w.z, dthr);
+                kf[3] = keep_flags4(w.w, dthr);
+              }
+#pragma unroll
+              for (int e8 = 0; e8 < 8; ++e8) {
+                const int e = hf * 8 + e8;
+                const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), mul, neg_m));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
+                acc[(2 * e) & 7] += p0;
+                acc[(2 * e + 1) & 7] += p1;
+                ph[e8] = pack_bf16x2(p0, p1);
+                if (kDrop)  // keys 2e8, 2e8 + 1 of the half: flag bytes (2e8) % 4, +1 of word e8 / 2
+                  ph[e8] &= keep_mask_pair(kf[e8 >> 1], 2 * (e8 & 1));
+              }
+              tmem_st8(tS + c * 16 + hf * 8, ph);
             }
+          } else {
+            uint32_t pk[16];
 #pragma unroll
-            for (int e8 = 0; e8 < 8; ++e8) {
-              const int e = hf * 8 + e8;
+            for (int e = 0; e < 16; ++e) {
               const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), mul, neg_m));
               const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
               acc[(2 * e) & 7] += p0;
               acc[(2 * e + 1) & 7] += p1;
-              ph[e8] = pack_bf16x2(p0, p1);
-              if (kDrop)  // keys 2e8, 2e8 + 1 of the half: flag bytes (2e8) % 4, +1 of word e8 / 2
-                ph[e8] &= keep_mask_pair(kf[e8 >> 1], 2 * (e8 & 1));
+              pk[e] = pack_bf16x2(p0, p1);
             }
-            tmem_st8(tS + c * 16 + hf * 8, ph);
+            tmem_st16(tS + c * 16, pk);
           }
         }
       }
