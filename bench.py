@@ -126,8 +126,8 @@ KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", 
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201400576 + 46058240,
-                    "sha256": "e6f07bb72070c4c545f27501734bc4eeba9a1bfa31e5aff474e7769b7c9f1f5f"},
+    "fwd_tc_kernel": {"bytes": 201422336 + 45881600,
+                    "sha256": "a8cf4429bbeeececdf2c77fbad30ca7fa66cf6ccea806652359bc0f427221973"},
     "rowdot_kernel": {"bytes": 135301120 + 734720,
                     "sha256": "75b3397d3eb84e18561f4d87abb9ef7961b5d444a6a2e1441b0fe90db9fefd5a"},
     "dkdv_kernel": {"bytes": 270629120 + 102725888,

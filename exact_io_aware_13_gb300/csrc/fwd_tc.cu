@@ -393,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run *= corr;
       }
       // FP8: exp2(s - m + 7) = 2^7 p, the scale e4m3 rounding wants, at no extra cost
-      const float neg_m = (m_run == -INFINITY ? 0.f : -m_run) + (kFp8 ? kPScaleLog2Fp8 : 0.f);
+      float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+      if constexpr (kFp8) neg_m += kPScaleLog2Fp8;
       const float mul = fast ? k1j : 1.f;  // p = exp2(v * mul - m)
       const DropThr dthr = drop_thr_words(kDrop ? p.drop_thr : 0);
       float acc[8];
