@@ -192,6 +192,57 @@ def workload_config(w, extra=None):
     return cfg
 
 
+def pipelined_e2e(steps, stream, dev, host_in, in_sets, out_sets, host_out, run_step):
+    """End-to-end time of `steps` steps, ms per step. Step s copies `host_in` (pinned) into
+    device input set s % 2, runs `run_step(s % 2)` on the compute stream and copies output
+    set s % 2 into `host_out` (pinned). The inputs of step s + 1 arrive and the outputs of
+    step s leave on their own streams (one per tensor) while the kernels run; events order
+    each copy after the kernels that last used its buffers."""
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    s_in_t = [torch.cuda.Stream(device=dev) for _ in host_in]
+    s_out_t = [torch.cuda.Stream(device=dev) for _ in host_out]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def fan_out(main, subs, pairs, done):
+        start = torch.cuda.Event()
+        start.record(main)
+        for st_, (dst, src) in zip(subs, pairs):
+            st_.wait_event(start)
+            with torch.cuda.stream(st_):
+                dst.copy_(src, non_blocking=True)
+            fin = torch.cuda.Event()
+            fin.record(st_)
+            main.wait_event(fin)
+        done.record(main)
+
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    fan_out(s_in, s_in_t, list(zip(in_sets[0], host_in)), ev_in[0])
+    for st_i in range(steps):
+        x = st_i % 2
+        stream.wait_event(ev_in[x])
+        if st_i >= 2:
+            stream.wait_event(ev_out[x])  # outputs of step st_i - 2 copied out
+        run_step(x)
+        ev_done[x].record(stream)
+        if st_i + 1 < steps:
+            if st_i >= 1:
+                s_in.wait_event(ev_done[1 - x])  # step st_i - 1 is done with those inputs
+            fan_out(s_in, s_in_t, list(zip(in_sets[1 - x], host_in)), ev_in[1 - x])
+        s_out.wait_event(ev_done[x])
+        fan_out(s_out, s_out_t, list(zip(host_out, out_sets[x])), ev_out[x])
+    stream.wait_event(ev_out[(steps - 1) % 2])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def run_ours(args, w=CAUSAL_FWD_BWD):
     from exact_io_aware_13_gb300 import build as libbuild
     libbuild.build()  # compiles libattn.so from source if it is missing or stale
@@ -416,14 +467,9 @@ def run_forward(args, w, fp8=False):
 
         def fwd():
             ea.fwd_fp8_into(q8, sq, k8, sk, v8t, sv, o, lse, Nkv=w.Nkv, **kw)
-
-        def fwd_e2e():  # the public FP8 call: quantise, then the FP8 forward
-            (a8, a_s), (b8, b_s), (c8, c_s) = ea.fp8_inputs(qd, kd, vd)
-            ea.fwd_fp8_into(a8, a_s, b8, b_s, c8, c_s, o, lse, Nkv=w.Nkv, **kw)
     else:
         def fwd():
             ea.fwd_into(qd, kd, vd, o, lse, **kw)
-        fwd_e2e = fwd
     for _ in range(args.warmup):
         fwd()
     torch.cuda.synchronize()
@@ -451,19 +497,20 @@ def run_forward(args, w, fp8=False):
     outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = sum(t.numel() * t.element_size() for t in outs_host)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        for dst, src in zip((qd, kd, vd), host):
-            dst.copy_(src, non_blocking=True)
-        fwd_e2e()
-        for dst, src in zip(outs_host, (o, lse)):
-            dst.copy_(src, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
+    in_sets = [(qd, kd, vd), tuple(torch.empty_like(t) for t in (qd, kd, vd))]
+    out_sets = [(o, lse), (torch.empty_like(o), torch.empty_like(lse))]
+
+    def run_step(x):  # the public call on buffer set x (FP8: quantise, then the FP8 forward)
+        (bq, bk, bv), (bo, blse) = in_sets[x], out_sets[x]
+        if fp8:
+            (a8, a_s), (b8, b_s), (c8, c_s) = ea.fp8_inputs(bq, bk, bv)
+            ea.fwd_fp8_into(a8, a_s, b8, b_s, c8, c_s, bo, blse, Nkv=w.Nkv, **kw)
+        else:
+            ea.fwd_into(bq, bk, bv, bo, blse, **kw)
+
+    if world > 1:
+        torch.distributed.barrier()
+    ms_e2e = pipelined_e2e(args.steps, stream, dev, host, in_sets, out_sets, outs_host, run_step)
     pk = peaks()
     ach = f_fwd / (statistics.mean(times) * 1e-3) / 1e12
     peak = pk["bf16_tflops"] * (2 if fp8 else 1)  # FP8 dense rate: 2x bf16 (nominal ratio)
