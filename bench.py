@@ -316,69 +316,23 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
 
     # ------------------------------------------------------------ end to end, host buffers
     # Every step copies its inputs in from pinned host memory, runs attn_fwd + attn_bwd
-    # through the public entry points and copies its results out. Two sets of device
-    # buffers let the inputs of step s + 1 arrive (one copy stream) and the results of
-    # step s leave (another) while the kernels of the next step run; events order each
-    # copy after the kernels that last used its buffers.
+    # through the public entry points and copies its results out (pipelined_e2e: two
+    # buffer sets, the copies overlap the kernels of the neighbouring steps).
     outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                  for t in (o, lse, dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = sum(t.numel() * t.element_size() for t in outs_host)
-    bufs = [(qd, kd, vd, dod, o, lse, dq, dk, dv),
-            tuple(torch.empty_like(t) for t in (qd, kd, vd, dod, o, lse, dq, dk, dv))]
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    # one stream per tensor copy, so that several copy engines share each direction
-    s_in_t = [torch.cuda.Stream(device=dev) for _ in range(4)]
-    s_out_t = [torch.cuda.Stream(device=dev) for _ in range(5)]
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_done = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    in_sets = [(qd, kd, vd, dod), tuple(torch.empty_like(t) for t in (qd, kd, vd, dod))]
+    out_sets = [(o, lse, dq, dk, dv), tuple(torch.empty_like(t) for t in (o, lse, dq, dk, dv))]
 
-    def fan_out(main, subs, pairs, done):
-        """Copies dst <- src, one per stream of `subs`, after what `main` has queued;
-        `done` records on `main` once all of them finished."""
-        start = torch.cuda.Event()
-        start.record(main)
-        for st_, (dst, src) in zip(subs, pairs):
-            st_.wait_event(start)
-            with torch.cuda.stream(st_):
-                dst.copy_(src, non_blocking=True)
-            fin = torch.cuda.Event()
-            fin.record(st_)
-            main.wait_event(fin)
-        done.record(main)
-
-    def copy_in(x):
-        fan_out(s_in, s_in_t, list(zip(bufs[x][:4], host)), ev_in[x])
+    def run_step(x):
+        (bq, bk, bv, bdo), (bo, blse, bdq, bdk, bdv) = in_sets[x], out_sets[x]
+        ea.fwd_into(bq, bk, bv, bo, blse, **kw)
+        ea.bwd_into(bq, bk, bv, bo, blse, bdo, bdq, bdk, bdv, ws, **kw)
 
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    s_in.wait_event(e0)
-    s_out.wait_event(e0)
-    copy_in(0)
-    for st_i in range(args.steps):
-        x = st_i % 2
-        bq, bk, bv, bdo, bo, blse, bdq, bdk, bdv = bufs[x]
-        stream.wait_event(ev_in[x])
-        if st_i >= 2:
-            stream.wait_event(ev_out[x])  # results of step st_i - 2 copied out
-        ea.fwd_into(bq, bk, bv, bo, blse, **kw)
-        ea.bwd_into(bq, bk, bv, bo, blse, bdo, bdq, bdk, bdv, ws, **kw)
-        ev_done[x].record(stream)
-        if st_i + 1 < args.steps:
-            if st_i >= 1:
-                s_in.wait_event(ev_done[1 - x])  # step st_i - 1 is done with those inputs
-            copy_in(1 - x)
-        s_out.wait_event(ev_done[x])
-        fan_out(s_out, s_out_t, list(zip(outs_host, (bo, blse, bdq, bdk, bdv))), ev_out[x])
-    stream.wait_event(ev_out[(args.steps - 1) % 2])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
+    ms_e2e = pipelined_e2e(args.steps, stream, dev, host, in_sets, out_sets, outs_host, run_step)
     e2e_value = world * f_step / (ms_e2e * 1e-3) / 1e12
 
     pk = peaks()
