@@ -200,3 +200,25 @@ def test_dropout_full_size_sampled_kv_head():
     b, g = w.B - 1, 5
     ref = H.oracle_backward(w, inputs, kv_heads=[(b, g)])
     H.check_grads([x[b, g:g + 1] for x in got], [x[b, g:g + 1] for x in ref], w.name)
+
+
+def test_dropout_backward_phases_match_one_call():
+    """The row kernel, the dK/dV kernel and the dQ kernel run one at a time through
+    attn_bwd_phases (the launches the benchmark times) give the bits of attn_bwd."""
+    import exact_io_aware_13_gb300 as ea
+    w = _drop(H.small_workload("drop phases", MASK_CAUSAL, SCORE_ALIBI, B=1, Hq=4, Hkv=2,
+                               N=330, d=64, seed=17), 0.3, 99)
+    q, k, v, do, _ = make_inputs(w, with_dout=True)
+    qd, kd, vd, dod = H.to_dev(q, k, v, do)
+    kw = dict(scale=w.scale, mask_kind=w.mask_kind, score_kind=w.score_kind,
+              dropout_p=w.dropout_p, dropout_seed=w.dropout_seed)
+    o, lse = ea.forward(qd, kd, vd, **kw)
+    g1 = ea.backward(qd, kd, vd, o, lse, dod, **kw)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(max(ea.bwd_workspace_size(qd, kd), 256), dtype=torch.uint8, device="cuda")
+    for ph in (ea.BWD_ROWDOT, ea.BWD_DKDV, ea.BWD_DQ):
+        ea.bwd_phases_into(ph, qd, kd, vd, o, lse, dod, dq, dk, dv, ws, **kw)
+    torch.cuda.synchronize()
+    assert ea.device_status() == 0
+    for a, b in zip(g1, (dq, dk, dv)):
+        assert torch.equal(a, b)
