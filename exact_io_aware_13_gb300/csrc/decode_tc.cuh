@@ -23,13 +23,14 @@
 //     list (items ordered sequence, head, row tile, chunk; every warp derives the same
 //     list from seq_lens), and streams the items' key tiles through one ring without a
 //     pause between items;
-//   * warp 7 streams K and V tiles of 64 keys through a 5-stage shared-memory ring with
+//   * warp 7 streams K and V tiles of 64 keys through a 7-stage shared-memory ring with
 //     TMA (128-byte swizzle), one box per page piece (page sizes below 64 take several
-//     boxes per tile), reading the page table 32 entries at a time, one item ahead; the
-//     Q tile of a run of items with the same (sequence, head, row tile) goes into one of
-//     two buffers;
+//     boxes per tile), reading the page table 32 entries at a time, one item ahead;
+//   * the Q tile of a run of items with the same (sequence, head, row tile) lives in
+//     one of two tensor-memory buffers (bf16 pairs), written by the epilogue warps one
+//     item ahead, so S = Q K^T is a TMEM-operand MMA;
 //   * warp 1 issues S = Q K^T (M = 128, N = 64) and O += P V from one elected thread,
-//     with P in tensor memory; it waits only on hardware named barriers (a
+//     with Q and P in tensor memory; it waits only on hardware named barriers (a
 //     shared-memory access by the thread that issues MMAs stalls the tensor pipe), fed
 //     by warp 3, which turns the TMA completions into barrier arrivals and clears the
 //     unused V rows of a sequence's last tile;
@@ -39,8 +40,9 @@
 //     the softmax; warps 4 and 6 do the online softmax (one thread per row) and rescale
 //     O in tensor memory when the max grows by more than 2^8; warps 0 and 2 write each
 //     item's result from the other O buffer while the softmax goes on with the next.
-// Tensor memory: S0 cols [0,64), S1 [64,128), O0 [128,128+d), O1 [128+d,128+2d), the
-// row max and sum of O buffer b at cols 384 + 2b, 385 + 2b.
+// Tensor memory: S0 cols [0,64), S1 [64,128), O0 [128,128+d), O1 [128+d,128+2d), Q0 and
+// Q1 (d/2 columns each) after them; the row max and sum of each O buffer are handed from
+// the softmax to the epilogue warps in shared memory.
 //
 // The last tile of a sequence can end inside a page whose later slots hold no token
 // (possibly NaN). S columns past the sequence are masked before the max; the V rows
