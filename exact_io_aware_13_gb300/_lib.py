@@ -56,6 +56,7 @@ SIGNATURES = {
     "attn_decode_workspace_size": (ctypes.c_size_t, [_I] * 7),
     "attn_decode_split_keys": (_I, [_I, _I, _I, _I, ctypes.c_longlong, _I]),
     "attn_device_status": (_I, [_P]),
+    "attn_selftest_wait_timeout": (_I, [_P]),
     "attn_strerror": (ctypes.c_char_p, [_I]),
 }
 

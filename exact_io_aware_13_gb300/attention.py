@@ -184,6 +184,13 @@ def device_status(stream=None) -> int:
 FP8_TILES, FP8_V_TRANSPOSED = 0, 1
 
 
+def selftest_wait_timeout(stream=None) -> None:
+    """Launch the failure-path self-test (attn_selftest_wait_timeout): a bounded device
+    wait that nothing completes gives up after about 2 s; device_status() then reports
+    ATTN_ERR_DEVICE_TIMEOUT."""
+    _lib.check(_lib.load().attn_selftest_wait_timeout(_stream(stream)), "attn_selftest_wait_timeout")
+
+
 def quantize_fp8(x: torch.Tensor, layout: int = FP8_TILES, stream=None):
     """bf16 x [B, H, N, d] -> (e4m3 codes as uint8, fp32 scales) via attn_quantize_fp8.
     FP8_TILES: codes [B, H, N, d], scales [B*H, ceil(N/128)];

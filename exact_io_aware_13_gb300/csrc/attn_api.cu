@@ -585,6 +585,13 @@ attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_para
   return from_cuda(launch_classify(p.mask, classes, static_cast<cudaStream_t>(stream)));
 }
 
+attn_status attn_selftest_wait_timeout(void* stream) {
+  DeviceInfo* dev = nullptr;
+  attn_status s = current_device(&dev);
+  if (s != ATTN_OK) return s;
+  return from_cuda(launch_selftest_wait(dev->status, static_cast<cudaStream_t>(stream)));
+}
+
 attn_status attn_device_status(void* stream) {
   DeviceInfo* dev = nullptr;
   attn_status s = current_device(&dev);

@@ -348,6 +348,16 @@ attn_status attn_bwd_simt(const void* q, const void* k, const void* v, const voi
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Self-test of the failure path every kernel shares: launches one warp whose wait on a
+ * shared-memory barrier that nothing completes is the library's bounded wait. After the
+ * wait limit (2 s of the device clock) it gives up and records ATTN_ERR_DEVICE_TIMEOUT
+ * in the device status word, which attn_device_status then reports and clears; the
+ * context stays usable. Asynchronous on `stream`. Returns ATTN_ERR_ARCH or
+ * ATTN_ERR_LAUNCH if the kernel cannot be launched.
+ */
+attn_status attn_selftest_wait_timeout(void* stream);
+
+/*
  * Synchronises `stream` and reports whether a kernel of this library on the
  * current device gave up a bounded wait since the last call (ATTN_ERR_DEVICE_TIMEOUT),
  * met an out-of-range device input (ATTN_ERR_DEVICE_INPUT), or whether the stream
