@@ -12,9 +12,27 @@
 
 #include "attn.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace attn {
 namespace {
+// Failure-path self-test: thread 0 waits on a fresh mbarrier that nothing arrives on,
+// with the same bounded wait as every kernel; it gives up after kWaitLimitNs, raising
+// the CTA's abort flag and DEV_TIMEOUT in the library's status word, and returns.
+__global__ void selftest_wait_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncwarp();
+  WaitCtx wc{&abort_flag, status};
+  if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, wc);
+  __syncwarp();
+}
+
 
 // Sticky device status word of this library (one per device that loads it).
 __device__ int g_device_status;
@@ -589,7 +607,8 @@ attn_status attn_selftest_wait_timeout(void* stream) {
   DeviceInfo* dev = nullptr;
   attn_status s = current_device(&dev);
   if (s != ATTN_OK) return s;
-  return from_cuda(launch_selftest_wait(dev->status, static_cast<cudaStream_t>(stream)));
+  attn::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status);
+  return from_cuda(cudaGetLastError());
 }
 
 attn_status attn_device_status(void* stream) {

@@ -64,9 +64,6 @@ cudaError_t launch_bwd_rowdot(const Problem& p, const __nv_bfloat16* o,
 cudaError_t launch_fill_masked(long long rows, int d, __nv_bfloat16* o, float* lse,
                                cudaStream_t st);
 cudaError_t launch_classify(const MaskSpec& m, int32_t* classes, cudaStream_t st);
-// One warp whose bounded wait on a barrier nothing completes gives up (the failure path
-// of every kernel), recording DEV_TIMEOUT in `status`.
-cudaError_t launch_selftest_wait(int* status, cudaStream_t st);
 
 // ---- tcgen05 tensor-core kernels.
 cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,

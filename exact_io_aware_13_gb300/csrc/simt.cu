@@ -6,7 +6,6 @@
 // partial output rescaled by exp(m_old - m_new) whenever the max grows. Here the
 // recurrence advances one key at a time, in fp32 with accurate expf/tanhf.
 #include "kernels.h"
-#include "ptx.cuh"
 
 namespace attn {
 namespace {
@@ -335,28 +334,6 @@ cudaError_t launch_bwd_rowdot(const Problem& p, const __nv_bfloat16* o,
   if (p.d == 64) rowdot_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
   else if (p.d == 128) rowdot_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
   else rowdot_kernel<256><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
-  return cudaGetLastError();
-}
-
-// Failure-path self-test: thread 0 waits on a fresh mbarrier that nothing arrives on,
-// with the same bounded wait as every kernel; it gives up after kWaitLimitNs, raising
-// the CTA's abort flag and DEV_TIMEOUT in the library's status word, and returns.
-__global__ void selftest_wait_kernel(int* status) {
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ int abort_flag;
-  if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bar), 1);
-    abort_flag = 0;
-    fence_barrier_init();
-  }
-  __syncwarp();
-  WaitCtx wc{&abort_flag, status};
-  if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, wc);
-  __syncwarp();
-}
-
-cudaError_t launch_selftest_wait(int* status, cudaStream_t st) {
-  selftest_wait_kernel<<<1, 32, 0, st>>>(status);
   return cudaGetLastError();
 }
 
