@@ -54,6 +54,23 @@ def _dims(q: torch.Tensor, k: torch.Tensor):
     return B, Hq, Hkv, Nq, Nkv, d
 
 
+_BF16, _F32, _U8 = torch.bfloat16, torch.float32, torch.uint8
+
+
+def _check_dtypes(*named):
+    """named: (tensor or None, dtype, name) triples. The C ABI takes untyped pointers, so
+    a tensor of another dtype would be read as the expected one: refuse it here."""
+    for t, dtype, name in named:
+        if t is not None and t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _check_bwd_dtypes(q, k, v, o, lse, dout, dq, dk, dv):
+    _check_dtypes((q, _BF16, "q"), (k, _BF16, "k"), (v, _BF16, "v"), (o, _BF16, "o"),
+                  (lse, _F32, "lse"), (dout, _BF16, "dout"), (dq, _BF16, "dq"),
+                  (dk, _BF16, "dk"), (dv, _BF16, "dv"))
+
+
 def _check_tensors(*ts):
     for t in ts:
         if t is None:
@@ -69,6 +86,8 @@ def fwd_into(q, k, v, o, lse, *, scale: float, mask_kind: int = MASK_NONE, windo
     """Run attn_fwd (impl="tc") or attn_fwd_simt (impl="simt") into o and lse. A positive
     dropout_p drops elements of P by the Philox4x32-10 mask of dropout_seed."""
     _check_tensors(q, k, v, o, lse, doc_offsets)
+    _check_dtypes((q, _BF16, "q"), (k, _BF16, "k"), (v, _BF16, "v"), (o, _BF16, "o"),
+                  (lse, _F32, "lse"))
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
     mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap, dropout_p, dropout_seed)
@@ -110,6 +129,7 @@ def bwd_into(q, k, v, o, lse, dout, dq, dk, dv, workspace, *, scale: float,
     """Run attn_bwd (impl="tc") or attn_bwd_simt into dq, dk, dv; dropout_p and
     dropout_seed must be those of the forward."""
     _check_tensors(q, k, v, o, lse, dout, dq, dk, dv, workspace, doc_offsets)
+    _check_bwd_dtypes(q, k, v, o, lse, dout, dq, dk, dv)
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
     mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap, dropout_p, dropout_seed)
@@ -130,6 +150,7 @@ def bwd_phases_into(phases: int, q, k, v, o, lse, dout, dq, dk, dv, workspace, *
     """Run some of the backward's kernels (BWD_ROWDOT | BWD_DKDV | BWD_DQ) via
     attn_bwd_phases; BWD_ROWDOT must have run on the same workspace first."""
     _check_tensors(q, k, v, o, lse, dout, dq, dk, dv, workspace, doc_offsets)
+    _check_bwd_dtypes(q, k, v, o, lse, dout, dq, dk, dv)
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
     mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap, dropout_p, dropout_seed)
@@ -196,6 +217,7 @@ def quantize_fp8(x: torch.Tensor, layout: int = FP8_TILES, stream=None):
     FP8_TILES: codes [B, H, N, d], scales [B*H, ceil(N/128)];
     FP8_V_TRANSPOSED: codes [B, H, d, attn_fp8_v_row_bytes(N)], scales [B*H]."""
     _check_tensors(x)
+    _check_dtypes((x, _BF16, "x"))
     lib = _lib.load()
     B, H, N, d = x.shape
     if layout == FP8_TILES:
@@ -222,6 +244,8 @@ def fwd_fp8_into(q8, sq, k8, sk, v8t, sv, o, lse, *, Nkv: int, scale: float,
                  score_kind: int = SCORE_NONE, softcap: float = 0.0, stream=None) -> None:
     """Run attn_fwd_fp8 into o (bf16 [B,Hq,Nq,128]) and lse."""
     _check_tensors(q8, sq, k8, sk, v8t, sv, o, lse, doc_offsets)
+    _check_dtypes((q8, _U8, "q8"), (k8, _U8, "k8"), (v8t, _U8, "v8t"), (sq, _F32, "sq"),
+                  (sk, _F32, "sk"), (sv, _F32, "sv"), (o, _BF16, "o"), (lse, _F32, "lse"))
     lib = _lib.load()
     B, Hq, Nq, d = q8.shape
     Hkv = k8.shape[1]
@@ -275,6 +299,8 @@ def decode_paged_into(q, k_cache, v_cache, page_table, seq_lens, o, lse, workspa
     q [B, Hq, Nq, d], caches [pages, Hkv, page_size, d], page_table int32 [B, max_pages],
     seq_lens int32 [B]; writes o and lse."""
     _check_tensors(q, k_cache, v_cache, page_table, seq_lens, o, lse, workspace)
+    _check_dtypes((q, _BF16, "q"), (k_cache, _BF16, "k_cache"), (v_cache, _BF16, "v_cache"),
+                  (o, _BF16, "o"), (lse, _F32, "lse"))
     B, Hq, Nq, d = q.shape
     num_pages, Hkv, page_size, dk = k_cache.shape
     if dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):

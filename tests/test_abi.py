@@ -166,3 +166,19 @@ def test_decode_workspace_size_and_split_keys(lib):
         assert keys >= 256 and keys % 64 == 0, args
     assert lib.attn_decode_split_keys(64, 32, 8, 1, 64 * 4352, 152) == 1472  # ceil64(1466.1)
     assert lib.attn_decode_split_keys(1, 8, 8, 1, 100, 152) == 256
+
+
+def test_binding_refuses_wrong_dtypes():
+    """The C ABI takes untyped pointers: the torch binding checks every tensor's dtype
+    (bf16 inputs and outputs, fp32 lse and FP8 scales, uint8 FP8 codes) before a call."""
+    import torch
+
+    from exact_io_aware_13_gb300 import attention as A
+    bf, f32 = torch.zeros(2, dtype=torch.bfloat16), torch.zeros(2, dtype=torch.float32)
+    A._check_dtypes((bf, torch.bfloat16, "q"), (f32, torch.float32, "lse"), (None, torch.uint8, "x"))
+    with pytest.raises(ValueError, match="q must be torch.bfloat16"):
+        A._check_dtypes((f32, torch.bfloat16, "q"))
+    with pytest.raises(ValueError, match="lse must be torch.float32"):
+        A._check_bwd_dtypes(bf, bf, bf, bf, bf, bf, bf, bf, bf)
+    with pytest.raises(ValueError, match="dv must be torch.bfloat16"):
+        A._check_bwd_dtypes(bf, bf, bf, bf, f32, bf, bf, bf, f32)
