@@ -65,6 +65,19 @@ def _check_dtypes(*named):
             raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _check_shapes(q, k, v, o=None, lse=None, dout=None, dq=None, dk=None, dv=None):
+    """Every buffer must have the shape the kernels index it with: q, o, dout, dq
+    [B, Hq, Nq, d]; k, v, dk, dv [B, Hkv, Nkv, d]; lse [B, Hq, Nq]."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be [B, H, N, d]")
+    for t, ref, name in ((v, k, "v"), (o, q, "o"), (dout, q, "dout"), (dq, q, "dq"),
+                         (dk, k, "dk"), (dv, k, "dv")):
+        if t is not None and tuple(t.shape) != tuple(ref.shape):
+            raise ValueError(f"{name} must have shape {tuple(ref.shape)}, got {tuple(t.shape)}")
+    if lse is not None and tuple(lse.shape) != tuple(q.shape[:-1]):
+        raise ValueError(f"lse must have shape {tuple(q.shape[:-1])}, got {tuple(lse.shape)}")
+
+
 def _check_bwd_dtypes(q, k, v, o, lse, dout, dq, dk, dv):
     _check_dtypes((q, _BF16, "q"), (k, _BF16, "k"), (v, _BF16, "v"), (o, _BF16, "o"),
                   (lse, _F32, "lse"), (dout, _BF16, "dout"), (dq, _BF16, "dq"),
@@ -88,6 +101,7 @@ def fwd_into(q, k, v, o, lse, *, scale: float, mask_kind: int = MASK_NONE, windo
     _check_tensors(q, k, v, o, lse, doc_offsets)
     _check_dtypes((q, _BF16, "q"), (k, _BF16, "k"), (v, _BF16, "v"), (o, _BF16, "o"),
                   (lse, _F32, "lse"))
+    _check_shapes(q, k, v, o, lse)
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
     mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap, dropout_p, dropout_seed)
@@ -130,6 +144,7 @@ def bwd_into(q, k, v, o, lse, dout, dq, dk, dv, workspace, *, scale: float,
     dropout_seed must be those of the forward."""
     _check_tensors(q, k, v, o, lse, dout, dq, dk, dv, workspace, doc_offsets)
     _check_bwd_dtypes(q, k, v, o, lse, dout, dq, dk, dv)
+    _check_shapes(q, k, v, o, lse, dout, dq, dk, dv)
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
     mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap, dropout_p, dropout_seed)
@@ -151,6 +166,7 @@ def bwd_phases_into(phases: int, q, k, v, o, lse, dout, dq, dk, dv, workspace, *
     attn_bwd_phases; BWD_ROWDOT must have run on the same workspace first."""
     _check_tensors(q, k, v, o, lse, dout, dq, dk, dv, workspace, doc_offsets)
     _check_bwd_dtypes(q, k, v, o, lse, dout, dq, dk, dv)
+    _check_shapes(q, k, v, o, lse, dout, dq, dk, dv)
     lib = _lib.load()
     B, Hq, Hkv, Nq, Nkv, d = _dims(q, k)
     mp, sp, keep = _params(mask_kind, window, doc_offsets, softcap, dropout_p, dropout_seed)
@@ -301,6 +317,8 @@ def decode_paged_into(q, k_cache, v_cache, page_table, seq_lens, o, lse, workspa
     _check_tensors(q, k_cache, v_cache, page_table, seq_lens, o, lse, workspace)
     _check_dtypes((q, _BF16, "q"), (k_cache, _BF16, "k_cache"), (v_cache, _BF16, "v_cache"),
                   (o, _BF16, "o"), (lse, _F32, "lse"))
+    if q.dim() != 4 or tuple(o.shape) != tuple(q.shape) or tuple(lse.shape) != tuple(q.shape[:-1]):
+        raise ValueError("q, o must be [B, Hq, Nq, d] and lse [B, Hq, Nq]")
     B, Hq, Nq, d = q.shape
     num_pages, Hkv, page_size, dk = k_cache.shape
     if dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):

@@ -182,3 +182,20 @@ def test_binding_refuses_wrong_dtypes():
         A._check_bwd_dtypes(bf, bf, bf, bf, bf, bf, bf, bf, bf)
     with pytest.raises(ValueError, match="dv must be torch.bfloat16"):
         A._check_bwd_dtypes(bf, bf, bf, bf, f32, bf, bf, bf, f32)
+
+
+def test_binding_refuses_wrong_shapes():
+    """A buffer smaller than the shape the kernels index would be written past its end:
+    the binding compares every buffer's shape with q's and k's before a call."""
+    import torch
+
+    from exact_io_aware_13_gb300 import attention as A
+    q, k = torch.zeros(1, 4, 10, 64), torch.zeros(1, 2, 12, 64)
+    A._check_shapes(q, k, k.clone(), q.clone(), torch.zeros(1, 4, 10), q.clone(), q.clone(),
+                    k.clone(), k.clone())
+    with pytest.raises(ValueError, match="lse must have shape"):
+        A._check_shapes(q, k, k, q, torch.zeros(1, 4, 9))
+    with pytest.raises(ValueError, match="dk must have shape"):
+        A._check_shapes(q, k, k, q, None, None, None, torch.zeros(1, 2, 11, 64))
+    with pytest.raises(ValueError, match="o must have shape"):
+        A._check_shapes(q, k, k, torch.zeros(1, 4, 10, 32))
