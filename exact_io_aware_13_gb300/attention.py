@@ -85,11 +85,21 @@ def _check_bwd_dtypes(q, k, v, o, lse, dout, dq, dk, dv):
 
 
 def _check_tensors(*ts):
+    """Contiguous CUDA tensors, all on the current device (the library launches there,
+    on that device's stream)."""
+    index = None
     for t in ts:
         if t is None:
             continue
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("tensors must be contiguous CUDA tensors")
+        if index is None:
+            index = t.device.index
+        elif t.device.index != index:
+            raise ValueError("tensors must all be on one device")
+    if index is not None and index != torch.cuda.current_device():
+        raise ValueError(f"tensors are on cuda:{index}, the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
 
 
 def fwd_into(q, k, v, o, lse, *, scale: float, mask_kind: int = MASK_NONE, window: int = 0,
