@@ -3,15 +3,17 @@ online softmax, backward rebuilding P from the LSE) on the causal fwd+bwd worklo
 (B=2, H=16, N=8192, d=128, bf16), timed with CUDA events.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload fwd_bwd|causal_fwd|gqa_window_fwd|docs_fwd|tiny_fwd|fp8_causal_fwd
-                            |causal_fwd_d256|paged_decode]
+                [--workload fwd_bwd|fwd_bwd_dropout|fwd_bwd_d256|causal_fwd|gqa_window_fwd
+                            |docs_fwd|tiny_fwd|fp8_causal_fwd|causal_fwd_d256|paged_decode]
 
 Prints one JSON line. `value` is useful TFLOP/s (masked-out work excluded) summed
 over ranks; with N > 1 each rank runs its own replica of the workload (the heads
 are independent, so there is no data-path collective). --impl reference times the
 float64 CPU oracle on a bounded sample of the same workload on the host cores.
---workload picks one of the other workloads; those are forward-only, so a step is
-one forward pass and the line reports the forward's useful TFLOP/s. fp8_causal_fwd
+--workload picks one of the other workloads: fwd_bwd_dropout and fwd_bwd_d256 are the
+fwd+bwd step with dropout p = 0.1 and at head dimension 256; the *_fwd ones are
+forward-only, so a step is one forward pass and the line reports the forward's useful
+TFLOP/s. fp8_causal_fwd
 runs the FP8 forward (e4m3 inputs with block scales, quantised once before the timed
 steps; the end-to-end number includes the quantisation). paged_decode times one decode
 step over a paged KV cache and reports GB/s against the HBM roofline.
