@@ -3,13 +3,23 @@ online softmax, backward rebuilding P from the LSE) on the causal fwd+bwd worklo
 (B=2, H=16, N=8192, d=128, bf16), timed with CUDA events.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--min-seconds S]
                 [--workload fwd_bwd|fwd_bwd_dropout|fwd_bwd_d256|causal_fwd|gqa_window_fwd
-                            |docs_fwd|tiny_fwd|fp8_causal_fwd|causal_fwd_d256|paged_decode]
+                            |docs_fwd|tiny_fwd|fp8_causal_fwd|causal_fwd_d256|paged_decode
+                            |cpu_replica_check]
 
 Prints one JSON line. `value` is useful TFLOP/s (masked-out work excluded) summed
 over ranks; with N > 1 each rank runs its own replica of the workload (the heads
-are independent, so there is no data-path collective). --impl reference times the
-float64 CPU oracle on a bounded sample of the same workload on the host cores.
+are independent, so there is no data-path collective). Launched under
+torch.distributed.run, the ranks come from its environment; `--gpus N` given alone
+starts the N ranks itself the same way (127.0.0.1 rendezvous, one GPU per rank).
+The timed region, exactly K steps between a barrier and a device synchronisation
+on both sides, is repeated until the repetitions cover at least --min-seconds of
+GPU time (default 2 s), so that the clock samplers see the kernels under load; the
+line reports the mean per step over all repetitions and how many there were.
+--impl reference times the float64 CPU oracle on a bounded sample of the same
+workload on the host cores. cpu_replica_check runs the launcher and the cross-rank
+reduction on CPU (gloo ranks, a float64 matmul as the step); the tests use it.
 --workload picks one of the other workloads: fwd_bwd_dropout and fwd_bwd_d256 are the
 fwd+bwd step with dropout p = 0.1 and at head dimension 256; the *_fwd ones are
 forward-only, so a step is one forward pass and the line reports the forward's useful
@@ -181,6 +191,58 @@ def dist_env():
     return world, rank, local
 
 
+def check_world(args, world: int) -> None:
+    if world != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}: give --gpus N "
+                         "alone, or launch N ranks with torch.distributed.run and --gpus N")
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_replicas(n: int, argv) -> int:
+    """`--gpus N` (N > 1) without a launcher: start N ranks of this script through
+    torch.distributed.run (one process per GPU, 127.0.0.1 rendezvous). Every rank runs
+    its own replica of the workload; rank 0 prints the line. Returns the exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1",
+           "--master-port", str(free_port()), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
+def init_ranks(args, backend: str = "nccl"):
+    """(world, rank, local rank) from the launcher's environment, checked against
+    --gpus; joins the process group when there is more than one rank."""
+    world, rank, local = dist_env()
+    check_world(args, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def repeat_timed(args, world: int, dev, rep):
+    """Run `rep` (one timed region of exactly args.steps steps, bracketed by a barrier and
+    a synchronisation; it returns one list of kernel times in ms per step) until the
+    repetitions cover at least args.min_seconds of GPU time, with the clocks sampled
+    throughout. Every rank runs the same number of repetitions (the maximum of the
+    ranks' estimates). Returns (rows of all repetitions, repetitions, clock summary)."""
+    import math
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        rows = rep()
+        gpu_ms = sum(sum(r) for r in rows)
+        n = max(1, math.ceil(args.min_seconds * 1e3 / max(gpu_ms, 1e-3)))
+        if world > 1:
+            n = int(max_over_ranks(n, dev))
+        for _ in range(n - 1):
+            rows += rep()
+    return rows, n, clk.summary()
+
+
 def workload_config(w, extra=None):
     n_in = 4 if w.backward else 3  # q, k, v (and dO)
     mib = (n_in - 2) * w.B * w.Hq * w.Nq * w.d * 2 + 2 * w.B * w.Hkv * w.Nkv * w.d * 2
@@ -250,10 +312,7 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
     libbuild.build()  # compiles libattn.so from source if it is missing or stale
     import exact_io_aware_13_gb300 as ea
     from exact_io_aware_13_gb300 import flops
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    world, rank, local = init_ranks(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pairs = flops.allowed_pairs(w.mask_kind, w.Nq, w.Nkv)
@@ -291,11 +350,13 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
     # (at d = 256 the dK/dV phase is two kernels, the dV and the dK walk)
     names = (["fwd256_kernel", "rowdot_kernel", "dkdv256_kernel", "dq256_kernel"] if w.d == 256
              else ["fwd_tc_kernel", "rowdot_kernel", "dkdv_kernel", "dq_kernel"])
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+
+    def timed_rep():
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+              for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         for s in range(args.steps):
             flush.zero_()  # evict the previous step's tensors from L2 (untimed)
             ev[s][0].record(stream)
@@ -305,15 +366,19 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
                 ea.bwd_phases_into(ph, qd, kd, vd, o, lse, dod, dq, dk, dv, ws, **kw)
                 ev[s][2 + k_].record(stream)
         torch.cuda.synchronize()
+        return [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in ev]
+
+    rows, reps, clocks = repeat_timed(args, world, dev, timed_rep)
     if ea.device_status() != 0:
         raise RuntimeError("a kernel gave up a bounded wait during the timed steps")
-    per_kernel = {n: [e[i].elapsed_time(e[i + 1]) for e in ev] for i, n in enumerate(names)}
+    n_timed = len(rows)
+    per_kernel = {n: [r[i] for r in rows] for i, n in enumerate(names)}
     t_fwd = per_kernel[names[0]]
-    t_bwd = [sum(per_kernel[n][s] for n in names[1:]) for s in range(args.steps)]
-    t_step = sum(a + b for a, b in zip(t_fwd, t_bwd))  # ms over K steps
+    t_bwd = [sum(r[1:]) for r in rows]
+    t_step = sum(sum(r) for r in rows)  # ms over all timed steps
     if world > 1:
         t_step = max_over_ranks(t_step, dev)
-    ms_step = t_step / args.steps
+    ms_step = t_step / n_timed
     value = world * f_step / (ms_step * 1e-3) / 1e12
 
     # ------------------------------------------------------------ end to end, host buffers
@@ -382,8 +447,9 @@ def run_ours(args, w=CAUSAL_FWD_BWD):
                      "traffic": ncu_traffic(dom) if w.dropout_p == 0 else None},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
-        "gpu_launches": (5 if w.d == 256 else 4) * args.steps,  # d = 256: dV and dK walks
-        "clocks": clk.summary(),
+        "timed_repeats": reps, "timed_steps": n_timed,
+        "gpu_launches": (5 if w.d == 256 else 4) * n_timed,  # d = 256: dV and dK walks
+        "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
@@ -400,10 +466,7 @@ def run_forward(args, w, fp8=False):
     libbuild.build()
     import exact_io_aware_13_gb300 as ea
     from exact_io_aware_13_gb300 import flops
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    world, rank, local = init_ranks(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     q, k, v, _, offs = make_inputs(w, with_dout=False)
@@ -431,24 +494,28 @@ def run_forward(args, w, fp8=False):
     torch.cuda.synchronize()
     if ea.device_status() != 0:
         raise RuntimeError("a kernel gave up a bounded wait during warm-up")
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    def timed_rep():
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+              for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         for s in range(args.steps):
             flush.zero_()
             ev[s][0].record(stream)
             fwd()
             ev[s][1].record(stream)
         torch.cuda.synchronize()
+        return [[e[0].elapsed_time(e[1])] for e in ev]
+
+    rows, reps, clocks = repeat_timed(args, world, dev, timed_rep)
     if ea.device_status() != 0:
         raise RuntimeError("a kernel gave up a bounded wait during the timed steps")
-    times = [e[0].elapsed_time(e[1]) for e in ev]
+    times = [r[0] for r in rows]
     t_all = sum(times)
     if world > 1:
         t_all = max_over_ranks(t_all, dev)
-    ms_step = t_all / args.steps
+    ms_step = t_all / len(times)
     value = world * f_fwd / (ms_step * 1e-3) / 1e12
     outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
     h2d = sum(t.numel() * t.element_size() for t in host)
@@ -494,9 +561,12 @@ def run_forward(args, w, fp8=False):
         "e2e": {"value": round(world * f_fwd / (ms_e2e * 1e-3) / 1e12, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 4)},
-        "gpu_launches": args.steps,
-        "clocks": clk.summary(),
+        "timed_repeats": reps, "timed_steps": len(times),
+        "gpu_launches": len(times),
+        "clocks": clocks,
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_forward(w, offs, seconds=args.cpu_seconds)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -511,10 +581,7 @@ def run_decode(args, w):
     from exact_io_aware_13_gb300 import build as libbuild
     libbuild.build()
     import exact_io_aware_13_gb300 as ea
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    world, rank, local = init_ranks(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     q, kc, vc, table, lens = make_decode_inputs(w)
@@ -546,24 +613,28 @@ def run_decode(args, w):
     torch.cuda.synchronize()
     if ea.device_status() != 0:
         raise RuntimeError("a kernel reported a device error during warm-up")
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    def timed_rep():
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+              for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         for s in range(args.steps):
             flush.zero_()
             ev[s][0].record(stream)
             step()
             ev[s][1].record(stream)
         torch.cuda.synchronize()
+        return [[e[0].elapsed_time(e[1])] for e in ev]
+
+    rows, reps, clocks = repeat_timed(args, world, dev, timed_rep)
     if ea.device_status() != 0:
         raise RuntimeError("a kernel reported a device error during the timed steps")
-    times = [e[0].elapsed_time(e[1]) for e in ev]
+    times = [r[0] for r in rows]
     t_all = sum(times)
     if world > 1:
         t_all = max_over_ranks(t_all, dev)
-    ms_step = t_all / args.steps
+    ms_step = t_all / len(times)
     gbs = world * io_bytes / (ms_step * 1e-3) / 1e9
     outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
     h2d = sum(t.numel() * t.element_size() for t in host)
@@ -610,9 +681,12 @@ def run_decode(args, w):
         "e2e": {"value": round(world * io_bytes / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 4)},
-        "gpu_launches": launches * args.steps,
-        "clocks": clk.summary(),
+        "timed_repeats": reps, "timed_steps": len(times),
+        "gpu_launches": launches * len(times),
+        "clocks": clocks,
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(w, seconds=args.cpu_seconds)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -640,40 +714,158 @@ def cpu_baseline(w, seconds: float = 20.0, heads: int = 1):
     f = flops.attention_flops(1, done, w.d, pairs, True) + flops.attention_flops(1, done, w.d,
                                                                                   pairs, False)
     return {"value": round(f / el / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(),
-            "kind": "oracle", "seconds": round(el, 2),
+            "kind": "oracle", "seconds": round(el, 6),
             "sample": f"{done} of {w.B * w.Hq} heads (full N={w.Nq}), forward + backward, "
                       "float64 numpy oracle (BLAS threads = all cores)"}
 
 
+def cpu_baseline_forward(w, offs, seconds: float = 20.0, block: int = 512):
+    """Time the float64 oracle's forward on blocks of `block` query rows of the workload's
+    heads, taken in a seeded random order, on the host cores, for about `seconds` (at least
+    one block). The value is the useful TFLOP/s of the rows done (allowed pairs only), the
+    metric of the GPU line. The inputs are widened to float64 once, before the clock."""
+    import oracle
+    from exact_io_aware_13_gb300 import flops
+    q, k, v, _, _ = make_inputs(w, with_dout=False)
+    q64, k64, v64 = (t.to(torch.float64).numpy() for t in (q, k, v))
+    n_blocks = -(-w.Nq // block)
+    order = np.random.default_rng(0).permutation(w.B * w.Hq * n_blocks)
+    done = []
+    t0 = time.perf_counter()
+    for idx in order:
+        bh, rb = divmod(int(idx), n_blocks)
+        b, h = divmod(bh, w.Hq)
+        rows = np.arange(rb * block, min(w.Nq, (rb + 1) * block))
+        oracle.forward(q64, k64, v64, w.scale, mask_kind=w.mask_kind, window=w.window,
+                       doc_offsets=offs, score_kind=w.score_kind, softcap=w.softcap,
+                       rows=rows, heads=[(b, h)], dropout_p=w.dropout_p,
+                       dropout_seed=w.dropout_seed)
+        done.append(rows)
+        if time.perf_counter() - t0 > seconds:
+            break
+    el = time.perf_counter() - t0
+    pairs = sum(flops.allowed_pairs_rows(w.mask_kind, r, w.Nkv, w.window, offs) for r in done)
+    f = flops.attention_flops(1, 1, w.d, pairs, backward=False)
+    n_rows = sum(len(r) for r in done)
+    return {"value": round(f / el / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(el, 6),
+            "sample": f"{len(done)} blocks of up to {block} query rows ({n_rows} of "
+                      f"{w.B * w.Hq * w.Nq} rows, seeded order over heads), forward only, "
+                      "float64 numpy oracle (BLAS threads = all cores)"}
+
+
+def cpu_baseline_decode(w, seconds: float = 20.0):
+    """Time the float64 decode oracle on (sequence, kv head) units of the decode workload,
+    each with the G query heads that share its cache, in a seeded order, for about
+    `seconds` (at least one unit). The value is GB/s of the bytes the GPU line counts for
+    those units (their K and V once, Q in, O and LSE out). The caches are widened to
+    float64 once, before the clock."""
+    from oracle import decode_oracle
+    q, kc, vc, table, lens = make_decode_inputs(w)
+    q64 = q.to(torch.float64).numpy()
+    kc64, vc64 = kc.to(torch.float64).numpy(), vc.to(torch.float64).numpy()
+    G = w.Hq // w.Hkv
+    order = np.random.default_rng(0).permutation(w.B * w.Hkv)
+    nbytes, units = 0, 0
+    t0 = time.perf_counter()
+    for idx in order:
+        b, g = divmod(int(idx), w.Hkv)
+        decode_oracle.decode_forward(q64[b:b + 1], kc64, vc64, table[b:b + 1], lens[b:b + 1],
+                                     w.scale, w.mask_kind, w.window, w.score_kind, w.softcap,
+                                     heads=[(0, h) for h in range(g * G, (g + 1) * G)])
+        nbytes += int(lens[b]) * w.d * 2 * 2 + G * w.Nq * (w.d * 2 * 2 + 4)
+        units += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": round(nbytes / el / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(el, 6),
+            "sample": f"{units} of {w.B * w.Hkv} (sequence, kv head) units with their {G} query "
+                      "heads, float64 numpy decode oracle (BLAS threads = all cores)"}
+
+
+REFERENCE_WORKLOADS = {"fwd_bwd": CAUSAL_FWD_BWD, "fwd_bwd_dropout": CAUSAL_FWD_BWD_DROPOUT,
+                       "fwd_bwd_d256": CAUSAL_D256_FWD_BWD}
+
+
 def run_reference(args):
+    """The reference arm: the float64 oracle on the host cores, each step one bounded
+    sample of the same workload (fwd+bwd: one head, forward and backward; forward-only:
+    one block of query rows; decode: one (sequence, kv head) unit), with the metric and
+    unit of our line. Only rank 0 runs; the other ranks exit without work."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    w = CAUSAL_FWD_BWD
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state; warm-up steps are accepted and skipped
-    times, cb = [], None
-    for _ in range(args.steps):
-        cb = cpu_baseline(w, seconds=0.0, heads=1)
-        times.append(cb["seconds"])
-    value = statistics.mean([cb["value"]]) if cb else 0.0
-    from exact_io_aware_13_gb300 import flops
-    pairs = flops.allowed_pairs(w.mask_kind, w.Nq, w.Nkv)
-    f_head = (flops.attention_flops(1, 1, w.d, pairs, True)
-              + flops.attention_flops(1, 1, w.d, pairs, False))
-    ms = statistics.mean(times) * 1e3
-    value = f_head / (ms * 1e-3) / 1e12
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+    wl = args.workload
+    if wl == "paged_decode":
+        w = PAGED_DECODE
+        samples = [cpu_baseline_decode(w, seconds=0.0) for _ in range(args.steps)]
+        metric = ("attention paged decode: GB/s of KV cache, queries and outputs moved, and % "
+                  "of measured GB300 HBM copy bandwidth")
+        cfg = {"workload": w.describe(), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq,
+               "d": w.d, "page_size": w.page_size, "seed": w.seed}
+        dtype = "f64"
+    elif wl in FWD_WORKLOADS:
+        w = FWD_WORKLOADS[wl]
+        _, _, _, _, offs = make_inputs(w, with_dout=False)
+        samples = [cpu_baseline_forward(w, offs, seconds=0.0) for _ in range(args.steps)]
+        metric = "attention forward TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 peak"
+        if wl.startswith("fp8"):
+            metric = "attention FP8 forward TFLOP/s (unmasked FLOPs) and % of GB300 dense FP8 peak"
+        cfg = workload_config(w)
+        dtype = "f64"
+    else:
+        w = REFERENCE_WORKLOADS.get(wl, CAUSAL_FWD_BWD)
+        samples = [cpu_baseline(w, seconds=0.0, heads=1) for _ in range(args.steps)]
+        metric = METRIC
+        cfg = workload_config(w)
+        dtype = "f64"
+    # every sample is one step: the line's value is total work over total time
+    secs = [c["seconds"] for c in samples]
+    value = sum(c["value"] * c["seconds"] for c in samples) / max(sum(secs), 1e-9)
+    unit = samples[0]["unit"]
+    ms = statistics.mean(secs) * 1e3
+    cfg["sample"] = samples[0]["sample"] + " per step"
+    line = {"impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded randn rounded to bf16)",
-            "config": workload_config(w, {"sample": "1 of 32 heads per step"}),
-            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(),
-                             "kind": "oracle",
-                             "sample": "1 of 32 heads (full N=8192), forward + backward per step"},
-            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+            "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic (seeded randn rounded to bf16)", "config": cfg,
+            "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": cfg["sample"]},
+            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def run_cpu_replica_check(args):
+    """The replica launcher and the cross-rank reduction on CPU: gloo ranks, each timing
+    args.steps float64 256 x 256 matmuls; the job time is the maximum over ranks and the
+    value sums the ranks' work over it, as in the GPU lines."""
+    world, rank, _ = init_ranks(args, backend="gloo")
+    a = np.random.default_rng(rank).standard_normal((256, 256))
+    for _ in range(args.warmup):
+        a @ a
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        a @ a
+    ms = (time.perf_counter() - t0) * 1e3
+    ms_rank = ms
+    if world > 1:
+        ms = max_over_ranks(ms, "cpu")
+    work = 2.0 * 256 ** 3 * args.steps
+    line = {"metric": "cpu replica check: GFLOP/s of float64 256x256 matmuls",
+            "value": round(world * work / (ms * 1e-3) / 1e9, 4), "unit": "GFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms / args.steps, 6), "higher_is_better": True,
+            "scaling": "weak", "rank0_ms": round(ms_rank, 6),
+            "config": {"workload": "cpu replica check", "parallelism": f"replicas x{world}"}}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def main():
@@ -682,16 +874,23 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--min-seconds", type=float, default=2.0)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="fwd_bwd",
                     choices=["fwd_bwd", "fwd_bwd_dropout", "fwd_bwd_d256", *FWD_WORKLOADS,
-                             "paged_decode"])
+                             "paged_decode", "cpu_replica_check"])
     args = ap.parse_args()
+    if args.gpus < 1 or args.steps < 1:
+        raise SystemExit("bench.py: --gpus and --steps must be at least 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        raise SystemExit(launch_replicas(args.gpus, sys.argv[1:]))
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "cpu_replica_check":
+        run_cpu_replica_check(args)
     elif args.workload == "paged_decode":
         run_decode(args, PAGED_DECODE)
     elif args.workload == "fwd_bwd_dropout":

@@ -8,5 +8,5 @@ from .attention import (MASK_CAUSAL, MASK_DOCUMENT_CAUSAL, MASK_NONE,  # noqa: F
                         bwd_workspace_size, classify_tiles, device_status, forward, fwd_into,
                         FP8_TILES, FP8_V_TRANSPOSED, fp8_inputs, forward_fp8, fwd_fp8_into,
                         quantize_fp8, decode_paged, decode_paged_into, decode_split_keys,
-                        decode_workspace_size, selftest_wait_timeout)
+                        decode_workspace_size, selftest_wait_timeout, check_doc_offsets)
 from ._lib import AttnError  # noqa: F401

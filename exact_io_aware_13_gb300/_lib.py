@@ -55,6 +55,7 @@ SIGNATURES = {
                                                      _P]),
     "attn_decode_workspace_size": (ctypes.c_size_t, [_I] * 7),
     "attn_decode_split_keys": (_I, [_I, _I, _I, _I, ctypes.c_longlong, _I]),
+    "attn_check_doc_offsets": (_I, [_P, _I, _I, _P]),
     "attn_device_status": (_I, [_P]),
     "attn_selftest_wait_timeout": (_I, [_P]),
     "attn_strerror": (ctypes.c_char_p, [_I]),

@@ -222,6 +222,16 @@ def classify_tiles(mask_kind: int, Nq: int, Nkv: int, *, window: int = 0, doc_of
     return out
 
 
+def check_doc_offsets(doc_offsets: torch.Tensor, N: int, stream=None) -> None:
+    """Queue the device check of a document-offsets table (attn_check_doc_offsets); a
+    bad table shows up as ATTN_ERR_DEVICE_INPUT (8) in the next device_status()."""
+    _check_tensors(doc_offsets)
+    _check_dtypes((doc_offsets, torch.int32, "doc_offsets"))
+    _lib.check(_lib.load().attn_check_doc_offsets(_ptr(doc_offsets), doc_offsets.numel() - 1,
+                                                  int(N), _stream(stream)),
+               "attn_check_doc_offsets")
+
+
 def device_status(stream=None) -> int:
     """Synchronise and return the library's device status (0 = no kernel gave up)."""
     return int(_lib.load().attn_device_status(_stream(stream)))

@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -31,6 +32,19 @@ __global__ void selftest_wait_kernel(int* status) {
   WaitCtx wc{&abort_flag, status};
   if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, wc);
   __syncwarp();
+}
+
+
+// Check of a document-offsets table, one thread per entry: offs[0] = 0, non-decreasing,
+// offs[n_docs] = n. A violation sets DEV_BAD_INPUT in the status word. Reads only
+// offs[0 .. n_docs].
+__global__ void doc_offsets_check_kernel(const int32_t* offs, int n_docs, int n, int* status) {
+  const long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k > n_docs) return;
+  const int v = offs[k];
+  const bool bad = (k == 0 && v != 0) || (k == n_docs && v != n) ||
+                   (k < n_docs && offs[k + 1] < v);
+  if (bad) atomicOr(status, DEV_BAD_INPUT);
 }
 
 
@@ -163,6 +177,32 @@ attn_status make_map(CUtensorMap* map, const void* base, int BH, int N, int d,
 
 attn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH; }
 
+// Checked mode: the environment variable ATTN_CHECKED, set to anything but "" or "0"
+// when the library first looks at it, makes every call with the document mask check
+// its offsets on the device before its own kernels (a debugging aid: the table is
+// otherwise trusted).
+bool checked_mode() {
+  static const bool on = [] {
+    const char* e = std::getenv("ATTN_CHECKED");
+    return e != nullptr && *e != '\0' && std::strcmp(e, "0") != 0;
+  }();
+  return on;
+}
+
+attn_status launch_doc_check(const int32_t* offs, int n_docs, int n, int* status,
+                             cudaStream_t st) {
+  constexpr int kThreadsPerBlock = 256;
+  const long long blocks = ((long long)n_docs + kThreadsPerBlock) / kThreadsPerBlock;
+  if (blocks > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  doc_offsets_check_kernel<<<(int)blocks, kThreadsPerBlock, 0, st>>>(offs, n_docs, n, status);
+  return from_cuda(cudaGetLastError());
+}
+
+attn_status maybe_check_docs(const Problem& p, const DeviceInfo* dev, cudaStream_t st) {
+  if (p.mask.kind != ATTN_MASK_DOCUMENT_CAUSAL || !checked_mode()) return ATTN_OK;
+  return launch_doc_check(p.mask.doc, p.mask.n_docs, p.mask.nq, dev->status, st);
+}
+
 attn_status fwd_common(bool simt, const void* q, const void* k, const void* v, void* o,
                        float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int d, float scale,
                        int mask_kind, const attn_mask_params* mp, int score_kind,
@@ -183,6 +223,7 @@ attn_status fwd_common(bool simt, const void* q, const void* k, const void* v, v
   if ((s = current_device(&dev)) != ATTN_OK) return s;
   p.status = dev->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = maybe_check_docs(p, dev, st)) != ATTN_OK) return s;
   auto* ob = static_cast<__nv_bfloat16*>(o);
   if (Nkv == 0) return from_cuda(launch_fill_masked(rows_q, d, ob, lse, st));
   const auto* qb = static_cast<const __nv_bfloat16*>(q);
@@ -240,6 +281,7 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
   if ((s = current_device(&dev)) != ATTN_OK) return s;
   p.status = dev->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = maybe_check_docs(p, dev, st)) != ATTN_OK) return s;
   // With no queries nothing reaches the keys, and with no keys nothing reaches the
   // queries: those gradients are zero.
   if (rows_q == 0 || rows_k == 0) {
@@ -473,6 +515,7 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const 
   if ((s = current_device(&dev)) != ATTN_OK) return s;
   p.status = dev->status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = maybe_check_docs(p, dev, st)) != ATTN_OK) return s;
   auto* ob = static_cast<__nv_bfloat16*>(o);
   if (Nkv == 0) return from_cuda(launch_fill_masked(rows_q, d, ob, lse, st));
   CUtensorMap tq, tk, tvt;
@@ -600,7 +643,19 @@ attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_para
   if (!classes) return ATTN_ERR_ARG;
   DeviceInfo* dev = nullptr;
   if ((s = current_device(&dev)) != ATTN_OK) return s;
-  return from_cuda(launch_classify(p.mask, classes, static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = maybe_check_docs(p, dev, st)) != ATTN_OK) return s;
+  return from_cuda(launch_classify(p.mask, classes, st));
+}
+
+attn_status attn_check_doc_offsets(const int32_t* doc_offsets, int n_docs, int N,
+                                   void* stream) {
+  if (!doc_offsets || n_docs < 1 || N < 0) return ATTN_ERR_ARG;
+  if (!aligned4(doc_offsets)) return ATTN_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  attn_status s = current_device(&dev);
+  if (s != ATTN_OK) return s;
+  return launch_doc_check(doc_offsets, n_docs, N, dev->status, static_cast<cudaStream_t>(stream));
 }
 
 attn_status attn_selftest_wait_timeout(void* stream) {

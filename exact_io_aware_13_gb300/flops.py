@@ -33,6 +33,30 @@ def allowed_pairs(mask_kind: int, Nq: int, Nkv: int, window: int = 0,
     raise ValueError(mask_kind)
 
 
+def allowed_pairs_rows(mask_kind: int, rows: Sequence[int], Nkv: int, window: int = 0,
+                       doc_offsets: Optional[Sequence[int]] = None) -> int:
+    """Allowed pairs of the given query rows of one head (row by row, closed form per row)."""
+    offs = None if doc_offsets is None else [int(x) for x in doc_offsets]
+    total = 0
+    doc = 0
+    for i in sorted(int(r) for r in rows):
+        if mask_kind == MASK_NONE:
+            total += Nkv
+        elif mask_kind == MASK_CAUSAL:
+            total += max(0, min(i, Nkv - 1) + 1)
+        elif mask_kind == MASK_SLIDING_WINDOW:
+            lo, hi = max(0, i - max(window, 0) + 1), min(i, Nkv - 1)
+            total += max(0, hi - lo + 1)
+        elif mask_kind == MASK_DOCUMENT_CAUSAL:
+            while doc + 1 < len(offs) and offs[doc + 1] <= i:
+                doc += 1
+            if doc + 1 < len(offs) and offs[doc] <= i:
+                total += i - offs[doc] + 1
+        else:
+            raise ValueError(mask_kind)
+    return total
+
+
 def attention_flops(B: int, Hq: int, d: int, pairs_per_head: int, backward: bool) -> float:
     per_pair = (10 if backward else 4) * d
     return float(B) * Hq * pairs_per_head * per_pair

@@ -38,7 +38,10 @@
  *                                    given by int32 DEVICE offsets
  *                                    doc_offsets[0..n_docs]: doc_offsets[0] = 0,
  *                                    non-decreasing, doc_offsets[n_docs] = Nq = Nkv.
- *                                    The offsets are trusted (not read on the host).
+ *                                    The offsets are trusted (not read on the host);
+ *                                    attn_check_doc_offsets checks a table, and the
+ *                                    checked mode (ATTN_CHECKED, below) checks it in
+ *                                    every call.
  *     A query row with no allowed key gets O = 0 and lse = -inf, and zero gradients.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream). They allocate no device memory; the backward pass takes a
@@ -328,6 +331,25 @@ int attn_decode_split_keys(int B, int Hq, int Hkv, int Nq, long long total_kv_to
  */
 attn_status attn_classify_tiles(int mask_kind, const attn_mask_params* mask_params,
                                 int Nq, int Nkv, int32_t* classes, void* stream);
+
+/*
+ * Checks a document-offsets table on the device: doc_offsets[0] = 0, non-decreasing,
+ * doc_offsets[n_docs] = N (the contract of ATTN_MASK_DOCUMENT_CAUSAL). A violation is
+ * not returned here (the table is device memory and the call is asynchronous): it is
+ * recorded in the device status word, which the next attn_device_status reports as
+ * ATTN_ERR_DEVICE_INPUT. Reads doc_offsets[0 .. n_docs] only (DEVICE int32, 4-byte
+ * aligned). Returns ATTN_ERR_ARG for a null pointer, n_docs < 1 or N < 0.
+ *
+ * Checked mode: when the environment variable ATTN_CHECKED holds a value other than
+ * "" or "0" at the library's first look at it (once per process), every call with
+ * ATTN_MASK_DOCUMENT_CAUSAL (attn_fwd, attn_bwd and their variants, attn_fwd_fp8,
+ * attn_classify_tiles) first runs this check on its table, in stream order before its
+ * own kernels. The kernels of a call still run on a bad table; they read and write
+ * only inside their buffers whatever the offsets hold, but their results are then
+ * meaningless. The mode is for debugging; by default the table is trusted.
+ */
+attn_status attn_check_doc_offsets(const int32_t* doc_offsets, int n_docs, int N,
+                                   void* stream);
 
 /*
  * Plain CUDA-core versions of the forward and backward passes (one thread per

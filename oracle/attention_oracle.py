@@ -241,12 +241,6 @@ def backward(q, k, v, dout, scale: float, mask_kind: int = MASK_NONE, window: in
     return dq, dk, dv
 
 
-def row_sum_dout_out(dout, out) -> np.ndarray:
-    """D_i = sum_c dO_ic O_ic, which equals sum_j P_ij dP_ij (the backward's row
-    term). Returned in float64 for the given tensors."""
-    return (_f64(dout) * _f64(out)).sum(axis=-1)
-
-
 def classify_tiles(mask_kind: int, Nq: int, Nkv: int, tile_q: int, tile_k: int,
                    window: int = 0, doc_offsets=None) -> np.ndarray:
     """Per (q-tile, kv-tile) class by brute force over every (i, j) in the tile:

@@ -2,14 +2,20 @@
 seeded inputs and compare with the stated tolerances.
 
 Tolerances (bf16 inputs, fp32 accumulation):
-  forward : |O - O_ref| <= 1e-2 + half a bf16 ulp of O_ref, per element: O is stored as
-            bf16 (8 significant bits), whose rounding alone reaches 0.008 for |O| in
-            [2, 4) and 0.016 in [4, 8), so the 1e-2 bounds the error before that last
-            rounding;
+  forward : max|O - O_ref| <= 1e-2, flat, on every element with |O_ref| < 4. O is stored
+            as bf16 (8 significant bits); for |O_ref| >= 4 that storage rounding alone
+            reaches 2^-6 = 0.0156 > 1e-2, so there (and only there) the bound is
+            1e-2 + half a bf16 ulp of O_ref. Every check records its flat max|O - O_ref|,
+            and the session summary prints the largest (tests/conftest.py);
             max|LSE - LSE_ref| <= 1e-3 on finite entries, and -inf exactly where the
-            oracle has -inf. With dropout at rate p the kept terms are scaled by
-            1 / (1 - p) after the same per-element rounding of P, so the 1e-2 becomes
-            1e-2 / (1 - p);
+            oracle has -inf.
+            With dropout at rate p the kept terms of a row are multiplied by 1 / (1 - p),
+            so the output's own scale grows with them. The bound is stated relative to
+            that scale, per element: |O_ic - O_ref_ic| <= 1e-2 * max(1, A_ic) with
+            A_ic = sum_j (P_ij Z_ij / (1 - p)) |V_jc|, the magnitude of the terms summed
+            into O_ic (the oracle's forward with |V| in place of V). The kernel's own
+            error is at most 2^-9 A_ic from the bf16 rounding of P plus 2^-9 |O_ic| from
+            the storage of O, i.e. below 0.004 A_ic.
   backward: max|dX - dX_ref| <= 2e-2 * max|dX_ref| + 1e-5 for each of dq, dk, dv.
             The 1e-5 floor only matters where the exact gradient vanishes (one allowed
             key per row: P = 1 and dP - D = 0): there the kernels leave fp32
@@ -26,6 +32,7 @@ import oracle
 from workloads import MASK_DOCUMENT_CAUSAL, Workload, make_inputs
 
 O_TOL = 1e-2
+O_FLAT_BELOW = 4.0   # |O_ref| below which the forward bound is the flat O_TOL
 LSE_TOL = 1e-3
 GRAD_REL_TOL = 2e-2
 GRAD_ABS_FLOOR = 1e-5
@@ -61,17 +68,36 @@ def bf16_half_ulp(x):
     return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
 
 
-def check_forward(o, lse, o_ref, lse_ref, what="", o_tol=O_TOL):
+# (what, flat max|O - O_ref| over |O_ref| < 4, elements checked, elements at |O_ref| >= 4)
+# of every forward check in this process; tests/conftest.py prints the summary.
+FORWARD_LOG: list = []
+
+
+def check_forward(o, lse, o_ref, lse_ref, what="", o_scale=None):
+    """Forward parity. Without ``o_scale``: flat |O - O_ref| <= 1e-2 where |O_ref| < 4,
+    1e-2 + half a bf16 ulp of O_ref elsewhere. With ``o_scale`` (dropout: the per-element
+    output scale A, see the module docstring): |O - O_ref| <= 1e-2 * max(1, A)."""
     o = np.asarray(o, dtype=np.float64)
     lse = np.asarray(lse, dtype=np.float64)
     assert o.shape == o_ref.shape and lse.shape == lse_ref.shape
-    over = float((np.abs(o - o_ref) - bf16_half_ulp(o_ref)).max()) if o.size else 0.0
-    err_o = float(np.abs(o - o_ref).max()) if o.size else 0.0
+    err = np.abs(o - o_ref)
+    flat = np.abs(o_ref) < O_FLAT_BELOW
+    flat_max = float(err[flat].max()) if flat.any() else 0.0
+    err_o = float(err.max()) if o.size else 0.0
+    if o_scale is None:
+        bound = np.where(flat, O_TOL, O_TOL + bf16_half_ulp(o_ref))
+    else:
+        bound = O_TOL * np.maximum(1.0, np.asarray(o_scale, dtype=np.float64))
+    FORWARD_LOG.append((what, flat_max, int(o.size), int((~flat).sum())))
     ninf_ref = np.isneginf(lse_ref)
     assert (np.isneginf(lse) == ninf_ref).all(), f"{what}: -inf pattern of LSE differs"
     fin = ~ninf_ref
     err_l = float(np.abs(lse[fin] - lse_ref[fin]).max()) if fin.any() else 0.0
-    assert over <= o_tol, f"{what}: max(|dO| - bf16 half-ulp) = {over} (max|dO| = {err_o})"
+    if o.size:
+        worst = np.unravel_index(np.argmax(err - bound), err.shape)
+        assert (err <= bound).all(), (
+            f"{what}: |dO| = {err[worst]} > bound {bound[worst]} at {worst} "
+            f"(O_ref {o_ref[worst]}); flat max|dO| over |O_ref| < 4 = {flat_max}")
     assert err_l <= LSE_TOL, f"{what}: max|dLSE| = {err_l}"
     return err_o, err_l
 

@@ -82,3 +82,79 @@ def test_reference_arm_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["metric"] == bench.METRIC
+
+
+def _bench(*argv, env=None, timeout=600):
+    e = dict(os.environ)
+    for key in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        e.pop(key, None)
+    e.update(env or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *argv],
+                          capture_output=True, text=True, timeout=timeout, cwd=ROOT, env=e)
+
+
+def test_gpus_n_launches_n_replicas():
+    """`bench.py --gpus 2` started without a launcher starts two ranks itself (the same
+    torch.distributed.run entry the driver uses); the line reports n_gpus 2, the job time
+    is the slower rank's and the value sums both replicas' work over it. The step is the
+    CPU check workload (gloo ranks, no GPU)."""
+    r = _bench("--gpus", "2", "--workload", "cpu_replica_check", "--steps", "20",
+               "--warmup", "1")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1  # rank 0 alone prints
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["config"]["parallelism"] == "replicas x2"
+    work = 2.0 * 256 ** 3 * 20
+    ms_total = line["ms_per_step"] * 20
+    assert ms_total >= line["rank0_ms"] - 1e-4          # max over ranks (6-digit rounding)
+    assert abs(line["value"] - 2 * work / (ms_total * 1e-3) / 1e9) <= 1e-3 * line["value"]
+
+
+def test_world_size_must_match_gpus():
+    r = _bench("--gpus", "2", "--workload", "cpu_replica_check",
+               env={"WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    assert r.returncode != 0 and "WORLD_SIZE=1" in r.stderr
+
+
+def test_repeat_timed_covers_min_seconds(monkeypatch):
+    """The timed region (K steps) is repeated until its GPU time reaches --min-seconds."""
+    import types
+
+    class Quiet:
+        def __init__(self, index):
+            pass
+
+        def __enter__(self):
+            return self
+
+        def __exit__(self, *exc):
+            pass
+
+        def summary(self):
+            return {"samples": 0}
+
+    monkeypatch.setattr(bench, "ClockSampler", Quiet)
+    calls = []
+
+    def rep():  # 4 steps of 3 kernels, 25 ms per step
+        calls.append(1)
+        return [[10.0, 5.0, 10.0] for _ in range(4)]
+
+    args = types.SimpleNamespace(min_seconds=1.0, steps=4)
+    rows, n, _ = bench.repeat_timed(args, 1, types.SimpleNamespace(index=0), rep)
+    assert n == 10 and len(calls) == 10 and len(rows) == 40  # 10 x 100 ms >= 1 s
+    args.min_seconds = 0.0
+    rows, n, _ = bench.repeat_timed(args, 1, types.SimpleNamespace(index=0), rep)
+    assert n == 1 and len(rows) == 4
+
+
+def test_reference_arm_follows_the_workload():
+    """The reference arm of a forward-only workload times the oracle's forward on blocks
+    of query rows, with the forward metric."""
+    r = _bench("--impl", "reference", "--workload", "tiny_fwd", "--steps", "2", "--warmup", "1")
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 2
+    assert line["metric"].startswith("attention forward TFLOP/s")
+    assert "query rows" in line["cpu_baseline"]["sample"]

@@ -5,8 +5,8 @@ of a row gets the same probability, V (and dO) one-hot in the key (query) positi
 128 and a sliding window of 128 keys put each (query, key) pair of the band in its own
 output element, so O is nonzero exactly where the forward kept the pair and dV exactly
 where the backward's dK/dV kernel regenerated a kept pair. The values are checked with
-the forward/backward tolerances of the other parity tests, for every mask and score
-variant, d = 64 and 128, GQA, ragged and unequal lengths, several rates, and the
+the forward bound relative to each output element's scale (tests/helpers.py states it)
+and the backward tolerance of the other parity tests, for every mask and score variant, d = 64 and 128, GQA, ragged and unequal lengths, several rates, and the
 fwd+bwd workload at full size on a sampled kv head."""
 import numpy as np
 import pytest
@@ -32,9 +32,18 @@ def _drop(w, p, seed):
     return w.replace(dropout_p=p, dropout_seed=seed)
 
 
-def _check_forward(w, o, lse, o_ref, l_ref, what):
-    """The forward tolerance magnified by the 1 / (1 - p) that scales the kept terms."""
-    H.check_forward(o, lse, o_ref, l_ref, what, o_tol=H.O_TOL / (1.0 - w.dropout_p))
+def _oracle(w, inputs, rows=None, heads=None):
+    """Oracle O and LSE plus each element's output scale A = (P Z / (1 - p)) |V|: the
+    oracle's forward with |V| in place of V (same mask, same keep mask)."""
+    o_ref, l_ref = H.oracle_forward(w, inputs, rows=rows, heads=heads)
+    q, k, v, do, offs = inputs
+    a_ref, _ = H.oracle_forward(w, (q, k, v.float().abs(), do, offs), rows=rows, heads=heads)
+    return o_ref, l_ref, a_ref
+
+
+def _check_forward(w, o, lse, o_ref, l_ref, a_ref, what):
+    """|dO| <= 1e-2 * max(1, A) per element: the bound relative to the output's scale."""
+    H.check_forward(o, lse, o_ref, l_ref, what, o_scale=a_ref)
 
 
 def test_keep_mask_bit_exact_forward_and_dkdv():
@@ -83,7 +92,7 @@ def test_dropout_variants(mask, score, d):
     w = _drop(w, 0.2, 1000 + mask)
     inputs = make_inputs(w, with_dout=True)
     o, lse = H.run_forward(w, "tc", inputs)
-    _check_forward(w, o, lse, *H.oracle_forward(w, inputs), w.name)
+    _check_forward(w, o, lse, *_oracle(w, inputs), w.name)
     H.check_grads(H.run_backward(w, "tc", inputs), H.oracle_backward(w, inputs), w.name)
 
 
@@ -94,7 +103,7 @@ def test_dropout_rates_gqa(p):
     w = _drop(w, p, 77)
     inputs = make_inputs(w, with_dout=True)
     o, lse = H.run_forward(w, "tc", inputs)
-    _check_forward(w, o, lse, *H.oracle_forward(w, inputs), w.name)
+    _check_forward(w, o, lse, *_oracle(w, inputs), w.name)
     H.check_grads(H.run_backward(w, "tc", inputs), H.oracle_backward(w, inputs), w.name)
 
 
@@ -110,7 +119,7 @@ def test_dropout_unequal_lengths(nq, nkv):
     w = _drop(w, 0.5, 5)
     inputs = make_inputs(w, with_dout=True)
     o, lse = H.run_forward(w, "tc", inputs)
-    _check_forward(w, o, lse, *H.oracle_forward(w, inputs), w.name)
+    _check_forward(w, o, lse, *_oracle(w, inputs), w.name)
     H.check_grads(H.run_backward(w, "tc", inputs), H.oracle_backward(w, inputs), w.name)
 
 
@@ -192,10 +201,10 @@ def test_dropout_full_size_sampled_kv_head():
     rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 4096, w.Nq - 1],
                                      rng.integers(0, w.Nq, 24)]))
     heads = [(0, 3), (w.B - 1, w.Hq - 1)]
-    o_ref, l_ref = H.oracle_forward(w, inputs, rows=rows, heads=heads)
+    o_ref, l_ref, a_ref = _oracle(w, inputs, rows=rows, heads=heads)
     for b, h in heads:
         _check_forward(w, o[b, h][rows], lse[b, h][rows], o_ref[b, h], l_ref[b, h],
-                       f"{w.name} b={b} h={h}")
+                       a_ref[b, h], f"{w.name} b={b} h={h}")
     got = H.run_backward(w, "tc", inputs)
     b, g = w.B - 1, 5
     ref = H.oracle_backward(w, inputs, kv_heads=[(b, g)])
