@@ -2,11 +2,18 @@
 seeded inputs and compare with the stated tolerances.
 
 Tolerances (bf16 inputs, fp32 accumulation):
-  forward : max|O - O_ref| <= 1e-2, flat, on every element with |O_ref| < 4. O is stored
-            as bf16 (8 significant bits); for |O_ref| >= 4 that storage rounding alone
-            reaches 2^-6 = 0.0156 > 1e-2, so there (and only there) the bound is
-            1e-2 + half a bf16 ulp of O_ref. Every check records its flat max|O - O_ref|,
-            and the session summary prints the largest (tests/conftest.py);
+  forward : max|O - O_ref| <= 1e-2, flat, on every element with |O_ref| < 2, and
+            1e-2 + half a bf16 ulp of O_ref where |O_ref| >= 2. The method's own
+            arithmetic sets that edge: O is stored as bf16 (8 significant bits), whose
+            rounding alone is up to 2^-9 |O| (0.0039 below 2, 0.0078 in [2, 4), 0.0156
+            in [4, 8)), and P is rounded to bf16 for the P V product, which adds up to
+            2^-9 sum_j P_ij |V_jc|, about 2^-9 |O| in the rows where |O| is large (a few
+            keys carry the weight). Below 2 the two stay under 1e-2; from 2 on their
+            sum can pass it (storage 0.0078 + P 0.004 at |O| = 2.5), and a float64
+            model of exactly that rounding (fp32 softmax, P rounded once, O rounded once)
+            reproduces the kernels' largest errors there to five digits. Every check
+            records its flat max|O - O_ref| over |O_ref| < 2 and over |O_ref| < 4, and
+            the session summary prints the largest (tests/conftest.py);
             max|LSE - LSE_ref| <= 1e-3 on finite entries, and -inf exactly where the
             oracle has -inf.
             With dropout at rate p the kept terms of a row are multiplied by 1 / (1 - p),
@@ -32,7 +39,7 @@ import oracle
 from workloads import MASK_DOCUMENT_CAUSAL, Workload, make_inputs
 
 O_TOL = 1e-2
-O_FLAT_BELOW = 4.0   # |O_ref| below which the forward bound is the flat O_TOL
+O_FLAT_BELOW = 2.0   # |O_ref| below which the forward bound is the flat O_TOL
 LSE_TOL = 1e-3
 GRAD_REL_TOL = 2e-2
 GRAD_ABS_FLOOR = 1e-5
@@ -68,27 +75,32 @@ def bf16_half_ulp(x):
     return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
 
 
-# (what, flat max|O - O_ref| over |O_ref| < 4, elements checked, elements at |O_ref| >= 4)
-# of every forward check in this process; tests/conftest.py prints the summary.
+# (what, flat max|O - O_ref| over |O_ref| < 2, the same over |O_ref| < 4, elements
+# checked, elements at 2 <= |O_ref| < 4 with |O - O_ref| > 1e-2) of every forward check
+# in this process; tests/conftest.py prints the summary.
 FORWARD_LOG: list = []
 
 
 def check_forward(o, lse, o_ref, lse_ref, what="", o_scale=None):
-    """Forward parity. Without ``o_scale``: flat |O - O_ref| <= 1e-2 where |O_ref| < 4,
+    """Forward parity. Without ``o_scale``: flat |O - O_ref| <= 1e-2 where |O_ref| < 2,
     1e-2 + half a bf16 ulp of O_ref elsewhere. With ``o_scale`` (dropout: the per-element
     output scale A, see the module docstring): |O - O_ref| <= 1e-2 * max(1, A)."""
     o = np.asarray(o, dtype=np.float64)
     lse = np.asarray(lse, dtype=np.float64)
     assert o.shape == o_ref.shape and lse.shape == lse_ref.shape
     err = np.abs(o - o_ref)
-    flat = np.abs(o_ref) < O_FLAT_BELOW
+    mag = np.abs(o_ref)
+    flat = mag < O_FLAT_BELOW
     flat_max = float(err[flat].max()) if flat.any() else 0.0
+    below4 = mag < 4.0
+    max4 = float(err[below4].max()) if below4.any() else 0.0
+    over_2_4 = int(((mag >= O_FLAT_BELOW) & below4 & (err > O_TOL)).sum())
     err_o = float(err.max()) if o.size else 0.0
     if o_scale is None:
         bound = np.where(flat, O_TOL, O_TOL + bf16_half_ulp(o_ref))
     else:
         bound = O_TOL * np.maximum(1.0, np.asarray(o_scale, dtype=np.float64))
-    FORWARD_LOG.append((what, flat_max, int(o.size), int((~flat).sum())))
+    FORWARD_LOG.append((what, flat_max, max4, int(o.size), over_2_4, o_scale is not None))
     ninf_ref = np.isneginf(lse_ref)
     assert (np.isneginf(lse) == ninf_ref).all(), f"{what}: -inf pattern of LSE differs"
     fin = ~ninf_ref
@@ -97,7 +109,7 @@ def check_forward(o, lse, o_ref, lse_ref, what="", o_scale=None):
         worst = np.unravel_index(np.argmax(err - bound), err.shape)
         assert (err <= bound).all(), (
             f"{what}: |dO| = {err[worst]} > bound {bound[worst]} at {worst} "
-            f"(O_ref {o_ref[worst]}); flat max|dO| over |O_ref| < 4 = {flat_max}")
+            f"(O_ref {o_ref[worst]}); flat max|dO| over |O_ref| < 2 = {flat_max}")
     assert err_l <= LSE_TOL, f"{what}: max|dLSE| = {err_l}"
     return err_o, err_l
 
