@@ -19,16 +19,16 @@ constexpr int kRelayWarp = kEwWarps + 2;  // turns TMA completions into barrier 
 // Named barriers (the MMA warp waits only on these; see nb_sync in ptx.cuh):
 //   kNbStage + s   ring stage s loaded: relay warp (32) + MMA warp (32)
 //   dq:   kNbP + x     dS_x written to TMEM: pair x (256 threads) + MMA warp (32)
-//   dkdv: kNbKvRel     S^T / dP^T of the sub-step read: element-wise warps + MMA warp
-//         kNbKvP + x   P^T / dS^T of a sub-step u (x = u % 2) written: same threads
-//         kNbKvK       K tile written to tensor memory: same threads
+//   dkdv: kNbKvP + x   P^T / dS^T of a sub-step u (x = u % 2) written over S^T / dP^T of
+//                      buffer x: element-wise warps + MMA warp
+//   d=256 kernels: kNbKvRel, kNbKvP + x, kNbKvK (bwd256_tc.cu)
 //   dq:   kNbQL        Q and dO tiles written to tensor memory: element-wise warps + MMA warp
 constexpr uint32_t kNbP = 1, kNbPCount = 288;
 constexpr uint32_t kNbStage = 3, kNbStageCount = 64;
 constexpr uint32_t kNbKvRel = 9, kNbKvP = 10, kNbKvK = 12, kNbQL = 13;
 constexpr uint32_t kNbKvCount = (kEwWarps + 1) * 32;
 constexpr int kStagesQ = 6;      // dq ring depth, in sub-steps
-constexpr int kStagesKv = 5;     // dkdv ring depth
+constexpr int kStagesKv = 4;     // dkdv ring depth (its K and V tiles are fixed in smem)
 constexpr int kMaxStages = 6;
 // Stage barriers take IDs kNbStage .. kNbStage + kMaxStages - 1; the others must not
 // overlap them (one hardware barrier, one thread count), and IDs end at 15.
@@ -44,10 +44,16 @@ __device__ __forceinline__ uint32_t col_s(int x) { return x * 64; }
 __device__ __forceinline__ uint32_t col_dp(int x) { return 128 + x * 64; }
 constexpr uint32_t kColAcc = 256, kColQ = 384;
 template <int D> constexpr uint32_t col_do() { return kColQ + D / 2; }
-// Tensor memory columns of dkdv: S^T, dP^T (64 each), P^T / dS^T (bf16 pairs: P^T in
-// the first 32 columns, dS^T in the next 32), the K tile (bf16 pairs, A operand of
-// S^T = K Q^T), then dV and dK.
+// Tensor memory columns of the d = 256 dK/dV walks (bwd256_tc.cu): S^T, dP^T (64 each),
+// P^T / dS^T (bf16 pairs: P^T in the first 32 columns, dS^T in the next 32), the K tile
+// (bf16 pairs, A operand of S^T = K Q^T), then the accumulator.
 constexpr uint32_t kKvColS = 0, kKvColDP = 64, kKvColPD = 128, kKvColK = 192, kKvColAcc = 256;
+// Tensor memory columns of dkdv (head dimension 64 and 128): two buffers x of S^T and dP^T
+// (64 columns each; P^T and dS^T are written as bf16 pairs over the first half of each
+// warpgroup's 16 columns of them), then dV and dK.
+__device__ __forceinline__ uint32_t kv_col_s(int x) { return x * 128; }
+__device__ __forceinline__ uint32_t kv_col_dp(int x) { return x * 128 + 64; }
+constexpr uint32_t kKv2ColAcc = 256;
 
 // Element-wise constants: s2 = x*k1 + kb*(j - i) (log2 units), then the soft-cap.
 struct ScoreK {
@@ -136,9 +142,9 @@ __device__ __forceinline__ void dropout_flags_dq(const Problem& p, const DropThr
 }
 
 // Shared-memory layouts. dq: a ring of kS stages, each holding a 64-row slice of K and
-// V (Q and dO live in tensor memory). dkdv: the V tile (fixed; K lives in tensor
-// memory), a ring of 64-row slices of Q and dO, and each stage's row terms of those 64
-// query rows (lse2, delta, first key: 256 bytes each).
+// V (Q and dO live in tensor memory). dkdv: the V and K tiles (fixed, in that order), a
+// ring of 64-row slices of Q and dO, and each stage's row terms of those 64 query rows
+// (lse2, delta, first key: 256 bytes each).
 template <int D, int kS, int kFixTiles, bool kRowTerms>
 struct Layout {
   static constexpr int kStageCount = kS;
@@ -155,7 +161,7 @@ struct Layout {
   static constexpr int kAlloc = kBars + 256 + 1024;
 };
 template <int D> using LayoutQ = Layout<D, kStagesQ, 0, false>;
-template <int D> using LayoutKv = Layout<D, kStagesKv, 1, true>;
+template <int D> using LayoutKv = Layout<D, kStagesKv, 2, true>;  // fixed: V, then K
 static_assert(LayoutKv<128>::kAlloc <= 232448 && LayoutQ<128>::kAlloc <= 232448,
               "shared memory per CTA");
 
@@ -269,6 +275,21 @@ __device__ __forceinline__ void mma_pd_x_slice(bool pred, uint32_t d_tmem, uint3
               (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// D[128 x D] (+)= A_tmem[128 x 64] B[64 x D] with A written in place over a 64-column
+// fp32 buffer: k-step kk (16 rows of B) reads A columns [16 kk, 16 kk + 8), the bf16 pairs
+// the kk-th element-wise warpgroup wrote over the first half of its 16 columns. B as in
+// mma_tmem64_x_slice.
+template <int D>
+__device__ __forceinline__ void mma_inplace_x_slice(bool pred, uint32_t d_tmem, uint32_t a_tmem,
+                                                    uint32_t b, bool accumulate) {
+  constexpr uint32_t id = idesc_bf16_f32(BT, D, false, true);
+  const uint64_t db = smem_desc_sw128(b, SUB * 128, 1024);
+#pragma unroll
+  for (int kk = 0; kk < SUB / 16; ++kk)
+    mma_ts_if(pred, d_tmem, a_tmem + kk * 16, db + ((kk * 16 * 128) >> 4), id,
+              (accumulate || kk > 0) ? 1u : 0u);
+}
+
 // Write one accumulator row (D fp32 columns at TMEM `t`) times `mul` as bf16.
 // tcgen05.ld is warp-collective: every lane of the warp must call this with the same
 // `live`; `store` (per lane) only decides whether the row is written.
@@ -311,17 +332,22 @@ __device__ __forceinline__ void load_loop(uint8_t* smem, BwdBars* bars, const Wa
                                           int lane, const CUtensorMap* fa, int r0, int z,
                                           const CUtensorMap* sa,
                                           const CUtensorMap* sb, int subs, SliceFn slice,
-                                          const RowTerms* rt, int nq_pad) {
+                                          const RowTerms* rt, int nq_pad,
+                                          const CUtensorMap* fb = nullptr) {
   constexpr int kS = L::kStageCount;
   if (lane == 0) {
     tma_prefetch_desc(sa);
     tma_prefetch_desc(sb);
-    if (fa) {
+    if (fa) {  // the fixed tile(s): fa, and fb after it when given (same rows)
       const uint32_t bar = smem_u32(&bars->fixed_full);
-      mbar_arrive_expect_tx(bar, L::kFixTile);
+      mbar_arrive_expect_tx(bar, (fb ? 2 : 1) * L::kFixTile);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
+      for (int c = 0; c < D / 64; ++c) {
         tma_load_3d(smem_u32(smem + L::kFixA + c * L::kFixChunk), fa, bar, c * 64, r0, z);
+        if (fb)
+          tma_load_3d(smem_u32(smem + L::kFixA + L::kFixTile + c * L::kFixChunk), fb, bar,
+                      c * 64, r0, z);
+      }
     }
   }
   for (int u = 0; u < subs; ++u) {

@@ -21,18 +21,24 @@
 // epilogues multiply dV, dK and dQ by 1 / (1 - p).
 // Each sub-step streams its own 64-row slice of the two operands it walks (Q and dO,
 // or K and V; for dkdv also the 64 rows' L log2 e, D and first key) through a
-// shared-memory ring (5 stages for dkdv, 6 for dq), so loads run ahead of the MMAs. Warp 16 loads with TMA, warp 17
-// owns tensor memory and issues the MMAs, warp 18 relays TMA completions; warps 0-15
-// do the element-wise work, one thread per TMEM lane (= row of the CTA's tile). The
-// MMA warp waits only on hardware named barriers: a shared-memory access from the
-// thread that issues MMAs stalls the tensor pipe (see nb_sync in ptx.cuh).
-//   dkdv: every element-wise warp works on every sub-step (warpgroup w takes 16 of
-//     its 64 query columns). S^T / dP^T have one TMEM buffer: the warps release it as
-//     soon as they hold their columns in registers, so the next sub-step's S^T / dP^T
-//     MMAs start while they compute; P^T / dS^T go to one of two separate buffers.
+// shared-memory ring (4 stages for dkdv, 6 for dq), so loads run ahead of the MMAs. Warp
+// 16 loads with TMA, warp 17 owns tensor memory and issues the MMAs, warp 18 relays TMA
+// completions; warps 0-15 do the element-wise work, one thread per TMEM lane (= row of
+// the CTA's tile). The MMA warp waits only on hardware named barriers: a shared-memory
+// access from the thread that issues MMAs stalls the tensor pipe (see nb_sync in
+// ptx.cuh).
+//   dkdv: K and V are fixed in shared memory (A operands of S^T = K Q^T and dP^T =
+//     V dO^T); S^T / dP^T are double-buffered in tensor memory (sub-step u in buffer
+//     u % 2) and P^T / dS^T are written as bf16 pairs over them, so the MMA warp issues
+//     S^T / dP^T(u + 2) right behind dV / dK(u), without waiting for the element-wise
+//     warps: the tensor pipe runs a thread's MMAs in order, and the element-wise warps
+//     find S^T / dP^T(u + 1) done when they finish u. Every element-wise warp works on
+//     every sub-step (warpgroup w: 16 of its 64 query columns).
 //   dq: two pairs of warpgroups alternate sub-steps (pair p takes u % 2 == p, warpgroup
 //     w of the pair 32 key columns); S / dP are double-buffered and dS is written back
 //     over S.
+// The unmasked tiles without score mods take the element-wise step two columns per
+// instruction (packed fp32 pairs, each operation bit for bit the scalar one).
 #include "bwd_common.cuh"
 
 namespace attn {
@@ -47,6 +53,33 @@ __device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_
                                          const ScoreK& sk, float base, int j, int qs,
                                          bool key_ok, bool causal_type, const uint32_t (&kf)[4],
                                          uint32_t (&pp)[8], uint32_t (&dd)[8]) {
+  if constexpr (!kAlibi && !kSoftcap && !kMasked && !kDrop) {
+    // Two query columns per instruction (packed fp32 pairs): a = lse2 - k1 x, P = 2^-a
+    // (the same value as 2^(k1 x - lse2): the negation is exact), dS = P (dP - D).
+    const uint64_t nk1 = f32x2(-sk.k1, -sk.k1);
+#pragma unroll
+    for (int e4 = 0; e4 < 4; ++e4) {
+      const float4 lv = reinterpret_cast<const float4*>(lse2)[e4];
+      const float4 dv = reinterpret_cast<const float4*>(dl)[e4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int col = e4 * 4 + 2 * h;
+        const uint64_t l2 = h ? f32x2(lv.z, lv.w) : f32x2(lv.x, lv.y);
+        const uint64_t d2 = h ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y);
+        float a0, a1;
+        f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])),
+                              nk1, l2), a0, a1);
+        const float p0 = ex2_approx(-a0), p1 = ex2_approx(-a1);
+        const uint64_t t2 =
+            sub_f32x2(f32x2(__uint_as_float(dr[col]), __uint_as_float(dr[col + 1])), d2);
+        float s0, s1;
+        f32x2_split(mul_f32x2(f32x2(p0, p1), t2), s0, s1);
+        pp[col >> 1] = pack_bf16x2(p0, p1);
+        dd[col >> 1] = pack_bf16x2(s0, s1);
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int e4 = 0; e4 < 4; ++e4) {
     const float4 lv = reinterpret_cast<const float4*>(lse2)[e4];
@@ -82,6 +115,24 @@ __device__ __forceinline__ void dq_ds(const uint32_t (&sr)[32], const uint32_t (
                                       const ScoreK& sk, float base, float lse2, float delta,
                                       int c_lo, int c_hi, const uint32_t (&kf)[8],
                                       uint32_t (&dd)[16]) {
+  if constexpr (!kAlibi && !kSoftcap && !kMasked && !kDrop) {
+    // Two key columns per instruction (packed fp32 pairs), as in dkdv_pds.
+    const uint64_t nk1 = f32x2(-sk.k1, -sk.k1);
+    const uint64_t l2 = f32x2(lse2, lse2), d2 = f32x2(delta, delta);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float a0, a1;
+      f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
+                            nk1, l2), a0, a1);
+      const float p0 = ex2_approx(-a0), p1 = ex2_approx(-a1);
+      const uint64_t t2 =
+          sub_f32x2(f32x2(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), d2);
+      float s0, s1;
+      f32x2_split(mul_f32x2(f32x2(p0, p1), t2), s0, s1);
+      dd[e] = pack_bf16x2(s0, s1);
+    }
+    return;
+  }
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     float pr[2], ds[2];
@@ -145,13 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t colDV = kKvColAcc, colDK = kKvColAcc + D;
+  const uint32_t colDV = kKv2ColAcc, colDK = kKv2ColAcc + D;
+  constexpr int kS = L::kStageCount;
 
   if (warp == kLoadWarp) {
     load_loop<D, L>(smem, bars, wc, lane, &maps.v128, k0, bg, &maps.q64, &maps.do64, subs,
-                    slice, &a.rt, p.nq_pad);
+                    slice, &a.rt, p.nq_pad, &maps.k128);
   } else if (warp == kRelayWarp) {
-    relay_loop<L::kStageCount>(bars, wc, subs);
+    relay_loop<kS>(bars, wc, subs);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp walks the schedule and waits on named barriers; every lane executes
@@ -159,41 +211,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp never diverges (an elect.sync predicate issues an MMA in about 47 cycles, a
     // predicate computed from the lane index in about 82). If the fixed tiles never
     // arrive (`ok` false) the warp keeps every barrier operation and issues nothing.
-    // Issue order: S^T/dP^T(0), then per sub-step u: S^T/dP^T(u+1) as soon as the
-    // element-wise warps have read S^T/dP^T(u), and dV/dK(u) once P^T/dS^T(u) are
-    // written. The tensor pipe thus runs S^T/dP^T(u+1) and dV/dK(u-1) while the
-    // element-wise warps work on u.
-    const uint32_t sV = smem_u32(smem + L::kFixA);
+    // S^T / dP^T of sub-step v go to buffer v % 2. Issue order: S^T/dP^T(0) and (1), then
+    // per sub-step u: dV/dK(u) once P^T / dS^T(u) are written over buffer u % 2, and right
+    // behind them S^T/dP^T(u + 2) into the same buffer (the tensor pipe runs a thread's
+    // MMAs in order, so they overwrite it only after dV/dK(u) have read it). The tensor
+    // pipe thus has S^T/dP^T(u + 1) done and S^T/dP^T(u + 2) queued while the element-wise
+    // warps work on u + 1: they never wait for the MMA warp, nor it for their release.
+    const uint32_t sV = smem_u32(smem + L::kFixA), sK = sV + L::kFixTile;
     const uint32_t ring = smem_u32(smem + L::kRing);
     const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc));
     const bool issuer = elect_one();
-    nb_sync(kNbKvK, kNbKvCount);  // K tile in tensor memory
-    auto issue_sdp = [&](int v) {  // S^T and dP^T of sub-step v
-      const int s = v % L::kStageCount;
+    auto issue_sdp = [&](int v) {  // S^T and dP^T of sub-step v into buffer v % 2
+      const int s = v % kS, x = v & 1;
       nb_sync(kNbStage + s, kNbStageCount);
       tc_fence_after_sync();
       if (!ok) return;
       const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
-      mma_tmem_x64<D>(issuer, tmem + kKvColS, tmem + kKvColK, sQ);  // S^T = K Q^T
-      mma_128x64<D>(issuer, tmem + kKvColDP, sV, sDO);              // dP^T = V dO^T
-      mma_commit_if(issuer, smem_u32(&bars->s_full[0]));
+      mma_128x64<D>(issuer, tmem + kv_col_s(x), sK, sQ);    // S^T = K Q^T
+      mma_128x64<D>(issuer, tmem + kv_col_dp(x), sV, sDO);  // dP^T = V dO^T
+      mma_commit_if(issuer, smem_u32(&bars->s_full[x]));
     };
     issue_sdp(0);
+    if (subs > 1) issue_sdp(1);
     for (int u = 0; u < subs; ++u) {
-      const int s = u % L::kStageCount, x = u & 1;
-      if (u + 1 < subs) {
-        nb_sync(kNbKvRel, kNbKvCount);  // S^T / dP^T(u) are in registers
-        issue_sdp(u + 1);
-      }
-      nb_sync(kNbKvP + x, kNbKvCount);  // P^T / dS^T(u) written
+      const int s = u % kS, x = u & 1;
+      nb_sync(kNbKvP + x, kNbKvCount);  // P^T / dS^T(u) written over buffer x
       tc_fence_after_sync();
       if (ok) {
         const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
-        mma_pd_x_slice<D>(issuer, tmem + colDV, tmem + kKvColPD, sDO, u > 0);       // dV += P^T dO
-        mma_pd_x_slice<D>(issuer, tmem + colDK, tmem + kKvColPD + 32, sQ, u > 0);  // dK += dS^T Q
-        mma_commit_if(issuer, smem_u32(&bars->empty[s]));    // stage (and its row terms) free
-        mma_commit_if(issuer, smem_u32(&bars->pd_free[0]));  // P^T / dS^T free
+        mma_inplace_x_slice<D>(issuer, tmem + colDV, tmem + kv_col_s(x), sDO, u > 0);   // dV += P^T dO
+        mma_inplace_x_slice<D>(issuer, tmem + colDK, tmem + kv_col_dp(x), sQ, u > 0);  // dK += dS^T Q
+        mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage (and its row terms) free
       }
+      if (u + 2 < subs) issue_sdp(u + 2);
     }
     if (ok) mma_commit_if(issuer, smem_u32(&bars->acc_full));
   } else {
@@ -205,29 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const int c0 = wg * 16;
     const bool causal_type = p.mask.kind != ATTN_MASK_NONE;
-    {
-      // K rows of the tile into tensor memory (A operand of S^T = K Q^T): this thread's
-      // key row, head-dimension columns [wg D/4, (wg + 1) D/4) as bf16 pairs.
-      constexpr int kW = D / 8;  // 32-bit words per thread
-      uint32_t kr[kW];
-      if (j < p.Nkv) {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(a.k + ((size_t)bg * p.Nkv + j) * D + wg * (D / 4));
-#pragma unroll
-        for (int e = 0; e < kW / 4; ++e) {
-          const uint4 w = src[e];
-          kr[4 * e] = w.x; kr[4 * e + 1] = w.y; kr[4 * e + 2] = w.z; kr[4 * e + 3] = w.w;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < kW; ++e) kr[e] = 0u;
-      }
-      if constexpr (kW == 16) tmem_st16(tmem + lane_base + kKvColK + wg * kW, kr);
-      else tmem_st8(tmem + lane_base + kKvColK + wg * kW, kr);
-      tmem_wait_st();
-      tc_fence_before_sync();
-      nb_arrive(kNbKvK, kNbKvCount);
-    }
     bool ok_all = true;
     // (head, query tile) of sub-step u, its score constants and whether the tile needs
     // the per-element mask, advanced every second sub-step (the order `slice` gives)
@@ -236,8 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool need_mask = tile_needs_mask(p.mask, qr.lo * BT, k0, BT);
     const DropThr dthr = drop_thr_words(kDrop ? p.drop_thr : 0);
     for (int u = 0; u < subs; ++u) {
-      const int s = u % L::kStageCount, x = u & 1;
-      const bool rel = u + 1 < subs;  // the MMA warp waits for this release before u + 1
+      const int s = u % kS, x = u & 1;
       if (u > 0 && x == 0) {
         if (++st_q == n_q) {
           st_q = 0;
@@ -250,25 +276,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bh = b * p.Hq + g * G + st_h;
       const int qs = qrow + c0;                  // query of this thread's column 0
       if (ok_all)
-        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[0]), u & 1, wc));
+        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc));
       // the stage's row terms arrived with full[s]; observe them
       if (ok_all)
-        ok_all = __all_sync(0xffffffffu,
-                            mbar_wait(smem_u32(&bars->full[s]), (u / L::kStageCount) & 1, wc));
+        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (u / kS) & 1, wc));
       if (!ok_all) {  // aborted: keep the barrier schedule with the MMA warp
-        if (rel) nb_sync(kNbKvRel, kNbKvCount);
         nb_sync(kNbKvP + x, kNbKvCount);
         continue;
       }
       tc_fence_after_sync();
+      const uint32_t tS = tmem + lane_base + kv_col_s(x) + c0;
+      const uint32_t tDP = tmem + lane_base + kv_col_dp(x) + c0;
       uint32_t sr[16], dr[16];
-      tmem_ld16(tmem + lane_base + kKvColS + c0, sr);
-      tmem_ld16(tmem + lane_base + kKvColDP + c0, dr);
+      tmem_ld16(tS, sr);
+      tmem_ld16(tDP, dr);
       tmem_wait_ld();
       reg_fence16(sr);
       reg_fence16(dr);
-      tc_fence_before_sync();
-      if (rel) nb_arrive(kNbKvRel, kNbKvCount);
       const float* lse2 = reinterpret_cast<const float*>(smem + L::kRows + s * L::kRowStage) + c0;
       const float* dl = lse2 + SUB;
       const int* fk = reinterpret_cast<const int*>(dl + SUB);
@@ -282,15 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         dkdv_pds<kAlibi, kSoftcap, false, kDrop>(sr, dr, lse2, dl, fk, sk, base, j, qs, true,
                                                  causal_type, kf, pp, dd);
-      // P^T / dS^T of sub-step u - 1 must have been read by their MMAs
-      if (u >= 1)
-        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pd_free[0]), (u - 1) & 1, wc));
-      if (!ok_all) {
-        nb_sync(kNbKvP + x, kNbKvCount);
-        continue;
-      }
-      tmem_st8(tmem + lane_base + kKvColPD + wg * 8, pp);       // P^T, k-step wg
-      tmem_st8(tmem + lane_base + kKvColPD + 32 + wg * 8, dd);  // dS^T
+      // P^T and dS^T over the first half of this warpgroup's own 16 columns of S^T and
+      // dP^T (k-step wg of the dV and dK products); no other warp reads those columns
+      tmem_st8(tS, pp);
+      tmem_st8(tDP, dd);
       tmem_wait_st();
       tc_fence_before_sync();
       nb_arrive(kNbKvP + x, kNbKvCount);
