@@ -138,18 +138,15 @@ KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", 
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201422336 + 45881600,
-                    "sha256": "a8cf4429bbeeececdf2c77fbad30ca7fa66cf6ccea806652359bc0f427221973"},
-    "rowdot_kernel": {"bytes": 135301120 + 734720,
-                    "sha256": "75b3397d3eb84e18561f4d87abb9ef7961b5d444a6a2e1441b0fe90db9fefd5a"},
-    "dkdv_kernel": {"bytes": 270629120 + 102725888,
-                  "sha256": "6557cf33ebd337a424bddea71c23fc32168395b832aed68f25018d28f4a1adf4"},
-    "dq_kernel": {"bytes": 270628864 + 48264448,
-                "sha256": "6557cf33ebd337a424bddea71c23fc32168395b832aed68f25018d28f4a1adf4"},
-    "decode_tc_kernel": {"bytes": 1119357952 + 9291264,
-                       "sha256": "c614a56391ac51ec161b8ae159a4363fbbd3718fa106c1dd3d18ccc8c55fd5a8"},
+    "fwd_tc_kernel": {"bytes": 201400320 + 45842944,
+                    "sha256": "0a4eb45db33e9903192a16321cb171999cc0076f9756692a9b0c98ce96547790"},
+    "rowdot_kernel": {"bytes": 135299328 + 715776,
+                    "sha256": "841addfd8f49a7b13a642f56bd66d327f49d5c62e01ce0ba0d0c77b7f2e0f525"},
+    "dkdv_kernel": {"bytes": 270626304 + 99216640,
+                  "sha256": "b90bf7a2649263cff70e886b794d516dc474fd10a5178d947965a3dccb78dad1"},
+    "dq_kernel": {"bytes": 270711808 + 48381952,
+                "sha256": "b90bf7a2649263cff70e886b794d516dc474fd10a5178d947965a3dccb78dad1"},
 }
-
 
 def kernel_source_sha(kernel: str) -> str:
     """SHA-256 of the kernel's sources with // comments and blank space removed, so that
