@@ -158,3 +158,11 @@ def test_reference_arm_follows_the_workload():
     assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 2
     assert line["metric"].startswith("attention forward TFLOP/s")
     assert "query rows" in line["cpu_baseline"]["sample"]
+
+
+def test_roofline_peak_follows_the_timed_region():
+    """A timed region of a second or more is a sustained measurement under the power cap:
+    its tensor roofline takes the sustained bf16 figure; a short burst takes the burst one."""
+    pk = {"bf16_tflops": 1908.0, "bf16_sustained": 1728.7, "hbm_gbs": 6744.6}
+    assert bench.tensor_peak(pk, 2000.0) == (1728.7, "bf16 sustained (timed region >= 1 s)")
+    assert bench.tensor_peak(pk, 35.0) == (1908.0, "bf16 burst")
