@@ -23,6 +23,9 @@
 //     modifications, updates m and l with exp2, writes P as bf16 back into the
 //     score columns, and rescales its O row in TMEM when the max has grown by more
 //     than 2^8 (a stale max is exact: O and l share it until the final division).
+//   * warps 8-11 form the third warpgroup (warp 11 has no role); it drops to 40
+//     registers a thread so that each softmax thread can hold its 128 scores and the
+//     row state in 232 without spilling.
 // Tensor memory: S0 cols [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d).
 //
 // Dropout variant (kDrop, bf16 only): the bf16 P is ANDed with the keep mask (one Philox
@@ -51,7 +54,12 @@ constexpr int kStages = 4;     // K/V shared-memory ring depth (each stage one t
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kRelayWarp = 10;  // turns TMA completions into named-barrier arrivals
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;   // warp 11 only completes the third warpgroup
+// Registers per thread after the reallocation: the two softmax warpgroups hold a row of
+// 128 scores each; the third warpgroup (loader, MMA issuer, relay, idle) needs few.
+// 2 x 128 x 232 + 128 x 40 = 384 x 168, the pool the launch bounds give.
+constexpr int kRegsSoftmax = 232, kRegsOther = 40;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * 168, "register pool");
 // Named barriers (the MMA warp waits only on these; see nb_sync in ptx.cuh):
 //   kNbP + t      P_t written to TMEM: softmax warpgroup t (128) + MMA warp (32)
 //   kNbKv + s     ring stage s loaded: relay warp (32) + MMA warp (32)
@@ -178,139 +186,144 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == kLoadWarp) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      const uint32_t qbar = smem_u32(&bars->q_full);
-      mbar_arrive_expect_tx(qbar, kQTiles * L::kTile);
-#pragma unroll
-      for (int t = 0; t < kQTiles; ++t)
-#pragma unroll
-        for (int c = 0; c < L::kSlabs; ++c)
-          tma_load_3d(smem_u32(smem + L::kQ + t * L::kTile + c * L::kChunk), &tm_q, qbar,
-                      c * (128 / L::kElem), q0 + t * BM, bh);
-      for (int u = 0; u < 2 * n_kv; ++u) {
-        const int s = u % kStages, use = u / kStages;
-        if (!mbar_wait(smem_u32(&bars->kv_empty[s]), (use & 1) ^ 1, wc)) break;
-        const uint32_t fb = smem_u32(&bars->kv_full[s]);
-        mbar_arrive_expect_tx(fb, L::kTile);
-        const CUtensorMap* map = (u & 1) ? &tm_v : &tm_k;
-        const int krow = (lo + (u >> 1)) * BN;
-        if (kFp8 && (u & 1)) {  // V^T tile: keys krow.. (x), all d rows (y)
-          tma_load_3d(smem_u32(smem + L::kRing + s * L::kTile), map, fb, krow, 0, bg);
-        } else {
-#pragma unroll
+  if (warp >= 8) {
+    // The third warpgroup gives registers back before its warps take their roles.
+    setmaxnreg_dec<kRegsOther>();
+    if (warp == kLoadWarp) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        const uint32_t qbar = smem_u32(&bars->q_full);
+        mbar_arrive_expect_tx(qbar, kQTiles * L::kTile);
+  #pragma unroll
+        for (int t = 0; t < kQTiles; ++t)
+  #pragma unroll
           for (int c = 0; c < L::kSlabs; ++c)
-            tma_load_3d(smem_u32(smem + L::kRing + s * L::kTile + c * L::kChunk), map, fb,
-                        c * (128 / L::kElem), krow, bg);
+            tma_load_3d(smem_u32(smem + L::kQ + t * L::kTile + c * L::kChunk), &tm_q, qbar,
+                        c * (128 / L::kElem), q0 + t * BM, bh);
+        for (int u = 0; u < 2 * n_kv; ++u) {
+          const int s = u % kStages, use = u / kStages;
+          if (!mbar_wait(smem_u32(&bars->kv_empty[s]), (use & 1) ^ 1, wc)) break;
+          const uint32_t fb = smem_u32(&bars->kv_full[s]);
+          mbar_arrive_expect_tx(fb, L::kTile);
+          const CUtensorMap* map = (u & 1) ? &tm_v : &tm_k;
+          const int krow = (lo + (u >> 1)) * BN;
+          if (kFp8 && (u & 1)) {  // V^T tile: keys krow.. (x), all d rows (y)
+            tma_load_3d(smem_u32(smem + L::kRing + s * L::kTile), map, fb, krow, 0, bg);
+          } else {
+  #pragma unroll
+            for (int c = 0; c < L::kSlabs; ++c)
+              tma_load_3d(smem_u32(smem + L::kRing + s * L::kTile + c * L::kChunk), map, fb,
+                          c * (128 / L::kElem), krow, bg);
+          }
         }
+        // Do not leave while copies into this CTA's shared memory are in flight.
+        mbar_wait(qbar, 0, wc);
+        for (int u = imax(0, 2 * n_kv - kStages); u < 2 * n_kv; ++u)
+          mbar_wait(smem_u32(&bars->kv_full[u % kStages]), (u / kStages) & 1, wc);
       }
-      // Do not leave while copies into this CTA's shared memory are in flight.
-      mbar_wait(qbar, 0, wc);
-      for (int u = imax(0, 2 * n_kv - kStages); u < 2 * n_kv; ++u)
-        mbar_wait(smem_u32(&bars->kv_full[u % kStages]), (u / kStages) & 1, wc);
-    }
-  } else if (warp == kRelayWarp) {
-    // ------------------------------------------------------------ relay
-    // Ring use u is stage u % kStages; after its TMA bytes land, arrive on that
-    // stage's named barrier for the MMA warp. After an abort, rendezvous instead.
-    bool live = true;
-    for (int u = 0; u < 2 * n_kv; ++u) {
-      const int s = u % kStages;
-      if (live)
-        live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->kv_full[s]), (u / kStages) & 1, wc));
-      if (live) nb_arrive(kNbKv + s, kNbKvCount);
-      else nb_sync(kNbKv + s, kNbKvCount);
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp walks the schedule and waits on named barriers; every lane executes
-    // the MMA instructions predicated on `issuer`, the one lane elect.sync picks, so the
-    // warp never diverges (an elect.sync predicate issues an MMA in about 47 cycles, a
-    // predicate computed from the lane index in about 82). If the Q tiles never arrive
-    // (`ok` false) the warp keeps every barrier operation and issues nothing.
-    constexpr uint32_t idS = kFp8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false, false);
-    constexpr uint32_t idO = kFp8 ? idesc_e4m3_f32(BM, D) : idesc_bf16_f32(BM, D, false, true);
-    const uint32_t q_base = smem_u32(smem + L::kQ);
-    const uint32_t ring = smem_u32(smem + L::kRing);
-    int np[kQTiles] = {0, 0};  // P tiles consumed per query tile
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->q_full), 0, wc));
-    const bool issuer = elect_one();
-    auto commit = [&](uint64_t* bar) {
-      if (ok) mma_commit_if(issuer, smem_u32(bar));
-    };
+    } else if (warp == kRelayWarp) {
+      // ------------------------------------------------------------ relay
+      // Ring use u is stage u % kStages; after its TMA bytes land, arrive on that
+      // stage's named barrier for the MMA warp. After an abort, rendezvous instead.
+      bool live = true;
+      for (int u = 0; u < 2 * n_kv; ++u) {
+        const int s = u % kStages;
+        if (live)
+          live = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->kv_full[s]), (u / kStages) & 1, wc));
+        if (live) nb_arrive(kNbKv + s, kNbKvCount);
+        else nb_sync(kNbKv + s, kNbKvCount);
+      }
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------------ MMA issuer
+      // The whole warp walks the schedule and waits on named barriers; every lane executes
+      // the MMA instructions predicated on `issuer`, the one lane elect.sync picks, so the
+      // warp never diverges (an elect.sync predicate issues an MMA in about 47 cycles, a
+      // predicate computed from the lane index in about 82). If the Q tiles never arrive
+      // (`ok` false) the warp keeps every barrier operation and issues nothing.
+      constexpr uint32_t idS = kFp8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false, false);
+      constexpr uint32_t idO = kFp8 ? idesc_e4m3_f32(BM, D) : idesc_bf16_f32(BM, D, false, true);
+      const uint32_t q_base = smem_u32(smem + L::kQ);
+      const uint32_t ring = smem_u32(smem + L::kRing);
+      int np[kQTiles] = {0, 0};  // P tiles consumed per query tile
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->q_full), 0, wc));
+      const bool issuer = elect_one();
+      auto commit = [&](uint64_t* bar) {
+        if (ok) mma_commit_if(issuer, smem_u32(bar));
+      };
 
-    auto sync_stage = [&](int u) {
-      nb_sync(kNbKv + u % kStages, kNbKvCount);
-      tc_fence_after_sync();
-    };
-    auto issue_s = [&](int t, int u) {  // S_t = Q_t K^T with K in ring use u
-      if (!ok) return;
-      const uint32_t kb = ring + (u % kStages) * L::kTile;
-      const uint32_t qt = q_base + t * L::kTile;
-      const uint64_t dq = smem_desc_sw128(qt, 16, 1024), dk = smem_desc_sw128(kb, 16, 1024);
-      const uint32_t col = t == 0 ? L::kColS0 : L::kColS1;
-      // 32 bytes of the head dimension per instruction (16 bf16 or 32 e4m3 values)
-#pragma unroll
-      for (int kk = 0; kk < D * L::kElem / 32; ++kk) {
-        const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
-        if (kFp8) mma_f8_ss_if(issuer, tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
-        else mma_ss_if(issuer, tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
-      }
-      mma_commit_if(issuer, smem_u32(&bars->s_full[t]));
-    };
-    auto issue_pv = [&](int t, int u) {  // O_t += P_t V with V in ring use u
-      if (!ok) return;
-      const uint32_t vb = ring + (u % kStages) * L::kTile;
-      const uint32_t colS = t == 0 ? L::kColS0 : L::kColS1;
-      const uint32_t colO = t == 0 ? L::kColO0 : L::kColO1;
-      if (kFp8) {  // P (e4m3, 4 per column) x V^T tile (K-major): 32 keys per instruction
-        const uint64_t dv = smem_desc_sw128(vb, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < BN / 32; ++kk)
-          mma_f8_ts_if(issuer, tmem + colO, tmem + colS + kk * 8, dv + ((kk * 32) >> 4), idO,
-                       (np[t] > 0 || kk > 0) ? 1u : 0u);
-      } else {  // P (bf16 pairs) x V tile used MN-major: 16 keys per instruction
-        const uint64_t dv = smem_desc_sw128(vb, L::kChunk, 1024);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts_if(issuer, tmem + colO, tmem + colS + kk * 8, dv + ((kk * 16 * 128) >> 4), idO,
-                    (np[t] > 0 || kk > 0) ? 1u : 0u);
-      }
-    };
+      auto sync_stage = [&](int u) {
+        nb_sync(kNbKv + u % kStages, kNbKvCount);
+        tc_fence_after_sync();
+      };
+      auto issue_s = [&](int t, int u) {  // S_t = Q_t K^T with K in ring use u
+        if (!ok) return;
+        const uint32_t kb = ring + (u % kStages) * L::kTile;
+        const uint32_t qt = q_base + t * L::kTile;
+        const uint64_t dq = smem_desc_sw128(qt, 16, 1024), dk = smem_desc_sw128(kb, 16, 1024);
+        const uint32_t col = t == 0 ? L::kColS0 : L::kColS1;
+        // 32 bytes of the head dimension per instruction (16 bf16 or 32 e4m3 values)
+  #pragma unroll
+        for (int kk = 0; kk < D * L::kElem / 32; ++kk) {
+          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+          if (kFp8) mma_f8_ss_if(issuer, tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
+          else mma_ss_if(issuer, tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_if(issuer, smem_u32(&bars->s_full[t]));
+      };
+      auto issue_pv = [&](int t, int u) {  // O_t += P_t V with V in ring use u
+        if (!ok) return;
+        const uint32_t vb = ring + (u % kStages) * L::kTile;
+        const uint32_t colS = t == 0 ? L::kColS0 : L::kColS1;
+        const uint32_t colO = t == 0 ? L::kColO0 : L::kColO1;
+        if (kFp8) {  // P (e4m3, 4 per column) x V^T tile (K-major): 32 keys per instruction
+          const uint64_t dv = smem_desc_sw128(vb, 16, 1024);
+  #pragma unroll
+          for (int kk = 0; kk < BN / 32; ++kk)
+            mma_f8_ts_if(issuer, tmem + colO, tmem + colS + kk * 8, dv + ((kk * 32) >> 4), idO,
+                         (np[t] > 0 || kk > 0) ? 1u : 0u);
+        } else {  // P (bf16 pairs) x V tile used MN-major: 16 keys per instruction
+          const uint64_t dv = smem_desc_sw128(vb, L::kChunk, 1024);
+  #pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts_if(issuer, tmem + colO, tmem + colS + kk * 8, dv + ((kk * 16 * 128) >> 4), idO,
+                      (np[t] > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
 
-    sync_stage(0);
-#pragma unroll
-    for (int t = 0; t < kQTiles; ++t)
-      if (lo >= rng[t].lo && lo < rng[t].hi) issue_s(t, 0);
-    commit(&bars->kv_empty[0]);
-    for (int jj = 0; jj < n_kv; ++jj) {
-      const int j = lo + jj;
-      const int uv = 2 * jj + 1, uk = 2 * jj + 2;
-      const bool next = jj + 1 < n_kv;
-      sync_stage(uv);
-#pragma unroll
-      for (int t = 0; t < kQTiles; ++t) {
-        if (j >= rng[t].lo && j < rng[t].hi) {
-          nb_sync(kNbP + t, kNbPCount);
-          tc_fence_after_sync();
-          issue_pv(t, uv);
-          ++np[t];
+      sync_stage(0);
+  #pragma unroll
+      for (int t = 0; t < kQTiles; ++t)
+        if (lo >= rng[t].lo && lo < rng[t].hi) issue_s(t, 0);
+      commit(&bars->kv_empty[0]);
+      for (int jj = 0; jj < n_kv; ++jj) {
+        const int j = lo + jj;
+        const int uv = 2 * jj + 1, uk = 2 * jj + 2;
+        const bool next = jj + 1 < n_kv;
+        sync_stage(uv);
+  #pragma unroll
+        for (int t = 0; t < kQTiles; ++t) {
+          if (j >= rng[t].lo && j < rng[t].hi) {
+            nb_sync(kNbP + t, kNbPCount);
+            tc_fence_after_sync();
+            issue_pv(t, uv);
+            ++np[t];
+          }
+          if (next) {
+            if (t == 0) sync_stage(uk);
+            if (j + 1 >= rng[t].lo && j + 1 < rng[t].hi) issue_s(t, uk);
+          }
         }
-        if (next) {
-          if (t == 0) sync_stage(uk);
-          if (j + 1 >= rng[t].lo && j + 1 < rng[t].hi) issue_s(t, uk);
-        }
+        commit(&bars->kv_empty[uv % kStages]);
+        if (next) commit(&bars->kv_empty[uk % kStages]);
       }
-      commit(&bars->kv_empty[uv % kStages]);
-      if (next) commit(&bars->kv_empty[uk % kStages]);
+  #pragma unroll
+      for (int t = 0; t < kQTiles; ++t) commit(&bars->o_full[t]);
     }
-#pragma unroll
-    for (int t = 0; t < kQTiles; ++t) commit(&bars->o_full[t]);
   } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;                 // query tile of this warpgroup
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = row in the tile

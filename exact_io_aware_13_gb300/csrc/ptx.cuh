@@ -39,6 +39,21 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Register reallocation between warpgroups: every warp of a warpgroup executes the same
+// instruction. An increase waits until decreases elsewhere in the CTA have returned enough
+// registers to the pool the CTA was launched with, so the counts must add up to at most
+// that pool (threads x registers per thread at launch).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
