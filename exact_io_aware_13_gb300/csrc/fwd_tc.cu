@@ -379,17 +379,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Allowed columns of this row in this tile: [c_lo, c_hi].
         const int c_lo = fk - k0, c_hi = last_key - k0;
         const float base = kAlibi ? (float)(k0 - i) * kb : 0.f;
+        const uint64_t k1j2 = f32x2(k1j, k1j), one2 = f32x2(1.f, 1.f);
+        const uint64_t capA2 = f32x2(capA, capA), neg_2capA2 = f32x2(-2.f * capA, -2.f * capA);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
+          for (int e = 0; e < 32; e += 2) {  // column pairs: packed fp32x2 arithmetic
             const int col = c * 32 + e;
-            const float x = __uint_as_float(r[c][e]);
-            float s2 = kAlibi ? fmaf(x, k1j, fmaf((float)col, kb, base)) : x * k1j;
-            if (kSoftcap) s2 = capA - 2.0f * capA * rcp_approx(1.0f + ex2_approx(s2));
-            if (masked) s2 = (col >= c_lo && col <= c_hi) ? s2 : -INFINITY;
-            mx[e & 7] = fmaxf(mx[e & 7], s2);
-            r[c][e] = __float_as_uint(s2);
+            const uint64_t x2 = f32x2(__uint_as_float(r[c][e]), __uint_as_float(r[c][e + 1]));
+            uint64_t s2 = kAlibi ? fma_f32x2(x2, k1j2,
+                                             f32x2(fmaf((float)col, kb, base),
+                                                   fmaf((float)(col + 1), kb, base)))
+                                 : mul_f32x2(x2, k1j2);
+            if (kSoftcap) {  // capA - 2 capA / (1 + 2^s2): capA tanh of the pre-cap score
+              float a0, a1, d0, d1;
+              f32x2_split(s2, a0, a1);
+              f32x2_split(fma_f32x2(f32x2(ex2_approx(a0), ex2_approx(a1)), one2, one2), d0, d1);
+              s2 = fma_f32x2(f32x2(rcp_approx(d0), rcp_approx(d1)), neg_2capA2, capA2);
+            }
+            float v0, v1;
+            f32x2_split(s2, v0, v1);
+            if (masked) {
+              v0 = (col >= c_lo && col <= c_hi) ? v0 : -INFINITY;
+              v1 = (col + 1 >= c_lo && col + 1 <= c_hi) ? v1 : -INFINITY;
+            }
+            mx[e & 7] = fmaxf(mx[e & 7], v0);
+            mx[(e + 1) & 7] = fmaxf(mx[(e + 1) & 7], v1);
+            r[c][e] = __float_as_uint(v0);
+            r[c][e + 1] = __float_as_uint(v1);
           }
       }
       float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
