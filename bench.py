@@ -147,14 +147,16 @@ KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", 
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201400320 + 45842944,
-                    "sha256": "0a4eb45db33e9903192a16321cb171999cc0076f9756692a9b0c98ce96547790"},
-    "rowdot_kernel": {"bytes": 135299328 + 715776,
-                    "sha256": "841addfd8f49a7b13a642f56bd66d327f49d5c62e01ce0ba0d0c77b7f2e0f525"},
-    "dkdv_kernel": {"bytes": 270626304 + 99216640,
-                  "sha256": "b90bf7a2649263cff70e886b794d516dc474fd10a5178d947965a3dccb78dad1"},
-    "dq_kernel": {"bytes": 270711808 + 48381952,
-                "sha256": "b90bf7a2649263cff70e886b794d516dc474fd10a5178d947965a3dccb78dad1"},
+    "fwd_tc_kernel": {"bytes": 201399296 + 45270528,
+                    "sha256": "1b4fe1ac8a93db4f9b57ca31b5a0fff6b9211b4f6d0740a540bd4a14257f203d"},
+    "rowdot_kernel": {"bytes": 135301120 + 723456,
+                    "sha256": "e3f10b1049cb305469a507d32799ff9d6ed4d8e675ae1b8a3002df13b78e277d"},
+    "dkdv_kernel": {"bytes": 270627584 + 99481856,
+                  "sha256": "afda9888658aff93747f45983c9dd1d8a6e5182237ddbf58428056194019a1fb"},
+    "dq_kernel": {"bytes": 270753024 + 48598016,
+                "sha256": "afda9888658aff93747f45983c9dd1d8a6e5182237ddbf58428056194019a1fb"},
+    "decode_tc_kernel": {"bytes": 1119353088 + 8705536,
+                       "sha256": "89f74c5dfeeba63123aece6e2ff94a2c511ec0108a959143810c3f46fac1080e"},
 }
 
 def kernel_source_sha(kernel: str) -> str:
