@@ -97,6 +97,25 @@ def test_decode_more_queries_than_keys():
     _check(w, o, lse, inputs, what="Nq > seq_len")
 
 
+MANY_LENGTHS = (0, 3, 64, 129, 300, 517, 700, 845, 1000, 1100, 1280, 1400, 1500, 1663, 1789,
+                2000)
+
+
+@pytest.mark.parametrize("mask,window", [(MASK_NONE, 0), (MASK_CAUSAL, 0),
+                                         (MASK_SLIDING_WINDOW, 50), (MASK_SLIDING_WINDOW, 700)])
+@pytest.mark.parametrize("nq,page_size", [(1, 16), (3, 64)])
+def test_decode_many_items(mask, window, nq, page_size):
+    """Sixteen sequences of 0-2000 tokens over four kv heads at 128 keys per chunk: several
+    work items per CTA, CTA shares that begin and end in every kind of item (full chunks,
+    short last chunks, sequences of one chunk), and with a short sliding window chunks
+    that hold keys of no row."""
+    w = _w(Hq=16, Hkv=4, Nq=nq, lengths=MANY_LENGTHS, page_size=page_size, mask_kind=mask,
+           window=window, score_kind=SCORE_ALIBI, seed=60 + nq + window)
+    o, lse, status, inputs = _run(w, 128)
+    assert status == 0
+    _check(w, o, lse, inputs, what=f"many items mask {mask} W {window} nq {nq}")
+
+
 def test_decode_no_cache_at_all():
     w = _w(lengths=(0, 0))
     o, lse, status, inputs = _run(w, 256, max_seq_len=0)
