@@ -327,7 +327,8 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
   const bool run_kv = (phases & ATTN_BWD_DKDV) != 0, run_q = (phases & ATTN_BWD_DQ) != 0;
   if (d == 256)
     return from_cuda(launch_bwd256_tc(p, maps, rt, qb, dob, kb, dqb, dkb, dvb, run_kv, run_q, st));
-  return from_cuda(launch_bwd_tc(p, maps, rt, qb, dob, kb, dqb, dkb, dvb, run_kv, run_q, st));
+  return from_cuda(
+      launch_bwd_tc(p, maps, rt, qb, dob, kb, vb, dqb, dkb, dvb, run_kv, run_q, st));
 }
 
 // ---------------------------------------------------------------- static workspace

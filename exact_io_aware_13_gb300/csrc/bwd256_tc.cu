@@ -452,8 +452,8 @@ cudaError_t launch_bwd256_tc(const Problem& p, const BwdMaps& maps, const RowTer
                              const __nv_bfloat16* q, const __nv_bfloat16* dout,
                              const __nv_bfloat16* k, __nv_bfloat16* dq, __nv_bfloat16* dk,
                              __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st) {
-  BwdArgs ka{p, rt, q, dout, k, dq, dk, dv, ceil_div(p.Nkv, BT)};
-  BwdArgs qa{p, rt, q, dout, k, dq, dk, dv, ceil_div(p.Nq, BT)};
+  BwdArgs ka{p, rt, q, dout, k, nullptr, dq, dk, dv, ceil_div(p.Nkv, BT)};
+  BwdArgs qa{p, rt, q, dout, k, nullptr, dq, dk, dv, ceil_div(p.Nq, BT)};
   const long long gk = run_dkdv ? (long long)ka.n_tiles * p.B * p.Hkv : 0;
   const long long gq = run_dq ? (long long)qa.n_tiles * p.B * p.Hq : 0;
   if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;

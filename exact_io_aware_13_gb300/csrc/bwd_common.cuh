@@ -19,21 +19,24 @@ constexpr int kRelayWarp = kEwWarps + 2;  // turns TMA completions into barrier 
 // Named barriers (the MMA warp waits only on these; see nb_sync in ptx.cuh):
 //   kNbStage + s   ring stage s loaded: relay warp (32) + MMA warp (32)
 //   dq:   kNbP + x     dS_x written to TMEM: pair x (256 threads) + MMA warp (32)
-//   dkdv: kNbKvP + x   P^T / dS^T of a sub-step u (x = u % 2) written over S^T / dP^T of
-//                      buffer x: element-wise warps + MMA warp
+//   dkdv: kNbKvP + x   P^T of a sub-step u (x = u % 2) written over S^T buffer x:
+//                      element-wise warps + MMA warp
+//   dkdv: kNbKvF       dP^T of a sub-step read into registers: the same warps
+//   dkdv: kNbKvD       dS^T of a sub-step written into its S^T buffer: the same warps
+//   dkdv: kNbQL        the V tile written to tensor memory: the same warps
 //   d=256 kernels: kNbKvRel, kNbKvP + x, kNbKvK (bwd256_tc.cu)
 //   dq:   kNbQL        Q and dO tiles written to tensor memory: element-wise warps + MMA warp
 constexpr uint32_t kNbP = 1, kNbPCount = 288;
 constexpr uint32_t kNbStage = 3, kNbStageCount = 64;
-constexpr uint32_t kNbKvRel = 9, kNbKvP = 10, kNbKvK = 12, kNbQL = 13;
+constexpr uint32_t kNbKvRel = 9, kNbKvP = 10, kNbKvK = 12, kNbQL = 13, kNbKvD = 14, kNbKvF = 15;
 constexpr uint32_t kNbKvCount = (kEwWarps + 1) * 32;
 constexpr int kStagesQ = 6;      // dq ring depth, in sub-steps
-constexpr int kStagesKv = 4;     // dkdv ring depth (its K and V tiles are fixed in smem)
+constexpr int kStagesKv = 5;     // dkdv ring depth (its K tile is fixed in smem)
 constexpr int kMaxStages = 6;
 // Stage barriers take IDs kNbStage .. kNbStage + kMaxStages - 1; the others must not
 // overlap them (one hardware barrier, one thread count), and IDs end at 15.
 static_assert(kNbStage + kMaxStages <= kNbKvRel && kNbP + 2 <= kNbStage && kNbKvK < kNbQL &&
-                  kNbQL < 16,
+                  kNbQL < kNbKvD && kNbKvD < kNbKvF && kNbKvF < 16,
               "named barrier IDs");
 constexpr int kHeadGroup = 4;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -48,12 +51,12 @@ template <int D> constexpr uint32_t col_do() { return kColQ + D / 2; }
 // P^T / dS^T (bf16 pairs: P^T in the first 32 columns, dS^T in the next 32), the K tile
 // (bf16 pairs, A operand of S^T = K Q^T), then the accumulator.
 constexpr uint32_t kKvColS = 0, kKvColDP = 64, kKvColPD = 128, kKvColK = 192, kKvColAcc = 256;
-// Tensor memory columns of dkdv (head dimension 64 and 128): two buffers x of S^T and dP^T
-// (64 columns each; P^T and dS^T are written as bf16 pairs over the first half of each
-// warpgroup's 16 columns of them), then dV and dK.
-__device__ __forceinline__ uint32_t kv_col_s(int x) { return x * 128; }
-__device__ __forceinline__ uint32_t kv_col_dp(int x) { return x * 128 + 64; }
-constexpr uint32_t kKv2ColAcc = 256;
+// Tensor memory columns of dkdv (head dimension 64 and 128): two S^T buffers x (64 columns
+// each; P^T and dS^T of the sub-step are written as bf16 pairs over the first and the
+// second half of each warpgroup's 16 columns of its buffer), one dP^T buffer (64), the V
+// tile (bf16 pairs, the A operand of dP^T = V dO^T; D / 2 columns), then dV and dK.
+__device__ __forceinline__ uint32_t kv_col_s(int x) { return x * 64; }
+constexpr uint32_t kKv2ColDP = 128, kKv2ColV = 192, kKv2ColAcc = 256;
 
 // Element-wise constants: s2 = x*k1 + kb*(j - i) (log2 units), then the soft-cap.
 struct ScoreK {
@@ -87,10 +90,10 @@ __device__ __forceinline__ ScoreK score_consts(const Problem& p, int h) {
 // per-lane condition around the exponential would make the compiler branch on every
 // element.
 template <bool kAlibi, bool kSoftcap>
-__device__ __forceinline__ void p_and_ds(float xs, const ScoreK& sk, float alibi, float lse2,
-                                         float dp, float delta, bool ok, uint32_t zm,
-                                         float& pr, float& ds) {
-  float arg, dcap = 1.f;
+__device__ __forceinline__ void p_only(float xs, const ScoreK& sk, float alibi, float lse2,
+                                       bool ok, float& pr, float& dcap) {
+  float arg;
+  dcap = 1.f;
   if (kSoftcap) {
     const float pre = kAlibi ? fmaf(xs, sk.k1, alibi) : xs * sk.k1;
     const float t = 1.0f - 2.0f * rcp_approx(1.0f + ex2_approx(pre));  // tanh(pre_cap / c)
@@ -102,8 +105,20 @@ __device__ __forceinline__ void p_and_ds(float xs, const ScoreK& sk, float alibi
     arg = fmaf(xs, sk.k1, -lse2);
   }
   pr = ex2_approx(ok ? arg : -INFINITY);
+}
+// dS of one element from its P (and soft-cap derivative), as p_and_ds.
+template <bool kSoftcap>
+__device__ __forceinline__ float ds_of(float pr, float dcap, float dp, float delta, uint32_t zm) {
   const float dpz = __uint_as_float(__float_as_uint(dp) & zm);
-  ds = kSoftcap ? pr * (dpz - delta) * dcap : pr * (dpz - delta);
+  return kSoftcap ? pr * (dpz - delta) * dcap : pr * (dpz - delta);
+}
+template <bool kAlibi, bool kSoftcap>
+__device__ __forceinline__ void p_and_ds(float xs, const ScoreK& sk, float alibi, float lse2,
+                                         float dp, float delta, bool ok, uint32_t zm,
+                                         float& pr, float& ds) {
+  float dcap;
+  p_only<kAlibi, kSoftcap>(xs, sk, alibi, lse2, ok, pr, dcap);
+  ds = ds_of<kSoftcap>(pr, dcap, dp, delta, zm);
 }
 
 // Dropout keep flags (keep_flags4 layout: flag of column c in byte c % 4 of word c / 4)
@@ -161,7 +176,7 @@ struct Layout {
   static constexpr int kAlloc = kBars + 256 + 1024;
 };
 template <int D> using LayoutQ = Layout<D, kStagesQ, 0, false>;
-template <int D> using LayoutKv = Layout<D, kStagesKv, 2, true>;  // fixed: V, then K
+template <int D> using LayoutKv = Layout<D, kStagesKv, 1, true>;  // fixed: K
 static_assert(LayoutKv<128>::kAlloc <= 232448 && LayoutQ<128>::kAlloc <= 232448,
               "shared memory per CTA");
 
@@ -169,7 +184,8 @@ struct BwdBars {
   uint64_t fixed_full;             // the two fixed tiles
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t s_full[2];              // S_x and dP_x in TMEM (dkdv: buffer 0 only)
+  uint64_t s_full[2];              // S_x and dP_x in TMEM (dkdv: S^T_x)
+  uint64_t dp_full;                // dkdv: dP^T in TMEM
   uint64_t pd_free[2];             // dkdv: P^T / dS^T read by their MMAs (entry 0)
   uint64_t acc_full;               // accumulators final
   uint32_t tmem_base;
@@ -179,9 +195,10 @@ struct BwdBars {
 struct BwdArgs {
   Problem p;
   RowTerms rt;
-  const __nv_bfloat16* q;     // Q, dO [B, Hq, Nq, d] and K [B, Hkv, Nkv, d]: the tiles the
-  const __nv_bfloat16* dout;  // kernels keep in tensor memory are copied from here
+  const __nv_bfloat16* q;     // Q, dO [B, Hq, Nq, d] and K, V [B, Hkv, Nkv, d]: the tiles
+  const __nv_bfloat16* dout;  // the kernels keep in tensor memory are copied from here
   const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -211,6 +228,7 @@ __device__ __forceinline__ void setup_common(BwdBars* bars, int stages) {
     mbar_init(smem_u32(&bars->s_full[x]), 1);
     mbar_init(smem_u32(&bars->pd_free[x]), 1);
   }
+  mbar_init(smem_u32(&bars->dp_full), 1);
   mbar_init(smem_u32(&bars->acc_full), 1);
   bars->abort_flag = 0;
   fence_barrier_init();

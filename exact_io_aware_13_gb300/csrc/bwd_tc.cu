@@ -44,38 +44,35 @@
 namespace attn {
 namespace {
 
-// dkdv element-wise step for one thread: key row j, 16 query columns starting at qs,
-// with their lse2 / delta / first key. Writes P^T and dS^T (bf16 pairs). kMasked adds
-// the per-element mask test; the caller picks the variant by a warp-uniform tile test.
+// dkdv element-wise step, first phase, for one thread: key row j, 16 query columns
+// starting at qs, with their lse2 / first key. Gives P (pv, kept for the second phase),
+// the soft-cap derivative (dc) and P^T (bf16 pairs, times the keep mask with dropout).
+// kMasked adds the per-element mask test; the caller picks the variant by a warp-uniform
+// tile test.
 template <bool kAlibi, bool kSoftcap, bool kMasked, bool kDrop>
-__device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_t (&dr)[16],
-                                         const float* lse2, const float* dl, const int* fk,
-                                         const ScoreK& sk, float base, int j, int qs,
-                                         bool key_ok, bool causal_type, const uint32_t (&kf)[4],
-                                         uint32_t (&pp)[8], uint32_t (&dd)[8]) {
+__device__ __forceinline__ void dkdv_p(const uint32_t (&sr)[16], const float* lse2,
+                                       const int* fk, const ScoreK& sk, float base, int j,
+                                       int qs, bool key_ok, bool causal_type,
+                                       const uint32_t (&kf)[4], float (&pv)[16],
+                                       float (&dc)[16], uint32_t (&pp)[8]) {
   if constexpr (!kAlibi && !kSoftcap && !kMasked && !kDrop) {
     // Two query columns per instruction (packed fp32 pairs): a = lse2 - k1 x, P = 2^-a
-    // (the same value as 2^(k1 x - lse2): the negation is exact), dS = P (dP - D).
+    // (the same value as 2^(k1 x - lse2): the negation is exact).
     const uint64_t nk1 = f32x2(-sk.k1, -sk.k1);
 #pragma unroll
     for (int e4 = 0; e4 < 4; ++e4) {
       const float4 lv = reinterpret_cast<const float4*>(lse2)[e4];
-      const float4 dv = reinterpret_cast<const float4*>(dl)[e4];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int col = e4 * 4 + 2 * h;
         const uint64_t l2 = h ? f32x2(lv.z, lv.w) : f32x2(lv.x, lv.y);
-        const uint64_t d2 = h ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y);
         float a0, a1;
         f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])),
                               nk1, l2), a0, a1);
-        const float p0 = ex2_approx(-a0), p1 = ex2_approx(-a1);
-        const uint64_t t2 =
-            sub_f32x2(f32x2(__uint_as_float(dr[col]), __uint_as_float(dr[col + 1])), d2);
-        float s0, s1;
-        f32x2_split(mul_f32x2(f32x2(p0, p1), t2), s0, s1);
-        pp[col >> 1] = pack_bf16x2(p0, p1);
-        dd[col >> 1] = pack_bf16x2(s0, s1);
+        pv[col] = ex2_approx(-a0);
+        pv[col + 1] = ex2_approx(-a1);
+        dc[col] = dc[col + 1] = 1.f;
+        pp[col >> 1] = pack_bf16x2(pv[col], pv[col + 1]);
       }
     }
     return;
@@ -83,10 +80,8 @@ __device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_
 #pragma unroll
   for (int e4 = 0; e4 < 4; ++e4) {
     const float4 lv = reinterpret_cast<const float4*>(lse2)[e4];
-    const float4 dv = reinterpret_cast<const float4*>(dl)[e4];
     const float lvs[4] = {lv.x, lv.y, lv.z, lv.w};
-    const float dvs[4] = {dv.x, dv.y, dv.z, dv.w};
-    float pv[4], dsv[4];
+    float pz[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int col = e4 * 4 + q;
@@ -95,16 +90,54 @@ __device__ __forceinline__ void dkdv_pds(const uint32_t (&sr)[16], const uint32_
         const int i = qs + col;
         ok = key_ok && (!causal_type || (i >= j && fk[col] <= j));
       }
-      const uint32_t zm = kDrop ? keep_mask_elem(kf[e4], q) : 0xffffffffu;
-      p_and_ds<kAlibi, kSoftcap>(__uint_as_float(sr[col]), sk,
-                                 kAlibi ? fmaf(-(float)col, sk.kb, base) : 0.f, lvs[q],
-                                 __uint_as_float(dr[col]), dvs[q], ok, zm, pv[q], dsv[q]);
-      if (kDrop) pv[q] = __uint_as_float(__float_as_uint(pv[q]) & zm);  // dV takes P Z
+      p_only<kAlibi, kSoftcap>(__uint_as_float(sr[col]), sk,
+                               kAlibi ? fmaf(-(float)col, sk.kb, base) : 0.f, lvs[q], ok,
+                               pv[col], dc[col]);
+      pz[q] = pv[col];
+      if (kDrop)  // dV takes P Z
+        pz[q] = __uint_as_float(__float_as_uint(pz[q]) & keep_mask_elem(kf[e4], q));
     }
-    pp[2 * e4] = pack_bf16x2(pv[0], pv[1]);
-    pp[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
-    dd[2 * e4] = pack_bf16x2(dsv[0], dsv[1]);
-    dd[2 * e4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+    pp[2 * e4] = pack_bf16x2(pz[0], pz[1]);
+    pp[2 * e4 + 1] = pack_bf16x2(pz[2], pz[3]);
+  }
+}
+
+// dkdv element-wise step, second phase: dS^T (bf16 pairs) from P, the soft-cap derivative
+// and dP^T of the thread's 16 columns with their delta; the same arithmetic as p_and_ds.
+template <bool kSoftcap, bool kDrop>
+__device__ __forceinline__ void dkdv_ds(const uint32_t (&dr)[16], const float* dl,
+                                        const float (&pv)[16], const float (&dc)[16],
+                                        const uint32_t (&kf)[4], uint32_t (&dd)[8]) {
+  if constexpr (!kSoftcap && !kDrop) {  // packed fp32 pairs: dS = P (dP - D)
+#pragma unroll
+    for (int e4 = 0; e4 < 4; ++e4) {
+      const float4 dv = reinterpret_cast<const float4*>(dl)[e4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int col = e4 * 4 + 2 * h;
+        const uint64_t d2 = h ? f32x2(dv.z, dv.w) : f32x2(dv.x, dv.y);
+        const uint64_t t2 =
+            sub_f32x2(f32x2(__uint_as_float(dr[col]), __uint_as_float(dr[col + 1])), d2);
+        float s0, s1;
+        f32x2_split(mul_f32x2(f32x2(pv[col], pv[col + 1]), t2), s0, s1);
+        dd[col >> 1] = pack_bf16x2(s0, s1);
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int e4 = 0; e4 < 4; ++e4) {
+    const float4 dv = reinterpret_cast<const float4*>(dl)[e4];
+    const float dvs[4] = {dv.x, dv.y, dv.z, dv.w};
+    float ds[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int col = e4 * 4 + q;
+      const uint32_t zm = kDrop ? keep_mask_elem(kf[e4], q) : 0xffffffffu;
+      ds[q] = ds_of<kSoftcap>(pv[col], dc[col], __uint_as_float(dr[col]), dvs[q], zm);
+    }
+    dd[2 * e4] = pack_bf16x2(ds[0], ds[1]);
+    dd[2 * e4 + 1] = pack_bf16x2(ds[2], ds[3]);
   }
 }
 
@@ -200,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kS = L::kStageCount;
 
   if (warp == kLoadWarp) {
-    load_loop<D, L>(smem, bars, wc, lane, &maps.v128, k0, bg, &maps.q64, &maps.do64, subs,
-                    slice, &a.rt, p.nq_pad, &maps.k128);
+    load_loop<D, L>(smem, bars, wc, lane, &maps.k128, k0, bg, &maps.q64, &maps.do64, subs,
+                    slice, &a.rt, p.nq_pad);
   } else if (warp == kRelayWarp) {
     relay_loop<kS>(bars, wc, subs);
   } else if (warp == kMmaWarp) {
@@ -209,41 +242,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp walks the schedule and waits on named barriers; every lane executes
     // the MMA instructions predicated on `issuer`, the one lane elect.sync picks, so the
     // warp never diverges (an elect.sync predicate issues an MMA in about 47 cycles, a
-    // predicate computed from the lane index in about 82). If the fixed tiles never
-    // arrive (`ok` false) the warp keeps every barrier operation and issues nothing.
-    // S^T / dP^T of sub-step v go to buffer v % 2. Issue order: S^T/dP^T(0) and (1), then
-    // per sub-step u: dV/dK(u) once P^T / dS^T(u) are written over buffer u % 2, and right
-    // behind them S^T/dP^T(u + 2) into the same buffer (the tensor pipe runs a thread's
-    // MMAs in order, so they overwrite it only after dV/dK(u) have read it). The tensor
-    // pipe thus has S^T/dP^T(u + 1) done and S^T/dP^T(u + 2) queued while the element-wise
-    // warps work on u + 1: they never wait for the MMA warp, nor it for their release.
-    const uint32_t sV = smem_u32(smem + L::kFixA), sK = sV + L::kFixTile;
+    // predicate computed from the lane index in about 82). If the fixed tile never
+    // arrives (`ok` false) the warp keeps every barrier operation and issues nothing.
+    // S^T(v) = K Q^T goes to buffer v % 2 (K in shared memory), dP^T(v) = V dO^T to the
+    // one dP^T buffer (V in tensor memory: the tensor core then reads only dO from shared
+    // memory, 32 instead of 48 cycles per N = 64 instruction). Per sub-step u: dV(u) once
+    // P^T(u) is written over the first halves of its S^T buffer; dP^T(u + 1) as soon as
+    // the element-wise warps hold dP^T(u) in registers; dK(u) once dS^T(u) is written over
+    // the second halves of the S^T buffer; then S^T(u + 2) into that buffer (the tensor
+    // pipe runs a thread's MMAs in order, so each overwrites a buffer only after the
+    // products reading it have run).
+    const uint32_t sK = smem_u32(smem + L::kFixA);
     const uint32_t ring = smem_u32(smem + L::kRing);
     const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc));
     const bool issuer = elect_one();
-    auto issue_sdp = [&](int v) {  // S^T and dP^T of sub-step v into buffer v % 2
-      const int s = v % kS, x = v & 1;
-      nb_sync(kNbStage + s, kNbStageCount);
+    auto stage = [&](int v) { return ring + (v % kS) * L::kStage; };  // Q slice, then dO
+    auto sync_stage = [&](int v) {
+      nb_sync(kNbStage + v % kS, kNbStageCount);
       tc_fence_after_sync();
-      if (!ok) return;
-      const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
-      mma_128x64<D>(issuer, tmem + kv_col_s(x), sK, sQ);    // S^T = K Q^T
-      mma_128x64<D>(issuer, tmem + kv_col_dp(x), sV, sDO);  // dP^T = V dO^T
-      mma_commit_if(issuer, smem_u32(&bars->s_full[x]));
     };
-    issue_sdp(0);
-    if (subs > 1) issue_sdp(1);
+    auto issue_s = [&](int v) {  // S^T(v); stage v synced
+      if (!ok) return;
+      mma_128x64<D>(issuer, tmem + kv_col_s(v & 1), sK, stage(v));
+      mma_commit_if(issuer, smem_u32(&bars->s_full[v & 1]));
+    };
+    auto issue_dp = [&](int v) {  // dP^T(v); stage v synced
+      if (!ok) return;
+      mma_tmem_x64<D>(issuer, tmem + kKv2ColDP, tmem + kKv2ColV, stage(v) + L::kSubTile);
+      mma_commit_if(issuer, smem_u32(&bars->dp_full));
+    };
+    nb_sync(kNbQL, kNbKvCount);  // the V tile is in tensor memory
+    tc_fence_after_sync();
+    sync_stage(0);
+    issue_s(0);
+    issue_dp(0);
+    if (subs > 1) {
+      sync_stage(1);
+      issue_s(1);
+    }
     for (int u = 0; u < subs; ++u) {
-      const int s = u % kS, x = u & 1;
-      nb_sync(kNbKvP + x, kNbKvCount);  // P^T / dS^T(u) written over buffer x
+      const int x = u & 1;
+      nb_sync(kNbKvP + x, kNbKvCount);  // P^T(u) written over S^T buffer x
       tc_fence_after_sync();
-      if (ok) {
-        const uint32_t sQ = ring + s * L::kStage, sDO = sQ + L::kSubTile;
-        mma_inplace_x_slice<D>(issuer, tmem + colDV, tmem + kv_col_s(x), sDO, u > 0);   // dV += P^T dO
-        mma_inplace_x_slice<D>(issuer, tmem + colDK, tmem + kv_col_dp(x), sQ, u > 0);  // dK += dS^T Q
-        mma_commit_if(issuer, smem_u32(&bars->empty[s]));  // stage (and its row terms) free
+      if (ok)  // dV += P^T dO
+        mma_inplace_x_slice<D>(issuer, tmem + colDV, tmem + kv_col_s(x), stage(u) + L::kSubTile,
+                               u > 0);
+      nb_sync(kNbKvF, kNbKvCount);  // dP^T(u) read: the buffer takes dP^T(u + 1)
+      tc_fence_after_sync();
+      if (u + 1 < subs) issue_dp(u + 1);  // its stage was synced for S^T(u + 1)
+      nb_sync(kNbKvD, kNbKvCount);  // dS^T(u) written over the second halves of buffer x
+      tc_fence_after_sync();
+      if (ok) {  // dK += dS^T Q
+        mma_inplace_x_slice<D>(issuer, tmem + colDK, tmem + kv_col_s(x) + 8, stage(u), u > 0);
+        mma_commit_if(issuer, smem_u32(&bars->empty[u % kS]));  // stage (and its row terms) free
       }
-      if (u + 2 < subs) issue_sdp(u + 2);
+      if (u + 2 < subs) {
+        sync_stage(u + 2);
+        issue_s(u + 2);
+      }
     }
     if (ok) mma_commit_if(issuer, smem_u32(&bars->acc_full));
   } else {
@@ -255,6 +311,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const int c0 = wg * 16;
     const bool causal_type = p.mask.kind != ATTN_MASK_NONE;
+    {
+      // This thread's V row into tensor memory (bf16 pairs, the A operand of dP^T =
+      // V dO^T): warpgroup wg copies words [wg D/8, (wg + 1) D/8) of the row's D/2 (zeros
+      // past Nkv).
+      constexpr int kW = D / 8;
+      uint32_t wv[kW];
+      const bool row_in = j < p.Nkv;
+      const uint4* src = reinterpret_cast<const uint4*>(
+                             a.v + ((size_t)bg * p.Nkv + (row_in ? j : 0)) * D) + wg * (kW / 4);
+#pragma unroll
+      for (int e = 0; e < kW / 4; ++e) {
+        const uint4 v = row_in ? src[e] : make_uint4(0, 0, 0, 0);
+        wv[4 * e] = v.x; wv[4 * e + 1] = v.y; wv[4 * e + 2] = v.z; wv[4 * e + 3] = v.w;
+      }
+      const uint32_t dst = tmem + lane_base + kKv2ColV + wg * kW;
+      if constexpr (kW == 16) tmem_st16(dst, wv);
+      else tmem_st8(dst, wv);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      nb_arrive(kNbQL, kNbKvCount);
+    }
     bool ok_all = true;
     // (head, query tile) of sub-step u, its score constants and whether the tile needs
     // the per-element mask, advanced every second sub-step (the order `slice` gives)
@@ -275,44 +352,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qrow = (qr.lo + st_q) * BT + x * SUB;
       const int bh = b * p.Hq + g * G + st_h;
       const int qs = qrow + c0;                  // query of this thread's column 0
+      const float* lse2 = reinterpret_cast<const float*>(smem + L::kRows + s * L::kRowStage) + c0;
+      const float* dl = lse2 + SUB;
+      const int* fk = reinterpret_cast<const int*>(dl + SUB);
+      // ---- first phase: P^T(u) over the first half of this warpgroup's 16 columns of
+      // S^T buffer x (k-step wg of the dV product); no other warp reads those columns
       if (ok_all)
         ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full[x]), (u >> 1) & 1, wc));
       // the stage's row terms arrived with full[s]; observe them
       if (ok_all)
         ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (u / kS) & 1, wc));
-      if (!ok_all) {  // aborted: keep the barrier schedule with the MMA warp
+      float pv[16], dc[16];
+      uint32_t kf[4] = {0u, 0u, 0u, 0u};
+      if (ok_all) {
+        tc_fence_after_sync();
+        const uint32_t tS = tmem + lane_base + kv_col_s(x) + c0;
+        uint32_t sr[16], pp[8];
+        tmem_ld16(tS, sr);
+        tmem_wait_ld();
+        reg_fence16(sr);
+        const float base = kAlibi ? sk.kb * (float)(j - qs) : 0.f;  // kb*(j - i) at column 0
+        if constexpr (kDrop) dropout_flags_dkdv(p, dthr, j, lane, qs, bh, kf);
+        if (need_mask)  // warp-uniform
+          dkdv_p<kAlibi, kSoftcap, true, kDrop>(sr, lse2, fk, sk, base, j, qs, j < p.Nkv,
+                                                causal_type, kf, pv, dc, pp);
+        else
+          dkdv_p<kAlibi, kSoftcap, false, kDrop>(sr, lse2, fk, sk, base, j, qs, true,
+                                                 causal_type, kf, pv, dc, pp);
+        tmem_st8(tS, pp);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        nb_arrive(kNbKvP + x, kNbKvCount);
+      } else {  // aborted: keep the barrier schedule with the MMA warp
         nb_sync(kNbKvP + x, kNbKvCount);
-        continue;
       }
-      tc_fence_after_sync();
-      const uint32_t tS = tmem + lane_base + kv_col_s(x) + c0;
-      const uint32_t tDP = tmem + lane_base + kv_col_dp(x) + c0;
-      uint32_t sr[16], dr[16];
-      tmem_ld16(tS, sr);
-      tmem_ld16(tDP, dr);
-      tmem_wait_ld();
-      reg_fence16(sr);
-      reg_fence16(dr);
-      const float* lse2 = reinterpret_cast<const float*>(smem + L::kRows + s * L::kRowStage) + c0;
-      const float* dl = lse2 + SUB;
-      const int* fk = reinterpret_cast<const int*>(dl + SUB);
-      const float base = kAlibi ? sk.kb * (float)(j - qs) : 0.f;  // kb*(j - i) at column 0
-      uint32_t kf[4];
-      if constexpr (kDrop) dropout_flags_dkdv(p, dthr, j, lane, qs, bh, kf);
-      uint32_t pp[8], dd[8];
-      if (need_mask)  // warp-uniform
-        dkdv_pds<kAlibi, kSoftcap, true, kDrop>(sr, dr, lse2, dl, fk, sk, base, j, qs,
-                                                j < p.Nkv, causal_type, kf, pp, dd);
-      else
-        dkdv_pds<kAlibi, kSoftcap, false, kDrop>(sr, dr, lse2, dl, fk, sk, base, j, qs, true,
-                                                 causal_type, kf, pp, dd);
-      // P^T and dS^T over the first half of this warpgroup's own 16 columns of S^T and
-      // dP^T (k-step wg of the dV and dK products); no other warp reads those columns
-      tmem_st8(tS, pp);
-      tmem_st8(tDP, dd);
-      tmem_wait_st();
-      tc_fence_before_sync();
-      nb_arrive(kNbKvP + x, kNbKvCount);
+      // ---- second phase: dP^T(u) into registers (then the buffer is released), dS^T(u)
+      // over the second half of this warpgroup's 16 columns of S^T buffer x (k-step wg of
+      // the dK product)
+      if (ok_all)
+        ok_all = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->dp_full), u & 1, wc));
+      if (ok_all) {
+        tc_fence_after_sync();
+        uint32_t dr[16], dd[8];
+        tmem_ld16(tmem + lane_base + kKv2ColDP + c0, dr);
+        tmem_wait_ld();
+        reg_fence16(dr);
+        tc_fence_before_sync();
+        nb_arrive(kNbKvF, kNbKvCount);
+        dkdv_ds<kSoftcap, kDrop>(dr, dl, pv, dc, kf, dd);
+        tmem_st8(tmem + lane_base + kv_col_s(x) + c0 + 8, dd);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        nb_arrive(kNbKvD, kNbKvCount);
+      } else {  // aborted: keep the barrier schedule with the MMA warp
+        nb_sync(kNbKvF, kNbKvCount);
+        nb_sync(kNbKvD, kNbKvCount);
+      }
     }
     // ---------------------------------------------------------- epilogue
     // warpgroups 0 and 1 write the two halves of dV, 2 and 3 those of dK (times the
@@ -543,11 +638,11 @@ cudaError_t launch_d(const BwdArgs& ka, const BwdArgs& qa, const BwdMaps& maps, 
 
 cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
                           const __nv_bfloat16* q, const __nv_bfloat16* dout,
-                          const __nv_bfloat16* k, __nv_bfloat16* dq, __nv_bfloat16* dk,
-                          __nv_bfloat16* dv,
+                          const __nv_bfloat16* k, const __nv_bfloat16* v, __nv_bfloat16* dq,
+                          __nv_bfloat16* dk, __nv_bfloat16* dv,
                           bool run_dkdv, bool run_dq, cudaStream_t st) {
-  BwdArgs ka{p, rt, q, dout, k, dq, dk, dv, ceil_div(p.Nkv, BT)};
-  BwdArgs qa{p, rt, q, dout, k, dq, dk, dv, ceil_div(p.Nq, BT)};
+  BwdArgs ka{p, rt, q, dout, k, v, dq, dk, dv, ceil_div(p.Nkv, BT)};
+  BwdArgs qa{p, rt, q, dout, k, v, dq, dk, dv, ceil_div(p.Nq, BT)};
   const long long gk = run_dkdv ? (long long)ka.n_tiles * p.B * p.Hkv : 0;
   const long long gq = run_dq ? (long long)qa.n_tiles * p.B * p.Hq : 0;
   if (gk > 0x7fffffffLL || gq > 0x7fffffffLL) return cudaErrorInvalidValue;

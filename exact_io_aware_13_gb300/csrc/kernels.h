@@ -95,8 +95,9 @@ struct BwdMaps {
 };
 cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
                           const __nv_bfloat16* q, const __nv_bfloat16* dout,
-                          const __nv_bfloat16* k, __nv_bfloat16* dq, __nv_bfloat16* dk,
-                          __nv_bfloat16* dv, bool run_dkdv, bool run_dq, cudaStream_t st);
+                          const __nv_bfloat16* k, const __nv_bfloat16* v, __nv_bfloat16* dq,
+                          __nv_bfloat16* dk, __nv_bfloat16* dv, bool run_dkdv, bool run_dq,
+                          cudaStream_t st);
 // Head dimension 256: dV, dK (two walks over the key tiles) and dQ.
 cudaError_t launch_bwd256_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
                              const __nv_bfloat16* q, const __nv_bfloat16* dout,
