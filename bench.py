@@ -147,16 +147,14 @@ KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", 
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201399296 + 45270528,
-                    "sha256": "1b4fe1ac8a93db4f9b57ca31b5a0fff6b9211b4f6d0740a540bd4a14257f203d"},
-    "rowdot_kernel": {"bytes": 135301120 + 723456,
-                    "sha256": "e3f10b1049cb305469a507d32799ff9d6ed4d8e675ae1b8a3002df13b78e277d"},
-    "dkdv_kernel": {"bytes": 270627584 + 99481856,
-                  "sha256": "afda9888658aff93747f45983c9dd1d8a6e5182237ddbf58428056194019a1fb"},
-    "dq_kernel": {"bytes": 270753024 + 48598016,
-                "sha256": "afda9888658aff93747f45983c9dd1d8a6e5182237ddbf58428056194019a1fb"},
-    "decode_tc_kernel": {"bytes": 1119353088 + 8705536,
-                       "sha256": "89f74c5dfeeba63123aece6e2ff94a2c511ec0108a959143810c3f46fac1080e"},
+    "fwd_tc_kernel": {"bytes": 201406208 + 45281280,
+                    "sha256": "19531e01ca6683a27cd5d4ade74c6fbb40e37d577e183b4684c84417914c75ba"},
+    "rowdot_kernel": {"bytes": 135297536 + 710656,
+                    "sha256": "ae2c590a5cc20eaad705db375e11707d86b543c6a10739e7cabc6ff933c78708"},
+    "dkdv_kernel": {"bytes": 270739712 + 99273728,
+                  "sha256": "3bb238afe581b8a9ff52da149c798556f438e3b0023e43740e50f7bd44108748"},
+    "dq_kernel": {"bytes": 270746880 + 48775936,
+                "sha256": "3bb238afe581b8a9ff52da149c798556f438e3b0023e43740e50f7bd44108748"},
 }
 
 def kernel_source_sha(kernel: str) -> str:
