@@ -21,19 +21,21 @@
 // epilogues multiply dV, dK and dQ by 1 / (1 - p).
 // Each sub-step streams its own 64-row slice of the two operands it walks (Q and dO,
 // or K and V; for dkdv also the 64 rows' L log2 e, D and first key) through a
-// shared-memory ring (4 stages for dkdv, 6 for dq), so loads run ahead of the MMAs. Warp
+// shared-memory ring (5 stages for dkdv, 6 for dq), so loads run ahead of the MMAs. Warp
 // 16 loads with TMA, warp 17 owns tensor memory and issues the MMAs, warp 18 relays TMA
 // completions; warps 0-15 do the element-wise work, one thread per TMEM lane (= row of
 // the CTA's tile). The MMA warp waits only on hardware named barriers: a shared-memory
 // access from the thread that issues MMAs stalls the tensor pipe (see nb_sync in
 // ptx.cuh).
-//   dkdv: K and V are fixed in shared memory (A operands of S^T = K Q^T and dP^T =
-//     V dO^T); S^T / dP^T are double-buffered in tensor memory (sub-step u in buffer
-//     u % 2) and P^T / dS^T are written as bf16 pairs over them, so the MMA warp issues
-//     S^T / dP^T(u + 2) right behind dV / dK(u), without waiting for the element-wise
-//     warps: the tensor pipe runs a thread's MMAs in order, and the element-wise warps
-//     find S^T / dP^T(u + 1) done when they finish u. Every element-wise warp works on
-//     every sub-step (warpgroup w: 16 of its 64 query columns).
+//   dkdv: K is fixed in shared memory (A operand of S^T = K Q^T) and V is copied once
+//     into tensor memory (A operand of dP^T = V dO^T, so that product reads only dO from
+//     shared memory); S^T is double-buffered in tensor memory (sub-step u in buffer
+//     u % 2), dP^T single-buffered. The element-wise warps write P^T and then dS^T as
+//     bf16 pairs into the two halves of their columns of the S^T buffer; the dP^T buffer
+//     is free as soon as they hold dP^T in registers, so dP^T(u + 1) runs while they form
+//     dS(u), and S^T(u + 2) follows dV / dK(u) into its buffer (the tensor pipe runs a
+//     thread's MMAs in order). Every element-wise warp works on every sub-step (warpgroup
+//     w: 16 of its 64 query columns).
 //   dq: two pairs of warpgroups alternate sub-steps (pair p takes u % 2 == p, warpgroup
 //     w of the pair 32 key columns); S / dP are double-buffered and dS is written back
 //     over S.
