@@ -157,9 +157,9 @@ __device__ __forceinline__ void dropout_flags_dq(const Problem& p, const DropThr
 }
 
 // Shared-memory layouts. dq: a ring of kS stages, each holding a 64-row slice of K and
-// V (Q and dO live in tensor memory). dkdv: the V and K tiles (fixed, in that order), a
-// ring of 64-row slices of Q and dO, and each stage's row terms of those 64 query rows
-// (lse2, delta, first key: 256 bytes each).
+// V (Q and dO live in tensor memory). dkdv: the K tile (fixed; V lives in tensor
+// memory), a ring of 64-row slices of Q and dO, and each stage's row terms of those 64
+// query rows (lse2, delta, first key: 256 bytes each).
 template <int D, int kS, int kFixTiles, bool kRowTerms>
 struct Layout {
   static constexpr int kStageCount = kS;
