@@ -155,6 +155,8 @@ NCU_TRAFFIC = {
                   "sha256": "3bb238afe581b8a9ff52da149c798556f438e3b0023e43740e50f7bd44108748"},
     "dq_kernel": {"bytes": 270746880 + 48775936,
                 "sha256": "3bb238afe581b8a9ff52da149c798556f438e3b0023e43740e50f7bd44108748"},
+    "decode_tc_kernel": {"bytes": 1119358208 + 9030400,
+                       "sha256": "86365cf5b845fa7e40eb7505626d17f26eae79312c8d6f763b31ee06139467db"},
 }
 
 def kernel_source_sha(kernel: str) -> str:
