@@ -197,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_v);
         const uint32_t qbar = smem_u32(&bars->q_full);
         mbar_arrive_expect_tx(qbar, kQTiles * L::kTile);
-  #pragma unroll
+#pragma unroll
         for (int t = 0; t < kQTiles; ++t)
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < L::kSlabs; ++c)
             tma_load_3d(smem_u32(smem + L::kQ + t * L::kTile + c * L::kChunk), &tm_q, qbar,
                         c * (128 / L::kElem), q0 + t * BM, bh);
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kFp8 && (u & 1)) {  // V^T tile: keys krow.. (x), all d rows (y)
             tma_load_3d(smem_u32(smem + L::kRing + s * L::kTile), map, fb, krow, 0, bg);
           } else {
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < L::kSlabs; ++c)
               tma_load_3d(smem_u32(smem + L::kRing + s * L::kTile + c * L::kChunk), map, fb,
                           c * (128 / L::kElem), krow, bg);
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dq = smem_desc_sw128(qt, 16, 1024), dk = smem_desc_sw128(kb, 16, 1024);
         const uint32_t col = t == 0 ? L::kColS0 : L::kColS1;
         // 32 bytes of the head dimension per instruction (16 bf16 or 32 e4m3 values)
-  #pragma unroll
+#pragma unroll
         for (int kk = 0; kk < D * L::kElem / 32; ++kk) {
           const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
           if (kFp8) mma_f8_ss_if(issuer, tmem + col, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
@@ -280,13 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t colO = t == 0 ? L::kColO0 : L::kColO1;
         if (kFp8) {  // P (e4m3, 4 per column) x V^T tile (K-major): 32 keys per instruction
           const uint64_t dv = smem_desc_sw128(vb, 16, 1024);
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < BN / 32; ++kk)
             mma_f8_ts_if(issuer, tmem + colO, tmem + colS + kk * 8, dv + ((kk * 32) >> 4), idO,
                          (np[t] > 0 || kk > 0) ? 1u : 0u);
         } else {  // P (bf16 pairs) x V tile used MN-major: 16 keys per instruction
           const uint64_t dv = smem_desc_sw128(vb, L::kChunk, 1024);
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts_if(issuer, tmem + colO, tmem + colS + kk * 8, dv + ((kk * 16 * 128) >> 4), idO,
                       (np[t] > 0 || kk > 0) ? 1u : 0u);
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       sync_stage(0);
-  #pragma unroll
+#pragma unroll
       for (int t = 0; t < kQTiles; ++t)
         if (lo >= rng[t].lo && lo < rng[t].hi) issue_s(t, 0);
       commit(&bars->kv_empty[0]);
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int uv = 2 * jj + 1, uk = 2 * jj + 2;
         const bool next = jj + 1 < n_kv;
         sync_stage(uv);
-  #pragma unroll
+#pragma unroll
         for (int t = 0; t < kQTiles; ++t) {
           if (j >= rng[t].lo && j < rng[t].hi) {
             nb_sync(kNbP + t, kNbPCount);
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit(&bars->kv_empty[uv % kStages]);
         if (next) commit(&bars->kv_empty[uk % kStages]);
       }
-  #pragma unroll
+#pragma unroll
       for (int t = 0; t < kQTiles; ++t) commit(&bars->o_full[t]);
     }
   } else {
@@ -430,6 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      // bf16 P: the exponent argument and the sum chains on column pairs (packed fp32x2
+      // FMAs; each element's operations and its chain order as with scalar ones)
+      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+      const uint64_t mul2 = f32x2(mul, mul), negm2 = f32x2(neg_m, neg_m), one2 = f32x2(1.f, 1.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         if (kFp8) {  // 2^7 P as e4m3, four per column: 32 keys in 8 columns
@@ -470,10 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e8 = 0; e8 < 8; ++e8) {
                 const int e = hf * 8 + e8;
-                const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), mul, neg_m));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
-                acc[(2 * e) & 7] += p0;
-                acc[(2 * e + 1) & 7] += p1;
+                float a0, a1;
+                f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[c][2 * e]),
+                                            __uint_as_float(r[c][2 * e + 1])), mul2, negm2),
+                            a0, a1);
+                const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+                acc2[e & 3] = fma_f32x2(f32x2(p0, p1), one2, acc2[e & 3]);  // acc + p
                 ph[e8] = pack_bf16x2(p0, p1);
                 if (kDrop)  // keys 2e8, 2e8 + 1 of the half: flag bytes (2e8) % 4, +1 of word e8 / 2
                   ph[e8] &= keep_mask_pair(kf[e8 >> 1], 2 * (e8 & 1));
@@ -484,15 +490,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e]), mul, neg_m));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * e + 1]), mul, neg_m));
-              acc[(2 * e) & 7] += p0;
-              acc[(2 * e + 1) & 7] += p1;
+              float a0, a1;
+              f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[c][2 * e]),
+                                          __uint_as_float(r[c][2 * e + 1])), mul2, negm2),
+                          a0, a1);
+              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+              acc2[e & 3] = fma_f32x2(f32x2(p0, p1), one2, acc2[e & 3]);  // acc + p
               pk[e] = pack_bf16x2(p0, p1);
             }
             tmem_st16(tS + c * 16, pk);
           }
         }
+      }
+      if constexpr (!kFp8) {  // chains (acc[2k], acc[2k + 1]) were kept in pairs
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f32x2_split(acc2[e], acc[2 * e], acc[2 * e + 1]);
       }
       l_run += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       if (warp_grow && n > 0) {  // O_t already holds P V of earlier tiles: rescale it
