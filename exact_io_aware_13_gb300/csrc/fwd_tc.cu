@@ -430,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-      // bf16 P: the exponent argument and the sum chains on column pairs (packed fp32x2
-      // FMAs; each element's operations and its chain order as with scalar ones)
+      // The exponent argument and the sum chains on column pairs (packed fp32x2 FMAs; each
+      // element's operations and its chain order as with scalar ones)
       uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
       const uint64_t mul2 = f32x2(mul, mul), negm2 = f32x2(neg_m, neg_m), one2 = f32x2(1.f, 1.f);
 #pragma unroll
@@ -442,9 +442,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 8; ++e) {
             float pv[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              pv[q] = ex2_approx(fmaf(__uint_as_float(r[c][4 * e + q]), mul, neg_m));
-              acc[(4 * e + q) & 7] += pv[q];
+            for (int h = 0; h < 2; ++h) {  // column pairs, as for bf16 P
+              float a0, a1;
+              f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[c][4 * e + 2 * h]),
+                                          __uint_as_float(r[c][4 * e + 2 * h + 1])),
+                                    mul2, negm2),
+                          a0, a1);
+              pv[2 * h] = ex2_approx(a0);
+              pv[2 * h + 1] = ex2_approx(a1);
+              const int k2 = ((4 * e + 2 * h) & 7) >> 1;  // chains (acc[2 k2], acc[2 k2 + 1])
+              acc2[k2] = fma_f32x2(f32x2(pv[2 * h], pv[2 * h + 1]), one2, acc2[k2]);
             }
             pk[e] = pack_e4m3x2(pv[0], pv[1]) | (pack_e4m3x2(pv[2], pv[3]) << 16);
           }
@@ -502,10 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if constexpr (!kFp8) {  // chains (acc[2k], acc[2k + 1]) were kept in pairs
 #pragma unroll
-        for (int e = 0; e < 4; ++e) f32x2_split(acc2[e], acc[2 * e], acc[2 * e + 1]);
-      }
+      for (int e = 0; e < 4; ++e)  // chains (acc[2k], acc[2k + 1]) were kept in pairs
+        f32x2_split(acc2[e], acc[2 * e], acc[2 * e + 1]);
       l_run += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       if (warp_grow && n > 0) {  // O_t already holds P V of earlier tiles: rescale it
 #pragma unroll
