@@ -147,13 +147,13 @@ KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", 
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201406208 + 45281280,
-                    "sha256": "19531e01ca6683a27cd5d4ade74c6fbb40e37d577e183b4684c84417914c75ba"},
-    "rowdot_kernel": {"bytes": 135297536 + 710656,
+    "fwd_tc_kernel": {"bytes": 201397760 + 45327616,
+                    "sha256": "406ec33d1c18136d7febe9959bd5404ef39a696788cdc95f8ae2cef91d8a98a5"},
+    "rowdot_kernel": {"bytes": 135297024 + 668672,
                     "sha256": "ae2c590a5cc20eaad705db375e11707d86b543c6a10739e7cabc6ff933c78708"},
-    "dkdv_kernel": {"bytes": 270739712 + 99273728,
+    "dkdv_kernel": {"bytes": 270658048 + 99216128,
                   "sha256": "3bb238afe581b8a9ff52da149c798556f438e3b0023e43740e50f7bd44108748"},
-    "dq_kernel": {"bytes": 270746880 + 48775936,
+    "dq_kernel": {"bytes": 270991872 + 48239872,
                 "sha256": "3bb238afe581b8a9ff52da149c798556f438e3b0023e43740e50f7bd44108748"},
     "decode_tc_kernel": {"bytes": 1119358208 + 9030400,
                        "sha256": "86365cf5b845fa7e40eb7505626d17f26eae79312c8d6f763b31ee06139467db"},
