@@ -243,8 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp walks the schedule and waits on named barriers; every lane executes
     // the MMA instructions predicated on `issuer`, the one lane elect.sync picks, so the
-    // warp never diverges (an elect.sync predicate issues an MMA in about 47 cycles, a
-    // predicate computed from the lane index in about 82). If the fixed tile never
+    // warp never diverges (with an elect.sync predicate MMAs go out back to back, each
+    // taking its tensor or shared-memory time; a predicate computed from the lane index
+    // costs about 82 cycles per MMA). If the fixed tile never
     // arrives (`ok` false) the warp keeps every barrier operation and issues nothing.
     // S^T(v) = K Q^T goes to buffer v % 2 (K in shared memory), dP^T(v) = V dO^T to the
     // one dP^T buffer (V in tensor memory: the tensor core then reads only dO from shared

@@ -240,8 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ MMA issuer
       // The whole warp walks the schedule and waits on named barriers; every lane executes
       // the MMA instructions predicated on `issuer`, the one lane elect.sync picks, so the
-      // warp never diverges (an elect.sync predicate issues an MMA in about 47 cycles, a
-      // predicate computed from the lane index in about 82). If the Q tiles never arrive
+      // warp never diverges (with an elect.sync predicate MMAs go out back to back, each
+      // taking its tensor or shared-memory time; a predicate computed from the lane index
+      // costs about 82 cycles per MMA). If the Q tiles never arrive
       // (`ok` false) the warp keeps every barrier operation and issues nothing.
       constexpr uint32_t idS = kFp8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idO = kFp8 ? idesc_e4m3_f32(BM, D) : idesc_bf16_f32(BM, D, false, true);
