@@ -149,9 +149,6 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (global_timer_ns() - t0 > kDrainLimitNs) return;
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // ------------------------------------------------------------------ the item list
 // Every warp walks the list itself (all lanes together); the functions below are pure

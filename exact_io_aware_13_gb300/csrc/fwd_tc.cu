@@ -65,6 +65,9 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * 168, "regi
 //   kNbKv + s     ring stage s loaded: relay warp (32) + MMA warp (32)
 constexpr uint32_t kNbP = 1, kNbPCount = 160;
 constexpr uint32_t kNbKv = 3, kNbKvCount = 64;
+//   kNbO + t      O_t staged in shared memory: softmax warpgroup t (128)
+constexpr uint32_t kNbO = kNbKv + kStages, kNbOCount = 128;
+static_assert(kNbO + kQTiles - 1 <= 15, "named barrier ids");
 constexpr int kHeadGroup = 4;  // heads whose CTAs are scheduled together (L2 reuse)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
@@ -124,8 +127,13 @@ __device__ __forceinline__ void cta_work(const FwdArgs& a, int& bh, int& qb) {
 template <int D, bool kAlibi, bool kSoftcap, bool kFp8, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdArgs a) {
   using L = Layout<D, kFp8>;
+  // O (bf16) is staged for its TMA store from offset 0, over the Q tiles (and for FP8 the
+  // first ring stages), all free once the last MMA has completed.
+  constexpr int kOTile = BM * D * 2, kOSlabs = D * 2 / 128;
+  static_assert(kQTiles * kOTile <= L::kBars, "O staging fits below the barriers");
   static_assert(!kFp8 || D == 128, "the FP8 path is built for d = 128");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -531,13 +539,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       nb_arrive(kNbP + t, kNbPCount);
     }
     // ---------------------------------------------------------- epilogue
-    bool have_o = n > 0;  // O_t holds at least one P V product
-    if (have_o) have_o = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full[t]), 0, wc));
+    // Every tile waits for the CTA's last MMA, also a tile without key tiles: the O
+    // staging below writes over shared memory that MMAs of the other tile read (for FP8
+    // the second tile's staging area is the first ring stages).
+    const bool mma_done = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->o_full[t]), 0, wc));
+    const bool have_o = n > 0 && mma_done;  // O_t holds at least one P V product
     tc_fence_after_sync();
     float inv = l_run > 0.f ? 1.f / l_run : 0.f;
     if (kDrop) inv *= p.drop_scale;  // the kept terms' 1 / (1 - p)
     if (kFp8) inv *= a.sv[bg];  // l holds 2^7 times the row sum, like O
-    uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * p.Nq + (i < p.Nq ? i : 0)) * D);
+    // O_t / l goes to shared memory in the layout of the O tensor map's boxes (128-byte
+    // rows of 64 columns, 16-byte chunk c of row r at chunk c ^ (r & 7)), then one thread
+    // stores the tile with TMA; rows past Nq are outside the map and are not written.
+    uint8_t* ostage = smem + t * kOTile + row * 128;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -549,17 +563,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
-      if (i < p.Nq) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-          orow[c * 4 + e] = w;
-        }
+      for (int e = 0; e < 4; ++e) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+        w.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+        w.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+        w.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+        const int g = c * 4 + e;  // 16-byte chunk of the row: slab g / 8, chunk g % 8
+        *reinterpret_cast<uint4*>(ostage + (g >> 3) * L::kChunk + (((g & 7) ^ (row & 7)) << 4)) = w;
       }
+    }
+    fence_proxy_async_smem();
+    nb_sync(kNbO + t, kNbOCount);
+    if (row == 0 && q0 + t * BM < p.Nq) {
+#pragma unroll
+      for (int c = 0; c < kOSlabs; ++c)
+        tma_store_3d(&tm_o, smem_u32(smem + t * kOTile + c * L::kChunk), c * 64, q0 + t * BM, bh);
+      bulk_commit_group();
+      bulk_wait_group_read0();
     }
     if (i < p.Nq)
       a.lse[(size_t)bh * p.Nq + i] =
@@ -579,37 +601,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool kAlibi, bool kSoftcap, bool kFp8 = false, bool kDrop = false>
 cudaError_t launch_variant(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, int grid, cudaStream_t st) {
+                           const CUtensorMap& tv, const CUtensorMap& to, int grid,
+                           cudaStream_t st) {
   auto kern = fwd_tc_kernel<D, kAlibi, kSoftcap, kFp8, kDrop>;
   const int smem = Layout<D, kFp8>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
 template <int D, bool kDrop>
 cudaError_t launch_dd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                      const CUtensorMap& tv, int grid, cudaStream_t st) {
+                      const CUtensorMap& tv, const CUtensorMap& to, int grid, cudaStream_t st) {
   const bool al = a.p.score_kind & ATTN_SCORE_ALIBI, sc = a.p.score_kind & ATTN_SCORE_SOFTCAP;
-  if (al && sc) return launch_variant<D, true, true, false, kDrop>(a, tq, tk, tv, grid, st);
-  if (al) return launch_variant<D, true, false, false, kDrop>(a, tq, tk, tv, grid, st);
-  if (sc) return launch_variant<D, false, true, false, kDrop>(a, tq, tk, tv, grid, st);
-  return launch_variant<D, false, false, false, kDrop>(a, tq, tk, tv, grid, st);
+  if (al && sc) return launch_variant<D, true, true, false, kDrop>(a, tq, tk, tv, to, grid, st);
+  if (al) return launch_variant<D, true, false, false, kDrop>(a, tq, tk, tv, to, grid, st);
+  if (sc) return launch_variant<D, false, true, false, kDrop>(a, tq, tk, tv, to, grid, st);
+  return launch_variant<D, false, false, false, kDrop>(a, tq, tk, tv, to, grid, st);
 }
 
 template <int D>
 cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                     const CUtensorMap& tv, int grid, cudaStream_t st) {
-  if (a.p.score_kind & ATTN_SCORE_DROPOUT) return launch_dd<D, true>(a, tq, tk, tv, grid, st);
-  return launch_dd<D, false>(a, tq, tk, tv, grid, st);
+                     const CUtensorMap& tv, const CUtensorMap& to, int grid, cudaStream_t st) {
+  if (a.p.score_kind & ATTN_SCORE_DROPOUT) return launch_dd<D, true>(a, tq, tk, tv, to, grid, st);
+  return launch_dd<D, false>(a, tq, tk, tv, to, grid, st);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, __nv_bfloat16* o, float* lse,
-                          cudaStream_t st) {
+                          const CUtensorMap& tv, const CUtensorMap& to, __nv_bfloat16* o,
+                          float* lse, cudaStream_t st) {
   FwdArgs a{};
   a.p = p;
   a.o = o;
@@ -618,8 +641,8 @@ cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtenso
   const long long grid = (long long)a.num_qblocks * p.B * p.Hq;
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (p.d == 64) return launch_d<64>(a, tq, tk, tv, (int)grid, st);
-  return launch_d<128>(a, tq, tk, tv, (int)grid, st);
+  if (p.d == 64) return launch_d<64>(a, tq, tk, tv, to, (int)grid, st);
+  return launch_d<128>(a, tq, tk, tv, to, (int)grid, st);
 }
 
 }  // namespace attn
@@ -627,8 +650,9 @@ cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtenso
 namespace attn {
 
 cudaError_t launch_fwd_fp8_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const CUtensorMap& tvt, const float* sq, const float* sk,
-                              const float* sv, __nv_bfloat16* o, float* lse, cudaStream_t st) {
+                              const CUtensorMap& tvt, const CUtensorMap& to, const float* sq,
+                              const float* sk, const float* sv, __nv_bfloat16* o, float* lse,
+                              cudaStream_t st) {
   FwdArgs a{};
   a.p = p;
   a.o = o;
@@ -643,10 +667,10 @@ cudaError_t launch_fwd_fp8_tc(const Problem& p, const CUtensorMap& tq, const CUt
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL || p.d != 128) return cudaErrorInvalidValue;
   const bool al = p.score_kind & ATTN_SCORE_ALIBI, sc = p.score_kind & ATTN_SCORE_SOFTCAP;
-  if (al && sc) return launch_variant<128, true, true, true>(a, tq, tk, tvt, (int)grid, st);
-  if (al) return launch_variant<128, true, false, true>(a, tq, tk, tvt, (int)grid, st);
-  if (sc) return launch_variant<128, false, true, true>(a, tq, tk, tvt, (int)grid, st);
-  return launch_variant<128, false, false, true>(a, tq, tk, tvt, (int)grid, st);
+  if (al && sc) return launch_variant<128, true, true, true>(a, tq, tk, tvt, to, (int)grid, st);
+  if (al) return launch_variant<128, true, false, true>(a, tq, tk, tvt, to, (int)grid, st);
+  if (sc) return launch_variant<128, false, true, true>(a, tq, tk, tvt, to, (int)grid, st);
+  return launch_variant<128, false, false, true>(a, tq, tk, tvt, to, (int)grid, st);
 }
 
 }  // namespace attn
