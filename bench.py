@@ -147,16 +147,16 @@ KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", 
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201397760 + 45327616,
-                    "sha256": "406ec33d1c18136d7febe9959bd5404ef39a696788cdc95f8ae2cef91d8a98a5"},
-    "rowdot_kernel": {"bytes": 135297024 + 668672,
-                    "sha256": "ae2c590a5cc20eaad705db375e11707d86b543c6a10739e7cabc6ff933c78708"},
-    "dkdv_kernel": {"bytes": 270658048 + 99216128,
-                  "sha256": "3bb238afe581b8a9ff52da149c798556f438e3b0023e43740e50f7bd44108748"},
-    "dq_kernel": {"bytes": 270991872 + 48239872,
-                "sha256": "3bb238afe581b8a9ff52da149c798556f438e3b0023e43740e50f7bd44108748"},
-    "decode_tc_kernel": {"bytes": 1119358208 + 9030400,
-                       "sha256": "86365cf5b845fa7e40eb7505626d17f26eae79312c8d6f763b31ee06139467db"},
+    "fwd_tc_kernel": {"bytes": 201570816 + 46057216,
+                    "sha256": "85565b1762344dbb20a93fe55b4f7d2f91a7ef02636590858178dc74c4b703b7"},
+    "rowdot_kernel": {"bytes": 135299072 + 642304,
+                    "sha256": "4c1616d6058462d758ebf4689822312e608faafb85dea15b5e6fb145ccc1e460"},
+    "dkdv_kernel": {"bytes": 270669312 + 99276544,
+                  "sha256": "b3c79c49994bf8e3212cd8560a14e46e0f25a217cfe7af1838e550e0ff5384b7"},
+    "dq_kernel": {"bytes": 270876416 + 48697856,
+                "sha256": "b3c79c49994bf8e3212cd8560a14e46e0f25a217cfe7af1838e550e0ff5384b7"},
+    "decode_tc_kernel": {"bytes": 1119378688 + 8812544,
+                       "sha256": "da0d6ed84259bcd381f21d21b683b1c7746977ad58b535c60c44fe27d0da5c63"},
 }
 
 def kernel_source_sha(kernel: str) -> str:
