@@ -236,12 +236,10 @@ attn_status fwd_common(bool simt, const void* q, const void* k, const void* v, v
     if ((s = make_map(&tv, v, B * Hkv, Nkv, d, 64)) != ATTN_OK) return s;
     return from_cuda(launch_fwd256_tc(p, qb, tk, tv, ob, lse, st));
   }
-  CUtensorMap to;
   if ((s = make_map(&tq, q, B * Hq, Nq, d)) != ATTN_OK) return s;
   if ((s = make_map(&tk, k, B * Hkv, Nkv, d)) != ATTN_OK) return s;
   if ((s = make_map(&tv, v, B * Hkv, Nkv, d)) != ATTN_OK) return s;
-  if ((s = make_map(&to, o, B * Hq, Nq, d)) != ATTN_OK) return s;
-  return from_cuda(launch_fwd_tc(p, tq, tk, tv, to, ob, lse, st));
+  return from_cuda(launch_fwd_tc(p, tq, tk, tv, ob, lse, st));
 }
 
 // Workspace of the backward: the three row-term arrays of RowTerms, each starting on
@@ -522,13 +520,11 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const 
   if ((s = maybe_check_docs(p, dev, st)) != ATTN_OK) return s;
   auto* ob = static_cast<__nv_bfloat16*>(o);
   if (Nkv == 0) return from_cuda(launch_fill_masked(rows_q, d, ob, lse, st));
-  CUtensorMap tq, tk, tvt, to;
+  CUtensorMap tq, tk, tvt;
   if ((s = make_map8(&tq, q8, d, Nq, B * Hq, d)) != ATTN_OK) return s;
   if ((s = make_map8(&tk, k8, d, Nkv, B * Hkv, d)) != ATTN_OK) return s;
   if ((s = make_map8(&tvt, v8t, Nkv, d, B * Hkv, attn_fp8_v_row_bytes(Nkv))) != ATTN_OK) return s;
-  if ((s = make_map(&to, o, B * Hq, Nq, d)) != ATTN_OK) return s;
-  return from_cuda(
-      launch_fwd_fp8_tc(p, tq, tk, tvt, to, q_scale, k_scale, v_scale, ob, lse, st));
+  return from_cuda(launch_fwd_fp8_tc(p, tq, tk, tvt, q_scale, k_scale, v_scale, ob, lse, st));
 }
 
 int attn_decode_split_keys(int B, int Hq, int Hkv, int Nq, long long total_kv_tokens,

@@ -65,9 +65,6 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * 168, "regi
 //   kNbKv + s     ring stage s loaded: relay warp (32) + MMA warp (32)
 constexpr uint32_t kNbP = 1, kNbPCount = 160;
 constexpr uint32_t kNbKv = 3, kNbKvCount = 64;
-//   kNbO + t      O_t staged in shared memory: softmax warpgroup t (128)
-constexpr uint32_t kNbO = kNbKv + kStages, kNbOCount = 128;
-static_assert(kNbO + kQTiles - 1 <= 15, "named barrier ids");
 constexpr int kHeadGroup = 4;  // heads whose CTAs are scheduled together (L2 reuse)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
@@ -127,12 +124,11 @@ __device__ __forceinline__ void cta_work(const FwdArgs& a, int& bh, int& qb) {
 template <int D, bool kAlibi, bool kSoftcap, bool kFp8, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const FwdArgs a) {
+                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   using L = Layout<D, kFp8>;
-  // O (bf16) is staged for its TMA store from offset 0, over the Q tiles (and for FP8 the
+  // O (bf16) is staged on its way out from offset 0, over the Q tiles (and for FP8 the
   // first ring stages), all free once the last MMA has completed.
-  constexpr int kOTile = BM * D * 2, kOSlabs = D * 2 / 128;
+  constexpr int kOTile = BM * D * 2;
   static_assert(kQTiles * kOTile <= L::kBars, "O staging fits below the barriers");
   static_assert(!kFp8 || D == 128, "the FP8 path is built for d = 128");
   extern __shared__ uint8_t smem_raw[];
@@ -184,6 +180,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bars->abort_flag = 0;
     fence_barrier_init();
+    // Q and the first ring uses go out before the rest of the set-up (the loader warp
+    // starts after them).
+    const uint32_t qbar = smem_u32(&bars->q_full);
+    mbar_arrive_expect_tx(qbar, kQTiles * L::kTile);
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t)
+#pragma unroll
+      for (int c = 0; c < L::kSlabs; ++c)
+        tma_load_3d(smem_u32(smem + L::kQ + t * L::kTile + c * L::kChunk), &tm_q, qbar,
+                    c * (128 / L::kElem), q0 + t * BM, bh);
+    for (int u = 0; u < imin(kStages, 2 * n_kv); ++u) {
+      const uint32_t fb = smem_u32(&bars->kv_full[u]);
+      mbar_arrive_expect_tx(fb, L::kTile);
+      const CUtensorMap* map = (u & 1) ? &tm_v : &tm_k;
+      const int krow = (lo + (u >> 1)) * BN;
+      if (kFp8 && (u & 1)) {
+        tma_load_3d(smem_u32(smem + L::kRing + u * L::kTile), map, fb, krow, 0, bg);
+      } else {
+#pragma unroll
+        for (int c = 0; c < L::kSlabs; ++c)
+          tma_load_3d(smem_u32(smem + L::kRing + u * L::kTile + c * L::kChunk), map, fb,
+                      c * (128 / L::kElem), krow, bg);
+      }
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_base), L::kTmemCols);
@@ -204,14 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         const uint32_t qbar = smem_u32(&bars->q_full);
-        mbar_arrive_expect_tx(qbar, kQTiles * L::kTile);
-#pragma unroll
-        for (int t = 0; t < kQTiles; ++t)
-#pragma unroll
-          for (int c = 0; c < L::kSlabs; ++c)
-            tma_load_3d(smem_u32(smem + L::kQ + t * L::kTile + c * L::kChunk), &tm_q, qbar,
-                        c * (128 / L::kElem), q0 + t * BM, bh);
-        for (int u = 0; u < 2 * n_kv; ++u) {
+        for (int u = imin(kStages, 2 * n_kv); u < 2 * n_kv; ++u) {
           const int s = u % kStages, use = u / kStages;
           if (!mbar_wait(smem_u32(&bars->kv_empty[s]), (use & 1) ^ 1, wc)) break;
           const uint32_t fb = smem_u32(&bars->kv_full[s]);
@@ -548,40 +561,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     float inv = l_run > 0.f ? 1.f / l_run : 0.f;
     if (kDrop) inv *= p.drop_scale;  // the kept terms' 1 / (1 - p)
     if (kFp8) inv *= a.sv[bg];  // l holds 2^7 times the row sum, like O
-    // O_t / l goes to shared memory in the layout of the O tensor map's boxes (128-byte
-    // rows of 64 columns, 16-byte chunk c of row r at chunk c ^ (r & 7)), then one thread
-    // stores the tile with TMA; rows past Nq are outside the map and are not written.
-    uint8_t* ostage = smem + t * kOTile + row * 128;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
+    // O_t / l: each warp stages its 32 rows in shared memory over its Q tile (128-byte
+    // rows of 64 columns, 16-byte chunk c of row r at chunk c ^ (r & 7)), then copies them
+    // out with each store instruction writing two whole rows (512 contiguous bytes).
+    uint8_t* otile = smem + t * kOTile;
+    {
+      uint32_t o[D];
       if (have_o) {  // warp-uniform
-        tmem_ld32(tO + c * 32, o);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          tmem_ld32(tO + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
         tmem_wait_ld();
-        reg_fence32(o);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
+        for (int e = 0; e < D; ++e) o[e] = 0u;
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int g = 0; g < D / 8; ++g) {  // 16-byte chunk g of the row: slab g / 8, chunk g % 8
         uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
-        w.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
-        w.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
-        w.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-        const int g = c * 4 + e;  // 16-byte chunk of the row: slab g / 8, chunk g % 8
-        *reinterpret_cast<uint4*>(ostage + (g >> 3) * L::kChunk + (((g & 7) ^ (row & 7)) << 4)) = w;
+        w.x = pack_bf16x2(__uint_as_float(o[8 * g + 0]) * inv, __uint_as_float(o[8 * g + 1]) * inv);
+        w.y = pack_bf16x2(__uint_as_float(o[8 * g + 2]) * inv, __uint_as_float(o[8 * g + 3]) * inv);
+        w.z = pack_bf16x2(__uint_as_float(o[8 * g + 4]) * inv, __uint_as_float(o[8 * g + 5]) * inv);
+        w.w = pack_bf16x2(__uint_as_float(o[8 * g + 6]) * inv, __uint_as_float(o[8 * g + 7]) * inv);
+        *reinterpret_cast<uint4*>(otile + (g >> 3) * L::kChunk + row * 128 +
+                                  (((g & 7) ^ (row & 7)) << 4)) = w;
       }
     }
-    fence_proxy_async_smem();
-    nb_sync(kNbO + t, kNbOCount);
-    if (row == 0 && q0 + t * BM < p.Nq) {
+    __syncwarp();
+    {
+      constexpr int kChunksPerRow = D / 8;               // 16-byte chunks per row
+      constexpr int kRowsPerStore = 32 / kChunksPerRow;  // rows one warp store covers
+      const int g = lane % kChunksPerRow;
+      const int r0 = (warp & 3) * 32;
 #pragma unroll
-      for (int c = 0; c < kOSlabs; ++c)
-        tma_store_3d(&tm_o, smem_u32(smem + t * kOTile + c * L::kChunk), c * 64, q0 + t * BM, bh);
-      bulk_commit_group();
-      bulk_wait_group_read0();
+      for (int k = 0; k < 32 / kRowsPerStore; ++k) {
+        const int r = r0 + k * kRowsPerStore + lane / kChunksPerRow;
+        const uint4 w = *reinterpret_cast<const uint4*>(otile + (g >> 3) * L::kChunk + r * 128 +
+                                                       (((g & 7) ^ (r & 7)) << 4));
+        const int ir = q0 + t * BM + r;
+        if (ir < p.Nq)
+          reinterpret_cast<uint4*>(a.o + ((size_t)bh * p.Nq + ir) * D)[g] = w;
+      }
     }
     if (i < p.Nq)
       a.lse[(size_t)bh * p.Nq + i] =
@@ -601,38 +623,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool kAlibi, bool kSoftcap, bool kFp8 = false, bool kDrop = false>
 cudaError_t launch_variant(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const CUtensorMap& to, int grid,
-                           cudaStream_t st) {
+                           const CUtensorMap& tv, int grid, cudaStream_t st) {
   auto kern = fwd_tc_kernel<D, kAlibi, kSoftcap, kFp8, kDrop>;
   const int smem = Layout<D, kFp8>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, to, a);
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
 template <int D, bool kDrop>
 cudaError_t launch_dd(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                      const CUtensorMap& tv, const CUtensorMap& to, int grid, cudaStream_t st) {
+                      const CUtensorMap& tv, int grid, cudaStream_t st) {
   const bool al = a.p.score_kind & ATTN_SCORE_ALIBI, sc = a.p.score_kind & ATTN_SCORE_SOFTCAP;
-  if (al && sc) return launch_variant<D, true, true, false, kDrop>(a, tq, tk, tv, to, grid, st);
-  if (al) return launch_variant<D, true, false, false, kDrop>(a, tq, tk, tv, to, grid, st);
-  if (sc) return launch_variant<D, false, true, false, kDrop>(a, tq, tk, tv, to, grid, st);
-  return launch_variant<D, false, false, false, kDrop>(a, tq, tk, tv, to, grid, st);
+  if (al && sc) return launch_variant<D, true, true, false, kDrop>(a, tq, tk, tv, grid, st);
+  if (al) return launch_variant<D, true, false, false, kDrop>(a, tq, tk, tv, grid, st);
+  if (sc) return launch_variant<D, false, true, false, kDrop>(a, tq, tk, tv, grid, st);
+  return launch_variant<D, false, false, false, kDrop>(a, tq, tk, tv, grid, st);
 }
 
 template <int D>
 cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                     const CUtensorMap& tv, const CUtensorMap& to, int grid, cudaStream_t st) {
-  if (a.p.score_kind & ATTN_SCORE_DROPOUT) return launch_dd<D, true>(a, tq, tk, tv, to, grid, st);
-  return launch_dd<D, false>(a, tq, tk, tv, to, grid, st);
+                     const CUtensorMap& tv, int grid, cudaStream_t st) {
+  if (a.p.score_kind & ATTN_SCORE_DROPOUT) return launch_dd<D, true>(a, tq, tk, tv, grid, st);
+  return launch_dd<D, false>(a, tq, tk, tv, grid, st);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& to, __nv_bfloat16* o,
-                          float* lse, cudaStream_t st) {
+                          const CUtensorMap& tv, __nv_bfloat16* o, float* lse,
+                          cudaStream_t st) {
   FwdArgs a{};
   a.p = p;
   a.o = o;
@@ -641,8 +662,8 @@ cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtenso
   const long long grid = (long long)a.num_qblocks * p.B * p.Hq;
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (p.d == 64) return launch_d<64>(a, tq, tk, tv, to, (int)grid, st);
-  return launch_d<128>(a, tq, tk, tv, to, (int)grid, st);
+  if (p.d == 64) return launch_d<64>(a, tq, tk, tv, (int)grid, st);
+  return launch_d<128>(a, tq, tk, tv, (int)grid, st);
 }
 
 }  // namespace attn
@@ -650,9 +671,8 @@ cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtenso
 namespace attn {
 
 cudaError_t launch_fwd_fp8_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const CUtensorMap& tvt, const CUtensorMap& to, const float* sq,
-                              const float* sk, const float* sv, __nv_bfloat16* o, float* lse,
-                              cudaStream_t st) {
+                              const CUtensorMap& tvt, const float* sq, const float* sk,
+                              const float* sv, __nv_bfloat16* o, float* lse, cudaStream_t st) {
   FwdArgs a{};
   a.p = p;
   a.o = o;
@@ -667,10 +687,10 @@ cudaError_t launch_fwd_fp8_tc(const Problem& p, const CUtensorMap& tq, const CUt
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL || p.d != 128) return cudaErrorInvalidValue;
   const bool al = p.score_kind & ATTN_SCORE_ALIBI, sc = p.score_kind & ATTN_SCORE_SOFTCAP;
-  if (al && sc) return launch_variant<128, true, true, true>(a, tq, tk, tvt, to, (int)grid, st);
-  if (al) return launch_variant<128, true, false, true>(a, tq, tk, tvt, to, (int)grid, st);
-  if (sc) return launch_variant<128, false, true, true>(a, tq, tk, tvt, to, (int)grid, st);
-  return launch_variant<128, false, false, true>(a, tq, tk, tvt, to, (int)grid, st);
+  if (al && sc) return launch_variant<128, true, true, true>(a, tq, tk, tvt, (int)grid, st);
+  if (al) return launch_variant<128, true, false, true>(a, tq, tk, tvt, (int)grid, st);
+  if (sc) return launch_variant<128, false, true, true>(a, tq, tk, tvt, (int)grid, st);
+  return launch_variant<128, false, false, true>(a, tq, tk, tvt, (int)grid, st);
 }
 
 }  // namespace attn

@@ -66,11 +66,9 @@ cudaError_t launch_fill_masked(long long rows, int d, __nv_bfloat16* o, float* l
 cudaError_t launch_classify(const MaskSpec& m, int32_t* classes, cudaStream_t st);
 
 // ---- tcgen05 tensor-core kernels.
-// tq, to over q and o [B*Hq, Nq, d] (to: the epilogue's TMA store), tk, tv over k, v; all
-// with 64-column x 128-row boxes and the 128-byte swizzle.
 cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& to, __nv_bfloat16* o,
-                          float* lse, cudaStream_t st);
+                          const CUtensorMap& tv, __nv_bfloat16* o, float* lse,
+                          cudaStream_t st);
 // Forward for head dimension 256: q [B*Hq, Nq, 256] bf16 (read by the softmax warps into
 // tensor memory), tk, tv over [B*Hkv, Nkv, 256] with 64 x 64 boxes.
 cudaError_t launch_fwd256_tc(const Problem& p, const __nv_bfloat16* q, const CUtensorMap& tk,
@@ -79,9 +77,8 @@ cudaError_t launch_fwd256_tc(const Problem& p, const __nv_bfloat16* q, const CUt
 // [B*Hkv, 128, Nkv rounded up to 16]; sq [B*Hq, ceil(Nq/128)], sk [B*Hkv, ceil(Nkv/128)],
 // sv [B*Hkv] dequantisation scales (device).
 cudaError_t launch_fwd_fp8_tc(const Problem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const CUtensorMap& tvt, const CUtensorMap& to, const float* sq,
-                              const float* sk, const float* sv, __nv_bfloat16* o, float* lse,
-                              cudaStream_t st);
+                              const CUtensorMap& tvt, const float* sq, const float* sk,
+                              const float* sv, __nv_bfloat16* o, float* lse, cudaStream_t st);
 // Quantisation to e4m3: tiles (one scale per 128 rows of [BH, N, d]) or, for V, one
 // scale per head with the output transposed to [BH, d, ceil16(N)] (zero padded).
 cudaError_t launch_quantize_tiles(const __nv_bfloat16* x, uint8_t* out, float* scales, int BH,

@@ -158,22 +158,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// 3-D tiled store of one box from this CTA's shared memory into global memory (bulk
-// async-group completion). Elements of the box past the tensor's extent are not written.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
-                                             int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
-      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Waits until every committed bulk store of this thread has read its shared memory.
-__device__ __forceinline__ void bulk_wait_group_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 // Orders this thread's ordinary shared-memory writes before later TMA (async-proxy)
 // accesses of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {
