@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const size_t krow = (size_t)bg * p.Nkv + (j < p.Nkv ? j : 0);
     store_acc_row<64>(tmem + lane_base + k256ColAcc + wg * 64, kDk ? p.scale : 1.f,
-                      out + krow * D256 + wg * 64, have, j < p.Nkv);
+                      out + krow * D256 + wg * 64, have, j < p.Nkv, ew_stage<L>(smem, warp));
   }
   teardown256(tmem, warp);
 }
@@ -418,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __all_sync(0xffffffffu, ok_all && mbar_wait(smem_u32(&bars->acc_full), 0, wc));
     tc_fence_after_sync();
     __nv_bfloat16* dst = a.dq + ((size_t)bh * p.Nq + (row_ok ? i : 0)) * D256 + wg * 64;
-    store_acc_row<64>(tmem + lane_base + k256ColAcc + wg * 64, p.scale, dst, have, row_ok);
+    store_acc_row<64>(tmem + lane_base + k256ColAcc + wg * 64, p.scale, dst, have, row_ok,
+                      ew_stage<L>(smem, warp));
   }
   teardown256(tmem, warp);
 }

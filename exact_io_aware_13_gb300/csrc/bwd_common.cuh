@@ -308,12 +308,27 @@ __device__ __forceinline__ void mma_inplace_x_slice(bool pred, uint32_t d_tmem, 
               (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// Write one accumulator row (D fp32 columns at TMEM `t`) times `mul` as bf16.
-// tcgen05.ld is warp-collective: every lane of the warp must call this with the same
-// `live`; `store` (per lane) only decides whether the row is written.
+// Shared memory an element-wise warp stages its output rows in at the end: 32 rows of a
+// 128-byte pitch per warp at the start of the ring, free once the last MMA has completed
+// (every stage consumed).
+constexpr int kStageRowsBytes = 32 * 128;
+template <class L>
+__device__ __forceinline__ uint8_t* ew_stage(uint8_t* smem, int warp) {
+  static_assert(L::kStageCount * L::kStage >= kEwWarps * kStageRowsBytes, "staging fits the ring");
+  return smem + L::kRing + warp * kStageRowsBytes;
+}
+
+// Write one accumulator row per lane (D <= 64 fp32 columns at TMEM `t`) times `mul` as
+// bf16 to `dst` (this lane's row). The warp stages its 32 rows in `stage` (the warp's
+// ew_stage area; 16-byte chunk c of row r at chunk c ^ (r & 7)) and then copies them out
+// with each store instruction writing whole rows. tcgen05.ld is warp-collective: every
+// lane must call this with the same `live`; `store` (per lane) decides whether its row is
+// written.
 template <int D>
 __device__ __forceinline__ void store_acc_row(uint32_t t, float mul, __nv_bfloat16* dst,
-                                              bool live, bool store) {
+                                              bool live, bool store, uint8_t* stage) {
+  static_assert(D % 32 == 0 && D <= 64, "rows of at most 128 bytes");
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
     uint32_t r[32];
@@ -325,18 +340,28 @@ __device__ __forceinline__ void store_acc_row(uint32_t t, float mul, __nv_bfloat
 #pragma unroll
       for (int e = 0; e < 32; ++e) r[e] = 0u;
     }
-    if (store) {
-      uint4* o = reinterpret_cast<uint4*>(dst) + c * 4;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * mul, __uint_as_float(r[8 * e + 1]) * mul);
-        w.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * mul, __uint_as_float(r[8 * e + 3]) * mul);
-        w.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * mul, __uint_as_float(r[8 * e + 5]) * mul);
-        w.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * mul, __uint_as_float(r[8 * e + 7]) * mul);
-        o[e] = w;
-      }
+    for (int e = 0; e < 4; ++e) {
+      uint4 w;
+      w.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * mul, __uint_as_float(r[8 * e + 1]) * mul);
+      w.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * mul, __uint_as_float(r[8 * e + 3]) * mul);
+      w.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * mul, __uint_as_float(r[8 * e + 5]) * mul);
+      w.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * mul, __uint_as_float(r[8 * e + 7]) * mul);
+      const int g = c * 4 + e;
+      *reinterpret_cast<uint4*>(stage + lane * 128 + ((g ^ (lane & 7)) << 4)) = w;
     }
+  }
+  __syncwarp();
+  constexpr int kChunks = D / 8;              // 16-byte chunks per row
+  constexpr int kRowsPerStore = 32 / kChunks;  // rows one warp store instruction covers
+  const int g = lane % kChunks;
+#pragma unroll
+  for (int k = 0; k < 32 / kRowsPerStore; ++k) {
+    const int rr = k * kRowsPerStore + lane / kChunks;  // row (= owning lane) of this piece
+    const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((g ^ (rr & 7)) << 4));
+    const auto d = reinterpret_cast<__nv_bfloat16*>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst), rr));
+    if (__shfl_sync(0xffffffffu, store ? 1 : 0, rr)) reinterpret_cast<uint4*>(d)[g] = w;
   }
 }
 

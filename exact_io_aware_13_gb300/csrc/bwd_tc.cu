@@ -423,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tacc = tmem + lane_base + (which ? colDK : colDV) + half * (D / 2);
     __nv_bfloat16* dst = (which ? a.dk : a.dv) + krow * D + half * (D / 2);
     const float dsc = kDrop ? p.drop_scale : 1.f;  // dV = (P Z)^T dO / (1 - p); dK from dS'
-    store_acc_row<D / 2>(tacc, which ? p.scale * dsc : dsc, dst, have, j < p.Nkv);
+    store_acc_row<D / 2>(tacc, which ? p.scale * dsc : dsc, dst, have, j < p.Nkv,
+                         ew_stage<L>(smem, warp));
   }
   __syncwarp();
   tc_fence_before_sync();
@@ -592,7 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (pair == 0) {  // warp-uniform
       const uint32_t tq = tmem + lane_base + kColAcc + wg * (D / 2);
       __nv_bfloat16* dst = a.dq + ((size_t)bh * p.Nq + (row_ok ? i : 0)) * D + wg * (D / 2);
-      store_acc_row<D / 2>(tq, kDrop ? p.scale * p.drop_scale : p.scale, dst, have, row_ok);
+      store_acc_row<D / 2>(tq, kDrop ? p.scale * p.drop_scale : p.scale, dst, have, row_ok,
+                           ew_stage<L>(smem, warp));
     }
   }
   __syncwarp();
