@@ -147,16 +147,16 @@ KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", 
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201570816 + 46057216,
-                    "sha256": "85565b1762344dbb20a93fe55b4f7d2f91a7ef02636590858178dc74c4b703b7"},
-    "rowdot_kernel": {"bytes": 135299072 + 642304,
-                    "sha256": "4c1616d6058462d758ebf4689822312e608faafb85dea15b5e6fb145ccc1e460"},
-    "dkdv_kernel": {"bytes": 270669312 + 99276544,
-                  "sha256": "b3c79c49994bf8e3212cd8560a14e46e0f25a217cfe7af1838e550e0ff5384b7"},
-    "dq_kernel": {"bytes": 270876416 + 48697856,
-                "sha256": "b3c79c49994bf8e3212cd8560a14e46e0f25a217cfe7af1838e550e0ff5384b7"},
-    "decode_tc_kernel": {"bytes": 1119378688 + 8812544,
-                       "sha256": "da0d6ed84259bcd381f21d21b683b1c7746977ad58b535c60c44fe27d0da5c63"},
+    "fwd_tc_kernel": {"bytes": 201403904 + 46800896,
+                    "sha256": "ce2256683d2f8ec8a8eba8f75671eb30acd26e3ba090ba3d330d98a4debd0e1f"},
+    "rowdot_kernel": {"bytes": 135301632 + 701696,
+                    "sha256": "aa357bacfc18cf468b69fe3fbea6de8b548e9bdaac7e5a9094642e26c787a625"},
+    "dkdv_kernel": {"bytes": 270621440 + 102216448,
+                  "sha256": "584517da90c4e9abd58ba0034f5448a373e88130e9bce108802fd6af9c5c6c80"},
+    "dq_kernel": {"bytes": 270723584 + 49688576,
+                "sha256": "584517da90c4e9abd58ba0034f5448a373e88130e9bce108802fd6af9c5c6c80"},
+    "decode_tc_kernel": {"bytes": 1119356928 + 9036288,
+                       "sha256": "4bc63c3b1dc1b0ec5e7aace43140a00561f1968f7531061ebc33fa050ccc14c6"},
 }
 
 def kernel_source_sha(kernel: str) -> str:
