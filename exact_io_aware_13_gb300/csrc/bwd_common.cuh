@@ -58,7 +58,8 @@ constexpr uint32_t kKvColS = 0, kKvColDP = 64, kKvColPD = 128, kKvColK = 192, kK
 __device__ __forceinline__ uint32_t kv_col_s(int x) { return x * 64; }
 constexpr uint32_t kKv2ColDP = 128, kKv2ColV = 192, kKv2ColAcc = 256;
 
-// Element-wise constants: s2 = x*k1 + kb*(j - i) (log2 units), then the soft-cap.
+// Element-wise constants: s2 = x*k1 + kb*(j - i) (log2 units); with the soft-cap c the
+// same expression gives the pre-cap score over c and s2 = c log2(e) tanh of it.
 struct ScoreK {
   float k1, kb, capA;
 };
@@ -68,9 +69,8 @@ __device__ __forceinline__ ScoreK score_consts(const Problem& p, int h) {
   const float slope = kAlibi ? alibi_slope(h, p.Hq) : 0.f;
   ScoreK s;
   if (kSoftcap) {
-    const float c2 = 2.0f * kLog2e / p.softcap;
-    s.k1 = p.scale * c2;
-    s.kb = slope * c2;
+    s.k1 = p.scale / p.softcap;
+    s.kb = slope / p.softcap;
     s.capA = p.softcap * kLog2e;
   } else {
     s.k1 = p.scale * kLog2e;
@@ -85,7 +85,7 @@ __device__ __forceinline__ ScoreK score_consts(const Problem& p, int h) {
 // (all ones without dropout, 0 where the element is dropped). With dropout the row term
 // is D' = D (1 - p) and the result dS' = P (dP Z - D') is dS (1 - p); the factor
 // 1 / (1 - p) is applied with the softmax scale in the dK and dQ epilogues. Under the
-// soft-cap the pre-cap score is in 2 log2e / c units and the tanh derivative scales dS. A
+// soft-cap the pre-cap score is divided by c and the tanh derivative scales dS. A
 // masked element (ok false) takes the exponent -inf, so P = dS = 0 with no branch: a
 // per-lane condition around the exponential would make the compiler branch on every
 // element.
@@ -96,7 +96,7 @@ __device__ __forceinline__ void p_only(float xs, const ScoreK& sk, float alibi, 
   dcap = 1.f;
   if (kSoftcap) {
     const float pre = kAlibi ? fmaf(xs, sk.k1, alibi) : xs * sk.k1;
-    const float t = 1.0f - 2.0f * rcp_approx(1.0f + ex2_approx(pre));  // tanh(pre_cap / c)
+    const float t = tanh_approx(pre);  // tanh(pre-cap score / c)
     arg = sk.capA * t - lse2;
     dcap = 1.0f - t * t;
   } else if (kAlibi) {

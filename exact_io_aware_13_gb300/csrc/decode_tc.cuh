@@ -608,8 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t p_count = 32u * (a.n_part + 1);
     float* xmax = reinterpret_cast<float*>(smem + L::kXchg);  // [2][2][32]
-    const float cap2 = kSoftcap ? 2.0f * kLog2e / p.softcap : 0.f;
-    const float k1 = kSoftcap ? p.scale * cap2 : p.scale * kLog2e;
+    // with the soft-cap c: the pre-cap score over c, then s2 = c log2(e) tanh of it
+    const float k1 = kSoftcap ? p.scale / p.softcap : p.scale * kLog2e;
     const float capA = kSoftcap ? p.softcap * kLog2e : 0.f;
     const bool raw_ok = !kAlibi && !kSoftcap && k1 > 0.f;
     bool live = true;
@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int lo_r = 0, hi_r = 0;
       if (valid_row) decode_row_keys(p.mask_kind, p.window, it.Lb, p.Nq, i, lo_r, hi_r);
       const float slope = kAlibi ? alibi_slope(h, p.Hq) : 0.f;
-      const float kb = kSoftcap ? slope * cap2 : slope * kLog2e;
+      const float kb = kSoftcap ? slope / p.softcap : slope * kLog2e;
       const int k = items_with_tiles++;
       const int ob = k & 1;
       const uint32_t tO = tmem + lane_base + L::kColO + ob * D;
@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int col = cbase + ch * 16 + e;
                 const float x = __uint_as_float(r[ch][e]);
                 float s2 = kAlibi ? fmaf(x, k1, fmaf((float)col, kb, base)) : x * k1;
-                if (kSoftcap) s2 = capA - 2.0f * capA * rcp_approx(1.0f + ex2_approx(s2));
+                if (kSoftcap) s2 = capA * tanh_approx(s2);
                 if (masked) s2 = (col >= c_lo && col < c_hi) ? s2 : -INFINITY;
                 mx[e & 7] = fmaxf(mx[e & 7], s2);
                 r[ch][e] = __float_as_uint(s2);

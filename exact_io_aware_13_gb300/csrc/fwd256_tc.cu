@@ -246,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int fk = first_key(p.mask, valid ? i : p.Nq - 1);
     const int last_key = p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1);
     const float slope = kAlibi ? alibi_slope(h, p.Hq) : 0.f;
-    const float cap2 = kSoftcap ? 2.0f * kLog2e / p.softcap : 0.f;
-    const float k1 = kSoftcap ? p.scale * cap2 : p.scale * kLog2e;
-    const float kb = kSoftcap ? slope * cap2 : slope * kLog2e;
+    // with the soft-cap c: the pre-cap score over c, then s2 = c log2(e) tanh of it
+    const float k1 = kSoftcap ? p.scale / p.softcap : p.scale * kLog2e;
+    const float kb = kSoftcap ? slope / p.softcap : slope * kLog2e;
     const float capA = kSoftcap ? p.softcap * kLog2e : 0.f;
     const bool raw_ok = !kAlibi && !kSoftcap && k1 > 0.f;
     float m_run = -INFINITY, l_run = 0.f;
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col = c * 32 + e;
             const float x = __uint_as_float(r[c][e]);
             float s2 = kAlibi ? fmaf(x, k1, fmaf((float)col, kb, base)) : x * k1;
-            if (kSoftcap) s2 = capA - 2.0f * capA * rcp_approx(1.0f + ex2_approx(s2));
+            if (kSoftcap) s2 = capA * tanh_approx(s2);
             if (masked) s2 = (col >= c_lo && col <= c_hi) ? s2 : -INFINITY;
             mx[e & 7] = fmaxf(mx[e & 7], s2);
             r[c][e] = __float_as_uint(s2);

@@ -354,11 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + (t == 0 ? L::kColS0 : L::kColS1);
     const uint32_t tO = tmem + lane_base + (t == 0 ? L::kColO0 : L::kColO1);
     const int fk = first_key(p.mask, i < p.Nq ? i : p.Nq - 1);
-    // Scores in log2 units: s2 = x * k1 + (j - i) * kb, then the soft-cap.
+    // Scores in log2 units: s2 = x * k1 + (j - i) * kb. With the soft-cap c the same
+    // expression gives the pre-cap score over c; the pass keeps t = tanh of it and the
+    // exponent pass multiplies by capA = c log2(e), as the raw-score path does with k1.
     const float slope = kAlibi ? alibi_slope(h, p.Hq) : 0.f;
-    const float cap2 = kSoftcap ? 2.0f * kLog2e / p.softcap : 0.f;
-    const float k1 = kSoftcap ? p.scale * cap2 : p.scale * kLog2e;
-    const float kb = kSoftcap ? slope * cap2 : slope * kLog2e;
+    const float k1 = kSoftcap ? p.scale / p.softcap : p.scale * kLog2e;
+    const float kb = kSoftcap ? slope / p.softcap : slope * kLog2e;
     const float capA = kSoftcap ? p.softcap * kLog2e : 0.f;
     // The common case (no score mod, positive scale, tile fully allowed) works on the
     // raw scores x: max over x, then p = exp2(x * k1 - m) in one FFMA + ex2.
@@ -401,8 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Allowed columns of this row in this tile: [c_lo, c_hi].
         const int c_lo = fk - k0, c_hi = last_key - k0;
         const float base = kAlibi ? (float)(k0 - i) * kb : 0.f;
-        const uint64_t k1j2 = f32x2(k1j, k1j), one2 = f32x2(1.f, 1.f);
-        const uint64_t capA2 = f32x2(capA, capA), neg_2capA2 = f32x2(-2.f * capA, -2.f * capA);
+        const uint64_t k1j2 = f32x2(k1j, k1j);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -413,11 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              f32x2(fmaf((float)col, kb, base),
                                                    fmaf((float)(col + 1), kb, base)))
                                  : mul_f32x2(x2, k1j2);
-            if (kSoftcap) {  // capA - 2 capA / (1 + 2^s2): capA tanh of the pre-cap score
-              float a0, a1, d0, d1;
+            if (kSoftcap) {  // t = tanh of the pre-cap score over c (capA t in log2 units)
+              float a0, a1;
               f32x2_split(s2, a0, a1);
-              f32x2_split(fma_f32x2(f32x2(ex2_approx(a0), ex2_approx(a1)), one2, one2), d0, d1);
-              s2 = fma_f32x2(f32x2(rcp_approx(d0), rcp_approx(d1)), neg_2capA2, capA2);
+              s2 = f32x2(tanh_approx(a0), tanh_approx(a1));
             }
             float v0, v1;
             f32x2_split(s2, v0, v1);
@@ -434,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                        fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       if (fast) mt *= k1j;  // into log2 units
+      else if (kSoftcap) mt *= capA;
       const float m_new = fmaxf(m_run, mt);
       const bool grow = m_new > m_run + (kFp8 ? kRescaleLog2Fp8 : kRescaleLog2);
       const bool warp_grow = __any_sync(0xffffffffu, grow);
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // FP8: exp2(s - m + 7) = 2^7 p, the scale e4m3 rounding wants, at no extra cost
       float neg_m = m_run == -INFINITY ? 0.f : -m_run;
       if constexpr (kFp8) neg_m += kPScaleLog2Fp8;
-      const float mul = fast ? k1j : 1.f;  // p = exp2(v * mul - m)
+      const float mul = fast ? k1j : (kSoftcap ? capA : 1.f);  // p = exp2(v * mul - m)
       const DropThr dthr = drop_thr_words(kDrop ? p.drop_thr : 0);
       float acc[8];
 #pragma unroll
