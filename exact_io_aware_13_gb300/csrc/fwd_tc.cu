@@ -11,7 +11,10 @@
 // GB300 mapping (the FlashAttention-4 ideas named in "El FlexAttention de PyTorch
 // con FlashAttention-4 es un cambio radical": tensor memory, asynchronous MMAs,
 // warp specialisation, 256 x 128 tiles on Blackwell):
-//   * one CTA = 2 query tiles of 128 rows (256 rows) against key tiles of 128;
+//   * one CTA = 2 query tiles of 128 rows (256 rows) against key tiles of 128; under
+//     grouped-query attention with an even group size (kPairs) the two tiles are the same
+//     128 rows of two query heads of one KV group instead: equal key-tile ranges, the same
+//     K/V tiles, so neither tile idles while the other takes a key tile alone;
 //   * warp 8 streams Q once and K_j, V_j through a shared-memory ring with TMA
 //     (128-byte swizzle), skipping the key tiles the mask empties;
 //   * warp 9 allocates tensor memory and issues every tcgen05.mma from one thread:
@@ -100,7 +103,11 @@ struct FwdArgs {
   Problem p;
   __nv_bfloat16* o;
   float* lse;
-  int num_qblocks;  // ceil(Nq / 256)
+  int num_qblocks;  // query blocks per unit: ceil(Nq / 256), or ceil(Nq / 128) with head pairs
+  // Head pairs (grouped-query attention with an even group size): a CTA takes the same 128
+  // query rows of two query heads of one KV group, whose key-tile ranges are equal and
+  // whose K/V tiles are the same, instead of two adjacent 128-row tiles of one head.
+  int head_pairs;
   // FP8 only: dequantisation scales of Q [B*Hq, nqt], K [B*Hkv, nkt], V [B*Hkv]
   const float* sq;
   const float* sk;
@@ -108,11 +115,12 @@ struct FwdArgs {
   int nqt, nkt;     // 128-row tiles per head of Q and K
 };
 
-// CTA -> (batch*head, 256-row query block). Heads are taken kHeadGroup at a time
-// so the CTAs running together share K/V in L2; inside a group the longest query
-// blocks (most key tiles under causal masks) come first.
+// CTA -> (unit, query block): a unit is a query head (batch*head), or with head pairs
+// two consecutive query heads. Units are taken kHeadGroup at a time so the CTAs running
+// together share K/V in L2; inside a group the longest query blocks (most key tiles
+// under causal masks) come first.
 __device__ __forceinline__ void cta_work(const FwdArgs& a, int& bh, int& qb) {
-  const int BH = a.p.B * a.p.Hq, nqb = a.num_qblocks;
+  const int BH = a.p.B * a.p.Hq / (a.head_pairs ? 2 : 1), nqb = a.num_qblocks;
   const int per_group = kHeadGroup * nqb;
   const int grp = blockIdx.x / per_group;
   const int rem = blockIdx.x - grp * per_group;
@@ -121,7 +129,7 @@ __device__ __forceinline__ void cta_work(const FwdArgs& a, int& bh, int& qb) {
   bh = grp * kHeadGroup + rem % gh;
 }
 
-template <int D, bool kAlibi, bool kSoftcap, bool kFp8, bool kDrop>
+template <int D, bool kAlibi, bool kSoftcap, bool kFp8, bool kDrop, bool kPairs>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -139,16 +147,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  int bh, qb;
-  cta_work(a, bh, qb);
-  const int b = bh / p.Hq, h = bh - b * p.Hq;
-  const int g = h / (p.Hq / p.Hkv);
+  int unit, qb;
+  cta_work(a, unit, qb);
+  // Query tile t: rows q0 + t * dq .. + 127 of query head bh0 + t * dh.
+  constexpr bool hp = kPairs;
+  const int bh0 = hp ? 2 * unit : unit;
+  const int dq = hp ? 0 : BM, dh = hp ? 1 : 0;
+  const int q0 = qb * (hp ? BM : kQTiles * BM);
+  const int b = bh0 / p.Hq, h0 = bh0 - b * p.Hq;
+  const int g = h0 / (p.Hq / p.Hkv);  // the pair's heads share it
   const int bg = b * p.Hkv + g;
-  const int q0 = qb * (kQTiles * BM);
 
   TileRange rng[kQTiles];
 #pragma unroll
-  for (int t = 0; t < kQTiles; ++t) rng[t] = kv_tiles_for_rows(p.mask, q0 + t * BM, BM);
+  for (int t = 0; t < kQTiles; ++t) rng[t] = kv_tiles_for_rows(p.mask, q0 + t * dq, BM);
   int lo = 1 << 30, hi = 0;
 #pragma unroll
   for (int t = 0; t < kQTiles; ++t)
@@ -156,7 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (hi <= lo) {  // the mask leaves these rows no key: O = 0, L = -inf
     for (int r = threadIdx.x; r < kQTiles * BM; r += kThreads) {
-      const int i = q0 + r;
+      const int t = r / BM, i = q0 + t * dq + (r - t * BM);
+      const int bh = bh0 + t * dh;
       if (i >= p.Nq) continue;
       uint4* orow = reinterpret_cast<uint4*>(a.o + ((size_t)bh * p.Nq + i) * D);
 #pragma unroll
@@ -189,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < L::kSlabs; ++c)
         tma_load_3d(smem_u32(smem + L::kQ + t * L::kTile + c * L::kChunk), &tm_q, qbar,
-                    c * (128 / L::kElem), q0 + t * BM, bh);
+                    c * (128 / L::kElem), q0 + t * dq, bh0 + t * dh);
     for (int u = 0; u < imin(kStages, 2 * n_kv); ++u) {
       const uint32_t fb = smem_u32(&bars->kv_full[u]);
       mbar_arrive_expect_tx(fb, L::kTile);
@@ -349,13 +362,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;                 // query tile of this warpgroup
     const int row = (warp & 3) * 32 + lane;  // TMEM lane = row in the tile
-    const int i = q0 + t * BM + row;         // query position
+    const int r0 = q0 + t * dq;              // the tile's first query row
+    const int i = r0 + row;                  // query position
+    const int bh = bh0 + t * dh, h = h0 + t * dh;  // the tile's query head
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (t == 0 ? L::kColS0 : L::kColS1);
     const uint32_t tO = tmem + lane_base + (t == 0 ? L::kColO0 : L::kColO1);
     const int fk = first_key(p.mask, i < p.Nq ? i : p.Nq - 1);
     // Scores in log2 units: s2 = x * k1 + (j - i) * kb. With the soft-cap c the same
-    // expression gives the pre-cap score over c; the pass keeps t = tanh of it and the
+    // expression gives the pre-cap score over c; the pass keeps the tanh of it and the
     // exponent pass multiplies by capA = c log2(e), as the raw-score path does with k1.
     const float slope = kAlibi ? alibi_slope(h, p.Hq) : 0.f;
     const float k1 = kSoftcap ? p.scale / p.softcap : p.scale * kLog2e;
@@ -365,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // raw scores x: max over x, then p = exp2(x * k1 - m) in one FFMA + ex2.
     const bool raw_ok = !kAlibi && !kSoftcap && k1 > 0.f;
     // FP8: the tile pair's dequantisation factor s_q s_k scales k1 (and kb stays)
-    const int qtile = q0 / BM + t;  // may lie past the last tile (then no key tile runs)
+    const int qtile = r0 / BM;  // may lie past the last tile (then no key tile runs)
     const float sqv = (kFp8 && qtile < a.nqt) ? a.sq[(size_t)bh * a.nqt + qtile] : 1.f;
     const int last_key = (p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1));
     float m_run = -INFINITY, l_run = 0.f;
@@ -387,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) reg_fence32(r[c]);
       const int k0 = j * BN;
-      const bool masked = tile_needs_mask(p.mask, q0 + t * BM, k0, BN);
+      const bool masked = tile_needs_mask(p.mask, r0, k0, BN);
       const bool fast = raw_ok && !masked;  // warp-uniform
       // Row max in eight independent chains (the scores stay in r).
       float mx[8];
@@ -579,30 +594,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < D; ++e) o[e] = 0u;
       }
 #pragma unroll
-      for (int g = 0; g < D / 8; ++g) {  // 16-byte chunk g of the row: slab g / 8, chunk g % 8
+      for (int gc = 0; gc < D / 8; ++gc) {  // 16-byte chunk gc of the row: slab gc / 8
         uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[8 * g + 0]) * inv, __uint_as_float(o[8 * g + 1]) * inv);
-        w.y = pack_bf16x2(__uint_as_float(o[8 * g + 2]) * inv, __uint_as_float(o[8 * g + 3]) * inv);
-        w.z = pack_bf16x2(__uint_as_float(o[8 * g + 4]) * inv, __uint_as_float(o[8 * g + 5]) * inv);
-        w.w = pack_bf16x2(__uint_as_float(o[8 * g + 6]) * inv, __uint_as_float(o[8 * g + 7]) * inv);
-        *reinterpret_cast<uint4*>(otile + (g >> 3) * L::kChunk + row * 128 +
-                                  (((g & 7) ^ (row & 7)) << 4)) = w;
+        w.x = pack_bf16x2(__uint_as_float(o[8 * gc + 0]) * inv, __uint_as_float(o[8 * gc + 1]) * inv);
+        w.y = pack_bf16x2(__uint_as_float(o[8 * gc + 2]) * inv, __uint_as_float(o[8 * gc + 3]) * inv);
+        w.z = pack_bf16x2(__uint_as_float(o[8 * gc + 4]) * inv, __uint_as_float(o[8 * gc + 5]) * inv);
+        w.w = pack_bf16x2(__uint_as_float(o[8 * gc + 6]) * inv, __uint_as_float(o[8 * gc + 7]) * inv);
+        *reinterpret_cast<uint4*>(otile + (gc >> 3) * L::kChunk + row * 128 +
+                                  (((gc & 7) ^ (row & 7)) << 4)) = w;
       }
     }
     __syncwarp();
     {
       constexpr int kChunksPerRow = D / 8;               // 16-byte chunks per row
       constexpr int kRowsPerStore = 32 / kChunksPerRow;  // rows one warp store covers
-      const int g = lane % kChunksPerRow;
-      const int r0 = (warp & 3) * 32;
+      const int gc = lane % kChunksPerRow;
+      const int w0 = (warp & 3) * 32;  // this warp's first row in the tile
 #pragma unroll
       for (int k = 0; k < 32 / kRowsPerStore; ++k) {
-        const int r = r0 + k * kRowsPerStore + lane / kChunksPerRow;
-        const uint4 w = *reinterpret_cast<const uint4*>(otile + (g >> 3) * L::kChunk + r * 128 +
-                                                       (((g & 7) ^ (r & 7)) << 4));
-        const int ir = q0 + t * BM + r;
+        const int r = w0 + k * kRowsPerStore + lane / kChunksPerRow;
+        const uint4 w = *reinterpret_cast<const uint4*>(otile + (gc >> 3) * L::kChunk + r * 128 +
+                                                       (((gc & 7) ^ (r & 7)) << 4));
+        const int ir = r0 + r;
         if (ir < p.Nq)
-          reinterpret_cast<uint4*>(a.o + ((size_t)bh * p.Nq + ir) * D)[g] = w;
+          reinterpret_cast<uint4*>(a.o + ((size_t)bh * p.Nq + ir) * D)[gc] = w;
       }
     }
     if (i < p.Nq)
@@ -621,10 +636,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Head pairs when the query heads of a KV group come in pairs (then Hq is even too).
+void set_units(FwdArgs& a) {
+  a.head_pairs = (a.p.Hq / a.p.Hkv) % 2 == 0 ? 1 : 0;
+  a.num_qblocks = ceil_div(a.p.Nq, a.head_pairs ? BM : kQTiles * BM);
+}
+
 template <int D, bool kAlibi, bool kSoftcap, bool kFp8 = false, bool kDrop = false>
 cudaError_t launch_variant(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int grid, cudaStream_t st) {
-  auto kern = fwd_tc_kernel<D, kAlibi, kSoftcap, kFp8, kDrop>;
+  auto kern = a.head_pairs ? fwd_tc_kernel<D, kAlibi, kSoftcap, kFp8, kDrop, true>
+                           : fwd_tc_kernel<D, kAlibi, kSoftcap, kFp8, kDrop, false>;
   const int smem = Layout<D, kFp8>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -658,8 +680,8 @@ cudaError_t launch_fwd_tc(const Problem& p, const CUtensorMap& tq, const CUtenso
   a.p = p;
   a.o = o;
   a.lse = lse;
-  a.num_qblocks = ceil_div(p.Nq, kQTiles * BM);
-  const long long grid = (long long)a.num_qblocks * p.B * p.Hq;
+  set_units(a);
+  const long long grid = (long long)a.num_qblocks * p.B * p.Hq / (a.head_pairs ? 2 : 1);
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (p.d == 64) return launch_d<64>(a, tq, tk, tv, (int)grid, st);
@@ -677,13 +699,13 @@ cudaError_t launch_fwd_fp8_tc(const Problem& p, const CUtensorMap& tq, const CUt
   a.p = p;
   a.o = o;
   a.lse = lse;
-  a.num_qblocks = ceil_div(p.Nq, kQTiles * BM);
+  set_units(a);
   a.sq = sq;
   a.sk = sk;
   a.sv = sv;
   a.nqt = ceil_div(p.Nq, BM);
   a.nkt = ceil_div(p.Nkv, BN);
-  const long long grid = (long long)a.num_qblocks * p.B * p.Hq;
+  const long long grid = (long long)a.num_qblocks * p.B * p.Hq / (a.head_pairs ? 2 : 1);
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL || p.d != 128) return cudaErrorInvalidValue;
   const bool al = p.score_kind & ATTN_SCORE_ALIBI, sc = p.score_kind & ATTN_SCORE_SOFTCAP;
