@@ -6,6 +6,7 @@
 // partial output rescaled by exp(m_old - m_new) whenever the max grows. Here the
 // recurrence advances one key at a time, in fp32 with accurate expf/tanhf.
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace attn {
 namespace {
@@ -217,61 +218,86 @@ __global__ void __launch_bounds__(kRows) dkdv_simt_kernel(Problem p, const __nv_
   }
 }
 
-// Row terms of the backward (see RowTerms), one padded query row per group of D/8
-// lanes: each lane reads 16 bytes (8 elements) of the row's O and dO, and the group
-// sums its products with a fixed butterfly, so D_i does not depend on the launch.
-// A warp handles kUnroll rows per lane group at once to keep enough loads in flight.
+// Row terms of the backward (see RowTerms). A block takes kBlockRows padded query rows of
+// one head (16 KB of O and 16 KB of dO rows: nq_pad is a multiple of 128, so a block never
+// straddles two heads), copies the valid rows of O and dO into shared memory with two bulk
+// copies (so a few blocks per SM keep a few hundred KB in flight), and then one group of
+// D/8 lanes per row multiplies its 16-byte pieces and sums them with a fixed butterfly, so
+// D_i does not depend on the launch.
 template <int D>
-__global__ void __launch_bounds__(256) rowdot_kernel(Problem p, long long rows,
-                                                     const __nv_bfloat16* o,
+struct RowdotShape {
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kBlockRows = 16384 / kRowBytes;  // 128, 64 or 32 rows
+  static constexpr int kThreads = 128;
+  static constexpr int kLanes = D / 8;                   // lanes per row
+  static constexpr int kGroups = 32 / kLanes;            // rows per warp and pass
+  static constexpr int kPasses = kBlockRows / (kThreads / 32) / kGroups;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128) rowdot_kernel(Problem p, const __nv_bfloat16* o,
                                                      const __nv_bfloat16* dout,
                                                      const float* lse, RowTerms rt) {
-  constexpr int kLanes = D / 8;             // lanes per row
-  constexpr int kGroups = 32 / kLanes;      // rows per warp and pass
-  constexpr int kUnroll = 4;
-  constexpr long long kRowsPerWarp = (long long)kGroups * kUnroll;
-  const int lane = threadIdx.x & 31, grp = lane / kLanes, sub = lane % kLanes;
-  const long long warp0 = ((long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kRowsPerWarp;
-  uint4 av[kUnroll], bv[kUnroll];
-  long long src[kUnroll];
-  bool real[kUnroll];
-#pragma unroll
-  for (int r = 0; r < kUnroll; ++r) {  // issue every load first
-    const long long row = warp0 + r * kGroups + grp;
-    const long long bh = row / p.nq_pad;
-    const int i = (int)(row - bh * p.nq_pad);
-    real[r] = row < rows && i < p.Nq;
-    src[r] = bh * p.Nq + i;
-    av[r] = real[r] ? reinterpret_cast<const uint4*>(o + src[r] * D)[sub] : make_uint4(0, 0, 0, 0);
-    bv[r] = real[r] ? reinterpret_cast<const uint4*>(dout + src[r] * D)[sub] : make_uint4(0, 0, 0, 0);
+  using S = RowdotShape<D>;
+  __shared__ alignas(128) uint8_t rows_o[S::kBlockRows * S::kRowBytes];
+  __shared__ alignas(128) uint8_t rows_do[S::kBlockRows * S::kRowBytes];
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  const int blocks_per_head = p.nq_pad / S::kBlockRows;
+  const long long bh = blockIdx.x / blocks_per_head;
+  const int i0 = (int)(blockIdx.x - bh * blocks_per_head) * S::kBlockRows;
+  const int nvalid = imax(0, imin(S::kBlockRows, p.Nq - i0));
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
   }
+  __syncthreads();
+  if (threadIdx.x == 0 && nvalid > 0) {
+    const uint32_t bytes = (uint32_t)nvalid * S::kRowBytes;
+    const size_t src = ((size_t)bh * p.Nq + i0) * D;
+    mbar_arrive_expect_tx(smem_u32(&bar), 2 * bytes);
+    bulk_load(smem_u32(rows_o), o + src, bytes, smem_u32(&bar));
+    bulk_load(smem_u32(rows_do), dout + src, bytes, smem_u32(&bar));
+  }
+  const WaitCtx wc{&abort_flag, p.status};
+  const bool have = nvalid == 0 || mbar_wait(smem_u32(&bar), 0, wc);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int grp = lane / S::kLanes, sub = lane % S::kLanes;
 #pragma unroll
-  for (int r = 0; r < kUnroll; ++r) {
-    const long long row = warp0 + r * kGroups + grp;
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av[r]);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv[r]);
+  for (int ps = 0; ps < S::kPasses; ++ps) {
+    const int r = (warp * S::kPasses + ps) * S::kGroups + grp;  // row in the block
+    const int i = i0 + r;
+    const bool real = r < nvalid;
     float s = 0.f;
+    if (real && have) {
+      const uint4 av = reinterpret_cast<const uint4*>(rows_o + r * S::kRowBytes)[sub];
+      const uint4 bv = reinterpret_cast<const uint4*>(rows_do + r * S::kRowBytes)[sub];
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float2 x = __bfloat1622float2(a2[t]), y = __bfloat1622float2(b2[t]);
-      s = fmaf(x.x, y.x, s);
-      s = fmaf(x.y, y.y, s);
+      for (int t = 0; t < 4; ++t) {
+        const float2 x = __bfloat1622float2(a2[t]), y = __bfloat1622float2(b2[t]);
+        s = fmaf(x.x, y.x, s);
+        s = fmaf(x.y, y.y, s);
+      }
     }
 #pragma unroll
-    for (int off = kLanes / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (sub == 0 && row < rows) {
-      const long long bh = row / p.nq_pad;
-      const int i = (int)(row - bh * p.nq_pad);
+    for (int off = S::kLanes / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (sub == 0) {
+      const long long row = bh * p.nq_pad + i;
       float l2 = INFINITY;
-      if (real[r]) {
-        const float L = lse[src[r]];
+      if (real) {
+        const float L = lse[(size_t)bh * p.Nq + i];
         l2 = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
       }
-      rt.delta[row] = real[r] ? s * p.drop_keep : 0.f;  // with dropout D (1 - p)
+      rt.delta[row] = real ? s * p.drop_keep : 0.f;  // with dropout D (1 - p)
       rt.lse2[row] = l2;
-      if (bh == 0) rt.first[i] = i < p.Nq ? first_key(p.mask, i) : 0x7fffffff;
+      if (bh == 0) rt.first[i] = real ? first_key(p.mask, i) : 0x7fffffff;
     }
   }
+  // No copy may land in shared memory after the block has left.
+  if (threadIdx.x == 0 && nvalid > 0 && !have) mbar_wait(smem_u32(&bar), 0, wc);
 }
 
 // Rows with no key at all: O = 0, lse = -inf.
@@ -328,12 +354,12 @@ cudaError_t launch_bwd_rowdot(const Problem& p, const __nv_bfloat16* o,
                               cudaStream_t st) {
   const long long rows = (long long)p.B * p.Hq * p.nq_pad;
   if (rows == 0) return cudaSuccess;
-  const long long per_block = 8LL * (32 / (p.d / 8)) * 4;  // warps x rows per warp
-  const long long blocks = (rows + per_block - 1) / per_block;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (p.d == 64) rowdot_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
-  else if (p.d == 128) rowdot_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
-  else rowdot_kernel<256><<<(unsigned)blocks, 256, 0, st>>>(p, rows, o, dout, lse, rt);
+  const int block_rows = 16384 / (p.d * 2);  // RowdotShape<d>::kBlockRows
+  const long long blocks = rows / block_rows;  // nq_pad is a multiple of 128
+  if (blocks > 0x7fffffffLL || p.nq_pad % block_rows != 0) return cudaErrorInvalidValue;
+  if (p.d == 64) rowdot_kernel<64><<<(unsigned)blocks, 128, 0, st>>>(p, o, dout, lse, rt);
+  else if (p.d == 128) rowdot_kernel<128><<<(unsigned)blocks, 128, 0, st>>>(p, o, dout, lse, rt);
+  else rowdot_kernel<256><<<(unsigned)blocks, 128, 0, st>>>(p, o, dout, lse, rt);
   return cudaGetLastError();
 }
 
