@@ -147,16 +147,16 @@ KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", 
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201403904 + 46800896,
-                    "sha256": "ce2256683d2f8ec8a8eba8f75671eb30acd26e3ba090ba3d330d98a4debd0e1f"},
-    "rowdot_kernel": {"bytes": 135301632 + 701696,
-                    "sha256": "aa357bacfc18cf468b69fe3fbea6de8b548e9bdaac7e5a9094642e26c787a625"},
-    "dkdv_kernel": {"bytes": 270621440 + 102216448,
-                  "sha256": "584517da90c4e9abd58ba0034f5448a373e88130e9bce108802fd6af9c5c6c80"},
-    "dq_kernel": {"bytes": 270723584 + 49688576,
-                "sha256": "584517da90c4e9abd58ba0034f5448a373e88130e9bce108802fd6af9c5c6c80"},
-    "decode_tc_kernel": {"bytes": 1119356928 + 9036288,
-                       "sha256": "4bc63c3b1dc1b0ec5e7aace43140a00561f1968f7531061ebc33fa050ccc14c6"},
+    "fwd_tc_kernel": {"bytes": 201401856 + 46906880,
+                    "sha256": "f2035381381d425626d0346da62b9235efa4587e3cf84f6894afbafca6373bb6"},
+    "rowdot_kernel": {"bytes": 135311616 + 498688,
+                    "sha256": "6bf774e08dded1c49bfce5e41d3b0adbb6d495a45f322126d274bd99fd43dc8c"},
+    "dkdv_kernel": {"bytes": 270683392 + 101847552,
+                  "sha256": "a245868791e0a6e87bb37b2a3df24067e1ff8005bf06601e658de8c243dfc3f6"},
+    "dq_kernel": {"bytes": 270634496 + 49656832,
+                "sha256": "a245868791e0a6e87bb37b2a3df24067e1ff8005bf06601e658de8c243dfc3f6"},
+    "decode_tc_kernel": {"bytes": 1119389440 + 9509376,
+                       "sha256": "43f62fe2b35363eb468b63ca50e963145d60432a764d8956e4d030d7913e7c38"},
 }
 
 def kernel_source_sha(kernel: str) -> str:
