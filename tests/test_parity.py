@@ -83,6 +83,27 @@ def test_forward_large_logits_stay_finite():
     H.check_forward(o, lse, o_ref, l_ref, w.name)
 
 
+@pytest.mark.parametrize("score", [SCORE_SOFTCAP, SCORE_ALIBI | SCORE_SOFTCAP],
+                         ids=["softcap", "alibi_softcap"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_softcap_saturated_scores(score, d):
+    """Scores of a few hundred against a soft-cap of 20 (s / c up to about 20, where tanh is
+    saturated and the capped scores of many keys sit near the cap): the kernels' tanh,
+    scaled by c, feeds every P here. Forward and gradients against the oracle, which
+    takes numpy's tanh."""
+    w = H.small_workload(f"capsat{d}", MASK_CAUSAL, score, B=1, Hq=4, Hkv=2, N=300, d=d,
+                         softcap=20.0, seed=11 + d)
+    q, k, v, do, offs = make_inputs(w, with_dout=True)
+    q = (q.float() * 8).to(torch.bfloat16)
+    k = (k.float() * 8).to(torch.bfloat16)
+    inputs = (q, k, v, do, offs)
+    o, lse = H.run_forward(w, "tc", inputs)
+    o_ref, l_ref = H.oracle_forward(w, inputs)
+    H.check_forward(o, lse, o_ref, l_ref, w.name)
+    got = H.run_backward(w, "tc", inputs)
+    H.check_grads(got, H.oracle_backward(w, inputs), w.name)
+
+
 def _sampled_rows(w, n=48, seed=0):
     rng = np.random.default_rng(seed)
     rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, w.Nq - 1],
