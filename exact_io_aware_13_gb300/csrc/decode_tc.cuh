@@ -93,7 +93,6 @@ constexpr uint32_t kNbXCount = 64;
 static_assert(kNbKV + kStages - 1 <= 15, "named barrier IDs");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr unsigned long long kDrainLimitNs = 200000000ull;  // waits for own copies at exit
 
 template <int D>
 struct Layout {
@@ -139,15 +138,6 @@ struct Args {
   long long rows_total;  // B * Hq * Nq
   bool direct;           // one chunk per sequence: results written in place, no combine
 };
-
-// Waits for a copy this CTA issued, ignoring the abort flag (shared memory must not be
-// left while a copy into it is in flight), for at most kDrainLimitNs.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return;
-  const unsigned long long t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > kDrainLimitNs) return;
-}
 
 
 // ------------------------------------------------------------------ the item list

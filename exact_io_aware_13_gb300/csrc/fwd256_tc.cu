@@ -41,7 +41,6 @@ static_assert(kNbKv + kStages - 1 <= 15, "named barrier IDs");
 constexpr int kHeadGroup = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr unsigned long long kDrainLimitNs = 200000000ull;
 
 struct Bars {
   uint64_t full[kStages];
@@ -61,13 +60,6 @@ struct Args {
   float* lse;
   int nqb;  // 128-row query tiles per head
 };
-
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return;
-  const unsigned long long t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > kDrainLimitNs) return;
-}
 
 // Whether every (row, key) of rows [q0, q1] x keys [k0, k0 + 63] is allowed.
 __device__ __forceinline__ bool keys_full(const MaskSpec& m, int q0, int q1, int k0) {

@@ -105,6 +105,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// Waits for a copy this CTA issued, ignoring the abort flag (shared memory must not be
+// left while a copy into it is in flight), for at most kDrainLimitNs.
+constexpr unsigned long long kDrainLimitNs = 200000000ull;
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kDrainLimitNs) return;
+}
+
 // ---------------------------------------------------------------- named barriers
 // Hardware CTA barriers 1..15 (0 is __syncthreads). Waiting on one touches no shared
 // memory, so a thread that issues tcgen05.mma can wait on it without stalling the

@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(128) rowdot_kernel(Problem p, const __nv_bfloa
     }
   }
   // No copy may land in shared memory after the block has left.
-  if (threadIdx.x == 0 && nvalid > 0 && !have) mbar_wait(smem_u32(&bar), 0, wc);
+  if (threadIdx.x == 0 && nvalid > 0 && !have) drain_wait(smem_u32(&bar), 0);
 }
 
 // Rows with no key at all: O = 0, lse = -inf.
