@@ -311,8 +311,9 @@ attn_status bwd_common(bool simt, const void* q, const void* k, const void* v, c
     if ((s = make_map(&maps.do64, dout, B * Hq, Nq, d, 64)) != ATTN_OK) return s;
     if ((s = make_map(&maps.k64, k, B * Hkv, Nkv, d, 64)) != ATTN_OK) return s;
     if ((s = make_map(&maps.v64, v, B * Hkv, Nkv, d, 64)) != ATTN_OK) return s;
-    if (d == 256 && (s = make_map(&maps.do128, dout, B * Hq, Nq, d)) != ATTN_OK) return s;
+    if ((s = make_map(&maps.do128, dout, B * Hq, Nq, d)) != ATTN_OK) return s;
     if (d <= 128 && (s = make_map(&maps.k128, k, B * Hkv, Nkv, d)) != ATTN_OK) return s;
+    if (d <= 128 && (s = make_map(&maps.q128, q, B * Hq, Nq, d)) != ATTN_OK) return s;
   }
   if ((phases & ATTN_BWD_ROWDOT) &&
       (s = from_cuda(launch_bwd_rowdot(p, static_cast<const __nv_bfloat16*>(o), dob, lse, rt,

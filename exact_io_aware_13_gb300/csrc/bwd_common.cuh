@@ -30,7 +30,7 @@ constexpr uint32_t kNbP = 1, kNbPCount = 288;
 constexpr uint32_t kNbStage = 3, kNbStageCount = 64;
 constexpr uint32_t kNbKvRel = 9, kNbKvP = 10, kNbKvK = 12, kNbQL = 13, kNbKvD = 14, kNbKvF = 15;
 constexpr uint32_t kNbKvCount = (kEwWarps + 1) * 32;
-constexpr int kStagesQ = 6;      // dq ring depth, in sub-steps
+constexpr int kStagesQ = 5;      // dq ring depth, in sub-steps (its Q and dO tiles are fixed)
 constexpr int kStagesKv = 5;     // dkdv ring depth (its K tile is fixed in smem)
 constexpr int kMaxStages = 6;
 // Stage barriers take IDs kNbStage .. kNbStage + kMaxStages - 1; the others must not
@@ -175,7 +175,7 @@ struct Layout {
   static constexpr int kBars = kRows + (kRowTerms ? kS * kRowStage : 0);
   static constexpr int kAlloc = kBars + 256 + 1024;
 };
-template <int D> using LayoutQ = Layout<D, kStagesQ, 0, false>;
+template <int D> using LayoutQ = Layout<D, kStagesQ, 2, false>;  // fixed: Q, dO
 template <int D> using LayoutKv = Layout<D, kStagesKv, 1, true>;  // fixed: K
 static_assert(LayoutKv<128>::kAlloc <= 232448 && LayoutQ<128>::kAlloc <= 232448,
               "shared memory per CTA");

@@ -482,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == kLoadWarp) {
-    load_loop<D, L>(smem, bars, wc, lane, nullptr, q0, bh, &maps.k64, &maps.v64, subs, slice,
-                    nullptr, p.nq_pad);
+    load_loop<D, L>(smem, bars, wc, lane, &maps.q128, q0, bh, &maps.k64, &maps.v64, subs, slice,
+                    nullptr, p.nq_pad, &maps.do128);
   } else if (warp == kRelayWarp) {
     relay_loop<L::kStageCount>(bars, wc, subs);
   } else if (warp == kMmaWarp) {
@@ -534,16 +534,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int last_key = (p.mask.kind == ATTN_MASK_NONE ? p.Nkv - 1 : imin(i, p.Nkv - 1));
     {
-      // Q and dO rows of the tile into tensor memory: warpgroups 0 and 1 copy the two
-      // halves of this thread's Q row, 2 and 3 those of its dO row (zeros past Nq).
+      // Q and dO rows of the tile into tensor memory, from the fixed tiles the loader
+      // brought into shared memory with TMA (128-byte swizzle: 16-byte chunk c of row r of
+      // a 64-column slab at r * 128 + ((c ^ (r & 7)) << 4); rows past Nq read as zeros):
+      // warpgroups 0 and 1 copy the two halves of this thread's Q row, 2 and 3 those of
+      // its dO row.
       const int wq = warp >> 2, half = wq & 1;
       constexpr int kW = D / 4;  // 32-bit words (bf16 pairs) per thread
       uint32_t wv[kW];
-      const uint4* src = reinterpret_cast<const uint4*>(
-          (wq < 2 ? a.q : a.dout) + ((size_t)bh * p.Nq + (row_ok ? i : 0)) * D + half * (D / 2));
+      const bool got =
+          __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->fixed_full), 0, wc));
+      const uint8_t* tile = smem + L::kFixA + (wq < 2 ? 0 : L::kFixTile);
 #pragma unroll
       for (int e = 0; e < kW / 4; ++e) {
-        const uint4 v = row_ok ? src[e] : make_uint4(0, 0, 0, 0);
+        const int cg = half * (kW / 4) + e;  // 16-byte chunk of the row
+        const uint4 v = got ? *reinterpret_cast<const uint4*>(
+                                  tile + (cg >> 3) * L::kFixChunk + row * 128 +
+                                  (((cg & 7) ^ (row & 7)) << 4))
+                            : make_uint4(0, 0, 0, 0);
         wv[4 * e] = v.x; wv[4 * e + 1] = v.y; wv[4 * e + 2] = v.z; wv[4 * e + 3] = v.w;
       }
       const uint32_t dst = tmem + lane_base + (wq < 2 ? kColQ : col_do<D>()) + half * (D / 4);

@@ -91,7 +91,8 @@ cudaError_t launch_quantize_v_transposed(const __nv_bfloat16* x, uint8_t* out, f
 struct BwdMaps {
   CUtensorMap v128, q64, do64, k64, v64;
   CUtensorMap k128;   // head dimension <= 128: the K tile a dK/dV CTA loads once
-  CUtensorMap do128;  // head dimension 256 only: the dQ kernel's fixed dO tile
+  CUtensorMap q128;   // head dimension <= 128: the Q tile a dQ CTA loads once
+  CUtensorMap do128;  // the dQ kernel's fixed dO tile
 };
 cudaError_t launch_bwd_tc(const Problem& p, const BwdMaps& maps, const RowTerms& rt,
                           const __nv_bfloat16* q, const __nv_bfloat16* dout,
