@@ -126,12 +126,12 @@ __device__ __forceinline__ void p_and_ds(float xs, const ScoreK& sk, float alibi
 // One Philox call covers 16 keys of one query row, so lane L draws the call of query
 // qs + L % 16 and key block (j - lane) / 16 + L / 16; a byte transpose within each
 // half-warp then hands every lane the bytes of its own key.
-__device__ __forceinline__ void dropout_flags_dkdv(const Problem& p, const DropThr& th, int j,
-                                                   int lane, int qs, int bh,
+__device__ __forceinline__ void dropout_flags_dkdv(const PhiloxKeys& pk, const DropThr& th,
+                                                   int j, int lane, int qs, int bh,
                                                    uint32_t (&kf)[4]) {
   const int jw = j - lane;  // first key of the warp, a multiple of 32
   const uint4 r = philox4x32_10((uint32_t)((jw >> 4) + (lane >> 4)), (uint32_t)(qs + (lane & 15)),
-                                (uint32_t)bh, 0u, p.drop_seed_lo, p.drop_seed_hi);
+                                (uint32_t)bh, 0u, pk);
   kf[0] = r.x;
   kf[1] = r.y;
   kf[2] = r.z;
@@ -143,12 +143,11 @@ __device__ __forceinline__ void dropout_flags_dkdv(const Problem& p, const DropT
 
 // Dropout keep flags of the 32 key columns ks .. ks + 31 (ks a multiple of 16) of query
 // row i, for the dQ layout (thread = query row): two Philox calls.
-__device__ __forceinline__ void dropout_flags_dq(const Problem& p, const DropThr& th, int i,
+__device__ __forceinline__ void dropout_flags_dq(const PhiloxKeys& pk, const DropThr& th, int i,
                                                  int ks, int bh, uint32_t (&kf)[8]) {
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
-    const uint4 r = philox4x32_10((uint32_t)((ks >> 4) + hh), (uint32_t)i, (uint32_t)bh, 0u,
-                                  p.drop_seed_lo, p.drop_seed_hi);
+    const uint4 r = philox4x32_10((uint32_t)((ks >> 4) + hh), (uint32_t)i, (uint32_t)bh, 0u, pk);
     kf[4 * hh + 0] = keep_flags4(r.x, th);
     kf[4 * hh + 1] = keep_flags4(r.y, th);
     kf[4 * hh + 2] = keep_flags4(r.z, th);

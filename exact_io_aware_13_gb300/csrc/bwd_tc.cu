@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ScoreK sk = score_consts<kAlibi, kSoftcap>(p, g * G);
     bool need_mask = tile_needs_mask(p.mask, qr.lo * BT, k0, BT);
     const DropThr dthr = drop_thr_words(kDrop ? p.drop_thr : 0);
+    const PhiloxKeys pk = philox_keys(p.drop_seed_lo, p.drop_seed_hi);  // unused without dropout
     for (int u = 0; u < subs; ++u) {
       const int s = u % kS, x = u & 1;
       if (u > 0 && x == 0) {
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence16(sr);
         const float base = kAlibi ? sk.kb * (float)(j - qs) : 0.f;  // kb*(j - i) at column 0
-        if constexpr (kDrop) dropout_flags_dkdv(p, dthr, j, lane, qs, bh, kf);
+        if constexpr (kDrop) dropout_flags_dkdv(pk, dthr, j, lane, qs, bh, kf);
         if (need_mask)  // warp-uniform
           dkdv_p<kAlibi, kSoftcap, true, kDrop>(sr, lse2, fk, sk, base, j, qs, j < p.Nkv,
                                                 causal_type, kf, pv, dc, pp);
@@ -525,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int x = pair;
     const ScoreK sk = score_consts<kAlibi, kSoftcap>(p, h);
     const DropThr dthr = drop_thr_words(kDrop ? p.drop_thr : 0);
+    const PhiloxKeys pk = philox_keys(p.drop_seed_lo, p.drop_seed_hi);  // unused without dropout
     float lse2 = INFINITY, dlt = 0.f;
     int fk = 0;
     if (row_ok) {  // row terms of the row kernel (lse2 is already L log2 e, +inf if empty)
@@ -582,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence32(dr);
       const float base = kAlibi ? sk.kb * (float)(ks - i) : 0.f;  // kb*(j - i) at column 0
       uint32_t kf[8];
-      if constexpr (kDrop) dropout_flags_dq(p, dthr, i, ks, bh, kf);
+      if constexpr (kDrop) dropout_flags_dq(pk, dthr, i, ks, bh, kf);
       uint32_t dd[16];
       if (tile_needs_mask(p.mask, q0, kt0, BT))  // warp-uniform
         dq_ds<kAlibi, kSoftcap, true, kDrop>(sr, dr, sk, base, lse2, dlt, fk - ks, last_key - ks,

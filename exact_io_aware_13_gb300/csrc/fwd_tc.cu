@@ -508,8 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int hf = 0; hf < 2; ++hf) {
               uint32_t ph[8], kf[4];
               if (kDrop) {
+                // round keys formed inside the call: kept live across the loop they cost
+                // the softmax warps more than their adds
                 const uint4 w = philox4x32_10((uint32_t)((k0 + c * 32) >> 4) + hf, (uint32_t)i,
-                                              (uint32_t)bh, 0u, p.drop_seed_lo, p.drop_seed_hi);
+                                              (uint32_t)bh, 0u,
+                                              philox_keys(p.drop_seed_lo, p.drop_seed_hi));
                 kf[0] = keep_flags4(w.x, dthr);
                 kf[1] = keep_flags4(w.y, dthr);
                 kf[2] = keep_flags4(w.z, dthr);

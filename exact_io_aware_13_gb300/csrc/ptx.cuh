@@ -427,20 +427,33 @@ __device__ __forceinline__ void mma_f8_ts_if(bool pred, uint32_t d_tmem, uint32_
 // numbers: as easy as 1, 2, 3", SC 2011): ten rounds of
 //   (hi0, lo0) = M0 x0, (hi1, lo1) = M1 x2, (x0, x1, x2, x3) <- (hi1^x1^k0, lo1, hi0^x3^k1, lo0)
 // with the key (k0, k1) advanced by (W0, W1) after each round.
+// The round keys of one seed (k0 + r W0, k1 + r W1 for rounds r = 0 .. 9): the same for
+// every call with that seed, so a thread computes them once.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+__device__ __forceinline__ PhiloxKeys philox_keys(uint32_t k0, uint32_t k1) {
+  constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+  PhiloxKeys k;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = k0 + (uint32_t)r * W0;
+    k.k1[r] = k1 + (uint32_t)r * W1;
+  }
+  return k;
+}
 __device__ __forceinline__ uint4 philox4x32_10(uint32_t x0, uint32_t x1, uint32_t x2,
-                                               uint32_t x3, uint32_t k0, uint32_t k1) {
-  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+                                               uint32_t x3, const PhiloxKeys& k) {
+  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     const uint64_t p0 = (uint64_t)M0 * x0, p1 = (uint64_t)M1 * x2;  // one wide multiply each
     const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
     const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
-    x0 = hi1 ^ x1 ^ k0;
+    x0 = hi1 ^ x1 ^ k.k0[r];
     x1 = lo1;
-    x2 = hi0 ^ x3 ^ k1;
+    x2 = hi0 ^ x3 ^ k.k1[r];
     x3 = lo0;
-    k0 += W0;
-    k1 += W1;
   }
   return make_uint4(x0, x1, x2, x3);
 }
