@@ -15,8 +15,10 @@
 //     grouped-query attention with an even group size (kPairs) the two tiles are the same
 //     128 rows of two query heads of one KV group instead: equal key-tile ranges, the same
 //     K/V tiles, so neither tile idles while the other takes a key tile alone;
-//   * warp 8 streams Q once and K_j, V_j through a shared-memory ring with TMA
-//     (128-byte swizzle), skipping the key tiles the mask empties;
+//   * thread 0 issues the TMA copies of the two Q tiles and of the first four ring uses
+//     as soon as the barriers are initialised; warp 8 then streams the remaining K_j, V_j
+//     through the shared-memory ring (128-byte swizzle), skipping the key tiles the mask
+//     empties;
 //   * warp 9 allocates tensor memory and issues every tcgen05.mma from one thread:
 //     S_t = Q_t K_j^T into TMEM, then O_t += P_t V_j with P_t read from TMEM;
 //     the two query tiles ping-pong so that the softmax of one tile overlaps the
@@ -25,7 +27,9 @@
 //     per query row reads its 128 scores from TMEM, applies the score and mask
 //     modifications, updates m and l with exp2, writes P as bf16 back into the
 //     score columns, and rescales its O row in TMEM when the max has grown by more
-//     than 2^8 (a stale max is exact: O and l share it until the final division).
+//     than 2^8 (a stale max is exact: O and l share it until the final division);
+//     at the end each warp stages its 32 rows of O / l in shared memory over its Q tile
+//     and writes them out as whole rows.
 //   * warps 8-11 form the third warpgroup (warp 11 has no role); it drops to 40
 //     registers a thread so that each softmax thread can hold its 128 scores and the
 //     row state in 232 without spilling.
