@@ -147,16 +147,16 @@ KERNEL_SOURCES = {"fwd_tc_kernel": ("fwd_tc.cu",), "dkdv_kernel": ("bwd_tc.cu", 
 SHARED_HEADERS = ("ptx.cuh", "mask.cuh", "kernels.h")
 # decode_tc_kernel: the paged-decode workload (B=64, lengths 512-8192).
 NCU_TRAFFIC = {
-    "fwd_tc_kernel": {"bytes": 201401856 + 46906880,
-                    "sha256": "f2035381381d425626d0346da62b9235efa4587e3cf84f6894afbafca6373bb6"},
-    "rowdot_kernel": {"bytes": 135311616 + 498688,
-                    "sha256": "6bf774e08dded1c49bfce5e41d3b0adbb6d495a45f322126d274bd99fd43dc8c"},
-    "dkdv_kernel": {"bytes": 270683392 + 101847552,
-                  "sha256": "a245868791e0a6e87bb37b2a3df24067e1ff8005bf06601e658de8c243dfc3f6"},
-    "dq_kernel": {"bytes": 270634496 + 49656832,
-                "sha256": "a245868791e0a6e87bb37b2a3df24067e1ff8005bf06601e658de8c243dfc3f6"},
-    "decode_tc_kernel": {"bytes": 1119389440 + 9509376,
-                       "sha256": "43f62fe2b35363eb468b63ca50e963145d60432a764d8956e4d030d7913e7c38"},
+    "fwd_tc_kernel": {"bytes": 201466112 + 47017728,
+                    "sha256": "a1501cbbd8b5048f95c2734dbc48c13a2eb13f54bc772e83e29c3bd13d491c1a"},
+    "rowdot_kernel": {"bytes": 135310080 + 485888,
+                    "sha256": "907130b51cc9542e5c71b7061ffeb7e26f7e76fde0a5700ed4eb6351009ceb8e"},
+    "dkdv_kernel": {"bytes": 270685440 + 101813760,
+                  "sha256": "526940b6bb4d74aa8715e5e80f5891713689e090d95e518855f0cf99c8c2d535"},
+    "dq_kernel": {"bytes": 270654208 + 49328640,
+                "sha256": "526940b6bb4d74aa8715e5e80f5891713689e090d95e518855f0cf99c8c2d535"},
+    "decode_tc_kernel": {"bytes": 1119356160 + 9067520,
+                       "sha256": "e5baa6b786d411da95b06bbe6b9f34436a88ad59aaa68a53ecd64ab8a0bbfa26"},
 }
 
 def kernel_source_sha(kernel: str) -> str:
